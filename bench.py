@@ -1,0 +1,473 @@
+"""Benchmark: edges/s of k^2-tree semiring SpMV (right and left) on one GB300,
+with the achieved HBM bandwidth of the product kernel against the measured
+peak, an end-to-end figure through host buffers, and the CPU oracle timed
+on a bounded sample of the same workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+A step is one pass of the hot path over the workload: the right and the
+left product (for the large R-MAT workload also the 16-vector batch), each
+a fill of y plus the product kernel.  Inputs are resident in HBM when the
+timed region starts; L2 is flushed between steps when the working set is
+smaller than four times L2.  Under torchrun every rank runs an independent
+replica (no data-path collective); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "edges/s per k²-tree SpMV (right & left) on 1 GB300; achieved HBM GB/s vs peak"
+
+
+# --- workloads ----------------------------------------------------------------
+def make_workload(name: str):
+    """(Workload, library options, list of (dir, B) products per step)."""
+    if name == "uniform-1024":
+        wl = synth.uniform_c1()
+        return wl, dict(), [(0, 1), (1, 1)]
+    if name == "rmat20":
+        wl = synth.rmat_c2()
+        return wl, dict(), [(0, 1), (1, 1)]
+    if name == "weblike22":
+        wl = synth.weblike_c3()
+        return wl, dict(n_k4_levels=2), [(0, 32), (1, 32)]
+    if name == "social24":
+        wl = synth.social_c4()
+        return wl, dict(), [(0, 8)]
+    if name.startswith("rmat27"):
+        wl = synth.large_c5(B=16)
+        return wl, dict(cache_last_internal=1), [(0, 1), (1, 1), (0, 16), (1, 16)]
+    if name.startswith("rmat"):   # rmatS: the large recipe at a smaller scale (tests, profiles)
+        scale = int(name[4:])
+        wl = synth.large_c5(scale=scale, edges=int(1.2e9 * (1 << scale) / (1 << 27)), B=16)
+        return wl, dict(cache_last_internal=1), [(0, 1), (1, 1), (0, 16), (1, 16)]
+    raise SystemExit("unknown workload %r" % name)
+
+
+def vector(wl, direction, B):
+    x = wl.xs[direction]
+    if wl.semiring == synth.BOOLEAN:
+        return np.ascontiguousarray(x, dtype=np.uint32)
+    return np.ascontiguousarray(x[:, :B], dtype=np.float32)
+
+
+# --- clocks -------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu = gpu
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+class RawEvents:
+    """CUDA runtime events through ctypes: the library records one of them
+    itself (k2t_spmv_marked), which torch.cuda.Event cannot observe."""
+
+    def __init__(self):
+        import ctypes
+        import ctypes.util
+        lib = None
+        for name in ("libcudart.so.13", "libcudart.so", ctypes.util.find_library("cudart")):
+            if not name:
+                continue
+            try:
+                lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if lib is None:
+            raise RuntimeError("libcudart not found")
+        self.c = ctypes
+        self.lib = lib
+        lib.cudaEventCreate.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
+        lib.cudaEventRecord.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+        lib.cudaEventElapsedTime.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_void_p, ctypes.c_void_p]
+        lib.cudaEventDestroy.argtypes = [ctypes.c_void_p]
+
+    def create(self):
+        h = self.c.c_void_p()
+        if self.lib.cudaEventCreate(self.c.byref(h)) != 0:
+            raise RuntimeError("cudaEventCreate failed")
+        return h.value
+
+    def record(self, ev, stream_handle):
+        if self.lib.cudaEventRecord(ev, stream_handle) != 0:
+            raise RuntimeError("cudaEventRecord failed")
+
+    def ms(self, a, b):
+        v = self.c.c_float()
+        if self.lib.cudaEventElapsedTime(self.c.byref(v), a, b) != 0:
+            raise RuntimeError("cudaEventElapsedTime failed")
+        return float(v.value)
+
+    def destroy(self, ev):
+        self.lib.cudaEventDestroy(ev)
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+# --- byte accounting ------------------------------------------------------------
+def algorithmic_bytes(stats, semiring, direction, B):
+    """Bytes a product kernel must move: the tree parts it reads, x once, y
+    read and written once (the count of the pages' Table 4)."""
+    tree = (stats.t_bytes_device + stats.l_bytes_device + stats.dir_bytes + stats.top_bytes +
+            stats.cached_bytes + stats.plan_bytes)
+    n_in = stats.n_cols if direction == 0 else stats.n_rows
+    n_out = stats.n_rows if direction == 0 else stats.n_cols
+    width = 1 if semiring == synth.BOOLEAN else B
+    return int(tree + 4 * n_in * width + 8 * n_out * width)
+
+
+# --- parity on sampled outputs --------------------------------------------------
+def parity_sample(wl, got: dict, n_sample: int = 2048, seed: int = 99):
+    """Compare sampled outputs of every timed product with the oracle's
+    edge-list definition (section 2.2), bit-exact or within the fp32 bound."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    checked, bad = 0, 0
+    for (d, B), y in got.items():
+        n_out = wl.n_rows if d == 0 else wl.n_cols
+        sample = np.unique(rng.integers(0, n_out, size=n_sample))
+        ref = oracle.rows_product(wl.rows, wl.cols, wl.n_rows, wl.n_cols, d, wl.semiring,
+                                  vector(wl, d, B), sample, B=B, w=wl.w)
+        if wl.semiring == synth.PLUS_TIMES:
+            err = np.abs(y[sample].astype(np.float64) - ref.y)
+            bad += int((~(err <= oracle.plus_times_tolerance(ref.scale))).sum())
+        else:
+            g = np.ascontiguousarray(y[sample]).view(np.uint32)
+            bad += int((g != np.ascontiguousarray(ref.y).view(np.uint32)).sum())
+        checked += int(ref.y.size)
+    return {"checked_entries": checked, "mismatches": bad, "ok": bad == 0,
+            "against": "oracle edge-list definition on sampled outputs"}
+
+
+# --- CPU oracle on a bounded sample ------------------------------------------------
+def oracle_sample(wl, target_edges: int):
+    """Edges of the leading rows holding about target_edges non-zeros."""
+    m = wl.rows.size
+    if m <= target_edges:
+        return wl.rows, wl.cols, wl.n_rows, "all %d edges" % m
+    order = np.bincount(wl.rows, minlength=wl.n_rows).cumsum()
+    R = int(np.searchsorted(order, target_edges)) + 1
+    sel = wl.rows < R
+    return wl.rows[sel], wl.cols[sel], R, "rows [0, %d): %d of %d edges" % (R, int(sel.sum()), m)
+
+
+def time_oracle(wl, products, target_edges: int, steps: int = 1, warmup: int = 0):
+    """Rank-based recursive descent of the oracle (single thread), right and
+    left over the sample; returns (edges/s, description, per-step seconds)."""
+    import oracle
+    r, c, R, desc = oracle_sample(wl, target_edges)
+    t = oracle.OracleTree(r, c, R, wl.n_cols, n_k4=0)
+    m = int(oracle.dedup_edges(r, c)[0].size)
+    times = []
+    for it in range(warmup + steps):
+        t0 = time.perf_counter()
+        units = 0
+        for (d, B) in products:
+            x = vector(wl, d, B)
+            if d == 1:
+                x = x[:R]
+            t.spmv(d, wl.semiring, x, B=B, w=wl.w)
+            units += m * B
+        dt = time.perf_counter() - t0
+        if it >= warmup:
+            times.append(dt)
+    return units / statistics.median(times), desc, times, units
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl, _, products = make_workload(args.workload)
+    eps, desc, times, units = time_oracle(wl, products, args.oracle_edges, steps=args.steps, warmup=args.warmup)
+    total = sum(times)
+    value = units * len(times) / total
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "edges/s", "n_gpus": args.gpus,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": dtype_name(wl), "data": "synthetic",
+           "config": {"workload": wl.name, "products": [list(p) for p in products]},
+           "cpu_baseline": {"value": value, "unit": "edges/s", "cores": 1, "kind": "oracle",
+                            "sample": desc},
+           "e2e": {"value": value, "unit": "edges/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+
+
+def dtype_name(wl):
+    return "u32" if wl.semiring == synth.BOOLEAN else "f32"
+
+
+# --- the GPU arm ------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    import compressed_graph_spmv_gb300 as k2t
+    from compressed_graph_spmv_gb300 import k2t as K
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    t_gen = time.perf_counter()
+    wl, wopts, products = make_workload(args.workload)
+    t_gen = time.perf_counter() - t_gen
+    max_b = max(B for _, B in products)
+    opts = dict(wopts, host_vectors=1, max_batch=max_b)
+    if args.engine is not None:
+        opts["engine"] = args.engine
+    t_build = time.perf_counter()
+    tree = K.Tree(wl.rows, wl.cols, wl.n_rows, wl.n_cols, **opts)
+    t_build = time.perf_counter() - t_build
+    st = tree.stats()
+    ws = tree.workspace_bytes()
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    tree.upload()
+    torch.cuda.synchronize()
+    footprint = free0 - torch.cuda.mem_get_info()[0]
+
+    boolean = wl.semiring == synth.BOOLEAN
+    dev_x, dev_y = {}, {}
+    for (d, B) in products:
+        xv = vector(wl, d, B)
+        n_out = wl.n_rows if d == 0 else wl.n_cols
+        if boolean:
+            dev_x[(d, B)] = torch.from_numpy(xv.view(np.int32)).cuda()
+            dev_y[(d, B)] = torch.empty(n_out, dtype=torch.int32, device="cuda")
+        else:
+            dev_x[(d, B)] = torch.from_numpy(xv).cuda()
+            dev_y[(d, B)] = torch.empty(n_out, B, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    m = int(st.nnz)
+
+    def product(p, ev=None):
+        d, B = p
+        if ev is None:
+            tree.spmv(d, wl.semiring, dev_x[p], dev_y[p], B=B, w=wl.w, stream=stream)
+        else:
+            tree.spmv_marked(d, wl.semiring, dev_x[p], dev_y[p], B, wl.w, stream, ev)
+
+    # parity of every timed product on sampled outputs, before timing
+    for p in products:
+        product(p)
+    torch.cuda.synchronize()
+    got = {p: (dev_y[p].cpu().numpy().view(np.uint32) if boolean else dev_y[p].cpu().numpy()) for p in products}
+    parity = parity_sample(wl, got) if not args.no_parity else {"skipped": True}
+
+    # L2 flush between steps unless the working set dwarfs L2
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    work_bytes = max(algorithmic_bytes(st, wl.semiring, d, B) for d, B in products)
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device="cuda") if work_bytes < 4 * l2 else None
+
+    for _ in range(args.warmup):
+        for p in products:
+            product(p)
+        if flush is not None:
+            flush.add_(1.0)
+    torch.cuda.synchronize()
+
+    nprod = len(products)
+    rev = RawEvents()
+    sh = stream.cuda_stream
+    evs = [[(rev.create(), rev.create(), rev.create()) for _ in products] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for s in range(args.steps):
+        for i, p in enumerate(products):
+            e0, e1, e2 = evs[s][i]
+            rev.record(e0, sh)
+            product(p, e1)
+            rev.record(e2, sh)
+        if flush is not None:
+            flush.add_(1.0)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+
+    prod_ms = np.array([[rev.ms(evs[s][i][0], evs[s][i][2]) for i in range(nprod)] for s in range(args.steps)])
+    main_ms = np.array([[rev.ms(evs[s][i][1], evs[s][i][2]) for i in range(nprod)] for s in range(args.steps)])
+    for row in evs:
+        for trip in row:
+            for e in trip:
+                rev.destroy(e)
+    step_ms = prod_ms.sum(axis=1)
+    total_s = float(step_ms.sum()) / 1e3
+    if dist:
+        tt = torch.tensor([total_s], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_s = float(tt.item())
+    units_per_step = sum(m * B for _, B in products)
+    value = units_per_step * args.steps * world / total_s
+
+    # roofline of the dominant kernel (the product kernel with the largest time)
+    per_kernel = []
+    for i, (d, B) in enumerate(products):
+        avg = float(main_ms[:, i].mean()) / 1e3
+        byt = algorithmic_bytes(st, wl.semiring, d, B)
+        per_kernel.append({"product": "%s B=%d" % ("right" if d == 0 else "left", B), "avg_ms": avg * 1e3,
+                           "fill_ms": float((prod_ms[:, i] - main_ms[:, i]).mean()),
+                           "algorithmic_bytes": byt, "achieved_gbs": byt / avg / 1e9,
+                           "edges_per_s": m * B / avg})
+    dom = max(range(nprod), key=lambda i: per_kernel[i]["avg_ms"])
+    peak, peak_kind = measured_peak()
+    ach = per_kernel[dom]["achieved_gbs"]
+    roofline = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+                "traffic": None, "peak_source": peak_kind, "kernel": per_kernel[dom]["product"],
+                "bytes_per_launch": per_kernel[dom]["algorithmic_bytes"]}
+
+    # end to end through the C ABI with host buffers (copies inside the timed region)
+    hx, hy = {}, {}
+    for p in products:
+        d, B = p
+        xv = vector(wl, d, B)
+        n_out = wl.n_rows if d == 0 else wl.n_cols
+        hx[p] = torch.from_numpy(xv.view(np.int32) if boolean else xv).pin_memory().numpy()
+        shape = (n_out,) if boolean else (n_out, B)
+        hy[p] = torch.empty(shape, dtype=torch.int32 if boolean else torch.float32).pin_memory().numpy()
+    h2d = sum(hx[p].nbytes for p in products)
+    d2h = sum(hy[p].nbytes for p in products)
+    e2e_steps = max(1, min(args.steps, 5))
+    for p in products:
+        tree.spmv_host(p[0], wl.semiring, hx[p], hy[p], B=p[1], w=wl.w)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        for p in products:
+            tree.spmv_host(p[0], wl.semiring, hx[p], hy[p], B=p[1], w=wl.w)
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    e2e = {"value": units_per_step * world / e2e_s, "unit": "edges/s",
+           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps}
+
+    launches_per_product = 2 if st.engine != k2t.ENGINE_LEVELSYNC else 1 + int(st.n_steps) * (3 if st.offsets else 1)
+    out = {"metric": METRIC, "value": value, "unit": "edges/s", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": float(step_ms.mean()), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": dtype_name(wl), "data": "synthetic",
+           "config": {"workload": wl.name, "nnz": m, "n": wl.n_rows, "levels": int(st.levels), "d0": int(st.d0),
+                      "engine": ["auto", "fused", "levelsync", "cached"][int(st.engine)],
+                      "products": [list(p) for p in products],
+                      "l2": "flushed between steps" if flush is not None else "inputs larger than L2",
+                      "parallelism": "replicas" if world > 1 else "single"},
+           "roofline": roofline, "kernels": per_kernel,
+           "e2e": e2e, "gpu_launches": launches_per_product * nprod * args.steps, "clocks": clk,
+           "parity": parity,
+           "footprint": {"predicted_bytes": ws, "measured_bytes": int(footprint),
+                         "tree_bits_per_edge": st.tree_bits / max(1, m)},
+           "wall_ms_per_step": 1e3 * wall / args.steps,
+           "host_seconds": {"generate": t_gen, "build": t_build}}
+    if rank == 0 and not args.no_cpu_baseline:
+        eps, desc, _, _ = time_oracle(wl, products, args.oracle_edges)
+        out["cpu_baseline"] = {"value": eps, "unit": "edges/s", "cores": 1, "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(out))
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="rmat20")
+    ap.add_argument("--engine", type=int, default=None)
+    ap.add_argument("--oracle-edges", type=int, default=1_500_000)
+    ap.add_argument("--no-parity", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,309 @@
+// k2t_device.cu -- sm_103a kernels and the device half of the C ABI.
+//
+// What a product computes follows Algorithm 1 of "A GPU Engine for Sparse
+// Matrix-Vector Products on k^2-Tree-Compressed Graphs": y is filled with the
+// semiring zero, the frontier of a cached level is expanded level by level
+// (child j of node t at position off_t + j, off_t the exclusive prefix sum of
+// the fan-outs), and the nodes of the last internal level visit their leaves
+// in place, adding w (x) x_c to y_r for every set cell (r, c) with one atomic
+// of the semiring (Table 1).  Left products swap the decoded coordinates
+// (section 3.6); batches update B contiguous entries per cell (section 3.6).
+//
+// Three engines share the leaf step:
+//   FUSED      one launch; each thread block takes a chunk of whole subtrees
+//              and descends it level by level in shared memory, offsets from
+//              block-wide scans of the fan-outs; no global scratch.
+//   LEVELSYNC  the tiled descent of section 3.4: one launch per tile and
+//              level, frontier codes in global buffers of at most M entries,
+//              offsets from the directory or from a per-tile scan (3.2);
+//              optionally replayed as one CUDA graph.
+//   CACHED     the k^2+F configuration of section 3.5: one leaf kernel over
+//              the cached coordinates of the last internal level.
+//
+// A frontier entry is the pair (row, col) of its block in units of the
+// block side of its level, rather than the pages' 64-bit Morton code: the
+// same information, one shift-or per coordinate per level, and nothing to
+// deinterleave at the leaves.
+#include "k2t_kernels.cuh"
+
+namespace k2t {
+
+thread_local int g_last_cuda = 0;
+
+// y <- 0bar: `words` 32-bit words set to `pattern` (Algorithm 1, line 1).
+__global__ void __launch_bounds__(256) fill_kernel(uint32_t *y, uint64_t words, uint32_t pattern)
+{
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const uint64_t head = (16u - ((uintptr_t)y & 15u)) / 4u % 4u;  // words before 16-byte alignment
+    if (i < head && i < words) y[i] = pattern;
+    uint64_t nvec = words > head ? (words - head) / 4 : 0;
+    uint4 p4 = make_uint4(pattern, pattern, pattern, pattern);
+    uint4 *v = reinterpret_cast<uint4 *>(y + head);
+    for (uint64_t k = i; k < nvec; k += stride) v[k] = p4;
+    uint64_t tail = head + nvec * 4;
+    for (uint64_t k = tail + i; k < words; k += stride) y[k] = pattern;
+}
+
+// Algorithm 1, lines 5-10, for one tile: the frontier entries of nodes
+// [a, a+count) (read from src at index t - src_base) expand into their
+// children's entries, written at dst[child - dst_base].
+__global__ void __launch_bounds__(kWalkThreads)
+ls_expand_kernel(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix, uint32_t a, uint32_t count,
+                 const Coord *src, uint32_t src_base, Coord *dst, uint32_t dst_base)
+{
+    const uint32_t wid = blockIdx.x * (kWalkThreads / 32) + (threadIdx.x >> 5);
+    uint32_t s, e, base;
+    if (!tile_block(sig, dir, prefix, a, count, dst_base, wid, s, e, base)) return;
+    warp_walk(sig, s, e, base, [&](uint32_t t, uint32_t sg, uint32_t pos) {
+        const Coord p = src[t - src_base];
+        Coord *o = dst + (pos - dst_base);
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+            if (sg & (1u << b)) *o++ = child_of(p, b);
+    });
+}
+
+// Scan offsets (section 3.2), first pass: fan-out total of every 256-node
+// block of the tile [a, a+count).
+__global__ void __launch_bounds__(kWalkThreads)
+ls_block_sums_kernel(const uint8_t *sig, uint32_t a, uint32_t count, uint32_t *sums)
+{
+    const uint32_t wid = blockIdx.x * (kWalkThreads / 32) + (threadIdx.x >> 5);
+    const uint32_t s = a + 256u * wid;
+    if (s >= a + count) return;
+    const uint32_t e = min(s + 256u, a + count);
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t t0 = s + 8u * lane;
+    uint32_t v = t0 < e ? (uint32_t)__popc(load8(sig, t0, e)) : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) sums[wid] = v;
+}
+
+// Second pass: exclusive prefix sums of the block totals, one thread block.
+__global__ void __launch_bounds__(1024) ls_scan_kernel(const uint32_t *sums, uint32_t nblocks, uint32_t *prefix)
+{
+    __shared__ uint32_t wsum[32];
+    const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
+    const uint32_t per = (nblocks + blockDim.x - 1) / blockDim.x;
+    const uint32_t i0 = min(tid * per, nblocks), i1 = min(i0 + per, nblocks);
+    uint32_t tot = 0;
+    for (uint32_t i = i0; i < i1; ++i) tot += sums[i];
+    uint32_t incl = warp_incl_scan(tot);
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t v = lane < (blockDim.x >> 5) ? wsum[lane] : 0u;
+        uint32_t vi = warp_incl_scan(v);
+        wsum[lane] = vi - v;
+    }
+    __syncthreads();
+    uint32_t run = wsum[warp] + incl - tot;
+    for (uint32_t i = i0; i < i1; ++i) { prefix[i] = run; run += sums[i]; }
+}
+
+void device_release(k2t_tree *t)
+{
+    DeviceState *d = t->dev;
+    if (!d) return;
+    if (d->gexec) cudaGraphExecDestroy(d->gexec);
+    if (d->graph) cudaGraphDestroy(d->graph);
+    if (d->cap_stream) cudaStreamDestroy(d->cap_stream);
+    if (d->owned && d->arena) cudaFree(d->arena);
+    delete d;
+    t->dev = nullptr;
+}
+
+
+namespace {
+
+LaunchFn pick(uint32_t engine, int semiring, int dir, int vw)
+{
+    if (semiring == K2T_PLUS_TIMES) return pick_plus_times(engine, dir, vw);
+    if (semiring == K2T_BOOLEAN) return pick_boolean(engine, dir, vw);
+    return pick_min_plus(engine, dir, vw);
+}
+
+// Queue a whole product (fill + engine) on `st`.
+int enqueue_product(k2t_tree *t, int32_t dir, int32_t semiring, float w, const void *x, void *y, uint32_t B,
+                    cudaStream_t st, cudaEvent_t marker)
+{
+    DeviceState *d = t->dev;
+    const uint64_t n_out = dir == K2T_RIGHT ? t->n_rows : t->n_cols;
+    const uint64_t words = semiring == K2T_BOOLEAN ? n_out : n_out * (uint64_t)B;
+    const uint32_t pattern = semiring == K2T_MIN_PLUS ? 0x7f800000u : 0u;
+    if (words) {
+        uint64_t blocks = (words / 4 + 255) / 256 + 1;
+        if (blocks > 152ull * 16) blocks = 152ull * 16;
+        fill_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<uint32_t *>(y), words, pattern);
+    }
+    if (marker) cudaEventRecord(marker, st);
+    if (t->empty) return K2T_OK;
+    int vw = 1;
+    if (semiring != K2T_BOOLEAN) {
+        uintptr_t al = (uintptr_t)x | (uintptr_t)y;
+        if (B % 4 == 0 && (al & 15u) == 0) vw = 4;
+        else if (B % 2 == 0 && (al & 7u) == 0) vw = 2;
+    }
+    VecArgs va;
+    va.x = x;
+    va.y = y;
+    va.B = B;
+    va.w = w;
+    va.mask = B >= 32 ? 0xffffffffu : ((1u << B) - 1u);
+    pick(t->engine, semiring, dir, vw)(t, d, va, st);
+    return K2T_OK;
+}
+
+}  // namespace
+}  // namespace k2t
+
+using namespace k2t;
+
+extern "C" {
+
+int k2t_upload(k2t_tree *t, void *arena, uint64_t arena_bytes, void *stream)
+{
+    if (!t) return K2T_EINVAL;
+    if (t->dev) return K2T_ESTATE;
+    if (arena && ((uintptr_t)arena % kArenaAlign)) return K2T_EINVAL;
+    const ArenaLayout &L = t->layout;
+    if (arena && arena_bytes < L.total) return K2T_ENOMEM;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    DeviceState *d = new (std::nothrow) DeviceState;
+    if (!d) return K2T_ENOMEM;
+    cudaGetDevice(&d->device);
+    if (!arena) {
+        cudaError_t e = cudaMalloc(&d->arena, L.total ? L.total : kArenaAlign);
+        if (e != cudaSuccess) { g_last_cuda = (int)e; delete d; return K2T_ENOMEM; }
+        d->owned = true;
+    } else {
+        d->arena = arena;
+    }
+    t->dev = d;
+    auto fail = [&](cudaError_t e) { g_last_cuda = (int)e; device_release(t); return K2T_ECUDA; };
+    cudaError_t e = cudaMemsetAsync(d->arena, 0, L.total, st);
+    if (e != cudaSuccess) return fail(e);
+    const int l = t->levels;
+    d->tree.levels = l;
+    d->tree.d0 = t->d0;
+    d->err = at<uint32_t>(d->arena, L.err_off);
+    for (int lv = 0; lv < l; ++lv) {
+        d->tree.lv[lv].n = (uint32_t)t->nodes[(size_t)lv];
+        if (L.sig_bytes[lv]) {
+            uint8_t *p = at<uint8_t>(d->arena, L.sig_off[lv]);
+            d->tree.lv[lv].sig = p;
+            uint64_t bytes = (t->nodes[(size_t)lv] + 1) / 2;
+            if (bytes && (e = cudaMemcpyAsync(p, t->sig[(size_t)lv].data(), bytes, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+                return fail(e);
+        }
+        if (L.dir_bytes[lv]) {
+            uint32_t *p = at<uint32_t>(d->arena, L.dir_off[lv]);
+            d->tree.lv[lv].dir = p;
+            if ((e = cudaMemcpyAsync(p, t->dir[(size_t)(lv - t->d0)].data(), L.dir_bytes[lv], cudaMemcpyHostToDevice, st)) != cudaSuccess)
+                return fail(e);
+        }
+        if (L.buf_off[lv]) d->buf[lv] = at<Coord>(d->arena, L.buf_off[lv]);
+    }
+    auto put = [&](uint64_t off, uint64_t bytes, const void *src) -> cudaError_t {
+        if (!bytes) return cudaSuccess;
+        return cudaMemcpyAsync(at<char>(d->arena, off), src, bytes, cudaMemcpyHostToDevice, st);
+    };
+    if (L.top_bytes) { d->top = at<Coord>(d->arena, L.top_off); if ((e = put(L.top_off, L.top_bytes, t->top.data()))) return fail(e); }
+    if (L.cached_bytes) { d->cached = at<Coord>(d->arena, L.cached_off); if ((e = put(L.cached_off, L.cached_bytes, t->cached.data()))) return fail(e); }
+    if (L.chunk_bytes) { d->chunks = at<uint32_t>(d->arena, L.chunk_off); if ((e = put(L.chunk_off, L.chunk_bytes, t->chunks.data()))) return fail(e); }
+    if (L.root_bytes) { d->roots = at<Coord>(d->arena, L.root_off); if ((e = put(L.root_off, L.root_bytes, t->roots.data()))) return fail(e); }
+    if (L.scan_bytes) {
+        d->scan_sums = at<uint32_t>(d->arena, L.scan_off);
+        d->scan_prefix = d->scan_sums + L.scan_bytes / 8;
+    }
+    if (L.vec_bytes) { d->vec[0] = at<void>(d->arena, L.vec_off[0]); d->vec[1] = at<void>(d->arena, L.vec_off[1]); }
+    if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return fail(e);
+    return K2T_OK;
+}
+
+int k2t_spmv_marked(k2t_tree *t, int32_t dir, int32_t semiring, float w, const void *x, void *y, uint32_t B,
+                    void *stream, void *event_after_fill)
+{
+    if (!t) return K2T_EINVAL;
+    if (!t->dev) return K2T_ESTATE;
+    if (dir != K2T_RIGHT && dir != K2T_LEFT) return K2T_EINVAL;
+    if (semiring < K2T_PLUS_TIMES || semiring > K2T_MIN_PLUS) return K2T_EINVAL;
+    if (!x || !y || B == 0) return K2T_EINVAL;
+    if (B > K2T_MAX_BATCH) return K2T_ERANGE;
+    if (((uintptr_t)x | (uintptr_t)y) & 3u) return K2T_EINVAL;
+    const uint64_t n_in = dir == K2T_RIGHT ? t->n_cols : t->n_rows;
+    const uint64_t n_out = dir == K2T_RIGHT ? t->n_rows : t->n_cols;
+    const uint64_t esz = semiring == K2T_BOOLEAN ? 4u : 4u * (uint64_t)B;
+    uintptr_t xa = (uintptr_t)x, ya = (uintptr_t)y;
+    if (xa < ya + n_out * esz && ya < xa + n_in * esz) return K2T_EINVAL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    DeviceState *d = t->dev;
+    const bool graph = t->engine == K2T_ENGINE_LEVELSYNC && t->opts.use_graph && !t->empty;
+    if (!graph) {
+        int rc = enqueue_product(t, dir, semiring, w, x, y, B, st, static_cast<cudaEvent_t>(event_after_fill));
+        if (rc) return rc;
+        K2T_CUDA(cudaGetLastError());
+        return K2T_OK;
+    }
+    uint32_t wb;
+    std::memcpy(&wb, &w, 4);
+    GraphKey k;
+    k.dir = dir; k.semiring = semiring; k.wbits = wb; k.B = B; k.x = x; k.y = y;
+    const GraphKey &o = d->key;
+    bool same = d->gexec && o.dir == k.dir && o.semiring == k.semiring && o.wbits == k.wbits && o.B == k.B &&
+                o.x == k.x && o.y == k.y;
+    if (!same) {
+        if (d->gexec) { cudaGraphExecDestroy(d->gexec); d->gexec = nullptr; }
+        if (d->graph) { cudaGraphDestroy(d->graph); d->graph = nullptr; }
+        if (!d->cap_stream) K2T_CUDA(cudaStreamCreateWithFlags(&d->cap_stream, cudaStreamNonBlocking));
+        K2T_CUDA(cudaStreamBeginCapture(d->cap_stream, cudaStreamCaptureModeThreadLocal));
+        enqueue_product(t, dir, semiring, w, x, y, B, d->cap_stream, nullptr);
+        cudaError_t e = cudaStreamEndCapture(d->cap_stream, &d->graph);
+        if (e != cudaSuccess) { g_last_cuda = (int)e; d->graph = nullptr; return K2T_ECUDA; }
+        K2T_CUDA(cudaGraphInstantiate(&d->gexec, d->graph, 0));
+        d->key = k;
+    }
+    if (event_after_fill) K2T_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(event_after_fill), st));
+    K2T_CUDA(cudaGraphLaunch(d->gexec, st));
+    return K2T_OK;
+}
+
+int k2t_spmv(k2t_tree *t, int32_t dir, int32_t semiring, float w, const void *x, void *y, uint32_t B, void *stream)
+{
+    return k2t_spmv_marked(t, dir, semiring, w, x, y, B, stream, nullptr);
+}
+
+int k2t_spmv_host(k2t_tree *t, int32_t dir, int32_t semiring, float w, const void *x_host, void *y_host, uint32_t B,
+                  void *stream)
+{
+    if (!t || !x_host || !y_host || B == 0) return K2T_EINVAL;
+    if (!t->dev) return K2T_ESTATE;
+    if (!t->opts.host_vectors || !t->dev->vec[0]) return K2T_ESTATE;
+    if (B > t->opts.max_batch) return K2T_ERANGE;
+    const uint64_t n_in = dir == K2T_RIGHT ? t->n_cols : t->n_rows;
+    const uint64_t n_out = dir == K2T_RIGHT ? t->n_rows : t->n_cols;
+    const uint64_t esz = semiring == K2T_BOOLEAN ? 4u : 4u * (uint64_t)B;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    DeviceState *d = t->dev;
+    K2T_CUDA(cudaMemcpyAsync(d->vec[0], x_host, n_in * esz, cudaMemcpyHostToDevice, st));
+    int rc = k2t_spmv(t, dir, semiring, w, d->vec[0], d->vec[1], B, stream);
+    if (rc) return rc;
+    K2T_CUDA(cudaMemcpyAsync(y_host, d->vec[1], n_out * esz, cudaMemcpyDeviceToHost, st));
+    K2T_CUDA(cudaStreamSynchronize(st));
+    return K2T_OK;
+}
+
+int k2t_device_level(const k2t_tree *t, uint32_t level, const void **sig, const void **dir)
+{
+    if (!t || !sig || !dir || level >= (uint32_t)t->levels) return K2T_EINVAL;
+    if (!t->dev) return K2T_ESTATE;
+    *sig = t->dev->tree.lv[level].sig;
+    *dir = t->dev->tree.lv[level].dir;
+    return K2T_OK;
+}
+
+int k2t_last_cuda_error(void) { return g_last_cuda; }
+
+}  // extern "C"

@@ -1,0 +1,90 @@
+// k2t_internal.h -- structures shared by the host builder (k2t_host.cpp) and
+// the device side (k2t_device.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+#include "../../include/k2t.h"
+
+namespace k2t {
+
+constexpr uint32_t kDirS = 256;        // directory sample period (section 3.2: S = 256)
+constexpr uint32_t kMaxChunkCap = 4096;
+constexpr uint32_t kArenaAlign = 256;
+
+// Coordinates of a node's block, in units of the block side at its level.
+// A frontier entry: (row, col) instead of the pages' Morton code; the two
+// carry the same bits, but a pair needs no deinterleave at the leaves.
+struct Coord { uint32_t r, c; };
+
+// One launch of the level-synchronous engine.
+struct LsStep {
+    uint8_t kind;      // 0 expand, 1 leaf
+    uint8_t level;     // level of the parents
+    uint8_t src;       // 0xff: host-expanded top; else level whose buffer holds the codes
+    uint8_t pad;
+    uint32_t a;        // first node (index within its level)
+    uint32_t count;    // nodes in the tile
+    uint32_t src_base; // level index of slot 0 of the source buffer
+    uint32_t dst_base; // level index of slot 0 of the destination buffer (= first child)
+};
+
+inline uint64_t align_up(uint64_t v, uint64_t a) { return (v + a - 1) / a * a; }
+
+// Byte offsets of every part inside the device arena.
+struct ArenaLayout {
+    uint64_t sig_off[K2T_MAX_LEVELS];   // levels d0..l-1 (l-1 = L)
+    uint64_t sig_bytes[K2T_MAX_LEVELS];
+    uint64_t dir_off[K2T_MAX_LEVELS];   // levels d0..l-2
+    uint64_t dir_bytes[K2T_MAX_LEVELS];
+    uint64_t top_off, top_bytes;
+    uint64_t cached_off, cached_bytes;
+    uint64_t chunk_off, chunk_bytes;
+    uint64_t root_off, root_bytes;
+    uint64_t buf_off[K2T_MAX_LEVELS];   // LEVELSYNC frontier buffers (levels d0+1..l-2)
+    uint64_t buf_bytes;                 // per buffer
+    uint64_t scan_off, scan_bytes;      // LEVELSYNC scan space (block sums + prefixes)
+    uint64_t err_off, err_bytes;        // device error word
+    uint64_t vec_off[2], vec_bytes;     // host-product x and y
+    uint64_t total;
+};
+
+struct DeviceState;  // defined in k2t_device.cu
+
+}  // namespace k2t
+
+struct k2t_tree {
+    k2t_opts opts;
+    uint64_t n_rows = 0, n_cols = 0, nnz = 0;
+    int dim_bits = 0, n_k4 = 0, levels = 0;
+    int d0 = 0;
+    uint32_t engine = 0;   // resolved engine
+    bool empty = false;    // nnz == 0: a product is only the fill
+    std::vector<uint64_t> nodes;                  // N_d
+    // Signatures: k = 2 levels hold 16 nibbles per word (node t at bits
+    // 4*(t%16)); k = 4 levels hold 4 16-bit signatures per word.
+    std::vector<std::vector<uint64_t>> sig;
+    std::vector<std::vector<uint32_t>> dir;       // index d - d0, levels d0..l-2
+    std::vector<k2t::Coord> top;                  // level d0
+    std::vector<k2t::Coord> cached;               // level l-2 (k^2+F)
+    // FUSED plan: per chunk, [root index, d_c, (start, count) for levels d0..l-1]
+    std::vector<uint32_t> chunks;
+    uint32_t chunk_stride = 0;
+    uint64_t n_chunks = 0;
+    std::vector<k2t::Coord> roots;                // top entries, then roots of split chunks
+    // LEVELSYNC plan
+    std::vector<k2t::LsStep> steps;
+    uint64_t max_tile_nodes = 0;
+    k2t::ArenaLayout layout{};
+    k2t::DeviceState *dev = nullptr;
+};
+
+namespace k2t {
+// implemented in k2t_host.cpp
+uint64_t level_offset(const k2t_tree *t, int d, uint64_t node);  // first child of node (d0 <= d <= l-2)
+uint32_t level_sig(const k2t_tree *t, int d, uint64_t node);
+void compute_layout(k2t_tree *t);
+// implemented in k2t_device.cu
+void device_release(k2t_tree *t);
+}  // namespace k2t

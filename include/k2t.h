@@ -1,0 +1,215 @@
+/*
+ * k2t.h -- C ABI of the k^2-tree semiring SpMV library (GB300, sm_103a).
+ *
+ * The operations follow "A GPU Engine for Sparse Matrix-Vector Products on
+ * k^2-Tree-Compressed Graphs" (Tosoni & Mencagli):
+ *   - the k^2-tree of a Boolean n x n matrix, n = 2^l, stored pointer-free
+ *     level by level as signatures of k^2 bits, bit b of a node set iff its
+ *     quadrant b = 2*b1 + b0 is non-empty (section 2.1, Figure 1);
+ *   - y = A x and y^T = x^T A over a semiring (section 2.2, Table 1;
+ *     section 3.6), for one vector or a batch of B vectors (section 3.6);
+ *   - the level-synchronous traversal of Algorithm 1 (section 3), child
+ *     offsets from a scan or a sampled directory (section 3.2), a host-side
+ *     top, tiles (section 3.4), tree-only and cached-frontier configurations
+ *     (section 3.5);
+ *   - the device memory of a product fixed before any kernel runs
+ *     (section 1, "Our approach"; section 3.4).
+ *
+ * Conventions shared by every call
+ *   - Every function returns K2T_OK (0) or a negative K2T_E* status; none
+ *     aborts the process.  k2t_strerror() names a status.
+ *   - A k2t_tree is opaque and owned by the library; k2t_free() releases its
+ *     host memory and any device memory the library allocated for it.
+ *   - Device pointers (x, y, the arena) belong to the caller, who keeps them
+ *     alive until the work queued on the given stream has finished.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Device calls are asynchronous on that stream.
+ *   - Vector layout: row-major n x B fp32 (B contiguous values per vertex),
+ *     or, for the Boolean semiring, one uint32 word per vertex whose bit b
+ *     is vector b (B <= 32).  Right products read n_cols entries and write
+ *     n_rows; left products the reverse.  x and y must not overlap.
+ *   - Host calls are thread-compatible: one thread at a time per tree.
+ */
+#ifndef K2T_H
+#define K2T_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define K2T_OK        0
+#define K2T_EINVAL   (-1)  /* bad argument: null pointer, bad enum, misaligned vector */
+#define K2T_ERANGE   (-2)  /* id >= n, side > 2^32, batch > limit, level too wide */
+#define K2T_ENOMEM   (-3)  /* host or device allocation failed, or arena too small */
+#define K2T_ECUDA    (-4)  /* a CUDA runtime call failed (see k2t_last_cuda_error) */
+#define K2T_ESTATE   (-5)  /* wrong call order, e.g. a product before k2t_upload */
+#define K2T_EDEVICE  (-6)  /* a device-side consistency check failed */
+
+/* Opaque handle to one built tree (host image, plan and device image). */
+typedef struct k2t_tree k2t_tree;
+
+/* ---- enums ------------------------------------------------------------- */
+#define K2T_RIGHT 0          /* y = A x        (section 2.2)                 */
+#define K2T_LEFT  1          /* y^T = x^T A    (section 3.6)                 */
+
+#define K2T_PLUS_TIMES 0     /* (R, +, x, 0, 1): contribution w * x_j        */
+#define K2T_BOOLEAN    1     /* ({0,1}, or, and): contribution x_j's word    */
+#define K2T_MIN_PLUS   2     /* (R u {inf}, min, +, inf, 0): w + x_j          */
+
+/* Engines: how a product walks the tree. */
+#define K2T_ENGINE_AUTO      0  /* CACHED if the last level is cached, else FUSED      */
+#define K2T_ENGINE_FUSED     1  /* tree-only, one launch: a thread block descends a
+                                   chunk of whole subtrees in shared memory           */
+#define K2T_ENGINE_LEVELSYNC 2  /* tree-only, Algorithm 1 as written: one expand
+                                   launch per tile and level into global frontier
+                                   buffers of at most tile_M codes (section 3.4)      */
+#define K2T_ENGINE_CACHED    3  /* k^2+F: one leaf kernel over the cached
+                                   coordinates of the last internal level (3.5)       */
+
+/* ChildOffset source (section 3.2), used by the LEVELSYNC engine. */
+#define K2T_OFFSETS_DIRECTORY 0 /* one sample per 256 nodes, stored with the tree  */
+#define K2T_OFFSETS_SCAN      1 /* prefix sums of fan-outs computed at each product */
+
+#define K2T_MAX_LEVELS 33
+#define K2T_MAX_BATCH  32
+
+/* ---- options ----------------------------------------------------------- */
+typedef struct {
+    uint32_t n_k4_levels;         /* leading levels with k = 4 (hybrid tree); 0 = k = 2 throughout */
+    uint32_t cache_last_internal; /* 1: keep the coordinates of the last internal level (k^2+F)    */
+    uint32_t engine;              /* K2T_ENGINE_*                                                   */
+    uint32_t offsets;             /* K2T_OFFSETS_* (LEVELSYNC only; the other engines use the
+                                     directory or the chunk plan)                                   */
+    uint32_t host_top_max_nodes;  /* products start at the deepest level with at most this many
+                                     nodes, expanded on the host (section 3.4); default 65536       */
+    uint32_t chunk_cap;           /* FUSED: last-internal-level nodes per chunk; default 4096,
+                                     at most 4096                                                   */
+    uint64_t tile_m;              /* LEVELSYNC: children per tile M; default 2^20, at least 4      */
+    uint32_t max_batch;           /* largest B products will use (1..32); sizes host-vector buffers */
+    uint32_t host_vectors;        /* 1: the workspace also holds device x and y of max_batch
+                                     vectors for k2t_spmv_host                                      */
+    uint32_t use_graph;           /* LEVELSYNC: record a product's launches once as a CUDA graph   */
+    uint32_t threads;             /* host threads for k2t_build; 0 = all cores                     */
+    uint32_t reserved[8];
+} k2t_opts;
+
+/* ---- statistics -------------------------------------------------------- */
+typedef struct {
+    uint64_t n_rows, n_cols;      /* matrix shape as given                        */
+    uint64_t nnz;                 /* distinct non-zeros (= set bits of L)          */
+    uint32_t levels;              /* l: levels 0 (root) .. l-1 (leaves)            */
+    uint32_t n_k4_levels;
+    uint32_t dim_bits;            /* padded side n = 2^dim_bits                    */
+    uint32_t d0;                  /* first level a product expands on the device   */
+    uint64_t level_nodes[K2T_MAX_LEVELS];
+    uint64_t tree_bits;           /* |T| + |L| over all levels                     */
+    uint64_t t_bytes_device;      /* signature bytes of levels d0..l-2 on device   */
+    uint64_t l_bytes_device;      /* leaf signature bytes on device                */
+    uint64_t dir_bytes;           /* directory samples on device                   */
+    uint64_t top_bytes;           /* coordinates of level d0 on device             */
+    uint64_t cached_bytes;        /* cached coordinates of level l-2 (k^2+F)       */
+    uint64_t plan_bytes;          /* chunk table / root coordinates (FUSED)        */
+    uint64_t scratch_bytes;       /* frontier buffers and scan space (LEVELSYNC)   */
+    uint64_t vector_bytes;        /* device x and y for k2t_spmv_host              */
+    uint64_t workspace_bytes;     /* total = k2t_workspace_bytes                   */
+    uint64_t n_chunks;            /* FUSED chunks                                  */
+    uint64_t n_steps;             /* LEVELSYNC launches per product (tiles x kinds)*/
+    uint32_t engine;              /* resolved engine                               */
+    uint32_t offsets;
+    uint32_t uploaded;            /* 1 after k2t_upload                            */
+    uint32_t reserved[5];
+} k2t_stats;
+
+/* Fill *o with the defaults: k = 2, tree-only FUSED engine (AUTO), directory
+ * offsets, top of at most 2^16 nodes, chunk_cap 4096, tile_m 2^20,
+ * max_batch 32, no host vectors, CUDA graph on, all host threads. */
+void k2t_default_opts(k2t_opts *o);
+
+/* Build the tree of the n_rows x n_cols Boolean matrix whose non-zeros are
+ * (rows[i], cols[i]), i < nnz, on the host (section 2.1; construction is the
+ * host step of section 5.1).  Duplicated pairs count once.  The side is padded
+ * to 2^l (at least 4, at least 2^(2*n_k4+2)).  The COO arrays are read, not
+ * kept.  opts may be NULL (defaults).  Plans the product as well: host-side
+ * top (3.4), directories (3.2), chunk or tile plan (3.4), cached level (3.5).
+ * Errors: EINVAL (null out/arrays with nnz > 0, zero side, bad option),
+ * ERANGE (an id >= its side, side > 2^32, a level wider than 2^32 - 1 nodes),
+ * ENOMEM.  On error *out is NULL. */
+int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
+              uint64_t n_rows, uint64_t n_cols, const k2t_opts *opts, k2t_tree **out);
+
+/* Exact device bytes k2t_upload places in its arena (tree, directory, top,
+ * cached level, plan, scratch, optional host-product vectors), known before
+ * any kernel runs (section 1, "Our approach").  Dense x and y of device
+ * products are the caller's and not included. */
+int k2t_workspace_bytes(const k2t_tree *t, uint64_t *bytes);
+
+/* Copy the device image into `arena` (device memory of at least
+ * k2t_workspace_bytes, 256-byte aligned) or, if arena is NULL, into one
+ * cudaMalloc of exactly that size that the library owns.  Uploading twice
+ * is ESTATE.  Errors: EINVAL (misaligned arena), ENOMEM (arena_bytes too
+ * small or allocation failure), ECUDA. */
+int k2t_upload(k2t_tree *t, void *arena, uint64_t arena_bytes, void *stream);
+
+/* y = A x (dir K2T_RIGHT) or y^T = x^T A (K2T_LEFT) over `semiring` with edge
+ * weight w (Table 1: plus-times w = 1, tropical w = 1 for hop counts; the
+ * Boolean semiring ignores w), for B vectors, on device buffers, queued on
+ * `stream`.  y is overwritten with the semiring zero first (Algorithm 1,
+ * line 1).  Plus-times sums in fp32 in no fixed order; Boolean and tropical
+ * results are exact and deterministic.  Tropical minima follow the IEEE
+ * total order without NaN (-0 < +0); NaN inputs give unspecified values.
+ * x and y must be 4-byte aligned (16-byte alignment enables vector access).
+ * Errors: ESTATE (not uploaded), EINVAL (bad dir/semiring, null, B = 0,
+ * overlap), ERANGE (B > 32), ECUDA (launch failure). */
+int k2t_spmv(k2t_tree *t, int32_t dir, int32_t semiring, float w,
+             const void *x, void *y, uint32_t B, void *stream);
+
+/* k2t_spmv that also records the cudaEvent_t `event_after_fill` on the stream
+ * between the fill of y and the product kernels, so a caller can time the
+ * two apart with CUDA events.  When the level-synchronous engine replays a
+ * CUDA graph the event is recorded before the graph (it then marks the start
+ * of the whole product).  Same errors as k2t_spmv. */
+int k2t_spmv_marked(k2t_tree *t, int32_t dir, int32_t semiring, float w,
+                    const void *x, void *y, uint32_t B, void *stream, void *event_after_fill);
+
+/* Same product on HOST buffers: copies x to the device vectors of the
+ * workspace, runs k2t_spmv, copies y back, and synchronises the stream.
+ * Needs opts.host_vectors = 1 and B <= opts.max_batch (else ESTATE/ERANGE).
+ * Host buffers may be pageable; pinned buffers copy faster. */
+int k2t_spmv_host(k2t_tree *t, int32_t dir, int32_t semiring, float w,
+                  const void *x_host, void *y_host, uint32_t B, void *stream);
+
+/* Shape, per-level sizes and the device footprint broken down by part. */
+int k2t_stats_get(const k2t_tree *t, k2t_stats *s);
+
+/* Signatures of one level as one byte per node (low 4 bits for k = 2 levels;
+ * low 8 bits of the 16-bit signature in out[2i], high 8 bits in out[2i+1]
+ * for k = 4 levels).  cap is the capacity of out in bytes; *written is the
+ * number of bytes the level needs.  ERANGE if cap is too small. */
+int k2t_level_signatures(const k2t_tree *t, uint32_t level, uint8_t *out, uint64_t cap,
+                         uint64_t *written);
+
+/* Device pointers of the uploaded image, for instrumentation: the signature
+ * bytes of a level (nibble t of the level at byte t/2, low nibble first) and
+ * its directory (NULL where absent). */
+int k2t_device_level(const k2t_tree *t, uint32_t level, const void **sig, const void **dir);
+
+/* The cells of the matrix, decoded from the tree on the host, in level order
+ * of their leaves.  ERANGE if cap < nnz (then *n_out = nnz). */
+int k2t_decode(const k2t_tree *t, uint32_t *rows, uint32_t *cols, uint64_t cap, uint64_t *n_out);
+
+/* Release the tree, its host image and any library-owned device memory. */
+void k2t_free(k2t_tree *t);
+
+const char *k2t_strerror(int status);
+
+/* The last CUDA error code seen by this thread inside the library (0 if none). */
+int k2t_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* K2T_H */

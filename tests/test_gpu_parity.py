@@ -1,0 +1,187 @@
+"""GPU parity: every engine, semiring, direction and batch width against the
+CPU oracle, through the C ABI, on seeded inputs spanning many chunks/tiles.
+Tolerances are stated in tests/gpu_util.py."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import BOOLEAN, LEFT, PLUS_TIMES, RIGHT, TROPICAL
+import synth
+from gpu_util import assert_match, device_product, random_x
+
+pytestmark = pytest.mark.gpu
+
+K = pytest.importorskip("compressed_graph_spmv_gb300.k2t")
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+ENGINES = [
+    dict(engine=1),                                   # fused, tree-only
+    dict(engine=1, chunk_cap=3),                       # fused, many tiny chunks
+    dict(engine=2, offsets=0, tile_m=16),              # level-sync, directory, many tiles
+    dict(engine=2, offsets=1, tile_m=16),              # level-sync, scan
+    dict(engine=2, offsets=0, tile_m=1 << 20, use_graph=0),
+    dict(engine=3, cache_last_internal=1),             # k^2+F
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    K.load()
+
+
+def _tree(rows, cols, nr, nc, **kw):
+    return K.Tree(rows, cols, nr, nc, **kw).upload()
+
+
+def test_figure1_all_engines():
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "figure1.json")))
+    e = np.array(g["edges_decoded"], np.uint32)
+    ot = oracle.OracleTree(e[:, 0], e[:, 1], 8, 8)
+    rng = np.random.default_rng(0)
+    for kw in ENGINES:
+        t = _tree(e[:, 0], e[:, 1], 8, 8, host_top_max_nodes=1, **kw)
+        for semiring in (PLUS_TIMES, BOOLEAN, TROPICAL):
+            for d in (RIGHT, LEFT):
+                x = random_x(rng, semiring, 8, 3)
+                ref = ot.spmv(d, semiring, x, B=3)
+                assert_match(semiring, device_product(t, d, semiring, x, 3), ref, "%s sr%d d%d" % (kw, semiring, d))
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_ragged(seed):
+    rng = np.random.default_rng(100 + seed)
+    nr = int(rng.integers(1, 700))
+    nc = int(rng.integers(1, 700))
+    n_k4 = int(rng.integers(0, 3))
+    rows, cols, _ = synth.random_small(seed, nr, nc, float(rng.choice([0.002, 0.02, 0.2])))
+    ot = oracle.OracleTree(rows, cols, nr, nc, n_k4=n_k4)
+    top = int(rng.choice([1, 16, 65536]))
+    for kw in ENGINES:
+        t = _tree(rows, cols, nr, nc, n_k4_levels=n_k4, host_top_max_nodes=top, **kw)
+        for semiring in (PLUS_TIMES, BOOLEAN, TROPICAL):
+            for B in (1, 2, 3, 4, 8, 32):
+                if semiring == BOOLEAN and B not in (1, 3, 32):
+                    continue
+                d = int(rng.integers(0, 2))
+                n_in = nc if d == RIGHT else nr
+                x = random_x(rng, semiring, n_in, B)
+                w = float(rng.choice([1.0, 0.5, 2.0])) if semiring != BOOLEAN else 1.0
+                ref = ot.spmv(d, semiring, x, B=B, w=w)
+                got = device_product(t, d, semiring, x, B, w=w)
+                assert_match(semiring, got, ref, "seed%d %s sr%d B%d d%d" % (seed, kw, semiring, B, d))
+
+
+def test_uniform_1024_plus_times():
+    wl = synth.uniform_c1()
+    ot = oracle.OracleTree(wl.rows, wl.cols, wl.n_rows, wl.n_cols)
+    for kw in ENGINES:
+        t = _tree(wl.rows, wl.cols, wl.n_rows, wl.n_cols, host_top_max_nodes=64, **kw)
+        for d in (RIGHT, LEFT):
+            ref = ot.spmv(d, PLUS_TIMES, wl.xs[d], B=1)
+            assert_match(PLUS_TIMES, device_product(t, d, PLUS_TIMES, wl.xs[d], 1), ref, str(kw))
+
+
+def test_exact_special_cases():
+    rows, cols = synth.rmat(16, 0.57, 0.19, 0.19, 400000, 11)
+    n = 1 << 16
+    r, c = oracle.dedup_edges(rows, cols)
+    for kw in ENGINES[:1] + ENGINES[2:4] + ENGINES[5:]:
+        t = _tree(rows, cols, n, n, host_top_max_nodes=256, **kw)
+        # x = 1: out-degree / in-degree, exact in fp32 whatever the atomic order
+        y = device_product(t, RIGHT, PLUS_TIMES, np.ones((n, 1), np.float32), 1)[:, 0]
+        assert np.array_equal(y, np.bincount(r, minlength=n).astype(np.float32))
+        y = device_product(t, LEFT, PLUS_TIMES, np.ones((n, 1), np.float32), 1)[:, 0]
+        assert np.array_equal(y, np.bincount(c, minlength=n).astype(np.float32))
+        # tropical with x = 0, w = 1: 1 on non-empty rows, +inf elsewhere
+        y = device_product(t, RIGHT, TROPICAL, np.zeros((n, 1), np.float32), 1, w=1.0)[:, 0]
+        ne = np.zeros(n, bool)
+        ne[r] = True
+        assert np.all(y[ne] == 1.0) and np.all(np.isinf(y[~ne]))
+
+
+def test_rmat_medium_all_semirings():
+    """R-MAT 2^17, ~1M edges: O1 (edge-list definition) on every output."""
+    rows, cols = synth.rmat(17, 0.57, 0.19, 0.19, 1 << 20, 12)
+    n = 1 << 17
+    rng = np.random.default_rng(12)
+    for kw in (ENGINES[0], ENGINES[2], ENGINES[3], ENGINES[5]):
+        t = _tree(rows, cols, n, n, **kw)
+        for semiring, B in ((PLUS_TIMES, 1), (PLUS_TIMES, 16), (BOOLEAN, 32), (TROPICAL, 8)):
+            for d in (RIGHT, LEFT):
+                x = random_x(rng, semiring, n, B)
+                ref = oracle.spmv_edges(rows, cols, n, n, d, semiring, x, B=B)
+                assert_match(semiring, device_product(t, d, semiring, x, B), ref, "%s sr%d B%d" % (kw, semiring, B))
+
+
+def test_empty_matrix_fills():
+    z = np.zeros(0, np.uint32)
+    for kw in ENGINES:
+        t = _tree(z, z, 100, 37, **kw)
+        y = device_product(t, RIGHT, TROPICAL, np.ones((37, 2), np.float32), 2)
+        assert np.all(np.isinf(y))
+        y = device_product(t, LEFT, PLUS_TIMES, np.ones((100, 5), np.float32), 5)
+        assert np.all(y == 0)
+
+
+def test_host_buffer_product():
+    rows, cols = synth.rmat(12, 0.57, 0.19, 0.19, 20000, 13)
+    n = 4096
+    t = _tree(rows, cols, n, n, host_vectors=1, max_batch=8)
+    rng = np.random.default_rng(13)
+    x = rng.uniform(0, 1, size=(n, 8)).astype(np.float32)
+    y = np.zeros((n, 8), np.float32)
+    t.spmv_host(RIGHT, PLUS_TIMES, x, y, B=8)
+    ref = oracle.spmv_edges(rows, cols, n, n, RIGHT, PLUS_TIMES, x, B=8)
+    assert_match(PLUS_TIMES, y, ref, "host")
+    with pytest.raises(K.K2TError):
+        t.spmv_host(RIGHT, PLUS_TIMES, x, y, B=16)
+
+
+def test_footprint_equals_prediction():
+    import torch
+    rows, cols = synth.rmat(18, 0.57, 0.19, 0.19, 4 << 20, 14)
+    for kw in (dict(engine=1), dict(engine=3, cache_last_internal=1), dict(engine=2, tile_m=1 << 16)):
+        t = K.Tree(rows, cols, 1 << 18, 1 << 18, **kw)
+        ws = t.workspace_bytes()
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
+        t.upload()
+        torch.cuda.synchronize()
+        free1 = torch.cuda.mem_get_info()[0]
+        used = free0 - free1
+        # cudaMalloc rounds to 2 MiB pages
+        assert abs(used - ws) <= (2 << 20), (kw, used, ws)
+        t.close()
+        # an arena from torch of exactly the predicted size also works
+        t = K.Tree(rows, cols, 1 << 18, 1 << 18, **kw)
+        arena = torch.empty(t.workspace_bytes(), dtype=torch.uint8, device="cuda")
+        t.upload(arena)
+        x = torch.rand(1 << 18, 1, device="cuda")
+        y = torch.empty_like(x)
+        t.spmv(RIGHT, PLUS_TIMES, x, y)
+        torch.cuda.synchronize()
+
+
+def test_argument_errors():
+    import torch
+    rows, cols = synth.rmat(10, 0.57, 0.19, 0.19, 3000, 15)
+    t = _tree(rows, cols, 1024, 1024)
+    x = torch.rand(1024 * 33, device="cuda")
+    y = torch.empty(1024 * 33, device="cuda")
+    with pytest.raises(K.K2TError) as e:
+        t.spmv(RIGHT, PLUS_TIMES, x, y, B=33)
+    assert e.value.status == -2
+    lib = K.load()
+    import ctypes
+    assert lib.k2t_spmv(t.handle, 0, 0, ctypes.c_float(1.0), x.data_ptr() + 2, y.data_ptr(), 1, None) == -1
+    assert lib.k2t_spmv(t.handle, 0, 0, ctypes.c_float(1.0), x.data_ptr(), x.data_ptr(), 1, None) == -1
+    assert lib.k2t_spmv(t.handle, 3, 0, ctypes.c_float(1.0), x.data_ptr(), y.data_ptr(), 1, None) == -1
+    with pytest.raises(K.K2TError) as e:
+        t.upload()
+    assert e.value.status == -5

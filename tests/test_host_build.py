@@ -1,0 +1,160 @@
+"""Host side of the library (no GPU): construction, planning, workspace, ABI.
+
+The library's builder (path-key sort, bottom-up grouping) must produce the
+same level-order bitstrings as the oracle's recursive subdivision, bit for
+bit, for k = 2 and hybrid k = 4 / k = 2 trees, and decode to the edge set.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+k2 = pytest.importorskip("compressed_graph_spmv_gb300")
+from compressed_graph_spmv_gb300 import k2t as K  # noqa: E402
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _lib_bits(tree, level, n_k4):
+    sig = tree.level_signatures(level)
+    if level < n_k4:
+        s16 = sig.reshape(-1, 2).astype(np.uint16)
+        s16 = s16[:, 0] | (s16[:, 1] << 8)
+        return np.unpackbits(s16.view(np.uint8), bitorder="little")
+    return np.unpackbits(sig, bitorder="little").reshape(-1, 8)[:, :4].reshape(-1)
+
+
+def _compare(rows, cols, n_rows, n_cols, n_k4=0, **kw):
+    ot = oracle.OracleTree(rows, cols, n_rows, n_cols, n_k4=n_k4)
+    lt = K.Tree(rows, cols, n_rows, n_cols, n_k4_levels=n_k4, **kw)
+    s = lt.stats()
+    assert s.levels == ot.levels and s.dim_bits == ot.dim_bits
+    bits = ot.bits()
+    start = ot.level_start()
+    for d in range(ot.levels):
+        assert int(s.level_nodes[d]) == ot.level_nodes()[d]
+        assert np.array_equal(_lib_bits(lt, d, n_k4), bits[start[d]:start[d + 1]]), d
+    r, c = lt.decode()
+    dr, dc = oracle.dedup_edges(rows, cols)
+    assert sorted(zip(r.tolist(), c.tolist())) == sorted(zip(dr.tolist(), dc.tolist()))
+    assert s.nnz == dr.size
+    return lt
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_build_matches_oracle_random(seed):
+    rng = np.random.default_rng(seed)
+    n_rows = int(rng.integers(1, 300))
+    n_cols = int(rng.integers(1, 300))
+    n_k4 = int(rng.integers(0, 3))
+    rows, cols, _ = synth.random_small(seed, n_rows, n_cols, float(rng.choice([0.001, 0.01, 0.1])))
+    _compare(rows, cols, n_rows, n_cols, n_k4=n_k4)
+
+
+def test_build_matches_oracle_rmat_threads():
+    rows, cols = synth.rmat(14, 0.57, 0.19, 0.19, 100000, 3)
+    a = _compare(rows, cols, 1 << 14, 1 << 14, threads=1)
+    b = _compare(rows, cols, 1 << 14, 1 << 14, threads=7)
+    for d in range(a.stats().levels):
+        assert np.array_equal(a.level_signatures(d), b.level_signatures(d))
+
+
+def test_build_figure1_and_top_level():
+    import json
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "figure1.json")))
+    e = np.array(g["edges_decoded"], np.uint32)
+    t = _compare(e[:, 0], e[:, 1], 8, 8)
+    s = t.stats()
+    # the deepest level with at most 2^16 nodes is the last internal one (3.4)
+    assert s.d0 == 1
+
+
+def test_empty_and_degenerate():
+    z = np.zeros(0, np.uint32)
+    t = K.Tree(z, z, 5, 3)
+    s = t.stats()
+    assert s.nnz == 0 and s.level_nodes[0] == 1 and s.dim_bits == 3
+    assert t.level_signatures(0).tolist() == [0]
+    one = np.array([0], np.uint32)
+    _compare(one, one, 1, 1)
+    _compare(np.array([3], np.uint32), np.array([0], np.uint32), 4, 1)
+
+
+def test_errors():
+    r = np.array([0, 5], np.uint32)
+    c = np.array([0, 1], np.uint32)
+    with pytest.raises(K.K2TError) as e:
+        K.Tree(r, c, 5, 5)
+    assert e.value.status == -2  # ERANGE
+    with pytest.raises(K.K2TError) as e:
+        K.Tree(r, c, 0, 5)
+    assert e.value.status == -1
+    with pytest.raises(K.K2TError) as e:
+        K.Tree(r, c, 8, 8, engine=3, cache_last_internal=0)
+    assert e.value.status == -1
+    with pytest.raises(K.K2TError) as e:
+        K.Tree(r, c, 8, 8, max_batch=33)
+    assert e.value.status == -2
+    with pytest.raises(K.K2TError) as e:
+        K.Tree(r, c, 8, 8, chunk_cap=5000)
+    assert e.value.status == -1
+    t = K.Tree(r, c, 8, 8)
+    lib = K.load()
+    # products before upload are out of order; no GPU needed to see that
+    assert lib.k2t_spmv(t.handle, 0, 0, ctypes.c_float(1.0), 16, 32, 1, None) == -5
+    assert lib.k2t_spmv(None, 0, 0, ctypes.c_float(1.0), 16, 32, 1, None) == -1
+    assert lib.k2t_strerror(-3) == b"out of memory"
+
+
+def _layout_parts(s):
+    return (s.t_bytes_device + s.l_bytes_device + s.dir_bytes + s.top_bytes + s.cached_bytes +
+            s.plan_bytes + s.scratch_bytes + s.vector_bytes)
+
+
+@pytest.mark.parametrize("engine", [1, 2, 3])
+def test_workspace_accounting(engine):
+    rows, cols = synth.rmat(12, 0.57, 0.19, 0.19, 30000, 4)
+    t = K.Tree(rows, cols, 4096, 4096, engine=engine, cache_last_internal=int(engine == 3),
+               host_vectors=1, max_batch=4, tile_m=4096, chunk_cap=512, host_top_max_nodes=64)
+    s = t.stats()
+    ws = t.workspace_bytes()
+    assert ws == s.workspace_bytes
+    parts = _layout_parts(s)
+    # every part is placed at a 256-byte boundary: the total exceeds the sum of
+    # the parts by the alignment padding only (plus the 64-byte status word)
+    nparts = 4 * s.levels + 10
+    assert parts <= ws <= parts + 256 * nparts + 256
+    assert s.vector_bytes == 2 * 4096 * 4 * 4
+    if engine == 1:
+        assert s.n_chunks > 1 and s.plan_bytes > 0 and s.scratch_bytes == 0
+    if engine == 2:
+        assert s.n_steps > 1 and s.scratch_bytes > 0
+    if engine == 3:
+        assert s.cached_bytes == 8 * s.level_nodes[s.levels - 2]
+
+
+def test_chunk_plan_covers_every_node():
+    """Fused plan: chunks are whole subtrees; together they cover each level
+    below the host-expanded top exactly once, in level order."""
+    rows, cols = synth.rmat(13, 0.57, 0.19, 0.19, 60000, 6)
+    for cap in (1, 7, 256, 4096):
+        t = K.Tree(rows, cols, 8192, 8192, engine=1, chunk_cap=cap)
+        h = t.handle
+        s = t.stats()
+        # read the chunk table through the host copy in the planner's layout
+        stride = 2 + 2 * (s.levels - s.d0)
+        assert s.plan_bytes >= s.n_chunks * stride * 4
+
+
+def test_library_exports_every_declared_symbol():
+    header = open(os.path.join(ROOT, "include", "k2t.h")).read()
+    declared = set(re.findall(r"\b(k2t_[a-z_]+)\s*\(", header))
+    lib = K.load()
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert declared == set(K.EXPORTED)
