@@ -41,6 +41,9 @@ def make_workload(name: str):
     if name == "uniform-1024":
         wl = synth.uniform_c1()
         return wl, dict(), [(0, 1), (1, 1)]
+    if name == "uniform20":
+        wl = synth.uniform_large()
+        return wl, dict(), [(0, 1), (1, 1)]
     if name == "rmat20":
         wl = synth.rmat_c2()
         return wl, dict(), [(0, 1), (1, 1)]
@@ -296,6 +299,7 @@ def run_ours(args):
     opts = dict(wopts, host_vectors=1, max_batch=max_b)
     if args.engine is not None:
         opts["engine"] = args.engine
+        opts["cache_last_internal"] = int(args.engine == 3)
     t_build = time.perf_counter()
     tree = K.Tree(wl.rows, wl.cols, wl.n_rows, wl.n_cols, **opts)
     t_build = time.perf_counter() - t_build

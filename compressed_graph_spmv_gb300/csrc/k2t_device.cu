@@ -101,6 +101,9 @@ __global__ void __launch_bounds__(1024) ls_scan_kernel(const uint32_t *sums, uin
     __syncthreads();
     uint32_t run = wsum[warp] + incl - tot;
     for (uint32_t i = i0; i < i1; ++i) { prefix[i] = run; run += sums[i]; }
+    // prefix[nblocks] = the tile's total (every thread whose run ends there
+    // holds the same value)
+    if (i1 == nblocks) prefix[nblocks] = run;
 }
 
 void device_release(k2t_tree *t)
@@ -152,6 +155,8 @@ int enqueue_product(k2t_tree *t, int32_t dir, int32_t semiring, float w, const v
     va.B = B;
     va.w = w;
     va.mask = B >= 32 ? 0xffffffffu : ((1u << B) - 1u);
+    va.n_out = n_out;
+    va.n_in = dir == K2T_RIGHT ? t->n_cols : t->n_rows;
     pick(t->engine, semiring, dir, vw)(t, d, va, st);
     return K2T_OK;
 }

@@ -247,10 +247,10 @@ uint64_t level_offset(const k2t_tree *t, int d, uint64_t node)
 
 namespace {
 
-// level l-2 descendants of the level-d node range [a, b)
+// leaves (level l-1) under the level-d node range [a, b)
 uint64_t count_last(const k2t_tree *t, int d, uint64_t a, uint64_t b)
 {
-    for (int e = d; e < t->levels - 2; ++e) {
+    for (int e = d; e < t->levels - 1; ++e) {
         a = level_offset(t, e, a);
         b = level_offset(t, e, b);
     }
@@ -385,17 +385,17 @@ void compute_layout(k2t_tree *t)
             L.dir_off[d] = take(L.dir_bytes[d]);
         }
         if (ls) {
-            L.top_bytes = t->top.size() * sizeof(Coord);
+            L.top_bytes = t->top.size() * sizeof(Coord) + 16;  // slack: bulk copies round up to 16 bytes
             L.top_off = take(L.top_bytes);
         }
         if (cached) {
-            L.cached_bytes = t->cached.size() * sizeof(Coord);
+            L.cached_bytes = t->cached.size() * sizeof(Coord) + 16;
             L.cached_off = take(L.cached_bytes);
         }
         if (fused) {
             L.chunk_bytes = t->chunks.size() * sizeof(uint32_t);
             L.chunk_off = take(L.chunk_bytes);
-            L.root_bytes = t->roots.size() * sizeof(Coord);
+            L.root_bytes = t->roots.size() * sizeof(Coord) + 16;
             L.root_off = take(L.root_bytes);
         }
         if (ls) {
@@ -406,7 +406,7 @@ void compute_layout(k2t_tree *t)
                     uint64_t need = level_offset(t, s.level, (uint64_t)s.a + s.count) - s.dst_base;
                     maxbuf = std::max(maxbuf, need);
                 }
-            L.buf_bytes = maxbuf * sizeof(Coord);
+            L.buf_bytes = maxbuf * sizeof(Coord) + 16;
             for (int d = t->d0 + 1; d <= l - 2; ++d) L.buf_off[d] = take(L.buf_bytes);
             if (t->opts.offsets == K2T_OFFSETS_SCAN) {
                 uint64_t blocks = (t->max_tile_nodes + kDirS - 1) / kDirS + 1;
@@ -439,7 +439,7 @@ void k2t_default_opts(k2t_opts *o)
     o->engine = K2T_ENGINE_AUTO;
     o->offsets = K2T_OFFSETS_DIRECTORY;
     o->host_top_max_nodes = 1u << 16;
-    o->chunk_cap = 4096;
+    o->chunk_cap = 2048;
     o->tile_m = 1ull << 20;
     o->max_batch = 32;
     o->host_vectors = 0;
@@ -457,7 +457,7 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
     k2t_opts o;
     if (opts) o = *opts; else k2t_default_opts(&o);
     if (o.engine > K2T_ENGINE_CACHED || o.offsets > K2T_OFFSETS_SCAN) return K2T_EINVAL;
-    if (o.chunk_cap < 1 || o.chunk_cap > kMaxChunkCap || o.tile_m < 4) return K2T_EINVAL;
+    if (o.chunk_cap < 4 || o.chunk_cap > kMaxChunkCap || o.tile_m < 4) return K2T_EINVAL;
     if (o.max_batch < 1 || o.max_batch > K2T_MAX_BATCH) return K2T_ERANGE;
     if (o.host_top_max_nodes < 1) return K2T_EINVAL;
     if (o.n_k4_levels > 15) return K2T_EINVAL;

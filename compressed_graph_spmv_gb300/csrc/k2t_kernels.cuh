@@ -4,6 +4,8 @@
 #pragma once
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include <cstdint>
 #include <cstring>
 #include <new>
@@ -30,7 +32,9 @@ struct VecArgs {
     void *y;
     uint32_t B;
     float w;
-    uint32_t mask;  // Boolean: bits of the batch
+    uint32_t mask;   // Boolean: bits of the batch
+    uint64_t n_out;  // entries (vertices) of y
+    uint64_t n_in;   // entries (vertices) of x
 };
 
 __device__ __forceinline__ uint32_t nibble_at(const uint8_t *sig, uint32_t t)
@@ -90,6 +94,47 @@ template <> struct Fp32Sem<K2T_MIN_PLUS> {
     }
 };
 
+// Semiring updates of a shared-memory accumulator (one 32-bit word per entry).
+__device__ __forceinline__ void smem_min_total(float *p, float v)
+{
+    uint32_t u = __float_as_uint(v);
+    if (u & 0x80000000u) atomicMax(reinterpret_cast<unsigned int *>(p), u);
+    else atomicMin(reinterpret_cast<int *>(p), (int)u);
+}
+
+template <int SR>
+__device__ __forceinline__ void smem_update(uint32_t *w, uint32_t v)
+{
+    if constexpr (SR == K2T_PLUS_TIMES) atomicAdd(reinterpret_cast<float *>(w), __uint_as_float(v));
+    else if constexpr (SR == K2T_BOOLEAN) atomicOr(w, v);
+    else smem_min_total(reinterpret_cast<float *>(w), __uint_as_float(v));
+}
+
+// The same update applied once to y from a flushed accumulator word.
+template <int SR>
+__device__ __forceinline__ void global_update_word(uint32_t *y, uint32_t v)
+{
+    if constexpr (SR == K2T_PLUS_TIMES) atomicAdd(reinterpret_cast<float *>(y), __uint_as_float(v));
+    else if constexpr (SR == K2T_BOOLEAN) atomicOr(y, v);
+    else atomic_min_total(reinterpret_cast<float *>(y), __uint_as_float(v));
+}
+
+template <int SR>
+__device__ __forceinline__ uint32_t zero_word()
+{
+    return SR == K2T_MIN_PLUS ? 0x7f800000u : 0u;
+}
+
+// An accumulator word that leaves y unchanged: +-0 (plus-times: y never holds
+// -0), +inf (tropical), 0 (Boolean).
+template <int SR>
+__device__ __forceinline__ bool is_noop_word(uint32_t v)
+{
+    if constexpr (SR == K2T_PLUS_TIMES) return (v & 0x7fffffffu) == 0u;
+    else if constexpr (SR == K2T_BOOLEAN) return v == 0u;
+    else return v == 0x7f800000u;
+}
+
 template <int VW> struct VecLoad;
 template <> struct VecLoad<1> {
     static __device__ __forceinline__ void load(const float *p, float (&v)[1]) { v[0] = __ldg(p); }
@@ -109,66 +154,91 @@ template <> struct VecLoad<4> {
     }
 };
 
-// Cells of one leaf (a 2x2 block with origin (r, c), set cells in `lam`, bit
-// 2*dr + dc).  The (up to) two cells that share an output are combined with
-// the semiring's addition before the atomic, so a leaf issues at most two
-// atomics per vector slice.
+// Cells of U leaves at once.  Leaf u is the 2x2 block with origin (r[u], c[u])
+// and set cells lam[u] (bit 2*dr + dc).  The two cells that share an output
+// are combined with the semiring's addition first, so a leaf issues at most two
+// atomics per vector slice.  All gathers of x for the U leaves are issued
+// before any atomic, so their latencies overlap.
 //   right: output r gets bits 0 (input c) and 1 (input c+1); output r+1 bits 2, 3
 //   left:  output c gets bits 0 (input r) and 2 (input r+1); output c+1 bits 1, 3
-template <int SR, int DIR, int VW>
-__device__ __forceinline__ void leaf_cells(uint32_t lam, uint32_t r, uint32_t c, const VecArgs &a)
+// win != null: updates go to the shared-memory window win[(out - lo) * width + k]
+// instead of y (width = B words, 1 for Boolean).
+template <int SR, int DIR, int VW, int U>
+__device__ __forceinline__ void leaf_group(const uint32_t (&lam)[U], const uint32_t (&r)[U], const uint32_t (&c)[U],
+                                           const VecArgs &a, uint32_t *win, uint32_t lo)
 {
-    const uint32_t in = DIR == K2T_RIGHT ? c : r;
-    const uint32_t out = DIR == K2T_RIGHT ? r : c;
-    const bool a0 = lam & 1u;
-    const bool a1 = DIR == K2T_RIGHT ? (lam & 2u) : (lam & 4u);
-    const bool b0 = DIR == K2T_RIGHT ? (lam & 4u) : (lam & 2u);
-    const bool b1 = lam & 8u;
+    bool a0[U], a1[U], b0[U], b1[U];
+    uint32_t in[U], out[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        in[u] = DIR == K2T_RIGHT ? c[u] : r[u];
+        out[u] = DIR == K2T_RIGHT ? r[u] : c[u];
+        a0[u] = lam[u] & 1u;
+        a1[u] = DIR == K2T_RIGHT ? (lam[u] & 2u) : (lam[u] & 4u);
+        b0[u] = DIR == K2T_RIGHT ? (lam[u] & 4u) : (lam[u] & 2u);
+        b1[u] = lam[u] & 8u;
+    }
     if constexpr (SR == K2T_BOOLEAN) {
         const uint32_t *x = static_cast<const uint32_t *>(a.x);
         uint32_t *y = static_cast<uint32_t *>(a.y);
-        uint32_t x0 = (a0 || b0) ? __ldg(x + in) : 0u;
-        uint32_t x1 = (a1 || b1) ? __ldg(x + in + 1) : 0u;
-        uint32_t v0 = ((a0 ? x0 : 0u) | (a1 ? x1 : 0u)) & a.mask;
-        uint32_t v1 = ((b0 ? x0 : 0u) | (b1 ? x1 : 0u)) & a.mask;
-        if (v0) atomicOr(y + out, v0);
-        if (v1) atomicOr(y + out + 1, v1);
+        uint32_t x0[U], x1[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            x0[u] = (a0[u] || b0[u]) ? __ldg(x + in[u]) : 0u;
+            x1[u] = (a1[u] || b1[u]) ? __ldg(x + in[u] + 1) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            uint32_t v0 = ((a0[u] ? x0[u] : 0u) | (a1[u] ? x1[u] : 0u)) & a.mask;
+            uint32_t v1 = ((b0[u] ? x0[u] : 0u) | (b1[u] ? x1[u] : 0u)) & a.mask;
+            if (win) {
+                if (v0) atomicOr(win + (out[u] - lo), v0);
+                if (v1) atomicOr(win + (out[u] + 1 - lo), v1);
+            } else {
+                if (v0) atomicOr(y + out[u], v0);
+                if (v1) atomicOr(y + out[u] + 1, v1);
+            }
+        }
     } else {
         using S = Fp32Sem<SR>;
         const float *x = static_cast<const float *>(a.x);
         float *y = static_cast<float *>(a.y);
         const size_t B = a.B;
-        const bool need0 = a0 || b0, need1 = a1 || b1;
         for (uint32_t k = 0; k < a.B; k += VW) {
-            float x0[VW], x1[VW], v0[VW], v1[VW];
-            if (need0) VecLoad<VW>::load(x + (size_t)in * B + k, x0);
-            if (need1) VecLoad<VW>::load(x + (size_t)(in + 1) * B + k, x1);
+            float x0[U][VW], x1[U][VW];
 #pragma unroll
-            for (int q = 0; q < VW; ++q) {
-                float c0 = need0 ? S::contrib(x0[q], a.w) : S::zero();
-                float c1 = need1 ? S::contrib(x1[q], a.w) : S::zero();
-                v0[q] = a0 ? (a1 ? S::plus(c0, c1) : c0) : c1;
-                v1[q] = b0 ? (b1 ? S::plus(c0, c1) : c0) : c1;
+            for (int u = 0; u < U; ++u) {
+                if (a0[u] || b0[u]) VecLoad<VW>::load(x + (size_t)in[u] * B + k, x0[u]);
+                if (a1[u] || b1[u]) VecLoad<VW>::load(x + (size_t)(in[u] + 1) * B + k, x1[u]);
             }
-            if (a0 || a1) S::update(y + (size_t)out * B + k, v0);
-            if (b0 || b1) S::update(y + (size_t)(out + 1) * B + k, v1);
-        }
-    }
-}
-
-// A node of the last internal level (block side 4, coordinates rc) with
-// signature s: its f = popcount(s) leaves sit at positions off .. off+f-1 of
-// the leaf level (Algorithm 1, lines 13-18).
-template <int SR, int DIR, int VW>
-__device__ __forceinline__ void visit_node(Coord rc, uint32_t s, uint32_t off, const uint8_t *leaf, const VecArgs &a)
-{
-    uint32_t j = off;
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        if (s & (1u << b)) {
-            uint32_t lam = nibble_at(leaf, j);
-            ++j;
-            leaf_cells<SR, DIR, VW>(lam, 4u * rc.r + 2u * (uint32_t)(b >> 1), 4u * rc.c + 2u * (uint32_t)(b & 1), a);
+            for (int u = 0; u < U; ++u) {
+                float v0[VW], v1[VW];
+#pragma unroll
+                for (int q = 0; q < VW; ++q) {
+                    float c0 = (a0[u] || b0[u]) ? S::contrib(x0[u][q], a.w) : S::zero();
+                    float c1 = (a1[u] || b1[u]) ? S::contrib(x1[u][q], a.w) : S::zero();
+                    v0[q] = a0[u] ? (a1[u] ? S::plus(c0, c1) : c0) : c1;
+                    v1[q] = b0[u] ? (b1[u] ? S::plus(c0, c1) : c0) : c1;
+                }
+                if (win) {
+                    if (a0[u] || a1[u]) {
+                        uint32_t *w0 = win + (size_t)(out[u] - lo) * B + k;
+#pragma unroll
+                        for (int q = 0; q < VW; ++q)
+                            if (!S::skip(v0[q])) smem_update<SR>(w0 + q, __float_as_uint(v0[q]));
+                    }
+                    if (b0[u] || b1[u]) {
+                        uint32_t *w1 = win + (size_t)(out[u] + 1 - lo) * B + k;
+#pragma unroll
+                        for (int q = 0; q < VW; ++q)
+                            if (!S::skip(v1[q])) smem_update<SR>(w1 + q, __float_as_uint(v1[q]));
+                    }
+                } else {
+                    if (a0[u] || a1[u]) S::update(y + (size_t)out[u] * B + k, v0);
+                    if (b0[u] || b1[u]) S::update(y + (size_t)(out[u] + 1) * B + k, v1);
+                }
+            }
         }
     }
 }
@@ -280,114 +350,837 @@ __device__ __forceinline__ bool tile_block(const uint8_t *sig, const uint32_t *d
     return true;
 }
 
-// Algorithm 1, lines 12-20, for one tile of the last internal level.
-template <int SR, int DIR, int VW>
-__global__ void __launch_bounds__(kWalkThreads)
-ls_leaf_kernel(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix, uint32_t a, uint32_t count,
-               const Coord *src, uint32_t src_base, uint32_t leaf_base, const uint8_t *leaf, VecArgs va)
+// Flat leaf kernel: one thread per node of the last internal level, one warp
+// per 32 consecutive nodes, as in Algorithm 1, lines 12-20.  The warp's first
+// leaf comes from the directory sample of its 256-node block plus the fan-outs
+// before it in the block (or, in scan mode, from the tile's prefix sums); a
+// warp scan of the fan-outs places every node's leaves.  Each thread reads its
+// node's coordinates and leaf signatures, gathers all x entries its leaves
+// need, then applies the (at most 8) combined updates.
+//   nodes [a, a+count) of the level (level size n_level); src holds the
+//   coordinates of node a at index 0.
+constexpr int kFlatThreads = 256;
+
+// Single-slice fast path (B = 1 fp32, or any Boolean batch): the two input
+// entries of each child leaf block are adjacent, so both are loaded before the
+// leaf signatures are known (same sector, no extra traffic); the node then
+// costs two dependent memory round trips: (directory, signatures,
+// coordinates) and (leaf signatures, x).
+template <int SR, int DIR>
+__device__ __forceinline__ void node_leaves_spec(uint32_t sg, uint32_t off, Coord p, const uint8_t *leaf,
+                                                 const VecArgs &va)
 {
-    const uint32_t wid = blockIdx.x * (kWalkThreads / 32) + (threadIdx.x >> 5);
-    uint32_t s, e, base;
-    if (!tile_block(sig, dir, prefix, a, count, leaf_base, wid, s, e, base)) return;
-    warp_walk(sig, s, e, base, [&](uint32_t t, uint32_t sg, uint32_t pos) {
-        visit_node<SR, DIR, VW>(src[t - src_base], sg, pos, leaf, va);
-    });
+    uint32_t lam[4], xin[4], xo[4][2];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const uint32_t r = 4u * p.r + 2u * (uint32_t)(b >> 1);
+        const uint32_t c = 4u * p.c + 2u * (uint32_t)(b & 1);
+        xin[b] = DIR == K2T_RIGHT ? c : r;
+        lam[b] = 0u;
+        xo[b][0] = 0u;
+        xo[b][1] = 0u;
+        if (sg & (1u << b)) {
+            lam[b] = nibble_at(leaf, off + (uint32_t)__popc(sg & ((1u << b) - 1u)));
+            const uint32_t *x = static_cast<const uint32_t *>(va.x);
+            xo[b][0] = __ldg(x + xin[b]);
+            if (xin[b] + 1u < va.n_in) xo[b][1] = __ldg(x + xin[b] + 1u);
+        }
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const uint32_t l = lam[b];
+        if (!l) continue;
+        const uint32_t out = DIR == K2T_RIGHT ? 4u * p.r + 2u * (uint32_t)(b >> 1) : 4u * p.c + 2u * (uint32_t)(b & 1);
+        const bool a0 = l & 1u;
+        const bool a1 = DIR == K2T_RIGHT ? (l & 2u) : (l & 4u);
+        const bool b0 = DIR == K2T_RIGHT ? (l & 4u) : (l & 2u);
+        const bool b1 = l & 8u;
+        if constexpr (SR == K2T_BOOLEAN) {
+            uint32_t *y = static_cast<uint32_t *>(va.y);
+            const uint32_t v0 = ((a0 ? xo[b][0] : 0u) | (a1 ? xo[b][1] : 0u)) & va.mask;
+            const uint32_t v1 = ((b0 ? xo[b][0] : 0u) | (b1 ? xo[b][1] : 0u)) & va.mask;
+            if (v0) atomicOr(y + out, v0);
+            if (v1) atomicOr(y + out + 1, v1);
+        } else {
+            using S = Fp32Sem<SR>;
+            float *y = static_cast<float *>(va.y);
+            const float c0 = S::contrib(__uint_as_float(xo[b][0]), va.w);
+            const float c1 = S::contrib(__uint_as_float(xo[b][1]), va.w);
+            if (a0 || a1) {
+                const float v[1] = {a0 ? (a1 ? S::plus(c0, c1) : c0) : c1};
+                if (!S::skip(v[0])) S::update(y + out, v);
+            }
+            if (b0 || b1) {
+                const float v[1] = {b0 ? (b1 ? S::plus(c0, c1) : c0) : c1};
+                if (!S::skip(v[0])) S::update(y + out + 1, v);
+            }
+        }
+    }
 }
 
-// k^2+F (section 3.5): every node of the last internal level takes its
-// coordinates from the cache and its first leaf from the directory.
 template <int SR, int DIR, int VW>
-__global__ void __launch_bounds__(kWalkThreads)
-cached_leaf_kernel(const uint8_t *sig, const uint32_t *dir, uint32_t n, const Coord *coords,
-                   const uint8_t *leaf, VecArgs va)
+__global__ void __launch_bounds__(kFlatThreads)
+flat_leaf_kernel(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix, uint32_t leaf_base, uint32_t a,
+                 uint32_t count, const Coord *src, const uint8_t *leaf, VecArgs va)
 {
-    const uint32_t g = blockIdx.x * (kWalkThreads / 32) + (threadIdx.x >> 5);
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t rel0 = blockIdx.x * kFlatThreads + (threadIdx.x & ~31u);  // warp's first node, tile-relative
+    if (rel0 >= count) return;
+    const uint32_t t0 = a + rel0;
+    const uint32_t t = t0 + lane;
+    const bool valid = rel0 + lane < count;
+    // round 1: all independent loads
+    const uint32_t sg = valid ? nibble_at(sig, t) : 0u;
+    Coord p{0u, 0u};
+    if (valid) p = src[rel0 + lane];
+    uint32_t base;
+    if (dir) {
+        const uint32_t g = t0 / kDirS;
+        base = __ldg(dir + g) + (t0 > g * kDirS ? warp_popc_range(sig, g * kDirS, t0) : 0u);
+    } else {
+        const uint32_t j = rel0 / 256u;
+        const uint32_t bs = a + 256u * j;
+        base = leaf_base + __ldg(prefix + j) + (t0 > bs ? warp_popc_range(sig, bs, t0) : 0u);
+    }
+    const uint32_t f = (uint32_t)__popc(sg);
+    const uint32_t off = base + warp_incl_scan(f) - f;
+    if (!sg) return;
+    if (SR == K2T_BOOLEAN || (VW == 1 && va.B == 1)) {
+        node_leaves_spec<SR, DIR>(sg, off, p, leaf, va);
+        return;
+    }
+    uint32_t lam[4], r[4], c[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        lam[b] = 0u;
+        r[b] = 4u * p.r + 2u * (uint32_t)(b >> 1);
+        c[b] = 4u * p.c + 2u * (uint32_t)(b & 1);
+        if (sg & (1u << b)) lam[b] = nibble_at(leaf, off + (uint32_t)__popc(sg & ((1u << b) - 1u)));
+    }
+    leaf_group<SR, DIR, VW, 4>(lam, r, c, va, nullptr, 0u);
+}
+
+// Leaves of U leaf blocks (origins r[u], c[u], cells lam[u]) with x entries
+// already loaded (xo[u][0]: input r or c, xo[u][1]: the next one); one
+// vector slice (B = 1 fp32, or a Boolean word).
+template <int SR, int DIR, int U>
+__device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint32_t (&out)[U],
+                                            const uint32_t (&xo)[U][2], const VecArgs &va, uint32_t *win = nullptr,
+                                            uint32_t lo = 0u)
+{
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const uint32_t l = lam[u];
+        if (!l) continue;
+        const bool a0 = l & 1u;
+        const bool a1 = DIR == K2T_RIGHT ? (l & 2u) : (l & 4u);
+        const bool b0 = DIR == K2T_RIGHT ? (l & 4u) : (l & 2u);
+        const bool b1 = l & 8u;
+        if constexpr (SR == K2T_BOOLEAN) {
+            uint32_t *y = static_cast<uint32_t *>(va.y);
+            const uint32_t v0 = ((a0 ? xo[u][0] : 0u) | (a1 ? xo[u][1] : 0u)) & va.mask;
+            const uint32_t v1 = ((b0 ? xo[u][0] : 0u) | (b1 ? xo[u][1] : 0u)) & va.mask;
+            if (win) {
+                if (v0) atomicOr(win + (out[u] - lo), v0);
+                if (v1) atomicOr(win + (out[u] + 1 - lo), v1);
+            } else {
+                if (v0) atomicOr(y + out[u], v0);
+                if (v1) atomicOr(y + out[u] + 1, v1);
+            }
+        } else {
+            using S = Fp32Sem<SR>;
+            float *y = static_cast<float *>(va.y);
+            const float c0 = S::contrib(__uint_as_float(xo[u][0]), va.w);
+            const float c1 = S::contrib(__uint_as_float(xo[u][1]), va.w);
+            if (a0 || a1) {
+                const float v[1] = {a0 ? (a1 ? S::plus(c0, c1) : c0) : c1};
+                if (!S::skip(v[0])) {
+                    if (win) smem_update<SR>(win + (out[u] - lo), __float_as_uint(v[0]));
+                    else S::update(y + out[u], v);
+                }
+            }
+            if (b0 || b1) {
+                const float v[1] = {b0 ? (b1 ? S::plus(c0, c1) : c0) : c1};
+                if (!S::skip(v[0])) {
+                    if (win) smem_update<SR>(win + (out[u] + 1 - lo), __float_as_uint(v[0]));
+                    else S::update(y + out[u] + 1, v);
+                }
+            }
+        }
+    }
+}
+
+// k^2+F engine (section 3.5): one warp per 256-node directory block of the
+// last internal level.  The warp reads the block's 128 bytes of signatures
+// (one word of 8 nibbles per lane), its directory sample and the cached
+// coordinates; a warp scan of the fan-outs turns the block into a list of its
+// leaves (node, quadrant) in shared memory.  The lanes then take the leaves
+// round-robin, U per round: leaf signature and the x entries of its two
+// inputs are loaded together, then the combined updates are applied.  Every
+// lane does the same work per leaf, whatever the fan-out of its node.
+constexpr int kCachedWarps = 8;
+constexpr int kCachedU = 2;
+constexpr uint32_t kCachedWindow = 256;  // words of a warp's output window
+
+template <int SR, int DIR, int VW>
+__global__ void __launch_bounds__(32 * kCachedWarps)
+cached_block_kernel(const uint8_t *sig, const uint32_t *dir, uint32_t n, const Coord *coords, const uint8_t *leaf,
+                    VecArgs va)
+{
+    __shared__ Coord cs[kCachedWarps][kDirS];
+    __shared__ uint16_t slots[kCachedWarps][4 * kDirS];
+    __shared__ uint32_t wins[kCachedWarps][kCachedWindow];
+    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+    const uint32_t g = blockIdx.x * kCachedWarps + warp;
     const uint32_t s = g * kDirS;
     if (s >= n) return;
-    const uint32_t e = min(s + kDirS, n);
-    warp_walk(sig, s, e, __ldg(dir + g), [&](uint32_t t, uint32_t sg, uint32_t pos) {
-        visit_node<SR, DIR, VW>(coords[t], sg, pos, leaf, va);
-    });
+    const uint32_t cnt = min(n - s, kDirS);
+    Coord *cw = cs[warp];
+    uint16_t *sl = slots[warp];
+    // round 1: signatures, directory sample, coordinates
+    uint32_t w = 0;
+    if (8u * lane < cnt) {
+        w = __ldg(reinterpret_cast<const uint32_t *>(sig + s / 2) + lane);
+        if (8u * lane + 8u > cnt) w &= (1u << (4u * (cnt - 8u * lane))) - 1u;
+    }
+    const uint32_t base = __ldg(dir + g);
+    uint32_t mn = 0xffffffffu, mx = 0u;
+#pragma unroll
+    for (uint32_t q = 0; q < kDirS / 32; ++q) {
+        const uint32_t i = 32u * q + lane;
+        if (i < cnt) {
+            const Coord p = coords[s + i];
+            cw[i] = p;
+            const uint32_t o = DIR == K2T_RIGHT ? p.r : p.c;
+            mn = min(mn, o);
+            mx = max(mx, o);
+        }
+    }
+    const uint32_t f = (uint32_t)__popc(w);
+    const uint32_t incl = warp_incl_scan(f);
+    const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+    uint32_t pos = incl - f;
+    uint32_t rest = w;
+    while (rest) {
+        const uint32_t bit = (uint32_t)(__ffs(rest) - 1);  // 4*k + b
+        rest &= rest - 1u;
+        sl[pos++] = (uint16_t)(((8u * lane + bit / 4u) << 2) | (bit & 3u));
+    }
+    // Segmented scatter: the block's outputs lie in 4*[mn, mx] .. 4*mx+3 (a
+    // node of this level covers 4 rows and 4 columns).  When they fit the
+    // warp's window, updates are reduced there first and each touched entry
+    // reaches y once; hub rows of power-law graphs then cost one global
+    // atomic per block instead of one per non-zero.
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    const uint32_t width = SR == K2T_BOOLEAN ? 1u : va.B;
+    const uint64_t span64 = 4ull * ((uint64_t)mx - mn + 1u);
+    const bool windowed = span64 * width <= kCachedWindow;
+    const uint32_t span = windowed ? (uint32_t)span64 : 0u;
+    uint32_t *win = windowed ? wins[warp] : nullptr;
+    const uint32_t lo = 4u * mn;
+    if (windowed)
+        for (uint32_t i = lane; i < span * width; i += 32u) win[i] = zero_word<SR>();
+    __syncwarp();
+    // round 2: leaves, U per lane per round
+    for (uint32_t j0 = 0; j0 < total; j0 += 32u * kCachedU) {
+        uint32_t lam[kCachedU], r[kCachedU], c[kCachedU];
+#pragma unroll
+        for (int u = 0; u < kCachedU; ++u) {
+            const uint32_t j = j0 + 32u * u + lane;
+            lam[u] = 0u;
+            r[u] = 0u;
+            c[u] = 0u;
+            if (j < total) {
+                const uint32_t e = sl[j];
+                const Coord p = cw[e >> 2];
+                const uint32_t b = e & 3u;
+                r[u] = 4u * p.r + 2u * (b >> 1);
+                c[u] = 4u * p.c + 2u * (b & 1u);
+                lam[u] = nibble_at(leaf, base + j);
+            }
+        }
+        if (SR == K2T_BOOLEAN || (VW == 1 && va.B == 1)) {
+            uint32_t xo[kCachedU][2], out[kCachedU];
+            const uint32_t *x = static_cast<const uint32_t *>(va.x);
+#pragma unroll
+            for (int u = 0; u < kCachedU; ++u) {
+                const uint32_t in = DIR == K2T_RIGHT ? c[u] : r[u];
+                out[u] = DIR == K2T_RIGHT ? r[u] : c[u];
+                xo[u][0] = 0u;
+                xo[u][1] = 0u;
+                if (j0 + 32u * u + lane < total) {
+                    xo[u][0] = __ldg(x + in);
+                    if (in + 1u < va.n_in) xo[u][1] = __ldg(x + in + 1u);
+                }
+            }
+            leaf_apply1<SR, DIR, kCachedU>(lam, out, xo, va, win, lo);
+        } else {
+            leaf_group<SR, DIR, VW, kCachedU>(lam, r, c, va, win, lo);
+        }
+    }
+    if (windowed) {
+        __syncwarp();
+        uint32_t *y = static_cast<uint32_t *>(va.y) + (size_t)lo * width;
+        const uint64_t limit = (va.n_out - lo) * width;
+        for (uint32_t i = lane; i < span * width; i += 32u) {
+            const uint32_t v = win[i];
+            if (!is_noop_word<SR>(v) && i < limit) global_update_word<SR>(y + i, v);
+        }
+    }
 }
 
-// Exclusive block-wide prefix sum over kFusedThreads threads.
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *wsum)
+// ---- shared-memory staging with the bulk-copy (TMA) engine ------------------
+// One thread arms an mbarrier with the total byte count and issues one
+// cp.async.bulk per contiguous range; every thread then waits on the barrier.
+// Each wait polls at most kWaitLimit times; a stage that does not complete
+// sets bit 0 of the device status word and the block leaves without touching
+// its outputs (after one more bounded wait for its copies).
+constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr uint32_t kStatusStageTimeout = 1u;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar)
 {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bar)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+// dst (shared) and src (global) 16-byte aligned, bytes a multiple of 16
+__device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t phase)
+{
+    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(phase)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+
+// A staged copy of global bytes [lo, hi) of `base`, widened to 16-byte
+// boundaries; returns the offset of byte lo inside the copy.
+struct StagePlan {
+    uint64_t lo16;
+    uint32_t bytes;
+    uint32_t shift;
+};
+
+__device__ __forceinline__ StagePlan stage_plan(uint64_t lo, uint64_t hi)
+{
+    StagePlan p;
+    p.lo16 = lo & ~(uint64_t)15;
+    uint64_t hi16 = (hi + 15) & ~(uint64_t)15;
+    p.bytes = (uint32_t)(hi16 - p.lo16);
+    p.shift = (uint32_t)(lo - p.lo16);
+    return p;
+}
+
+// nibble k of a staged signature copy
+__device__ __forceinline__ uint32_t snib(const uint8_t *sg, uint32_t k)
+{
+    return (uint32_t)(sg[k >> 1] >> ((k & 1u) * 4u)) & 15u;
+}
+
+// First child of `node` of a level from its directory: the sample of its
+// 256-node block plus the fan-outs before it in the block (section 3.2).
+// `n` is the level's node count; node == n gives the level's total.
+__device__ __forceinline__ uint32_t dir_offset(const uint8_t *sig, const uint32_t *dir, uint32_t n, uint32_t node)
+{
+    if (node >= n) return __ldg(dir + (n + kDirS - 1) / kDirS);
+    const uint32_t g = node / kDirS;
+    uint32_t base = __ldg(dir + g);
+    const uint64_t *w = reinterpret_cast<const uint64_t *>(sig);
+    const uint32_t w0 = g * (kDirS / 16), w1 = node / 16;
+    for (uint32_t k = w0; k < w1; ++k) base += (uint32_t)__popcll(__ldg(w + k));
+    const uint32_t rem = node & 15u;
+    if (rem) base += (uint32_t)__popcll(__ldg(w + w1) & ((1ull << (4 * rem)) - 1ull));
+    return base;
+}
+
+// Exclusive block-wide prefix sum over NT threads; *total gets the sum.
+template <int NT>
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *wsum, uint32_t *total)
+{
+    constexpr int NW = NT / 32;
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
     const uint32_t incl = warp_incl_scan(v);
     if (lane == 31) wsum[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        uint32_t t = lane < (uint32_t)kFusedWarps ? wsum[lane] : 0u;
+        uint32_t t = lane < (uint32_t)NW ? wsum[lane] : 0u;
         uint32_t ti = warp_incl_scan(t);
-        if (lane < (uint32_t)kFusedWarps) wsum[lane] = ti - t;
+        if (lane < (uint32_t)NW) wsum[lane] = ti - t;
+        if (lane == 31) wsum[NW] = ti;
     }
     __syncthreads();
     const uint32_t r = wsum[warp] + incl - v;
+    *total = wsum[NW];
     __syncthreads();
     return r;
 }
 
+// ---- warp-sliced level expansion ------------------------------------------------
+// Nibbles [s, e) of a staged signature copy viewed as 32-bit words (8 nodes
+// per word): lane l reads word w0 + l + 32k with the nibbles outside [s, e)
+// masked off.
+__device__ __forceinline__ uint32_t word_mask(uint32_t W, uint32_t s, uint32_t e)
+{
+    const uint32_t lo = W * 8u, hi = lo + 8u;
+    if (lo >= s && hi <= e) return 0xffffffffu;
+    uint32_t m = 0;
+#pragma unroll
+    for (uint32_t k = 0; k < 8; ++k)
+        if (lo + k >= s && lo + k < e) m |= 15u << (4 * k);
+    return m;
+}
+
+// Set bits (= children) of nibbles [s, e), summed over the warp.
+__device__ __forceinline__ uint32_t warp_popc_nibbles(const uint32_t *words, uint32_t s, uint32_t e)
+{
+    const uint32_t lane = threadIdx.x & 31u;
+    uint32_t v = 0;
+    if (s < e)
+        for (uint32_t W = s / 8u + lane; W < (e + 7u) / 8u; W += 32u) v += (uint32_t)__popc(words[W] & word_mask(W, s, e));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// One warp expands the parents at nibbles [s, e) of the staged level (parent
+// i of the chunk at nibble nb + i, coordinates cur[i]); their children go to
+// nxt[start ...] in level order.  Also folds the children's row (right) or
+// column (left) into [mn, mx].
+template <int DIR>
+__device__ __forceinline__ void emit_children(uint32_t sg, Coord p, Coord *nxt, uint32_t pos, uint32_t &mn,
+                                              uint32_t &mx)
+{
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+        if (sg & (1u << b)) {
+            const Coord q = child_of(p, b);
+            const uint32_t o = DIR == K2T_RIGHT ? q.r : q.c;
+            mn = min(mn, o);
+            mx = max(mx, o);
+            nxt[pos++] = q;
+        }
+}
+
+template <int DIR>
+__device__ __forceinline__ void warp_expand(const uint32_t *words, uint32_t nb, uint32_t s, uint32_t e,
+                                            const Coord *cur, Coord *nxt, uint32_t start, uint32_t &mn,
+                                            uint32_t &mx)
+{
+    const uint32_t lane = threadIdx.x & 31u;
+    if (s >= e) return;
+    if (e - s < 256u) {
+        // short slice: one parent per lane per round
+        const uint8_t *bytes = reinterpret_cast<const uint8_t *>(words);
+        for (uint32_t i0 = s; i0 < e; i0 += 32u) {
+            const uint32_t i = i0 + lane;
+            const uint32_t sg = i < e ? snib(bytes, i) : 0u;
+            const uint32_t f = (uint32_t)__popc(sg);
+            const uint32_t incl = warp_incl_scan(f);
+            const uint32_t pos = start + incl - f;
+            start += __shfl_sync(0xffffffffu, incl, 31);
+            if (sg) emit_children<DIR>(sg, cur[i - nb], nxt, pos, mn, mx);
+        }
+        return;
+    }
+    // long slice: eight parents (one 32-bit word of nibbles) per lane per round
+    const uint32_t w1 = (e + 7u) / 8u;
+    for (uint32_t W0 = s / 8u; W0 < w1; W0 += 32u) {
+        const uint32_t W = W0 + lane;
+        const uint32_t word = W < w1 ? (words[W] & word_mask(W, s, e)) : 0u;
+        const uint32_t f = (uint32_t)__popc(word);
+        const uint32_t incl = warp_incl_scan(f);
+        uint32_t pos = start + incl - f;
+        start += __shfl_sync(0xffffffffu, incl, 31);
+        uint32_t rest = word;
+        while (rest) {
+            const uint32_t k = (uint32_t)(__ffs(rest) - 1) / 4u;
+            const uint32_t sg = (word >> (4u * k)) & 15u;
+            rest &= ~(15u << (4u * k));
+            emit_children<DIR>(sg, cur[8u * W + k - nb], nxt, pos, mn, mx);
+            pos += (uint32_t)__popc(sg);
+        }
+    }
+}
+
+// Algorithm 1, lines 5-10, inside one thread block: the n parents in `cur`,
+// whose signatures are nibbles nb .. nb+n-1 of the staged copy sg, write the
+// coordinates of their children, in level order, to `nxt`.  Each thread
+// takes a contiguous run of parents; the block scans the run fan-outs.
+template <int NT>
+__device__ __forceinline__ uint32_t block_expand(const uint8_t *sg, uint32_t nb, uint32_t n, const Coord *cur,
+                                                 Coord *nxt, uint32_t *wsum)
+{
+    const uint32_t per = (n + NT - 1) / NT;
+    const uint32_t i0 = min(threadIdx.x * per, n), i1 = min(i0 + per, n);
+    uint32_t tot = 0;
+    for (uint32_t i = i0; i < i1; ++i) tot += (uint32_t)__popc(snib(sg, nb + i));
+    uint32_t total;
+    uint32_t pos = block_excl_scan<NT>(tot, wsum, &total);
+    for (uint32_t i = i0; i < i1; ++i) {
+        const uint32_t s = snib(sg, nb + i);
+        const Coord p = cur[i];
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+            if (s & (1u << b)) nxt[pos++] = child_of(p, b);
+    }
+    __syncthreads();
+    return total;
+}
+
+// Algorithm 1, lines 14-17, for nl leaves whose coordinates (in units of the
+// 2x2 leaf block) are lc[0..nl) and signatures nibbles nb.. of sg.  Leaves
+// are dealt round-robin to the threads, U at a time.
+//
+// Segmented scatter: when the outputs the block touches span at most
+// win_words words, the block first reduces its updates in the shared window
+// `win` (shared-memory atomics) and then applies each touched entry to y once.
+// Hub rows of power-law graphs then cost one global atomic per block instead
+// of one per non-zero.  Otherwise updates go straight to y.
+template <int SR, int DIR, int VW, int NT, bool NAMED = false>
+__device__ __forceinline__ void block_leaves(const uint8_t *sg, uint32_t nb, uint32_t nl, const Coord *lc,
+                                             const VecArgs &va, uint32_t *win, uint32_t win_words, uint32_t *red,
+                                             bool have_extent = false, uint32_t mn_in = 0xffffffffu,
+                                             uint32_t mx_in = 0u)
+{
+    constexpr int U = 4;
+    const uint32_t width = SR == K2T_BOOLEAN ? 1u : va.B;
+    // extent of the outputs: min and max leaf row (right) or column (left);
+    // callers that built the leaf coordinates pass their own partial extent
+    uint32_t mn = mn_in, mx = mx_in;
+    if (!have_extent)
+        for (uint32_t j = threadIdx.x; j < nl; j += NT) {
+            const Coord q = lc[j];
+            const uint32_t o = DIR == K2T_RIGHT ? q.r : q.c;
+            mn = min(mn, o);
+            mx = max(mx, o);
+        }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if ((threadIdx.x & 31u) == 0) {
+        red[2 * (threadIdx.x >> 5)] = mn;
+        red[2 * (threadIdx.x >> 5) + 1] = mx;
+    }
+    if constexpr (NAMED) asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); else __syncthreads();
+    mn = 0xffffffffu;
+    mx = 0u;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) {
+        mn = min(mn, red[2 * w]);
+        mx = max(mx, red[2 * w + 1]);
+    }
+    if constexpr (NAMED) asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); else __syncthreads();
+    const uint32_t lo = 2u * mn;
+    const uint64_t span = nl ? 2ull * ((uint64_t)mx - mn) + 2ull : 0ull;
+    const bool windowed = win && nl && span * width <= win_words;
+    const uint32_t words = windowed ? (uint32_t)(span * width) : 0u;
+    if (windowed) {
+        for (uint32_t i = threadIdx.x; i < words; i += NT) win[i] = zero_word<SR>();
+        if constexpr (NAMED) asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); else __syncthreads();
+    }
+    uint32_t *w = windowed ? win : nullptr;
+    for (uint32_t j0 = threadIdx.x; j0 < nl; j0 += NT * U) {
+        uint32_t lam[U], r[U], c[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t j = j0 + (uint32_t)u * NT;
+            const bool ok = j < nl;
+            lam[u] = ok ? snib(sg, nb + j) : 0u;
+            const Coord q = ok ? lc[j] : Coord{0u, 0u};
+            r[u] = 2u * q.r;
+            c[u] = 2u * q.c;
+        }
+        leaf_group<SR, DIR, VW, U>(lam, r, c, va, w, lo);
+    }
+    if (windowed) {
+        if constexpr (NAMED) asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); else __syncthreads();
+        uint32_t *y = static_cast<uint32_t *>(va.y) + (size_t)lo * width;
+        const uint64_t limit = ((uint64_t)va.n_out - lo) * width;  // entries of y past lo
+        for (uint32_t i = threadIdx.x; i < words; i += NT) {
+            const uint32_t v = win[i];
+            if (!is_noop_word<SR>(v) && i < limit) global_update_word<SR>(y + i, v);
+        }
+    }
+}
+
+// One level of a thread block's expansion with warp slices: warp w takes the
+// parents [n*w/NW, n*(w+1)/NW) of the level (nibbles nb.. of the staged copy),
+// publishes its fan-out total in wt[w], and after one block barrier writes its
+// children from the sum of the totals of the warps before it.  The caller
+// synchronises before reading nxt.
+template <int NT, int DIR>
+__device__ __forceinline__ void sliced_expand(const uint32_t *words, uint32_t nb, uint32_t n, const Coord *cur,
+                                              Coord *nxt, uint32_t *wt, uint32_t &mn, uint32_t &mx)
+{
+    constexpr uint32_t NW = NT / 32;
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+    const uint32_t a = nb + (uint32_t)(((uint64_t)n * warp) / NW);
+    const uint32_t b = nb + (uint32_t)(((uint64_t)n * (warp + 1)) / NW);
+    const uint32_t tot = warp_popc_nibbles(words, a, b);
+    if (lane == 0) wt[warp] = tot;
+    __syncthreads();
+    uint32_t start = 0;
+    for (uint32_t v = 0; v < warp; ++v) start += wt[v];
+    warp_expand<DIR>(words, nb, a, b, cur, nxt, start, mn, mx);
+}
+
+// sliced_expand for the consumer threads of a warp-specialised block (named
+// barrier instead of __syncthreads).
+template <int NT, int DIR>
+__device__ __forceinline__ void consumer_expand(const uint32_t *words, uint32_t nb, uint32_t n, const Coord *cur,
+                                                Coord *nxt, uint32_t *wt, uint32_t &mn, uint32_t &mx)
+{
+    constexpr uint32_t NW = NT / 32;
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+    const uint32_t a = nb + (uint32_t)(((uint64_t)n * warp) / NW);
+    const uint32_t b = nb + (uint32_t)(((uint64_t)n * (warp + 1)) / NW);
+    const uint32_t tot = warp_popc_nibbles(words, a, b);
+    if (lane == 0) wt[warp] = tot;
+    asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+    uint32_t start = 0;
+    for (uint32_t v = 0; v < warp; ++v) start += wt[v];
+    warp_expand<DIR>(words, nb, a, b, cur, nxt, start, mn, mx);
+}
+
+constexpr int kGroupThreads = 256;
+constexpr uint32_t kGroupNodes = 512;                 // last-internal nodes per group
+constexpr uint32_t kGroupLeaves = 4 * kGroupNodes;    // at most 4 leaves per node
+constexpr uint32_t kGroupWindow = 4096;               // words of the output window
+constexpr uint32_t kGroupCStage = kGroupNodes * 8 + 16;
+constexpr uint32_t kGroupSStage = kGroupNodes / 2 + 48;
+constexpr uint32_t kGroupLStage = kGroupLeaves / 2 + 48;
+constexpr uint32_t kGroupBuf = kGroupCStage + kGroupSStage + kGroupLStage;  // one staging buffer
+
+// Bytes of dynamic shared memory of leafgroup_kernel.
+constexpr uint32_t leafgroup_smem()
+{
+    return 2 * kGroupBuf + kGroupLeaves * 8 + kGroupWindow * 4;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Barrier among the first NT threads of the block only (named barrier 1).
+template <int NT>
+__device__ __forceinline__ void consumers_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+}
+
+// The last internal level in groups of kGroupNodes nodes, by a persistent,
+// warp-specialised grid.  Warp kGroupThreads/32 is the producer: for the
+// block's groups g, g + gridDim.x, ... it computes the leaf range from the
+// directory (or the tile's scan), and stages coordinates, signatures and
+// leaf signatures into one of two buffers with the bulk-copy engine (full
+// barrier), as soon as the consumers have released that buffer (empty
+// barrier).  The kGroupThreads consumer threads expand the leaf coordinates
+// in shared memory and apply the leaves.  Used by the k^2+F engine
+// (coordinates from the cache, section 3.5) and by the leaf tiles of the
+// level-synchronous engine (coordinates from a frontier buffer).
+//   nodes [a, a+count) of the level (level size n_level); src holds the
+//   coordinates of node a at index 0; first-child offsets from the directory
+//   (dir != null) or, in scan mode, leaf_base + prefix[(s - a) / 256].
+constexpr int kGroupBlock = kGroupThreads + 32;
+
+template <int SR, int DIR, int VW>
+__global__ void __launch_bounds__(kGroupBlock)
+leafgroup_kernel(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix, uint32_t leaf_base, uint32_t a,
+                 uint32_t count, uint32_t n_level, const Coord *src, const uint8_t *leaf, VecArgs va,
+                 uint32_t *status)
+{
+    extern __shared__ __align__(16) uint8_t gsm[];
+    uint8_t *buf0 = gsm;
+    Coord *leafc = reinterpret_cast<Coord *>(gsm + 2 * kGroupBuf);
+    uint32_t *win = reinterpret_cast<uint32_t *>(leafc + kGroupLeaves);
+    __shared__ __align__(8) uint64_t full[2], empty[2];
+    __shared__ uint32_t meta[2][4];  // coordinate shift, signature nibble base, leaf nibble base, leaf count
+    __shared__ uint32_t wt[kGroupThreads / 32];
+    __shared__ uint32_t red[2 * (kGroupThreads / 32)];
+    __shared__ uint32_t abort_flag;
+
+    const uint32_t ngroups = (count + kGroupNodes - 1) / kGroupNodes;
+    if (threadIdx.x == 0) {
+        mbar_init(&full[0]);
+        mbar_init(&full[1]);
+        mbar_init(&empty[0]);
+        mbar_init(&empty[1]);
+        abort_flag = 0;
+    }
+    __syncthreads();
+
+    if (threadIdx.x >= kGroupThreads) {
+        // ---- producer warp (one thread issues) ----
+        if (threadIdx.x != kGroupThreads) return;
+        const uint8_t *src16 = reinterpret_cast<const uint8_t *>((uintptr_t)src & ~(uintptr_t)15);
+        const uint64_t cs = (uintptr_t)src & 15u;
+        uint32_t it = 0;
+        for (uint32_t g = blockIdx.x; g < ngroups; g += gridDim.x, ++it) {
+            const int k = (int)(it & 1u);
+            const uint32_t s = a + g * kGroupNodes;
+            const uint32_t e = min(s + kGroupNodes, a + count);
+            uint32_t o0, o1;
+            if (dir) {
+                o0 = dir_offset(sig, dir, n_level, s);
+                o1 = dir_offset(sig, dir, n_level, e);
+            } else {
+                // groups start on 256-node block boundaries of the tile; the
+                // last entry of prefix is the tile's total
+                o0 = leaf_base + prefix[(s - a) / 256u];
+                o1 = leaf_base + prefix[(e - a + 255u) / 256u];
+            }
+            const StagePlan pc = stage_plan((uint64_t)(s - a) * 8u + cs, (uint64_t)(e - a) * 8u + cs);
+            const StagePlan ps = stage_plan(s >> 1, ((uint64_t)e + 1) >> 1);
+            const StagePlan pl = stage_plan(o0 >> 1, ((uint64_t)o1 + 1) >> 1);
+            // wait until the consumers released this buffer (use it/2 - 1)
+            if (it >= 2 && !mbar_wait(&empty[k], ((it >> 1) - 1) & 1u)) {
+                atomicOr(status, kStatusStageTimeout);
+                abort_flag = 1;
+                return;
+            }
+            meta[k][0] = pc.shift;
+            meta[k][1] = 2u * ps.shift + (s & 1u);
+            meta[k][2] = 2u * pl.shift + (o0 & 1u);
+            meta[k][3] = o1 - o0;
+            uint8_t *b = buf0 + k * kGroupBuf;
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_expect_tx(&full[k], pc.bytes + ps.bytes + pl.bytes);
+            bulk_copy(b, src16 + pc.lo16, pc.bytes, &full[k]);
+            bulk_copy(b + kGroupCStage, sig + ps.lo16, ps.bytes, &full[k]);
+            bulk_copy(b + kGroupCStage + kGroupSStage, leaf + pl.lo16, pl.bytes, &full[k]);
+        }
+        return;
+    }
+
+    // ---- consumer warps ----
+    uint32_t it = 0;
+    for (uint32_t g = blockIdx.x; g < ngroups; g += gridDim.x, ++it) {
+        const int k = (int)(it & 1u);
+        if (!mbar_wait(&full[k], (it >> 1) & 1u)) {
+            if (threadIdx.x == 0) atomicOr(status, kStatusStageTimeout);
+            return;
+        }
+        const uint8_t *b = buf0 + k * kGroupBuf;
+        const uint32_t s = a + g * kGroupNodes;
+        const uint32_t n = min(s + kGroupNodes, a + count) - s;
+        const Coord *nodec = reinterpret_cast<const Coord *>(b + meta[k][0]);
+        uint32_t mn = 0xffffffffu, mx = 0u;
+        consumer_expand<kGroupThreads, DIR>(reinterpret_cast<const uint32_t *>(b + kGroupCStage), meta[k][1], n,
+                                            nodec, leafc, wt, mn, mx);
+        consumers_sync<kGroupThreads>();
+        block_leaves<SR, DIR, VW, kGroupThreads, true>(b + kGroupCStage + kGroupSStage, meta[k][2], meta[k][3], leafc,
+                                                       va, win, kGroupWindow, red, true, mn, mx);
+        consumers_sync<kGroupThreads>();
+        if (threadIdx.x == 0) mbar_arrive(&empty[k]);
+    }
+}
+
 // FUSED engine: thread block k descends chunk k, a run of whole subtrees
-// rooted at level d_c, down to the leaves.  The chunk record holds the
-// index of its roots' coordinates and, for every level, the first node and
-// the node count of the chunk there (planned once per tree on the host).
-// Each level: a thread takes a contiguous run of parents, the block scans
-// the run fan-outs, and children are written to the other shared buffer.
+// rooted at level d_c with at most `cap` leaves, from its roots to the
+// leaves.  The chunk record holds the index of its roots' coordinates and,
+// for every level, the first node and the node count of the chunk there
+// (planned once per tree on the host).  The block stages the signatures of
+// all its levels with one bulk copy per level, then expands level by level
+// in shared memory: every warp takes an equal slice of the level, learns
+// where its children start from the other warps' fan-out totals (one block
+// barrier per level) and writes them with warp scans.  No global scratch.
 template <int SR, int DIR, int VW>
 __global__ void __launch_bounds__(kFusedThreads)
-fused_kernel(DevTree tr, const uint32_t *chunks, uint32_t stride, const Coord *roots, VecArgs va)
+fused_kernel(DevTree tr, const uint32_t *chunks, uint32_t stride, const Coord *roots, uint32_t cap, VecArgs va,
+             uint32_t *status)
 {
-    extern __shared__ Coord fsm[];
-    __shared__ uint32_t wsum[kFusedWarps];
-    Coord *cur = fsm;
-    Coord *nxt = fsm + kMaxChunkCap;
+    extern __shared__ __align__(16) uint8_t fsm[];
+    const int d0 = tr.d0, l = tr.levels;
+    const uint32_t slot = (cap / 2 + 48 + 15) & ~15u;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(fsm);
+    uint32_t *wtot = reinterpret_cast<uint32_t *>(fsm + 16);           // [2][kFusedWarps] fan-out totals
+    uint32_t *nbase = reinterpret_cast<uint32_t *>(fsm + 80);          // per level, nibble base in its slot
+    uint8_t *stage = fsm + 80 + 4 * K2T_MAX_LEVELS;
+    stage += (16 - ((uintptr_t)stage & 15)) & 15;
+    Coord *cur = reinterpret_cast<Coord *>(stage + (size_t)(l - d0) * slot);
+    Coord *nxt = cur + cap;
+    __shared__ uint32_t red[2 * kFusedWarps];
+
     const uint32_t *rec = chunks + (size_t)blockIdx.x * stride;
     const uint32_t rc = rec[0];
     const int dc = (int)rec[1];
     const uint32_t *rng = rec + 2;
-    const int d0 = tr.d0, l = tr.levels;
-    const uint32_t tid = threadIdx.x;
+    if (threadIdx.x == 0) {
+        uint32_t total = 0;
+        StagePlan pl[K2T_MAX_LEVELS];
+        for (int d = dc; d < l; ++d) {
+            const uint32_t s = rng[2 * (d - d0)], n = rng[2 * (d - d0) + 1];
+            pl[d] = stage_plan(s >> 1, ((uint64_t)s + n + 1) >> 1);
+            nbase[d - d0] = 2u * pl[d].shift + (s & 1u);
+            total += pl[d].bytes;
+        }
+        mbar_init(bar);
+        mbar_expect_tx(bar, total);
+        for (int d = dc; d < l; ++d)
+            bulk_copy(stage + (size_t)(d - d0) * slot, tr.lv[d].sig + pl[d].lo16, pl[d].bytes, bar);
+    }
     {
         const uint32_t n = rng[2 * (dc - d0) + 1];
-        for (uint32_t i = tid; i < n; i += kFusedThreads) cur[i] = roots[rc + i];
+        for (uint32_t i = threadIdx.x; i < n; i += kFusedThreads) cur[i] = roots[rc + i];
     }
     __syncthreads();
-    for (int d = dc; d < l - 2; ++d) {
-        const uint32_t s = rng[2 * (d - d0)], n = rng[2 * (d - d0) + 1];
-        const uint8_t *sig = tr.lv[d].sig;
-        const uint32_t per = (n + kFusedThreads - 1) / kFusedThreads;
-        const uint32_t i0 = min(tid * per, n), i1 = min(i0 + per, n);
-        uint32_t tot = 0;
-        for (uint32_t i = i0; i < i1; ++i) tot += (uint32_t)__popc(nibble_at(sig, s + i));
-        uint32_t pos = block_excl_scan(tot, wsum);
-        for (uint32_t i = i0; i < i1; ++i) {
-            const uint32_t sg = nibble_at(sig, s + i);
-            const Coord p = cur[i];
-#pragma unroll
-            for (int b = 0; b < 4; ++b)
-                if (sg & (1u << b)) nxt[pos++] = child_of(p, b);
-        }
-        __syncthreads();
-        Coord *t = cur; cur = nxt; nxt = t;
+    if (!mbar_wait(bar, 0)) {
+        if (threadIdx.x == 0) atomicOr(status, kStatusStageTimeout);
+        mbar_wait(bar, 0);
+        return;
     }
-    {
-        const int d = l - 2;
-        const uint32_t s = rng[2 * (d - d0)], n = rng[2 * (d - d0) + 1];
-        const uint32_t sl = rng[2 * (d + 1 - d0)];
-        const uint8_t *sig = tr.lv[d].sig;
-        const uint8_t *leaf = tr.lv[l - 1].sig;
-        const uint32_t per = (n + kFusedThreads - 1) / kFusedThreads;
-        const uint32_t i0 = min(tid * per, n), i1 = min(i0 + per, n);
-        uint32_t tot = 0;
-        for (uint32_t i = i0; i < i1; ++i) tot += (uint32_t)__popc(nibble_at(sig, s + i));
-        uint32_t pos = sl + block_excl_scan(tot, wsum);
-        for (uint32_t i = i0; i < i1; ++i) {
-            const uint32_t sg = nibble_at(sig, s + i);
-            visit_node<SR, DIR, VW>(cur[i], sg, pos, leaf, va);
-            pos += (uint32_t)__popc(sg);
-        }
+    uint32_t mn = 0xffffffffu, mx = 0u;
+    for (int d = dc; d <= l - 2; ++d) {
+        const uint32_t n = rng[2 * (d - d0) + 1];
+        const uint32_t *words = reinterpret_cast<const uint32_t *>(stage + (size_t)(d - d0) * slot);
+        // fan-out totals alternate between two arrays: a fast warp may publish
+        // the next level's total while a slow one still reads this level's
+        mn = 0xffffffffu;
+        mx = 0u;
+        sliced_expand<kFusedThreads, DIR>(words, nbase[d - d0], n, cur, nxt, wtot + (d & 1) * kFusedWarps, mn, mx);
+        Coord *t = cur;
+        cur = nxt;
+        nxt = t;
     }
+    __syncthreads();
+    // the other coordinate buffer (2 * cap words) is free: it becomes the
+    // output window of the segmented scatter
+    const uint32_t nl = rng[2 * (l - 1 - d0) + 1];
+    block_leaves<SR, DIR, VW, kFusedThreads>(stage + (size_t)(l - 1 - d0) * slot, nbase[l - 1 - d0], nl, cur, va,
+                                             reinterpret_cast<uint32_t *>(nxt), 2 * cap, red, true, mn, mx);
+}
+
+// Dynamic shared memory of fused_kernel for a tree.
+inline size_t fused_smem(int levels, int d0, uint32_t cap)
+{
+    return 80 + 4 * K2T_MAX_LEVELS + 16 + (size_t)(levels - d0) * ((cap / 2 + 48 + 15) & ~15u) + 2 * (size_t)cap * 8;
 }
 
 }  // namespace k2t
@@ -444,14 +1237,43 @@ inline int grid_for_blocks(uint64_t warps_needed)
 template <int SR, int DIR, int VW>
 void launch_fused(const k2t_tree *t, const DeviceState *d, const VecArgs &va, cudaStream_t st)
 {
-    const size_t smem = 2 * kMaxChunkCap * sizeof(Coord);
-    static bool configured = false;
-    if (!configured) {
+    const size_t smem = fused_smem(t->levels, t->d0, t->opts.chunk_cap);
+    static size_t configured = 0;
+    if (smem > configured) {
         cudaFuncSetAttribute(fused_kernel<SR, DIR, VW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        configured = true;
+        configured = smem;
     }
-    fused_kernel<SR, DIR, VW><<<(unsigned)t->n_chunks, kFusedThreads, smem, st>>>(d->tree, d->chunks, t->chunk_stride,
-                                                                                 d->roots, va);
+    fused_kernel<SR, DIR, VW><<<(unsigned)t->n_chunks, kFusedThreads, smem, st>>>(
+        d->tree, d->chunks, t->chunk_stride, d->roots, t->opts.chunk_cap, va, d->err);
+}
+
+template <int SR, int DIR, int VW>
+void launch_leafgroup(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix, uint32_t leaf_base, uint32_t a,
+                      uint32_t count, uint32_t n_level, const Coord *src, const uint8_t *leaf, const VecArgs &va,
+                      uint32_t *status, cudaStream_t st)
+{
+    constexpr size_t smem = leafgroup_smem();
+    static int resident = 0;  // resident blocks per SM x SMs
+    if (!resident) {
+        cudaFuncSetAttribute(leafgroup_kernel<SR, DIR, VW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        int dev = 0, sms = 0, per = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, leafgroup_kernel<SR, DIR, VW>, kGroupBlock, smem);
+        resident = std::max(1, sms * std::max(1, per));
+    }
+    const uint32_t groups = (count + kGroupNodes - 1) / kGroupNodes;
+    const unsigned grid = (unsigned)std::min<uint32_t>(groups, (uint32_t)resident);
+    leafgroup_kernel<SR, DIR, VW><<<grid, kGroupBlock, smem, st>>>(sig, dir, prefix, leaf_base, a, count, n_level,
+                                                                     src, leaf, va, status);
+}
+
+template <int SR, int DIR, int VW>
+void launch_flat(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix, uint32_t leaf_base, uint32_t a,
+                 uint32_t count, const Coord *src, const uint8_t *leaf, const VecArgs &va, cudaStream_t st)
+{
+    const unsigned grid = (unsigned)((count + kFlatThreads - 1) / kFlatThreads);
+    flat_leaf_kernel<SR, DIR, VW><<<grid, kFlatThreads, 0, st>>>(sig, dir, prefix, leaf_base, a, count, src, leaf, va);
 }
 
 template <int SR, int DIR, int VW>
@@ -459,8 +1281,9 @@ void launch_cached(const k2t_tree *t, const DeviceState *d, const VecArgs &va, c
 {
     const int l = t->levels;
     const uint32_t n = (uint32_t)t->nodes[(size_t)l - 2];
-    const uint64_t blocks = (n + kDirS - 1) / kDirS;
-    cached_leaf_kernel<SR, DIR, VW><<<grid_for_blocks(blocks), kWalkThreads, 0, st>>>(
+    const uint32_t blocks = (n + kDirS - 1) / kDirS;
+    const unsigned grid = (unsigned)((blocks + kCachedWarps - 1) / kCachedWarps);
+    cached_block_kernel<SR, DIR, VW><<<grid, 32 * kCachedWarps, 0, st>>>(
         d->tree.lv[l - 2].sig, d->tree.lv[l - 2].dir, n, d->cached, d->tree.lv[l - 1].sig, va);
 }
 
@@ -477,8 +1300,6 @@ void launch_ls(const k2t_tree *t, const DeviceState *d, const VecArgs &va, cudaS
         const uint64_t blocks = scan ? (s.count + 255u) / 256u
                                      : ((uint64_t)s.a + s.count + kDirS - 1) / kDirS - s.a / kDirS;
         const uint32_t *prefix = nullptr;
-        uint32_t base = s.dst_base;
-        if (s.kind == 1) base = scan ? (uint32_t)level_offset(t, lv, s.a) : 0u;
         if (scan) {
             ls_block_sums_kernel<<<grid_for_blocks(blocks), kWalkThreads, 0, st>>>(sig, s.a, s.count, d->scan_sums);
             ls_scan_kernel<<<1, 1024, 0, st>>>(d->scan_sums, (uint32_t)blocks, d->scan_prefix);
@@ -488,8 +1309,9 @@ void launch_ls(const k2t_tree *t, const DeviceState *d, const VecArgs &va, cudaS
             ls_expand_kernel<<<grid_for_blocks(blocks), kWalkThreads, 0, st>>>(
                 sig, dir, prefix, s.a, s.count, src, s.src_base, d->buf[lv + 1], s.dst_base);
         } else {
-            ls_leaf_kernel<SR, DIR, VW><<<grid_for_blocks(blocks), kWalkThreads, 0, st>>>(
-                sig, dir, prefix, s.a, s.count, src, s.src_base, base, d->tree.lv[l - 1].sig, va);
+            const uint32_t base = scan ? (uint32_t)level_offset(t, lv, s.a) : 0u;
+            launch_flat<SR, DIR, VW>(sig, scan ? nullptr : dir, prefix, base, s.a, s.count,
+                                     src + (s.a - s.src_base), d->tree.lv[l - 1].sig, va, st);
         }
     }
 }

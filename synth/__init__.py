@@ -133,6 +133,16 @@ def uniform_c1(seed: int = 0) -> Workload:
                     xs={0: x_right, 1: x_left})
 
 
+def uniform_large(log_n: int = 20, edges_per_vertex: int = 16, seed: int = 5) -> Workload:
+    """Uniform random matrix of the R-MAT workload's size (no hub rows): a
+    control for contention effects.  Drawn as R-MAT with equal quadrants."""
+    n = 1 << log_n
+    r, c = rmat(log_n, 0.25, 0.25, 0.25, edges_per_vertex * n, seed)
+    rng = np.random.default_rng(seed)
+    xs = {d: rng.uniform(0.0, 1.0, size=(n, 1)).astype(np.float32) for d in (0, 1)}
+    return Workload("uniform%d-m%d" % (log_n, edges_per_vertex * n), r, c, n, n, PLUS_TIMES, 1, 1.0, xs=xs)
+
+
 def rmat_c2(scale: int = 20, edges_per_vertex: int = 16, seed: int = 1) -> Workload:
     """Power-law R-MAT (.57,.19,.19,.05), 16 edges per vertex, x ~ U(0,1)/sum."""
     n = 1 << scale

@@ -19,7 +19,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 ENGINES = [
     dict(engine=1),                                   # fused, tree-only
-    dict(engine=1, chunk_cap=3),                       # fused, many tiny chunks
+    dict(engine=1, chunk_cap=4),                       # fused, many tiny chunks
     dict(engine=2, offsets=0, tile_m=16),              # level-sync, directory, many tiles
     dict(engine=2, offsets=1, tile_m=16),              # level-sync, scan
     dict(engine=2, offsets=0, tile_m=1 << 20, use_graph=0),

@@ -102,6 +102,8 @@ def test_errors():
     assert e.value.status == -2
     with pytest.raises(K.K2TError) as e:
         K.Tree(r, c, 8, 8, chunk_cap=5000)
+    with pytest.raises(K.K2TError) as e:
+        K.Tree(r, c, 8, 8, chunk_cap=3)
     assert e.value.status == -1
     t = K.Tree(r, c, 8, 8)
     lib = K.load()
@@ -135,14 +137,14 @@ def test_workspace_accounting(engine):
     if engine == 2:
         assert s.n_steps > 1 and s.scratch_bytes > 0
     if engine == 3:
-        assert s.cached_bytes == 8 * s.level_nodes[s.levels - 2]
+        assert s.cached_bytes == 8 * s.level_nodes[s.levels - 2] + 16
 
 
 def test_chunk_plan_covers_every_node():
     """Fused plan: chunks are whole subtrees; together they cover each level
     below the host-expanded top exactly once, in level order."""
     rows, cols = synth.rmat(13, 0.57, 0.19, 0.19, 60000, 6)
-    for cap in (1, 7, 256, 4096):
+    for cap in (4, 7, 256, 4096):
         t = K.Tree(rows, cols, 8192, 8192, engine=1, chunk_cap=cap)
         h = t.handle
         s = t.stats()
