@@ -519,7 +519,7 @@ __device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint
 // inputs are loaded together, then the combined updates are applied.  Every
 // lane does the same work per leaf, whatever the fan-out of its node.
 constexpr int kCachedWarps = 8;
-constexpr int kCachedU = 2;
+constexpr int kCachedU = 4;
 constexpr uint32_t kCachedWindow = 256;  // words of a warp's output window
 
 template <int SR, int DIR, int VW>
@@ -606,15 +606,23 @@ cached_block_kernel(const uint8_t *sig, const uint32_t *dir, uint32_t n, const C
         if (SR == K2T_BOOLEAN || (VW == 1 && va.B == 1)) {
             uint32_t xo[kCachedU][2], out[kCachedU];
             const uint32_t *x = static_cast<const uint32_t *>(va.x);
+            const bool x8 = ((uintptr_t)x & 7u) == 0;
 #pragma unroll
             for (int u = 0; u < kCachedU; ++u) {
-                const uint32_t in = DIR == K2T_RIGHT ? c[u] : r[u];
+                const uint32_t in = DIR == K2T_RIGHT ? c[u] : r[u];  // even
                 out[u] = DIR == K2T_RIGHT ? r[u] : c[u];
                 xo[u][0] = 0u;
                 xo[u][1] = 0u;
                 if (j0 + 32u * u + lane < total) {
-                    xo[u][0] = __ldg(x + in);
-                    if (in + 1u < va.n_in) xo[u][1] = __ldg(x + in + 1u);
+                    if (x8 && in + 1u < va.n_in) {
+                        // both inputs of the leaf block in one 8-byte load
+                        const uint2 v = __ldg(reinterpret_cast<const uint2 *>(x + in));
+                        xo[u][0] = v.x;
+                        xo[u][1] = v.y;
+                    } else {
+                        xo[u][0] = __ldg(x + in);
+                        if (in + 1u < va.n_in) xo[u][1] = __ldg(x + in + 1u);
+                    }
                 }
             }
             leaf_apply1<SR, DIR, kCachedU>(lam, out, xo, va, win, lo);

@@ -188,14 +188,15 @@ def social_c4(scale: int = 24, edges_per_vertex: int = 16, B: int = 8, seed: int
 
 
 def large_c5(scale: int = 27, edges: int = 1_200_000_000, B: int = 1, seed: int = 4) -> Workload:
-    """R-MAT (.57,.19,.19,.05), ids permuted then BFS-ordered; cached last level."""
+    """R-MAT (.57,.19,.19,.05), ids permuted then BFS-ordered; cached last level.
+    x ~ U(0,1) fp32; the square matrix uses one x for both directions."""
     n = 1 << scale
     r, c = rmat(scale, 0.57, 0.19, 0.19, edges, seed)
     permute_bfs(n, r, c, seed)
     rng = np.random.default_rng(seed)
-    xs = {d: _fp32_uniform(rng, (n, B), 0.0, 1.0) for d in (0, 1)}
+    x = rng.random(size=(n, B), dtype=np.float32)
     return Workload("rmat%d-bfs-%dM" % (scale, edges // 1_000_000), r, c, n, n, PLUS_TIMES, B, 1.0,
-                    cache_last_internal=True, xs=xs)
+                    cache_last_internal=True, xs={0: x, 1: x})
 
 
 def random_small(seed: int, n_rows: int, n_cols: int, density: float):
