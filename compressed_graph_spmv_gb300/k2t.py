@@ -29,7 +29,8 @@ STATUS = {0: "K2T_OK", -1: "K2T_EINVAL", -2: "K2T_ERANGE", -3: "K2T_ENOMEM",
 EXPORTED = ["k2t_default_opts", "k2t_build", "k2t_workspace_bytes", "k2t_upload", "k2t_spmv",
             "k2t_spmv_marked",
             "k2t_spmv_host", "k2t_stats_get", "k2t_level_signatures", "k2t_device_level",
-            "k2t_decode", "k2t_free", "k2t_strerror", "k2t_last_cuda_error"]
+            "k2t_decode", "k2t_free", "k2t_strerror", "k2t_last_cuda_error",
+            "k2t_spmv_noalloc", "k2t_noalloc_scratch_limit"]
 
 
 class Opts(ctypes.Structure):
@@ -83,6 +84,10 @@ def load() -> ctypes.CDLL:
         lib.k2t_upload.argtypes = [P, P, U64, P]
         lib.k2t_spmv.argtypes = [P, I32, I32, ctypes.c_float, P, P, U32, P]
         lib.k2t_spmv_marked.argtypes = [P, I32, I32, ctypes.c_float, P, P, U32, P, P]
+        lib.k2t_spmv_noalloc.argtypes = [P, I32, I32, ctypes.c_float, P, P, U32, P]
+        lib.k2t_spmv_noalloc.restype = ctypes.c_int
+        lib.k2t_noalloc_scratch_limit.argtypes = []
+        lib.k2t_noalloc_scratch_limit.restype = U64
         lib.k2t_spmv_host.argtypes = [P, I32, I32, ctypes.c_float, P, P, U32, P]
         lib.k2t_stats_get.argtypes = [P, ctypes.POINTER(Stats)]
         lib.k2t_level_signatures.argtypes = [P, U32, P, U64, ctypes.POINTER(U64)]
@@ -208,6 +213,13 @@ class Tree:
         _check("k2t_spmv_marked", load().k2t_spmv_marked(self._h, direction, semiring, ctypes.c_float(w),
                                                          _dev_ptr(x), _dev_ptr(y), B, _stream_ptr(stream),
                                                          event_after_fill))
+        return y
+
+    def spmv_noalloc(self, direction: int, semiring: int, x, y, B: int = 1, w: float = 1.0, stream=None):
+        """Level-synchronous product with scratch in the library's static device
+        array (no allocation); see k2t_spmv_noalloc in include/k2t.h."""
+        _check("k2t_spmv_noalloc", load().k2t_spmv_noalloc(self._h, direction, semiring, ctypes.c_float(w),
+                                                           _dev_ptr(x), _dev_ptr(y), B, _stream_ptr(stream)))
         return y
 
     def spmv_host(self, direction: int, semiring: int, x: np.ndarray, y: np.ndarray, B: int = 1,

@@ -181,6 +181,32 @@ int k2t_spmv_marked(k2t_tree *t, int32_t dir, int32_t semiring, float w,
 int k2t_spmv_host(k2t_tree *t, int32_t dir, int32_t semiring, float w,
                   const void *x_host, void *y_host, uint32_t B, void *stream);
 
+/* The level-synchronous product of k2t_spmv for callers that cannot call
+ * cudaMalloc: a framework that owns all device memory through its own pool,
+ * code that must never synchronise the device, or code held to a memory
+ * budget fixed before it starts.  The pages have no counterpart; it is an
+ * addition of this library.  It allocates nothing: its frontier buffers and
+ * scan space live in one file-scope device array of
+ * k2t_noalloc_scratch_limit() bytes (64 MiB), which every GPU that loads the
+ * library holds until the process exits.  The caller provides the uploaded
+ * tree (its arena may come from k2t_upload with a caller-owned buffer), x and
+ * y, with the layout and results of k2t_spmv.
+ *   - The tree must use the LEVELSYNC engine (else ESTATE) and its frontier
+ *     buffers plus scan space must fit the array (else ERANGE; lower
+ *     opts.tile_m to fit).
+ *   - The first call on a device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress); make that first call
+ *     before any stream capture.
+ *   - Every call shares the array.  Nothing in it needs to start at zero;
+ *     calls whose work overlaps on the GPU race on it, so order them (one
+ *     stream, or events).
+ *   - Other errors as k2t_spmv. */
+int k2t_spmv_noalloc(k2t_tree *t, int32_t dir, int32_t semiring, float w,
+                     const void *x, void *y, uint32_t B, void *stream);
+
+/* Size in bytes of the device array k2t_spmv_noalloc works in. */
+uint64_t k2t_noalloc_scratch_limit(void);
+
 /* Shape, per-level sizes and the device footprint broken down by part. */
 int k2t_stats_get(const k2t_tree *t, k2t_stats *s);
 
