@@ -267,6 +267,7 @@ namespace k2t {
 constexpr int kWalkThreads = 256;   // 8 warps, one 256-node block each
 constexpr int kFusedThreads = 256;
 constexpr int kFusedWarps = kFusedThreads / 32;
+constexpr uint32_t kFusedSolo = 256;  // levels this narrow are expanded by one warp
 
 // Kernels without template parameters, defined in k2t_device.cu.
 __global__ void fill_kernel(uint32_t *y, uint64_t words, uint32_t pattern);
@@ -510,17 +511,111 @@ __device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint
     }
 }
 
+// ---- per-warp leaf stage -------------------------------------------------------
+constexpr int kLeafU = 4;                 // leaves per lane per round
+constexpr uint32_t kWarpWindow = 256;     // words of a warp's output window
+
+// Per-warp segmented scatter.  [mn, mx] bounds the warp's output coordinates
+// in units of `unit` cells (4 for nodes of the last internal level, 2 for
+// leaves).  When the outputs fit the warp's window (kWarpWindow words), the
+// window is cleared and returned; updates are then reduced there and each
+// touched entry reaches y once (warp_window_flush).  Hub rows of power-law
+// graphs then cost one global atomic per warp instead of one per non-zero.
+template <int SR>
+__device__ __forceinline__ uint32_t *warp_window_begin(uint32_t mn, uint32_t mx, uint32_t unit, uint32_t width,
+                                                       uint32_t *mem, uint32_t &lo, uint32_t &span)
+{
+    const uint32_t lane = threadIdx.x & 31u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    lo = unit * mn;
+    span = 0;
+    if (mn > mx) return nullptr;
+    const uint64_t span64 = (uint64_t)unit * ((uint64_t)mx - mn + 1u);
+    if (span64 * width > kWarpWindow) return nullptr;
+    span = (uint32_t)span64;
+    for (uint32_t i = lane; i < span * width; i += 32u) mem[i] = zero_word<SR>();
+    __syncwarp();
+    return mem;
+}
+
+template <int SR>
+__device__ __forceinline__ void warp_window_flush(const uint32_t *win, uint32_t lo, uint32_t span, uint32_t width,
+                                                  const VecArgs &va)
+{
+    const uint32_t lane = threadIdx.x & 31u;
+    __syncwarp();
+    uint32_t *y = static_cast<uint32_t *>(va.y) + (size_t)lo * width;
+    const uint64_t limit = (va.n_out - lo) * width;
+    for (uint32_t i = lane; i < span * width; i += 32u) {
+        const uint32_t v = win[i];
+        if (!is_noop_word<SR>(v) && i < limit) global_update_word<SR>(y + i, v);
+    }
+}
+
+// Leaves [jb, je) of a warp, dealt round-robin to its lanes, kLeafU per lane
+// per round.  leaf_at(j, lam, r, c) gives leaf j's cells and the origin of its
+// 2x2 block.  For one vector slice (B = 1 fp32, or a Boolean word) both input
+// entries of the block are read with one 8-byte load together with the leaf
+// signature; updates go to the window when there is one, else to y.
+template <int SR, int DIR, int VW, class LeafAt>
+__device__ __forceinline__ void warp_leaf_rounds(uint32_t jb, uint32_t je, LeafAt &&leaf_at, const VecArgs &va,
+                                                 uint32_t *win, uint32_t lo)
+{
+    // one vector slice: four leaves in flight per lane; wider batches keep
+    // one leaf per lane (each leaf already loads B values per input)
+    constexpr int U = (SR == K2T_BOOLEAN || VW == 1) ? kLeafU : 1;
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t *x = static_cast<const uint32_t *>(va.x);
+    const bool x8 = ((uintptr_t)x & 7u) == 0;
+    for (uint32_t j0 = jb; j0 < je; j0 += 32u * U) {
+        uint32_t lam[U], r[U], c[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t j = j0 + 32u * u + lane;
+            lam[u] = 0u;
+            r[u] = 0u;
+            c[u] = 0u;
+            if (j < je) leaf_at(j, lam[u], r[u], c[u]);
+        }
+        if (SR == K2T_BOOLEAN || (VW == 1 && va.B == 1)) {
+            uint32_t xo[U][2], out[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const uint32_t in = DIR == K2T_RIGHT ? c[u] : r[u];  // even
+                out[u] = DIR == K2T_RIGHT ? r[u] : c[u];
+                xo[u][0] = 0u;
+                xo[u][1] = 0u;
+                if (lam[u]) {
+                    if (x8 && in + 1u < va.n_in) {
+                        const uint2 v = __ldg(reinterpret_cast<const uint2 *>(x + in));
+                        xo[u][0] = v.x;
+                        xo[u][1] = v.y;
+                    } else {
+                        xo[u][0] = __ldg(x + in);
+                        if (in + 1u < va.n_in) xo[u][1] = __ldg(x + in + 1u);
+                    }
+                }
+            }
+            leaf_apply1<SR, DIR, U>(lam, out, xo, va, win, lo);
+        } else {
+            leaf_group<SR, DIR, VW, U>(lam, r, c, va, win, lo);
+        }
+    }
+}
+
 // k^2+F engine (section 3.5): one warp per 256-node directory block of the
 // last internal level.  The warp reads the block's 128 bytes of signatures
 // (one word of 8 nibbles per lane), its directory sample and the cached
 // coordinates; a warp scan of the fan-outs turns the block into a list of its
 // leaves (node, quadrant) in shared memory.  The lanes then take the leaves
-// round-robin, U per round: leaf signature and the x entries of its two
-// inputs are loaded together, then the combined updates are applied.  Every
-// lane does the same work per leaf, whatever the fan-out of its node.
+// round-robin: leaf signature and the x entries of its two inputs are loaded
+// together, then the combined updates are applied.  Every lane does the same
+// work per leaf, whatever the fan-out of its node.
 constexpr int kCachedWarps = 8;
-constexpr int kCachedU = 4;
-constexpr uint32_t kCachedWindow = 256;  // words of a warp's output window
 
 template <int SR, int DIR, int VW>
 __global__ void __launch_bounds__(32 * kCachedWarps)
@@ -529,7 +624,7 @@ cached_block_kernel(const uint8_t *sig, const uint32_t *dir, uint32_t n, const C
 {
     __shared__ Coord cs[kCachedWarps][kDirS];
     __shared__ uint16_t slots[kCachedWarps][4 * kDirS];
-    __shared__ uint32_t wins[kCachedWarps][kCachedWindow];
+    __shared__ uint32_t wins[kCachedWarps][kWarpWindow];
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
     const uint32_t g = blockIdx.x * kCachedWarps + warp;
     const uint32_t s = g * kDirS;
@@ -537,7 +632,7 @@ cached_block_kernel(const uint8_t *sig, const uint32_t *dir, uint32_t n, const C
     const uint32_t cnt = min(n - s, kDirS);
     Coord *cw = cs[warp];
     uint16_t *sl = slots[warp];
-    // round 1: signatures, directory sample, coordinates
+    // signatures, directory sample, coordinates
     uint32_t w = 0;
     if (8u * lane < cnt) {
         w = __ldg(reinterpret_cast<const uint32_t *>(sig + s / 2) + lane);
@@ -566,79 +661,19 @@ cached_block_kernel(const uint8_t *sig, const uint32_t *dir, uint32_t n, const C
         rest &= rest - 1u;
         sl[pos++] = (uint16_t)(((8u * lane + bit / 4u) << 2) | (bit & 3u));
     }
-    // Segmented scatter: the block's outputs lie in 4*[mn, mx] .. 4*mx+3 (a
-    // node of this level covers 4 rows and 4 columns).  When they fit the
-    // warp's window, updates are reduced there first and each touched entry
-    // reaches y once; hub rows of power-law graphs then cost one global
-    // atomic per block instead of one per non-zero.
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    }
     const uint32_t width = SR == K2T_BOOLEAN ? 1u : va.B;
-    const uint64_t span64 = 4ull * ((uint64_t)mx - mn + 1u);
-    const bool windowed = span64 * width <= kCachedWindow;
-    const uint32_t span = windowed ? (uint32_t)span64 : 0u;
-    uint32_t *win = windowed ? wins[warp] : nullptr;
-    const uint32_t lo = 4u * mn;
-    if (windowed)
-        for (uint32_t i = lane; i < span * width; i += 32u) win[i] = zero_word<SR>();
+    uint32_t lo, span;
+    uint32_t *win = warp_window_begin<SR>(mn, mx, 4u, width, wins[warp], lo, span);
     __syncwarp();
-    // round 2: leaves, U per lane per round
-    for (uint32_t j0 = 0; j0 < total; j0 += 32u * kCachedU) {
-        uint32_t lam[kCachedU], r[kCachedU], c[kCachedU];
-#pragma unroll
-        for (int u = 0; u < kCachedU; ++u) {
-            const uint32_t j = j0 + 32u * u + lane;
-            lam[u] = 0u;
-            r[u] = 0u;
-            c[u] = 0u;
-            if (j < total) {
-                const uint32_t e = sl[j];
-                const Coord p = cw[e >> 2];
-                const uint32_t b = e & 3u;
-                r[u] = 4u * p.r + 2u * (b >> 1);
-                c[u] = 4u * p.c + 2u * (b & 1u);
-                lam[u] = nibble_at(leaf, base + j);
-            }
-        }
-        if (SR == K2T_BOOLEAN || (VW == 1 && va.B == 1)) {
-            uint32_t xo[kCachedU][2], out[kCachedU];
-            const uint32_t *x = static_cast<const uint32_t *>(va.x);
-            const bool x8 = ((uintptr_t)x & 7u) == 0;
-#pragma unroll
-            for (int u = 0; u < kCachedU; ++u) {
-                const uint32_t in = DIR == K2T_RIGHT ? c[u] : r[u];  // even
-                out[u] = DIR == K2T_RIGHT ? r[u] : c[u];
-                xo[u][0] = 0u;
-                xo[u][1] = 0u;
-                if (j0 + 32u * u + lane < total) {
-                    if (x8 && in + 1u < va.n_in) {
-                        // both inputs of the leaf block in one 8-byte load
-                        const uint2 v = __ldg(reinterpret_cast<const uint2 *>(x + in));
-                        xo[u][0] = v.x;
-                        xo[u][1] = v.y;
-                    } else {
-                        xo[u][0] = __ldg(x + in);
-                        if (in + 1u < va.n_in) xo[u][1] = __ldg(x + in + 1u);
-                    }
-                }
-            }
-            leaf_apply1<SR, DIR, kCachedU>(lam, out, xo, va, win, lo);
-        } else {
-            leaf_group<SR, DIR, VW, kCachedU>(lam, r, c, va, win, lo);
-        }
-    }
-    if (windowed) {
-        __syncwarp();
-        uint32_t *y = static_cast<uint32_t *>(va.y) + (size_t)lo * width;
-        const uint64_t limit = (va.n_out - lo) * width;
-        for (uint32_t i = lane; i < span * width; i += 32u) {
-            const uint32_t v = win[i];
-            if (!is_noop_word<SR>(v) && i < limit) global_update_word<SR>(y + i, v);
-        }
-    }
+    warp_leaf_rounds<SR, DIR, VW>(0u, total, [&](uint32_t j, uint32_t &lam, uint32_t &r, uint32_t &c) {
+        const uint32_t e = sl[j];
+        const Coord p = cw[e >> 2];
+        const uint32_t b = e & 3u;
+        r = 4u * p.r + 2u * (b >> 1);
+        c = 4u * p.c + 2u * (b & 1u);
+        lam = nibble_at(leaf, base + j);
+    }, va, win, lo);
+    if (win) warp_window_flush<SR>(win, lo, span, width, va);
 }
 
 // ---- shared-memory staging with the bulk-copy (TMA) engine ------------------
@@ -725,28 +760,6 @@ __device__ __forceinline__ uint32_t dir_offset(const uint8_t *sig, const uint32_
     return base;
 }
 
-// Exclusive block-wide prefix sum over NT threads; *total gets the sum.
-template <int NT>
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *wsum, uint32_t *total)
-{
-    constexpr int NW = NT / 32;
-    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
-    const uint32_t incl = warp_incl_scan(v);
-    if (lane == 31) wsum[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        uint32_t t = lane < (uint32_t)NW ? wsum[lane] : 0u;
-        uint32_t ti = warp_incl_scan(t);
-        if (lane < (uint32_t)NW) wsum[lane] = ti - t;
-        if (lane == 31) wsum[NW] = ti;
-    }
-    __syncthreads();
-    const uint32_t r = wsum[warp] + incl - v;
-    *total = wsum[NW];
-    __syncthreads();
-    return r;
-}
-
 // ---- warp-sliced level expansion ------------------------------------------------
 // Nibbles [s, e) of a staged signature copy viewed as 32-bit words (8 nodes
 // per word): lane l reads word w0 + l + 32k with the nibbles outside [s, e)
@@ -793,147 +806,27 @@ __device__ __forceinline__ void emit_children(uint32_t sg, Coord p, Coord *nxt, 
         }
 }
 
+// One warp expands the parents at nibbles [s, e) of the staged level (parent
+// i of the chunk at nibble nb + i, coordinates cur[i]), one parent per lane
+// per round: lanes read consecutive signatures and coordinates (no shared-
+// memory bank conflicts), a warp scan places the children, which go to
+// nxt[start ...] in level order.  Also folds the children's row (right) or
+// column (left) into [mn, mx].
 template <int DIR>
 __device__ __forceinline__ void warp_expand(const uint32_t *words, uint32_t nb, uint32_t s, uint32_t e,
                                             const Coord *cur, Coord *nxt, uint32_t start, uint32_t &mn,
                                             uint32_t &mx)
 {
     const uint32_t lane = threadIdx.x & 31u;
-    if (s >= e) return;
-    if (e - s < 256u) {
-        // short slice: one parent per lane per round
-        const uint8_t *bytes = reinterpret_cast<const uint8_t *>(words);
-        for (uint32_t i0 = s; i0 < e; i0 += 32u) {
-            const uint32_t i = i0 + lane;
-            const uint32_t sg = i < e ? snib(bytes, i) : 0u;
-            const uint32_t f = (uint32_t)__popc(sg);
-            const uint32_t incl = warp_incl_scan(f);
-            const uint32_t pos = start + incl - f;
-            start += __shfl_sync(0xffffffffu, incl, 31);
-            if (sg) emit_children<DIR>(sg, cur[i - nb], nxt, pos, mn, mx);
-        }
-        return;
-    }
-    // long slice: eight parents (one 32-bit word of nibbles) per lane per round
-    const uint32_t w1 = (e + 7u) / 8u;
-    for (uint32_t W0 = s / 8u; W0 < w1; W0 += 32u) {
-        const uint32_t W = W0 + lane;
-        const uint32_t word = W < w1 ? (words[W] & word_mask(W, s, e)) : 0u;
-        const uint32_t f = (uint32_t)__popc(word);
+    const uint8_t *bytes = reinterpret_cast<const uint8_t *>(words);
+    for (uint32_t i0 = s; i0 < e; i0 += 32u) {
+        const uint32_t i = i0 + lane;
+        const uint32_t sg = i < e ? snib(bytes, i) : 0u;
+        const uint32_t f = (uint32_t)__popc(sg);
         const uint32_t incl = warp_incl_scan(f);
-        uint32_t pos = start + incl - f;
+        const uint32_t pos = start + incl - f;
         start += __shfl_sync(0xffffffffu, incl, 31);
-        uint32_t rest = word;
-        while (rest) {
-            const uint32_t k = (uint32_t)(__ffs(rest) - 1) / 4u;
-            const uint32_t sg = (word >> (4u * k)) & 15u;
-            rest &= ~(15u << (4u * k));
-            emit_children<DIR>(sg, cur[8u * W + k - nb], nxt, pos, mn, mx);
-            pos += (uint32_t)__popc(sg);
-        }
-    }
-}
-
-// Algorithm 1, lines 5-10, inside one thread block: the n parents in `cur`,
-// whose signatures are nibbles nb .. nb+n-1 of the staged copy sg, write the
-// coordinates of their children, in level order, to `nxt`.  Each thread
-// takes a contiguous run of parents; the block scans the run fan-outs.
-template <int NT>
-__device__ __forceinline__ uint32_t block_expand(const uint8_t *sg, uint32_t nb, uint32_t n, const Coord *cur,
-                                                 Coord *nxt, uint32_t *wsum)
-{
-    const uint32_t per = (n + NT - 1) / NT;
-    const uint32_t i0 = min(threadIdx.x * per, n), i1 = min(i0 + per, n);
-    uint32_t tot = 0;
-    for (uint32_t i = i0; i < i1; ++i) tot += (uint32_t)__popc(snib(sg, nb + i));
-    uint32_t total;
-    uint32_t pos = block_excl_scan<NT>(tot, wsum, &total);
-    for (uint32_t i = i0; i < i1; ++i) {
-        const uint32_t s = snib(sg, nb + i);
-        const Coord p = cur[i];
-#pragma unroll
-        for (int b = 0; b < 4; ++b)
-            if (s & (1u << b)) nxt[pos++] = child_of(p, b);
-    }
-    __syncthreads();
-    return total;
-}
-
-// Algorithm 1, lines 14-17, for nl leaves whose coordinates (in units of the
-// 2x2 leaf block) are lc[0..nl) and signatures nibbles nb.. of sg.  Leaves
-// are dealt round-robin to the threads, U at a time.
-//
-// Segmented scatter: when the outputs the block touches span at most
-// win_words words, the block first reduces its updates in the shared window
-// `win` (shared-memory atomics) and then applies each touched entry to y once.
-// Hub rows of power-law graphs then cost one global atomic per block instead
-// of one per non-zero.  Otherwise updates go straight to y.
-template <int SR, int DIR, int VW, int NT, bool NAMED = false>
-__device__ __forceinline__ void block_leaves(const uint8_t *sg, uint32_t nb, uint32_t nl, const Coord *lc,
-                                             const VecArgs &va, uint32_t *win, uint32_t win_words, uint32_t *red,
-                                             bool have_extent = false, uint32_t mn_in = 0xffffffffu,
-                                             uint32_t mx_in = 0u)
-{
-    constexpr int U = 4;
-    const uint32_t width = SR == K2T_BOOLEAN ? 1u : va.B;
-    // extent of the outputs: min and max leaf row (right) or column (left);
-    // callers that built the leaf coordinates pass their own partial extent
-    uint32_t mn = mn_in, mx = mx_in;
-    if (!have_extent)
-        for (uint32_t j = threadIdx.x; j < nl; j += NT) {
-            const Coord q = lc[j];
-            const uint32_t o = DIR == K2T_RIGHT ? q.r : q.c;
-            mn = min(mn, o);
-            mx = max(mx, o);
-        }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    }
-    if ((threadIdx.x & 31u) == 0) {
-        red[2 * (threadIdx.x >> 5)] = mn;
-        red[2 * (threadIdx.x >> 5) + 1] = mx;
-    }
-    if constexpr (NAMED) asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); else __syncthreads();
-    mn = 0xffffffffu;
-    mx = 0u;
-#pragma unroll
-    for (int w = 0; w < NT / 32; ++w) {
-        mn = min(mn, red[2 * w]);
-        mx = max(mx, red[2 * w + 1]);
-    }
-    if constexpr (NAMED) asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); else __syncthreads();
-    const uint32_t lo = 2u * mn;
-    const uint64_t span = nl ? 2ull * ((uint64_t)mx - mn) + 2ull : 0ull;
-    const bool windowed = win && nl && span * width <= win_words;
-    const uint32_t words = windowed ? (uint32_t)(span * width) : 0u;
-    if (windowed) {
-        for (uint32_t i = threadIdx.x; i < words; i += NT) win[i] = zero_word<SR>();
-        if constexpr (NAMED) asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); else __syncthreads();
-    }
-    uint32_t *w = windowed ? win : nullptr;
-    for (uint32_t j0 = threadIdx.x; j0 < nl; j0 += NT * U) {
-        uint32_t lam[U], r[U], c[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint32_t j = j0 + (uint32_t)u * NT;
-            const bool ok = j < nl;
-            lam[u] = ok ? snib(sg, nb + j) : 0u;
-            const Coord q = ok ? lc[j] : Coord{0u, 0u};
-            r[u] = 2u * q.r;
-            c[u] = 2u * q.c;
-        }
-        leaf_group<SR, DIR, VW, U>(lam, r, c, va, w, lo);
-    }
-    if (windowed) {
-        if constexpr (NAMED) asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); else __syncthreads();
-        uint32_t *y = static_cast<uint32_t *>(va.y) + (size_t)lo * width;
-        const uint64_t limit = ((uint64_t)va.n_out - lo) * width;  // entries of y past lo
-        for (uint32_t i = threadIdx.x; i < words; i += NT) {
-            const uint32_t v = win[i];
-            if (!is_noop_word<SR>(v) && i < limit) global_update_word<SR>(y + i, v);
-        }
+        if (sg) emit_children<DIR>(sg, cur[i - nb], nxt, pos, mn, mx);
     }
 }
 
@@ -956,158 +849,6 @@ __device__ __forceinline__ void sliced_expand(const uint32_t *words, uint32_t nb
     uint32_t start = 0;
     for (uint32_t v = 0; v < warp; ++v) start += wt[v];
     warp_expand<DIR>(words, nb, a, b, cur, nxt, start, mn, mx);
-}
-
-// sliced_expand for the consumer threads of a warp-specialised block (named
-// barrier instead of __syncthreads).
-template <int NT, int DIR>
-__device__ __forceinline__ void consumer_expand(const uint32_t *words, uint32_t nb, uint32_t n, const Coord *cur,
-                                                Coord *nxt, uint32_t *wt, uint32_t &mn, uint32_t &mx)
-{
-    constexpr uint32_t NW = NT / 32;
-    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
-    const uint32_t a = nb + (uint32_t)(((uint64_t)n * warp) / NW);
-    const uint32_t b = nb + (uint32_t)(((uint64_t)n * (warp + 1)) / NW);
-    const uint32_t tot = warp_popc_nibbles(words, a, b);
-    if (lane == 0) wt[warp] = tot;
-    asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
-    uint32_t start = 0;
-    for (uint32_t v = 0; v < warp; ++v) start += wt[v];
-    warp_expand<DIR>(words, nb, a, b, cur, nxt, start, mn, mx);
-}
-
-constexpr int kGroupThreads = 256;
-constexpr uint32_t kGroupNodes = 512;                 // last-internal nodes per group
-constexpr uint32_t kGroupLeaves = 4 * kGroupNodes;    // at most 4 leaves per node
-constexpr uint32_t kGroupWindow = 4096;               // words of the output window
-constexpr uint32_t kGroupCStage = kGroupNodes * 8 + 16;
-constexpr uint32_t kGroupSStage = kGroupNodes / 2 + 48;
-constexpr uint32_t kGroupLStage = kGroupLeaves / 2 + 48;
-constexpr uint32_t kGroupBuf = kGroupCStage + kGroupSStage + kGroupLStage;  // one staging buffer
-
-// Bytes of dynamic shared memory of leafgroup_kernel.
-constexpr uint32_t leafgroup_smem()
-{
-    return 2 * kGroupBuf + kGroupLeaves * 8 + kGroupWindow * 4;
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// Barrier among the first NT threads of the block only (named barrier 1).
-template <int NT>
-__device__ __forceinline__ void consumers_sync()
-{
-    asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
-}
-
-// The last internal level in groups of kGroupNodes nodes, by a persistent,
-// warp-specialised grid.  Warp kGroupThreads/32 is the producer: for the
-// block's groups g, g + gridDim.x, ... it computes the leaf range from the
-// directory (or the tile's scan), and stages coordinates, signatures and
-// leaf signatures into one of two buffers with the bulk-copy engine (full
-// barrier), as soon as the consumers have released that buffer (empty
-// barrier).  The kGroupThreads consumer threads expand the leaf coordinates
-// in shared memory and apply the leaves.  Used by the k^2+F engine
-// (coordinates from the cache, section 3.5) and by the leaf tiles of the
-// level-synchronous engine (coordinates from a frontier buffer).
-//   nodes [a, a+count) of the level (level size n_level); src holds the
-//   coordinates of node a at index 0; first-child offsets from the directory
-//   (dir != null) or, in scan mode, leaf_base + prefix[(s - a) / 256].
-constexpr int kGroupBlock = kGroupThreads + 32;
-
-template <int SR, int DIR, int VW>
-__global__ void __launch_bounds__(kGroupBlock)
-leafgroup_kernel(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix, uint32_t leaf_base, uint32_t a,
-                 uint32_t count, uint32_t n_level, const Coord *src, const uint8_t *leaf, VecArgs va,
-                 uint32_t *status)
-{
-    extern __shared__ __align__(16) uint8_t gsm[];
-    uint8_t *buf0 = gsm;
-    Coord *leafc = reinterpret_cast<Coord *>(gsm + 2 * kGroupBuf);
-    uint32_t *win = reinterpret_cast<uint32_t *>(leafc + kGroupLeaves);
-    __shared__ __align__(8) uint64_t full[2], empty[2];
-    __shared__ uint32_t meta[2][4];  // coordinate shift, signature nibble base, leaf nibble base, leaf count
-    __shared__ uint32_t wt[kGroupThreads / 32];
-    __shared__ uint32_t red[2 * (kGroupThreads / 32)];
-    __shared__ uint32_t abort_flag;
-
-    const uint32_t ngroups = (count + kGroupNodes - 1) / kGroupNodes;
-    if (threadIdx.x == 0) {
-        mbar_init(&full[0]);
-        mbar_init(&full[1]);
-        mbar_init(&empty[0]);
-        mbar_init(&empty[1]);
-        abort_flag = 0;
-    }
-    __syncthreads();
-
-    if (threadIdx.x >= kGroupThreads) {
-        // ---- producer warp (one thread issues) ----
-        if (threadIdx.x != kGroupThreads) return;
-        const uint8_t *src16 = reinterpret_cast<const uint8_t *>((uintptr_t)src & ~(uintptr_t)15);
-        const uint64_t cs = (uintptr_t)src & 15u;
-        uint32_t it = 0;
-        for (uint32_t g = blockIdx.x; g < ngroups; g += gridDim.x, ++it) {
-            const int k = (int)(it & 1u);
-            const uint32_t s = a + g * kGroupNodes;
-            const uint32_t e = min(s + kGroupNodes, a + count);
-            uint32_t o0, o1;
-            if (dir) {
-                o0 = dir_offset(sig, dir, n_level, s);
-                o1 = dir_offset(sig, dir, n_level, e);
-            } else {
-                // groups start on 256-node block boundaries of the tile; the
-                // last entry of prefix is the tile's total
-                o0 = leaf_base + prefix[(s - a) / 256u];
-                o1 = leaf_base + prefix[(e - a + 255u) / 256u];
-            }
-            const StagePlan pc = stage_plan((uint64_t)(s - a) * 8u + cs, (uint64_t)(e - a) * 8u + cs);
-            const StagePlan ps = stage_plan(s >> 1, ((uint64_t)e + 1) >> 1);
-            const StagePlan pl = stage_plan(o0 >> 1, ((uint64_t)o1 + 1) >> 1);
-            // wait until the consumers released this buffer (use it/2 - 1)
-            if (it >= 2 && !mbar_wait(&empty[k], ((it >> 1) - 1) & 1u)) {
-                atomicOr(status, kStatusStageTimeout);
-                abort_flag = 1;
-                return;
-            }
-            meta[k][0] = pc.shift;
-            meta[k][1] = 2u * ps.shift + (s & 1u);
-            meta[k][2] = 2u * pl.shift + (o0 & 1u);
-            meta[k][3] = o1 - o0;
-            uint8_t *b = buf0 + k * kGroupBuf;
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_expect_tx(&full[k], pc.bytes + ps.bytes + pl.bytes);
-            bulk_copy(b, src16 + pc.lo16, pc.bytes, &full[k]);
-            bulk_copy(b + kGroupCStage, sig + ps.lo16, ps.bytes, &full[k]);
-            bulk_copy(b + kGroupCStage + kGroupSStage, leaf + pl.lo16, pl.bytes, &full[k]);
-        }
-        return;
-    }
-
-    // ---- consumer warps ----
-    uint32_t it = 0;
-    for (uint32_t g = blockIdx.x; g < ngroups; g += gridDim.x, ++it) {
-        const int k = (int)(it & 1u);
-        if (!mbar_wait(&full[k], (it >> 1) & 1u)) {
-            if (threadIdx.x == 0) atomicOr(status, kStatusStageTimeout);
-            return;
-        }
-        const uint8_t *b = buf0 + k * kGroupBuf;
-        const uint32_t s = a + g * kGroupNodes;
-        const uint32_t n = min(s + kGroupNodes, a + count) - s;
-        const Coord *nodec = reinterpret_cast<const Coord *>(b + meta[k][0]);
-        uint32_t mn = 0xffffffffu, mx = 0u;
-        consumer_expand<kGroupThreads, DIR>(reinterpret_cast<const uint32_t *>(b + kGroupCStage), meta[k][1], n,
-                                            nodec, leafc, wt, mn, mx);
-        consumers_sync<kGroupThreads>();
-        block_leaves<SR, DIR, VW, kGroupThreads, true>(b + kGroupCStage + kGroupSStage, meta[k][2], meta[k][3], leafc,
-                                                       va, win, kGroupWindow, red, true, mn, mx);
-        consumers_sync<kGroupThreads>();
-        if (threadIdx.x == 0) mbar_arrive(&empty[k]);
-    }
 }
 
 // FUSED engine: thread block k descends chunk k, a run of whole subtrees
@@ -1134,7 +875,6 @@ fused_kernel(DevTree tr, const uint32_t *chunks, uint32_t stride, const Coord *r
     stage += (16 - ((uintptr_t)stage & 15)) & 15;
     Coord *cur = reinterpret_cast<Coord *>(stage + (size_t)(l - d0) * slot);
     Coord *nxt = cur + cap;
-    __shared__ uint32_t red[2 * kFusedWarps];
 
     const uint32_t *rec = chunks + (size_t)blockIdx.x * stride;
     const uint32_t rc = rec[0];
@@ -1164,25 +904,64 @@ fused_kernel(DevTree tr, const uint32_t *chunks, uint32_t stride, const Coord *r
         mbar_wait(bar, 0);
         return;
     }
+    // Levels whose parents number at most kFusedSolo are expanded by warp 0
+    // alone (no block barrier); from the first wider level on, all warps
+    // share every level.  Levels never shrink downwards, so the first wide
+    // level's barrier also publishes warp 0's last writes.
+    const uint32_t warp = threadIdx.x >> 5;
     uint32_t mn = 0xffffffffu, mx = 0u;
     for (int d = dc; d <= l - 2; ++d) {
         const uint32_t n = rng[2 * (d - d0) + 1];
         const uint32_t *words = reinterpret_cast<const uint32_t *>(stage + (size_t)(d - d0) * slot);
-        // fan-out totals alternate between two arrays: a fast warp may publish
-        // the next level's total while a slow one still reads this level's
-        mn = 0xffffffffu;
-        mx = 0u;
-        sliced_expand<kFusedThreads, DIR>(words, nbase[d - d0], n, cur, nxt, wtot + (d & 1) * kFusedWarps, mn, mx);
+        const uint32_t nb = nbase[d - d0];
+        if (n <= kFusedSolo && d < l - 2) {
+            if (warp == 0) {
+                uint32_t a = 0, b = 0;
+                warp_expand<DIR>(words, nb, nb, nb + n, cur, nxt, 0u, a, b);
+            }
+            __syncwarp();
+        } else {
+            mn = 0xffffffffu;
+            mx = 0u;
+            sliced_expand<kFusedThreads, DIR>(words, nb, n, cur, nxt, wtot + (d & 1) * kFusedWarps, mn, mx);
+        }
         Coord *t = cur;
         cur = nxt;
         nxt = t;
     }
     __syncthreads();
-    // the other coordinate buffer (2 * cap words) is free: it becomes the
-    // output window of the segmented scatter
+    // Leaf stage: warp w takes the contiguous leaves [nl*w/NW, nl*(w+1)/NW)
+    // of the chunk (coordinates in cur, signatures in the staged leaf level),
+    // with its own output window carved from the free coordinate buffer.
     const uint32_t nl = rng[2 * (l - 1 - d0) + 1];
-    block_leaves<SR, DIR, VW, kFusedThreads>(stage + (size_t)(l - 1 - d0) * slot, nbase[l - 1 - d0], nl, cur, va,
-                                             reinterpret_cast<uint32_t *>(nxt), 2 * cap, red, true, mn, mx);
+    const uint32_t jb = (uint32_t)(((uint64_t)nl * warp) / kFusedWarps);
+    const uint32_t je = (uint32_t)(((uint64_t)nl * (warp + 1)) / kFusedWarps);
+    const uint8_t *lsig = stage + (size_t)(l - 1 - d0) * slot;
+    const uint32_t lnb = nbase[l - 1 - d0];
+    uint32_t wmn = 0xffffffffu, wmx = 0u;
+    for (uint32_t j = jb + (threadIdx.x & 31u); j < je; j += 32u) {
+        const Coord q = cur[j];
+        const uint32_t o = DIR == K2T_RIGHT ? q.r : q.c;
+        wmn = min(wmn, o);
+        wmx = max(wmx, o);
+    }
+    const uint32_t width = SR == K2T_BOOLEAN ? 1u : va.B;
+    uint32_t lo, span;
+    uint32_t *win = nullptr;
+    lo = 0u;
+    span = 0u;
+    if (2u * cap >= kFusedWarps * kWarpWindow)  // the free buffer holds every warp's window
+        win = warp_window_begin<SR>(wmn, wmx, 2u, width, reinterpret_cast<uint32_t *>(nxt) + warp * kWarpWindow,
+                                    lo, span);
+    warp_leaf_rounds<SR, DIR, VW>(jb, je, [&](uint32_t j, uint32_t &lam, uint32_t &r, uint32_t &c) {
+        const Coord q = cur[j];
+        r = 2u * q.r;
+        c = 2u * q.c;
+        lam = snib(lsig, lnb + j);
+    }, va, win, lo);
+    if (win) warp_window_flush<SR>(win, lo, span, width, va);
+    (void)mn;
+    (void)mx;
 }
 
 // Dynamic shared memory of fused_kernel for a tree.
@@ -1253,27 +1032,6 @@ void launch_fused(const k2t_tree *t, const DeviceState *d, const VecArgs &va, cu
     }
     fused_kernel<SR, DIR, VW><<<(unsigned)t->n_chunks, kFusedThreads, smem, st>>>(
         d->tree, d->chunks, t->chunk_stride, d->roots, t->opts.chunk_cap, va, d->err);
-}
-
-template <int SR, int DIR, int VW>
-void launch_leafgroup(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix, uint32_t leaf_base, uint32_t a,
-                      uint32_t count, uint32_t n_level, const Coord *src, const uint8_t *leaf, const VecArgs &va,
-                      uint32_t *status, cudaStream_t st)
-{
-    constexpr size_t smem = leafgroup_smem();
-    static int resident = 0;  // resident blocks per SM x SMs
-    if (!resident) {
-        cudaFuncSetAttribute(leafgroup_kernel<SR, DIR, VW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        int dev = 0, sms = 0, per = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, leafgroup_kernel<SR, DIR, VW>, kGroupBlock, smem);
-        resident = std::max(1, sms * std::max(1, per));
-    }
-    const uint32_t groups = (count + kGroupNodes - 1) / kGroupNodes;
-    const unsigned grid = (unsigned)std::min<uint32_t>(groups, (uint32_t)resident);
-    leafgroup_kernel<SR, DIR, VW><<<grid, kGroupBlock, smem, st>>>(sig, dir, prefix, leaf_base, a, count, n_level,
-                                                                     src, leaf, va, status);
 }
 
 template <int SR, int DIR, int VW>
