@@ -481,7 +481,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="rmat20")
+    ap.add_argument("--workload", default="rmat27")
     ap.add_argument("--engine", type=int, default=None)
     ap.add_argument("--products", default=None,
                     help="override the products of a step, e.g. 0:1,1:1 (direction:batch)")

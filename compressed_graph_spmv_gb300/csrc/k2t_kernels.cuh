@@ -561,27 +561,74 @@ __device__ __forceinline__ void warp_window_flush(const uint32_t *win, uint32_t 
 // 2x2 block.  For one vector slice (B = 1 fp32, or a Boolean word) both input
 // entries of the block are read with one 8-byte load together with the leaf
 // signature; updates go to the window when there is one, else to y.
+// One VW-wide vector slice k of one leaf (origin r, c; cells lam): gathers the
+// slice of the inputs it needs, combines per output, updates y or the window.
+template <int SR, int DIR, int VW>
+__device__ __forceinline__ void leaf_slice(uint32_t lam, uint32_t r, uint32_t c, uint32_t k, const VecArgs &va,
+                                           uint32_t *win, uint32_t lo)
+{
+    using S = Fp32Sem<SR>;
+    const uint32_t in = DIR == K2T_RIGHT ? c : r;
+    const uint32_t out = DIR == K2T_RIGHT ? r : c;
+    const bool a0 = lam & 1u;
+    const bool a1 = DIR == K2T_RIGHT ? (lam & 2u) : (lam & 4u);
+    const bool b0 = DIR == K2T_RIGHT ? (lam & 4u) : (lam & 2u);
+    const bool b1 = lam & 8u;
+    const float *x = static_cast<const float *>(va.x);
+    float *y = static_cast<float *>(va.y);
+    const size_t B = va.B;
+    float x0[VW], x1[VW];
+    if (a0 || b0) VecLoad<VW>::load(x + (size_t)in * B + k, x0);
+    if (a1 || b1) VecLoad<VW>::load(x + (size_t)(in + 1) * B + k, x1);
+    float v0[VW], v1[VW];
+#pragma unroll
+    for (int q = 0; q < VW; ++q) {
+        const float c0 = (a0 || b0) ? S::contrib(x0[q], va.w) : S::zero();
+        const float c1 = (a1 || b1) ? S::contrib(x1[q], va.w) : S::zero();
+        v0[q] = a0 ? (a1 ? S::plus(c0, c1) : c0) : c1;
+        v1[q] = b0 ? (b1 ? S::plus(c0, c1) : c0) : c1;
+    }
+    if (win) {
+#pragma unroll
+        for (int q = 0; q < VW; ++q) {
+            if ((a0 || a1) && !S::skip(v0[q])) smem_update<SR>(win + (size_t)(out - lo) * B + k + q, __float_as_uint(v0[q]));
+            if ((b0 || b1) && !S::skip(v1[q])) smem_update<SR>(win + (size_t)(out + 1 - lo) * B + k + q, __float_as_uint(v1[q]));
+        }
+    } else {
+        if (a0 || a1) S::update(y + (size_t)out * B + k, v0);
+        if (b0 || b1) S::update(y + (size_t)(out + 1) * B + k, v1);
+    }
+}
+
+// Leaves [jb, je) of a warp.  leaf_at(j, lam, r, c) gives leaf j's cells and
+// the origin of its 2x2 block.
+//  - One vector slice (B = 1 fp32, or a Boolean word): leaves dealt round-
+//    robin, kLeafU per lane per round; both input entries of a block come in
+//    one 8-byte load together with the leaf signature.
+//  - Batches (B > VW): G = B / VW adjacent lanes share a leaf, lane g owning
+//    the VW-wide slice g of every vector row, so a row of x is one coalesced
+//    load and a row of y one coalesced vector reduction (the pages' B
+//    adjacent threads per node, section 3.6).
+// Updates go to the window when there is one, else to y.
 template <int SR, int DIR, int VW, class LeafAt>
 __device__ __forceinline__ void warp_leaf_rounds(uint32_t jb, uint32_t je, LeafAt &&leaf_at, const VecArgs &va,
                                                  uint32_t *win, uint32_t lo)
 {
-    // one vector slice: four leaves in flight per lane; wider batches keep
-    // one leaf per lane (each leaf already loads B values per input)
-    constexpr int U = (SR == K2T_BOOLEAN || VW == 1) ? kLeafU : 1;
     const uint32_t lane = threadIdx.x & 31u;
-    const uint32_t *x = static_cast<const uint32_t *>(va.x);
-    const bool x8 = ((uintptr_t)x & 7u) == 0;
-    for (uint32_t j0 = jb; j0 < je; j0 += 32u * U) {
-        uint32_t lam[U], r[U], c[U];
+    if (SR == K2T_BOOLEAN || (VW == 1 && va.B == 1)) {
+        constexpr int U = kLeafU;
+        const uint32_t *x = static_cast<const uint32_t *>(va.x);
+        const bool x8 = ((uintptr_t)x & 7u) == 0;
+        for (uint32_t j0 = jb; j0 < je; j0 += 32u * U) {
+            uint32_t lam[U], r[U], c[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint32_t j = j0 + 32u * u + lane;
-            lam[u] = 0u;
-            r[u] = 0u;
-            c[u] = 0u;
-            if (j < je) leaf_at(j, lam[u], r[u], c[u]);
-        }
-        if (SR == K2T_BOOLEAN || (VW == 1 && va.B == 1)) {
+            for (int u = 0; u < U; ++u) {
+                const uint32_t j = j0 + 32u * u + lane;
+                lam[u] = 0u;
+                r[u] = 0u;
+                c[u] = 0u;
+                if (j < je) leaf_at(j, lam[u], r[u], c[u]);
+            }
             uint32_t xo[U][2], out[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
@@ -601,8 +648,32 @@ __device__ __forceinline__ void warp_leaf_rounds(uint32_t jb, uint32_t je, LeafA
                 }
             }
             leaf_apply1<SR, DIR, U>(lam, out, xo, va, win, lo);
-        } else {
-            leaf_group<SR, DIR, VW, U>(lam, r, c, va, win, lo);
+        }
+        return;
+    }
+    if constexpr (SR != K2T_BOOLEAN) {
+        constexpr int U = 2;
+        const uint32_t G = va.B / VW;                    // lanes per leaf (B is a multiple of VW)
+        const uint32_t per = G <= 32u ? 32u / G : 1u;    // leaves per lane-group round
+        const uint32_t groups = G <= 32u ? G : 32u;      // lanes that own a slice per round
+        const uint32_t slot = lane / groups, sub = lane % groups;
+        const bool active = slot < per;
+        for (uint32_t j0 = jb; j0 < je; j0 += per * U) {
+            uint32_t lam[U], r[U], c[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const uint32_t j = j0 + (uint32_t)u * per + slot;
+                lam[u] = 0u;
+                r[u] = 0u;
+                c[u] = 0u;
+                if (active && j < je) leaf_at(j, lam[u], r[u], c[u]);
+            }
+            // a group of G lanes covers the row; rows wider than 32 slices loop
+            for (uint32_t k = sub * VW; k < va.B; k += groups * VW) {
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (lam[u]) leaf_slice<SR, DIR, VW>(lam[u], r[u], c[u], k, va, win, lo);
+            }
         }
     }
 }
