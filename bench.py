@@ -475,6 +475,34 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_ceilings(args):
+    """Rates of the leaf step's memory patterns on this GPU (section 5.6 analogue)."""
+    import torch
+    from compressed_graph_spmv_gb300 import k2t as K
+    out = {"kind": "ceilings"}
+    rev = RawEvents()
+    sh = torch.cuda.current_stream().cuda_stream
+    for label, n in (("l2_resident_16MB", 1 << 22), ("hbm_2GB", 1 << 29)):
+        x = torch.rand(n, device="cuda")
+        y = torch.zeros(n, device="cuda")
+        res = {}
+        for kind, name, m in ((0, "copy_GBps", n), (1, "gather4_Gops", 1 << 28), (2, "gather8_Gops", 1 << 28),
+                              (3, "red_consecutive_Gops", 1 << 28), (4, "red_scattered_Gops", 1 << 28)):
+            for _ in range(2):
+                K.probe(kind, x, y, n, m)
+            e0, e1 = rev.create(), rev.create()
+            rev.record(e0, sh)
+            for _ in range(5):
+                K.probe(kind, x, y, n, m)
+            rev.record(e1, sh)
+            torch.cuda.synchronize()
+            ms = rev.ms(e0, e1) / 5
+            res[name] = (8.0 * n / (ms * 1e6)) if kind == 0 else (m / (ms * 1e6))
+        out[label] = res
+        del x, y
+    print(json.dumps(out))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -488,10 +516,13 @@ def main():
     ap.add_argument("--oracle-edges", type=int, default=1_500_000)
     ap.add_argument("--no-parity", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ceilings", action="store_true", help="measure the leaf step's memory ceilings and exit")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
-    if args.impl == "reference":
+    if args.ceilings:
+        run_ceilings(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

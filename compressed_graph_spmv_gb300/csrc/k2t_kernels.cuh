@@ -512,8 +512,14 @@ __device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint
 }
 
 // ---- per-warp leaf stage -------------------------------------------------------
-constexpr int kLeafU = 4;                 // leaves per lane per round
-constexpr uint32_t kWarpWindow = 256;     // words of a warp's output window
+#ifndef K2T_LEAF_U
+#define K2T_LEAF_U 8
+#endif
+#ifndef K2T_WARP_WINDOW
+#define K2T_WARP_WINDOW 256
+#endif
+constexpr int kLeafU = K2T_LEAF_U;                  // leaves per lane per round (one vector slice)
+constexpr uint32_t kWarpWindow = K2T_WARP_WINDOW;   // words of a warp's output window
 
 // Per-warp segmented scatter.  [mn, mx] bounds the warp's output coordinates
 // in units of `unit` cells (4 for nodes of the last internal level, 2 for

@@ -30,7 +30,7 @@ EXPORTED = ["k2t_default_opts", "k2t_build", "k2t_workspace_bytes", "k2t_upload"
             "k2t_spmv_marked",
             "k2t_spmv_host", "k2t_stats_get", "k2t_level_signatures", "k2t_device_level",
             "k2t_decode", "k2t_free", "k2t_strerror", "k2t_last_cuda_error",
-            "k2t_spmv_noalloc", "k2t_noalloc_scratch_limit"]
+            "k2t_spmv_noalloc", "k2t_noalloc_scratch_limit", "k2t_probe"]
 
 
 class Opts(ctypes.Structure):
@@ -88,6 +88,8 @@ def load() -> ctypes.CDLL:
         lib.k2t_spmv_noalloc.restype = ctypes.c_int
         lib.k2t_noalloc_scratch_limit.argtypes = []
         lib.k2t_noalloc_scratch_limit.restype = U64
+        lib.k2t_probe.argtypes = [I32, P, P, U64, U64, P]
+        lib.k2t_probe.restype = ctypes.c_int
         lib.k2t_spmv_host.argtypes = [P, I32, I32, ctypes.c_float, P, P, U32, P]
         lib.k2t_stats_get.argtypes = [P, ctypes.POINTER(Stats)]
         lib.k2t_level_signatures.argtypes = [P, U32, P, U64, ctypes.POINTER(U64)]
@@ -255,6 +257,12 @@ class Tree:
         _check("k2t_decode", lib.k2t_decode(self._h, r.ctypes.data if r.size else None,
                                             c.ctypes.data if c.size else None, r.size, ctypes.byref(n)))
         return r, c
+
+
+def probe(kind: int, x, y, n: int, m: int, stream=None):
+    """One pass of a memory-system ceiling probe (see k2t_probe in include/k2t.h)."""
+    _check("k2t_probe", load().k2t_probe(kind, _dev_ptr(x) if x is not None else None, _dev_ptr(y), n, m,
+                                         _stream_ptr(stream)))
 
 
 @dataclass

@@ -207,6 +207,17 @@ int k2t_spmv_noalloc(k2t_tree *t, int32_t dir, int32_t semiring, float w,
 /* Size in bytes of the device array k2t_spmv_noalloc works in. */
 uint64_t k2t_noalloc_scratch_limit(void);
 
+/* Memory-system ceilings for the leaf step's access patterns (the
+ * microbenchmark of section 5.6, re-measured on this device; instrumentation,
+ * not part of a product).  Launches one pass on `stream`; the caller times it.
+ *   kind 0: copy n floats x -> y (n a multiple of 4)
+ *   kind 1: m scattered 4-byte gathers from x[0..n)
+ *   kind 2: m scattered 8-byte gathers (adjacent pairs) from x[0..n)
+ *   kind 3: m consecutive reductions y[i mod n] += 1
+ *   kind 4: m scattered reductions y[h(i) mod n] += 1 (h a fixed hash)
+ * n must be a power of two for kinds 1-4.  Errors: EINVAL, ECUDA. */
+int k2t_probe(int32_t kind, const void *x, void *y, uint64_t n, uint64_t m, void *stream);
+
 /* Shape, per-level sizes and the device footprint broken down by part. */
 int k2t_stats_get(const k2t_tree *t, k2t_stats *s);
 
