@@ -304,7 +304,7 @@ def run_ours(args):
     opts = dict(wopts, host_vectors=1, max_batch=max_b)
     if args.engine is not None:
         opts["engine"] = args.engine
-        opts["cache_last_internal"] = int(args.engine == 3)
+        opts["cache_last_internal"] = int(args.engine in (3, 4))
     t_build = time.perf_counter()
     tree = K.Tree(wl.rows, wl.cols, wl.n_rows, wl.n_cols, **opts)
     t_build = time.perf_counter() - t_build
@@ -454,7 +454,7 @@ def run_ours(args):
            "warmup": args.warmup, "ms_per_step": float(step_ms.mean()), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": dtype_name(wl), "data": "synthetic",
            "config": {"workload": wl.name, "nnz": m, "n": wl.n_rows, "levels": int(st.levels), "d0": int(st.d0),
-                      "engine": ["auto", "fused", "levelsync", "cached"][int(st.engine)],
+                      "engine": ["auto", "fused", "levelsync", "cached", "banded"][int(st.engine)],
                       "products": [list(p) for p in products],
                       "l2": "flushed between steps" if flush is not None else "inputs larger than L2",
                       "parallelism": "replicas" if world > 1 else "single"},

@@ -216,7 +216,10 @@ int k2t_upload(k2t_tree *t, void *arena, uint64_t arena_bytes, void *stream)
         return cudaMemcpyAsync(at<char>(d->arena, off), src, bytes, cudaMemcpyHostToDevice, st);
     };
     if (L.top_bytes) { d->top = at<Coord>(d->arena, L.top_off); if ((e = put(L.top_off, L.top_bytes, t->top.data()))) return fail(e); }
-    if (L.cached_bytes) { d->cached = at<Coord>(d->arena, L.cached_off); if ((e = put(L.cached_off, L.cached_bytes, t->cached.data()))) return fail(e); }
+    if (L.cached_bytes) { d->cached = at<Coord>(d->arena, L.cached_off); if ((e = put(L.cached_off, t->cached.size() * sizeof(Coord), t->cached.data()))) return fail(e); }
+    if (L.bleaf_bytes) { d->bleaf = at<uint32_t>(d->arena, L.bleaf_off); if ((e = put(L.bleaf_off, t->bleaf.size() * 4, t->bleaf.data()))) return fail(e); }
+    if (L.bsig_bytes) { d->bsig = at<uint8_t>(d->arena, L.bsig_off); if ((e = put(L.bsig_off, (t->nodes[(size_t)t->levels - 2] + 1) / 2, t->bsig.data()))) return fail(e); }
+    if (L.bchunk_bytes) { d->bchunks = at<uint32_t>(d->arena, L.bchunk_off); if ((e = put(L.bchunk_off, L.bchunk_bytes, t->bchunks.data()))) return fail(e); }
     if (L.chunk_bytes) { d->chunks = at<uint32_t>(d->arena, L.chunk_off); if ((e = put(L.chunk_off, L.chunk_bytes, t->chunks.data()))) return fail(e); }
     if (L.root_bytes) { d->roots = at<Coord>(d->arena, L.root_off); if ((e = put(L.root_off, L.root_bytes, t->roots.data()))) return fail(e); }
     if (L.scan_bytes) {

@@ -352,6 +352,80 @@ struct LsPlanner {
     }
 };
 
+// BANDED: regroup the last internal level into 2-D tiles of band_rows rows by
+// band_cols columns, tiles ordered column band first (all row bands of one
+// column band, then the next), level order inside a tile; each node keeps its
+// first leaf and signature.  Thread blocks take tiles (cut into blocks of at
+// most kBandChunkNodes nodes) in that order, so the blocks running at the same
+// time share one column band of x (L2-resident) while each keeps its row band
+// of y in shared memory.
+void plan_bands(k2t_tree *t, int nt)
+{
+    const int d = t->levels - 2;
+    const uint64_t n = t->nodes[(size_t)d];
+    uint32_t shift = 0, cshift = 0;
+    while ((4u << shift) < t->opts.band_rows) ++shift;   // a node covers 4 rows
+    while ((4ull << cshift) < t->opts.band_cols) ++cshift;
+    t->band_shift = shift;
+    const uint64_t nrb = ((t->n_rows + 3) / 4 >> shift) + 1;
+    const uint64_t ncb = ((t->n_cols + 3) / 4 >> cshift) + 1;
+    const uint64_t ntiles = nrb * ncb;
+    auto tile_of = [&](const Coord &p) -> uint64_t { return (uint64_t)(p.c >> cshift) * nrb + (p.r >> shift); };
+    // first leaf of every node (level order): directory sample + popcount
+    std::vector<uint32_t> off(n);
+    parallel_for(nt, [&](int th) {
+        uint64_t lo = n * th / nt, hi = n * (th + 1) / nt;
+        if (lo >= hi) return;
+        uint64_t o = level_offset(t, d, lo);
+        for (uint64_t i = lo; i < hi; ++i) {
+            off[i] = (uint32_t)o;
+            o += (uint64_t)__builtin_popcount(level_sig(t, d, i));
+        }
+    });
+    // stable counting sort by tile
+    std::vector<uint64_t> cnt((size_t)nt * ntiles, 0);
+    parallel_for(nt, [&](int th) {
+        uint64_t lo = n * th / nt, hi = n * (th + 1) / nt;
+        uint64_t *c = &cnt[(size_t)th * ntiles];
+        for (uint64_t i = lo; i < hi; ++i) c[tile_of(t->cached[i])]++;
+    });
+    std::vector<uint64_t> tile_start(ntiles + 1, 0);
+    uint64_t run = 0;
+    for (uint64_t b = 0; b < ntiles; ++b) {
+        tile_start[b] = run;
+        for (int th = 0; th < nt; ++th) {
+            uint64_t c = cnt[(size_t)th * ntiles + b];
+            cnt[(size_t)th * ntiles + b] = run;
+            run += c;
+        }
+    }
+    tile_start[ntiles] = run;
+    std::vector<Coord> bc(n);
+    t->bleaf.assign(n, 0);
+    std::vector<uint8_t> sg(n);
+    parallel_for(nt, [&](int th) {
+        uint64_t lo = n * th / nt, hi = n * (th + 1) / nt;
+        uint64_t *c = &cnt[(size_t)th * ntiles];
+        for (uint64_t i = lo; i < hi; ++i) {
+            uint64_t dst = c[tile_of(t->cached[i])]++;
+            bc[dst] = t->cached[i];
+            t->bleaf[dst] = off[i];
+            sg[dst] = (uint8_t)level_sig(t, d, i);
+        }
+    });
+    t->cached.swap(bc);
+    t->bsig.assign((n + 15) / 16 + 1, 0);
+    for (uint64_t i = 0; i < n; ++i) t->bsig[i / 16] |= (uint64_t)sg[i] << (4 * (i % 16));
+    t->bchunks.clear();
+    for (uint64_t b = 0; b < ntiles; ++b)
+        for (uint64_t s0 = tile_start[b]; s0 < tile_start[b + 1]; s0 += kBandChunkNodes) {
+            uint64_t e = std::min<uint64_t>(tile_start[b + 1], s0 + kBandChunkNodes);
+            t->bchunks.push_back((uint32_t)(b % nrb));  // row band
+            t->bchunks.push_back((uint32_t)s0);
+            t->bchunks.push_back((uint32_t)(e - s0));
+        }
+}
+
 }  // namespace
 
 void compute_layout(k2t_tree *t)
@@ -367,19 +441,21 @@ void compute_layout(k2t_tree *t)
     const int l = t->levels;
     const bool fused = t->engine == K2T_ENGINE_FUSED;
     const bool ls = t->engine == K2T_ENGINE_LEVELSYNC;
-    const bool cached = t->engine == K2T_ENGINE_CACHED;
+    const bool banded = t->engine == K2T_ENGINE_BANDED;
+    const bool cached = t->engine == K2T_ENGINE_CACHED || banded;
     L.err_bytes = 64;
     L.err_off = take(L.err_bytes);
     if (!t->empty) {
         int first = cached ? l - 2 : t->d0;
         for (int d = first; d < l; ++d) {
+            if (banded && d == l - 2) continue;  // signatures are kept in band order
             // nibble bytes plus 16 bytes of slack for vector loads
             L.sig_bytes[d] = (t->nodes[(size_t)d] + 1) / 2 + 16;
             L.sig_off[d] = take(L.sig_bytes[d]);
         }
         bool want_dir = (ls && t->opts.offsets == K2T_OFFSETS_DIRECTORY);
         for (int d = t->d0; d <= l - 2; ++d) {
-            bool need = want_dir || (cached && d == l - 2);
+            bool need = want_dir || (cached && !banded && d == l - 2);
             if (!need) continue;
             L.dir_bytes[d] = t->dir[(size_t)(d - t->d0)].size() * sizeof(uint32_t);
             L.dir_off[d] = take(L.dir_bytes[d]);
@@ -391,6 +467,14 @@ void compute_layout(k2t_tree *t)
         if (cached) {
             L.cached_bytes = t->cached.size() * sizeof(Coord) + 16;
             L.cached_off = take(L.cached_bytes);
+        }
+        if (banded) {
+            L.bleaf_bytes = t->bleaf.size() * sizeof(uint32_t) + 16;
+            L.bleaf_off = take(L.bleaf_bytes);
+            L.bsig_bytes = (t->nodes[(size_t)l - 2] + 1) / 2 + 16;
+            L.bsig_off = take(L.bsig_bytes);
+            L.bchunk_bytes = t->bchunks.size() * sizeof(uint32_t);
+            L.bchunk_off = take(L.bchunk_bytes);
         }
         if (fused) {
             L.chunk_bytes = t->chunks.size() * sizeof(uint32_t);
@@ -445,6 +529,8 @@ void k2t_default_opts(k2t_opts *o)
     o->host_vectors = 0;
     o->use_graph = 1;
     o->threads = 0;
+    o->band_rows = 4096;
+    o->band_cols = 1u << 23;
 }
 
 int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
@@ -456,13 +542,16 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
     if (nnz && (!rows || !cols)) return K2T_EINVAL;
     k2t_opts o;
     if (opts) o = *opts; else k2t_default_opts(&o);
-    if (o.engine > K2T_ENGINE_CACHED || o.offsets > K2T_OFFSETS_SCAN) return K2T_EINVAL;
+    if (o.engine > K2T_ENGINE_BANDED || o.offsets > K2T_OFFSETS_SCAN) return K2T_EINVAL;
+    if (o.band_rows < 16 || o.band_rows > 65536 || (o.band_rows & (o.band_rows - 1))) return K2T_EINVAL;
+    if (o.band_cols && (o.band_cols < 16 || (o.band_cols & (o.band_cols - 1)))) return K2T_EINVAL;
+    if (!o.band_cols) o.band_cols = 1u << 31;
     if (o.chunk_cap < 4 || o.chunk_cap > kMaxChunkCap || o.tile_m < 4) return K2T_EINVAL;
     if (o.max_batch < 1 || o.max_batch > K2T_MAX_BATCH) return K2T_ERANGE;
     if (o.host_top_max_nodes < 1) return K2T_EINVAL;
     if (o.n_k4_levels > 15) return K2T_EINVAL;
     if (n_rows > (1ull << 32) || n_cols > (1ull << 32)) return K2T_ERANGE;
-    if (o.engine == K2T_ENGINE_CACHED && !o.cache_last_internal) return K2T_EINVAL;
+    if ((o.engine == K2T_ENGINE_CACHED || o.engine == K2T_ENGINE_BANDED) && !o.cache_last_internal) return K2T_EINVAL;
 
     k2t_tree *t = new (std::nothrow) k2t_tree;
     if (!t) return K2T_ENOMEM;
@@ -529,7 +618,7 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
                 if (nn >= (1ull << 32)) { delete t; return K2T_ERANGE; }
                 t->nodes[(size_t)d] = nn;
                 pack_level(t, d, sg.data(), nn, nt);
-                if (d == l - 2 && t->engine == K2T_ENGINE_CACHED) {
+                if (d == l - 2 && (t->engine == K2T_ENGINE_CACHED || t->engine == K2T_ENGINE_BANDED)) {
                     t->cached.resize(nn);
                     parallel_for(nt, [&](int th) {
                         size_t lo = nn * th / nt, hi = nn * (th + 1) / nt;
@@ -552,6 +641,7 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
         if (!t->empty) {
             t->dir.assign((size_t)(l - 1 - t->d0), std::vector<uint32_t>());
             for (int d = t->d0; d <= l - 2; ++d) build_directory(t, d, nt);
+            if (t->engine == K2T_ENGINE_BANDED) plan_bands(t, nt);
             if (t->engine == K2T_ENGINE_FUSED) {
                 t->chunk_stride = 2 + 2 * (uint32_t)(l - t->d0);
                 t->roots = t->top;
@@ -650,8 +740,9 @@ int k2t_stats_get(const k2t_tree *t, k2t_stats *s)
     s->l_bytes_device = L.sig_bytes[t->levels - 1];
     for (int d = 0; d < t->levels; ++d) s->dir_bytes += L.dir_bytes[d];
     s->top_bytes = L.top_bytes;
-    s->cached_bytes = L.cached_bytes;
-    s->plan_bytes = L.chunk_bytes + L.root_bytes;
+    s->cached_bytes = L.cached_bytes + L.bleaf_bytes + L.bsig_bytes;
+    s->plan_bytes = 0;
+    s->plan_bytes = L.chunk_bytes + L.root_bytes + L.bchunk_bytes;
     uint64_t nbuf = 0;
     for (int d = 0; d < t->levels; ++d) nbuf += L.buf_off[d] ? 1 : 0;
     s->scratch_bytes = nbuf * L.buf_bytes + L.scan_bytes;

@@ -12,6 +12,7 @@ namespace k2t {
 constexpr uint32_t kDirS = 256;        // directory sample period (section 3.2: S = 256)
 constexpr uint32_t kMaxChunkCap = 4096;
 constexpr uint32_t kArenaAlign = 256;
+constexpr uint32_t kBandChunkNodes = 16384;  // BANDED: nodes per thread block at most
 
 // Coordinates of a node's block, in units of the block side at its level.
 // A frontier entry: (row, col) instead of the pages' Morton code; the two
@@ -41,6 +42,9 @@ struct ArenaLayout {
     uint64_t top_off, top_bytes;
     uint64_t cached_off, cached_bytes;
     uint64_t chunk_off, chunk_bytes;
+    uint64_t bleaf_off, bleaf_bytes;    // BANDED: first leaf of each band-ordered node
+    uint64_t bsig_off, bsig_bytes;      // BANDED: signatures in band order
+    uint64_t bchunk_off, bchunk_bytes;  // BANDED: (band, first node, node count) per block
     uint64_t root_off, root_bytes;
     uint64_t buf_off[K2T_MAX_LEVELS];   // LEVELSYNC frontier buffers (levels d0+1..l-2)
     uint64_t buf_bytes;                 // per buffer
@@ -67,7 +71,12 @@ struct k2t_tree {
     std::vector<std::vector<uint64_t>> sig;
     std::vector<std::vector<uint32_t>> dir;       // index d - d0, levels d0..l-2
     std::vector<k2t::Coord> top;                  // level d0
-    std::vector<k2t::Coord> cached;               // level l-2 (k^2+F)
+    std::vector<k2t::Coord> cached;               // level l-2 (k^2+F; banded: in band order)
+    // BANDED: level l-2 regrouped by row band
+    std::vector<uint32_t> bleaf;                  // first leaf of each node
+    std::vector<uint64_t> bsig;                   // signatures, 16 nibbles per word
+    std::vector<uint32_t> bchunks;                // per block: band, first node, count
+    uint32_t band_shift = 0;                      // band of a node = node row >> band_shift
     // FUSED plan: per chunk, [root index, d_c, (start, count) for levels d0..l-1]
     std::vector<uint32_t> chunks;
     uint32_t chunk_stride = 0;

@@ -753,6 +753,98 @@ cached_block_kernel(const uint8_t *sig, const uint32_t *dir, uint32_t n, const C
     if (win) warp_window_flush<SR>(win, lo, span, width, va);
 }
 
+// BANDED engine: the cached last internal level grouped by row band (band_rows
+// rows each; level order inside a band), one thread block per block of at most
+// kBandChunkNodes nodes of one band.  Warps take 256-node tiles: coordinates,
+// first leaves and signatures are read coalesced, a warp scan turns a tile
+// into a leaf list (node, quadrant, rank) in shared memory, and the lanes take
+// the leaves round-robin.
+//  - Right products: every output row of the block lies in its band, so the
+//    block reduces y in a shared-memory window over the band (semiring shared
+//    atomics) and adds each touched row to y once, consecutively.  The only
+//    scattered access left per leaf is the gather of x.
+//  - Left products: the inputs are the band's rows, a small contiguous slice
+//    of x that stays in L1; the outputs (columns) are reduced straight into y.
+constexpr int kBandWarps = 8;
+constexpr uint32_t kBandWindow = 8192;  // words of the block's window
+constexpr size_t kBandSmem = kBandWindow * 4 + kBandWarps * kDirS * (8 + 4 + 8);
+
+template <int SR, int DIR, int VW>
+__global__ void __launch_bounds__(32 * kBandWarps)
+banded_kernel(const uint32_t *chunks, const Coord *coords, const uint32_t *bleaf, const uint8_t *bsig,
+              const uint8_t *leaf, uint32_t band_rows, VecArgs va)
+{
+    // one dynamic buffer (more than 48 KB: opted in at launch)
+    extern __shared__ __align__(16) uint8_t bsm[];
+    uint32_t *win = reinterpret_cast<uint32_t *>(bsm);
+    Coord (*cs)[kDirS] = reinterpret_cast<Coord (*)[kDirS]>(bsm + kBandWindow * 4);
+    uint32_t (*lf)[kDirS] = reinterpret_cast<uint32_t (*)[kDirS]>(bsm + kBandWindow * 4 + kBandWarps * kDirS * 8);
+    uint16_t (*slots)[4 * kDirS] =
+        reinterpret_cast<uint16_t (*)[4 * kDirS]>(bsm + kBandWindow * 4 + kBandWarps * kDirS * 12);
+    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+    const uint32_t band = chunks[3 * blockIdx.x], s0 = chunks[3 * blockIdx.x + 1], cnt = chunks[3 * blockIdx.x + 2];
+    const uint32_t width = SR == K2T_BOOLEAN ? 1u : va.B;
+    const uint64_t band_lo = (uint64_t)band * band_rows;
+    const uint64_t band_hi = min(band_lo + band_rows, (uint64_t)va.n_out);
+    const bool windowed = DIR == K2T_RIGHT && band_hi > band_lo && (band_hi - band_lo) * width <= kBandWindow;
+    const uint32_t words = windowed ? (uint32_t)((band_hi - band_lo) * width) : 0u;
+    if (windowed) {
+        for (uint32_t i = threadIdx.x; i < words; i += 32u * kBandWarps) win[i] = zero_word<SR>();
+        __syncthreads();
+    }
+    Coord *cw = cs[warp];
+    uint32_t *lw = lf[warp];
+    uint16_t *sl = slots[warp];
+    for (uint32_t t0 = 256u * warp; t0 < cnt; t0 += 256u * kBandWarps) {
+        const uint32_t tn = min(cnt - t0, 256u);
+        const uint32_t base = s0 + t0;
+        uint32_t w = 0;
+#pragma unroll
+        for (uint32_t k = 0; k < 8; ++k) {
+            const uint32_t i = 8u * lane + k;
+            if (i < tn) w |= nibble_at(bsig, base + i) << (4u * k);
+        }
+#pragma unroll
+        for (uint32_t q = 0; q < kDirS / 32; ++q) {
+            const uint32_t i = 32u * q + lane;
+            if (i < tn) {
+                cw[i] = coords[base + i];
+                lw[i] = bleaf[base + i];
+            }
+        }
+        const uint32_t f = (uint32_t)__popc(w);
+        const uint32_t incl = warp_incl_scan(f);
+        const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+        uint32_t pos = incl - f;
+#pragma unroll
+        for (uint32_t k = 0; k < 8; ++k) {
+            const uint32_t sg = (w >> (4u * k)) & 15u;
+            uint32_t rank = 0;
+#pragma unroll
+            for (uint32_t b = 0; b < 4; ++b)
+                if (sg & (1u << b)) sl[pos++] = (uint16_t)(((8u * lane + k) << 4) | (b << 2) | rank++);
+        }
+        __syncwarp();
+        warp_leaf_rounds<SR, DIR, VW>(0u, total, [&](uint32_t j, uint32_t &lam, uint32_t &r, uint32_t &c) {
+            const uint32_t e = sl[j];
+            const uint32_t node = e >> 4, b = (e >> 2) & 3u;
+            const Coord p = cw[node];
+            r = 4u * p.r + 2u * (b >> 1);
+            c = 4u * p.c + 2u * (b & 1u);
+            lam = nibble_at(leaf, lw[node] + (e & 3u));
+        }, va, windowed ? win : nullptr, (uint32_t)band_lo);
+        __syncwarp();
+    }
+    if (windowed) {
+        __syncthreads();
+        uint32_t *y = static_cast<uint32_t *>(va.y) + band_lo * width;
+        for (uint32_t i = threadIdx.x; i < words; i += 32u * kBandWarps) {
+            const uint32_t v = win[i];
+            if (!is_noop_word<SR>(v)) global_update_word<SR>(y + i, v);
+        }
+    }
+}
+
 // ---- shared-memory staging with the bulk-copy (TMA) engine ------------------
 // One thread arms an mbarrier with the total byte count and issues one
 // cp.async.bulk per contiguous range; every thread then waits on the barrier.
@@ -1078,6 +1170,9 @@ struct DeviceState {
     const Coord *cached = nullptr;
     const uint32_t *chunks = nullptr;
     const Coord *roots = nullptr;
+    const uint32_t *bchunks = nullptr;
+    const uint32_t *bleaf = nullptr;
+    const uint8_t *bsig = nullptr;
     Coord *buf[K2T_MAX_LEVELS] = {};
     uint32_t *scan_sums = nullptr;
     uint32_t *scan_prefix = nullptr;
@@ -1131,6 +1226,21 @@ void launch_cached(const k2t_tree *t, const DeviceState *d, const VecArgs &va, c
 }
 
 template <int SR, int DIR, int VW>
+void launch_banded(const k2t_tree *t, const DeviceState *d, const VecArgs &va, cudaStream_t st)
+{
+    const int l = t->levels;
+    const unsigned grid = (unsigned)(t->bchunks.size() / 3);
+    if (!grid) return;
+    static bool configured = false;
+    if (!configured) {
+        cudaFuncSetAttribute(banded_kernel<SR, DIR, VW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBandSmem);
+        configured = true;
+    }
+    banded_kernel<SR, DIR, VW><<<grid, 32 * kBandWarps, kBandSmem, st>>>(d->bchunks, d->cached, d->bleaf, d->bsig,
+                                                                          d->tree.lv[l - 1].sig, t->opts.band_rows, va);
+}
+
+template <int SR, int DIR, int VW>
 void launch_ls(const k2t_tree *t, const DeviceState *d, const VecArgs &va, cudaStream_t st)
 {
     const bool scan = t->opts.offsets == K2T_OFFSETS_SCAN;
@@ -1167,6 +1277,7 @@ LaunchFn pick_engine(uint32_t engine)
     switch (engine) {
     case K2T_ENGINE_FUSED: return launch_fused<SR, DIR, VW>;
     case K2T_ENGINE_CACHED: return launch_cached<SR, DIR, VW>;
+    case K2T_ENGINE_BANDED: return launch_banded<SR, DIR, VW>;
     default: return launch_ls<SR, DIR, VW>;
     }
 }

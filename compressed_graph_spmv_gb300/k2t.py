@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libk2t.so")
 
 RIGHT, LEFT = 0, 1
 PLUS_TIMES, BOOLEAN, MIN_PLUS = 0, 1, 2
-ENGINE_AUTO, ENGINE_FUSED, ENGINE_LEVELSYNC, ENGINE_CACHED = 0, 1, 2, 3
+ENGINE_AUTO, ENGINE_FUSED, ENGINE_LEVELSYNC, ENGINE_CACHED, ENGINE_BANDED = 0, 1, 2, 3, 4
 OFFSETS_DIRECTORY, OFFSETS_SCAN = 0, 1
 MAX_LEVELS = 33
 MAX_BATCH = 32
@@ -39,7 +39,8 @@ class Opts(ctypes.Structure):
                 ("host_top_max_nodes", ctypes.c_uint32), ("chunk_cap", ctypes.c_uint32),
                 ("tile_m", ctypes.c_uint64), ("max_batch", ctypes.c_uint32),
                 ("host_vectors", ctypes.c_uint32), ("use_graph", ctypes.c_uint32),
-                ("threads", ctypes.c_uint32), ("reserved", ctypes.c_uint32 * 8)]
+                ("threads", ctypes.c_uint32), ("band_rows", ctypes.c_uint32),
+                ("band_cols", ctypes.c_uint32), ("reserved", ctypes.c_uint32 * 6)]
 
 
 class Stats(ctypes.Structure):

@@ -68,6 +68,12 @@ typedef struct k2t_tree k2t_tree;
                                    buffers of at most tile_M codes (section 3.4)      */
 #define K2T_ENGINE_CACHED    3  /* k^2+F: one leaf kernel over the cached
                                    coordinates of the last internal level (3.5)       */
+#define K2T_ENGINE_BANDED    4  /* k^2+F ordered by row band: the cached level is
+                                   kept grouped by bands of band_rows rows, so a
+                                   thread block owns a band and keeps its part of
+                                   y (right product) or x (left product) in
+                                   shared memory: one scattered access per edge
+                                   instead of two                                    */
 
 /* ChildOffset source (section 3.2), used by the LEVELSYNC engine. */
 #define K2T_OFFSETS_DIRECTORY 0 /* one sample per 256 nodes, stored with the tree  */
@@ -93,7 +99,10 @@ typedef struct {
                                      vectors for k2t_spmv_host                                      */
     uint32_t use_graph;           /* LEVELSYNC: record a product's launches once as a CUDA graph   */
     uint32_t threads;             /* host threads for k2t_build; 0 = all cores                     */
-    uint32_t reserved[8];
+    uint32_t band_rows;           /* BANDED: rows per band (power of two, 16..65536); default 4096 */
+    uint32_t band_cols;           /* BANDED: columns per tile (power of two >= 16); default 2^23;
+                                     0 = one column band                                             */
+    uint32_t reserved[6];
 } k2t_opts;
 
 /* ---- statistics -------------------------------------------------------- */
@@ -110,7 +119,8 @@ typedef struct {
     uint64_t l_bytes_device;      /* leaf signature bytes on device                */
     uint64_t dir_bytes;           /* directory samples on device                   */
     uint64_t top_bytes;           /* coordinates of level d0 on device             */
-    uint64_t cached_bytes;        /* cached coordinates of level l-2 (k^2+F)       */
+    uint64_t cached_bytes;        /* cached coordinates of level l-2 (k^2+F; banded:
+                                     coordinates, first-leaf offsets, signatures)  */
     uint64_t plan_bytes;          /* chunk table / root coordinates (FUSED)        */
     uint64_t scratch_bytes;       /* frontier buffers and scan space (LEVELSYNC)   */
     uint64_t vector_bytes;        /* device x and y for k2t_spmv_host              */

@@ -24,6 +24,8 @@ ENGINES = [
     dict(engine=2, offsets=1, tile_m=16),              # level-sync, scan
     dict(engine=2, offsets=0, tile_m=1 << 20, use_graph=0),
     dict(engine=3, cache_last_internal=1),             # k^2+F
+    dict(engine=4, cache_last_internal=1),             # k^2+F by row band
+    dict(engine=4, cache_last_internal=1, band_rows=16),
 ]
 
 
@@ -110,7 +112,7 @@ def test_rmat_medium_all_semirings():
     rows, cols = synth.rmat(17, 0.57, 0.19, 0.19, 1 << 20, 12)
     n = 1 << 17
     rng = np.random.default_rng(12)
-    for kw in (ENGINES[0], ENGINES[2], ENGINES[3], ENGINES[5]):
+    for kw in (ENGINES[0], ENGINES[2], ENGINES[3], ENGINES[5], ENGINES[6]):
         t = _tree(rows, cols, n, n, **kw)
         for semiring, B in ((PLUS_TIMES, 1), (PLUS_TIMES, 16), (BOOLEAN, 32), (TROPICAL, 8)):
             for d in (RIGHT, LEFT):
@@ -146,7 +148,8 @@ def test_host_buffer_product():
 def test_footprint_equals_prediction():
     import torch
     rows, cols = synth.rmat(18, 0.57, 0.19, 0.19, 4 << 20, 14)
-    for kw in (dict(engine=1), dict(engine=3, cache_last_internal=1), dict(engine=2, tile_m=1 << 16)):
+    for kw in (dict(engine=1), dict(engine=3, cache_last_internal=1), dict(engine=2, tile_m=1 << 16),
+               dict(engine=4, cache_last_internal=1)):
         t = K.Tree(rows, cols, 1 << 18, 1 << 18, **kw)
         ws = t.workspace_bytes()
         torch.cuda.synchronize()

@@ -118,10 +118,10 @@ def _layout_parts(s):
             s.plan_bytes + s.scratch_bytes + s.vector_bytes)
 
 
-@pytest.mark.parametrize("engine", [1, 2, 3])
+@pytest.mark.parametrize("engine", [1, 2, 3, 4])
 def test_workspace_accounting(engine):
     rows, cols = synth.rmat(12, 0.57, 0.19, 0.19, 30000, 4)
-    t = K.Tree(rows, cols, 4096, 4096, engine=engine, cache_last_internal=int(engine == 3),
+    t = K.Tree(rows, cols, 4096, 4096, engine=engine, cache_last_internal=int(engine >= 3),
                host_vectors=1, max_batch=4, tile_m=4096, chunk_cap=512, host_top_max_nodes=64)
     s = t.stats()
     ws = t.workspace_bytes()
@@ -138,6 +138,28 @@ def test_workspace_accounting(engine):
         assert s.n_steps > 1 and s.scratch_bytes > 0
     if engine == 3:
         assert s.cached_bytes == 8 * s.level_nodes[s.levels - 2] + 16
+    if engine == 4:
+        n2 = s.level_nodes[s.levels - 2]
+        assert s.cached_bytes == (8 * n2 + 16) + (4 * n2 + 16) + ((n2 + 1) // 2 + 16)
+
+
+def test_options_struct_matches_header():
+    """The binding's k2t_opts mirrors the header: defaults round-trip."""
+    o = K.default_opts()
+    assert o.band_rows == 4096 and o.chunk_cap == 2048 and o.tile_m == 1 << 20 and o.max_batch == 32
+    assert ctypes.sizeof(K.Opts) == 80  # 6 x u32, u64, 5 x u32, 7 reserved
+    with pytest.raises(K.K2TError):
+        K.Tree(np.zeros(1, np.uint32), np.zeros(1, np.uint32), 8, 8, engine=4, cache_last_internal=1,
+               band_rows=100)
+
+
+def test_banded_layout():
+    rows, cols = synth.rmat(12, 0.57, 0.19, 0.19, 30000, 8)
+    a = K.Tree(rows, cols, 4096, 4096, engine=4, cache_last_internal=1, band_rows=64)
+    b = K.Tree(rows, cols, 4096, 4096, engine=3, cache_last_internal=1)
+    sa, sb = a.stats(), b.stats()
+    assert sa.engine == 4 and sb.engine == 3
+    assert sa.plan_bytes > 0 and sa.level_nodes[sa.levels - 2] == sb.level_nodes[sb.levels - 2]
 
 
 def test_chunk_plan_covers_every_node():
