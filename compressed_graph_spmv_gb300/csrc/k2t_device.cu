@@ -24,6 +24,8 @@
 // block side of its level, rather than the pages' 64-bit Morton code: the
 // same information, one shift-or per coordinate per level, and nothing to
 // deinterleave at the leaves.
+#include <algorithm>
+
 #include "k2t_kernels.cuh"
 
 namespace k2t {
@@ -104,6 +106,59 @@ __global__ void __launch_bounds__(1024) ls_scan_kernel(const uint32_t *sums, uin
     // prefix[nblocks] = the tile's total (every thread whose run ends there
     // holds the same value)
     if (i1 == nblocks) prefix[nblocks] = run;
+}
+
+// Multi-source search, one level: new = y & ~visited (bits of the batch);
+// visited |= new; frontier = new; dist[v][b] = level for every new bit b;
+// the number of vertices with a new bit is added to *count.
+__global__ void __launch_bounds__(256) msbfs_mark_kernel(const uint32_t *y, uint32_t *visited, uint32_t *frontier,
+                                                         int32_t *dist, uint64_t n, uint32_t B, uint32_t mask,
+                                                         int32_t level, unsigned long long *count)
+{
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    uint32_t found = 0;
+    for (uint64_t v = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; v < n; v += stride) {
+        const uint32_t nw = y[v] & ~visited[v] & mask;
+        frontier[v] = nw;
+        if (nw) {
+            visited[v] |= nw;
+            ++found;
+            uint32_t rest = nw;
+            while (rest) {
+                const uint32_t b = (uint32_t)(__ffs(rest) - 1);
+                rest &= rest - 1u;
+                dist[v * B + b] = level;
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) found += __shfl_xor_sync(0xffffffffu, found, o);
+    if ((threadIdx.x & 31u) == 0 && found) atomicAdd(count, (unsigned long long)found);
+}
+
+// Level 0: dist = -1 everywhere, visited = frontier = the sources' bits.
+__global__ void __launch_bounds__(256) msbfs_init_kernel(uint32_t *visited, uint32_t *frontier, int32_t *dist,
+                                                         uint64_t n, uint32_t B)
+{
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n * B; i += stride) dist[i] = -1;
+    for (uint64_t v = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; v < n; v += stride) {
+        visited[v] = 0u;
+        frontier[v] = 0u;
+    }
+}
+
+__global__ void msbfs_seed_kernel(const uint32_t *src, uint32_t B, uint32_t *visited, uint32_t *frontier,
+                                  int32_t *dist)
+{
+    // one thread seeds all sources in order (B <= 32), so repeated sources are safe
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    for (uint32_t b = 0; b < B; ++b) {
+        const uint32_t s = src[b];
+        visited[s] |= 1u << b;
+        frontier[s] |= 1u << b;
+        dist[(uint64_t)s * B + b] = 0;
+    }
 }
 
 void device_release(k2t_tree *t)
@@ -300,6 +355,54 @@ int k2t_spmv_host(k2t_tree *t, int32_t dir, int32_t semiring, float w, const voi
     if (rc) return rc;
     K2T_CUDA(cudaMemcpyAsync(y_host, d->vec[1], n_out * esz, cudaMemcpyDeviceToHost, st));
     K2T_CUDA(cudaStreamSynchronize(st));
+    return K2T_OK;
+}
+
+uint64_t k2t_msbfs_work_bytes(const k2t_tree *t)
+{
+    if (!t) return 0;
+    const uint64_t n = std::max(t->n_rows, t->n_cols);
+    return align_up(3 * n * 4 + 32 * 4 + 16, kArenaAlign);  // frontier, visited, y, sources, counter
+}
+
+int k2t_msbfs(k2t_tree *t, int32_t dir, const uint32_t *sources, uint32_t B, int32_t *dist, void *work,
+              uint32_t max_levels, uint32_t *levels, void *stream)
+{
+    if (!t || !sources || !dist || !work || !levels) return K2T_EINVAL;
+    if (!t->dev) return K2T_ESTATE;
+    if (t->n_rows != t->n_cols) return K2T_EINVAL;
+    if (dir != K2T_RIGHT && dir != K2T_LEFT) return K2T_EINVAL;
+    if (B == 0 || B > 32) return K2T_ERANGE;
+    const uint64_t n = t->n_rows;
+    for (uint32_t b = 0; b < B; ++b)
+        if (sources[b] >= n) return K2T_ERANGE;
+    if ((uintptr_t)work & 15u) return K2T_EINVAL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t *frontier = static_cast<uint32_t *>(work);
+    uint32_t *visited = frontier + n;
+    uint32_t *y = visited + n;
+    uint32_t *src = y + n;
+    unsigned long long *count = reinterpret_cast<unsigned long long *>(
+        static_cast<char *>(work) + align_up(3 * n * 4 + 32 * 4, 8));
+    const uint32_t mask = B >= 32 ? 0xffffffffu : ((1u << B) - 1u);
+    const unsigned grid = (unsigned)std::min<uint64_t>((n * B + 255) / 256 + 1, 152ull * 16);
+    msbfs_init_kernel<<<grid, 256, 0, st>>>(visited, frontier, dist, n, B);
+    K2T_CUDA(cudaMemcpyAsync(src, sources, B * sizeof(uint32_t), cudaMemcpyHostToDevice, st));
+    msbfs_seed_kernel<<<1, 32, 0, st>>>(src, B, visited, frontier, dist);
+    K2T_CUDA(cudaGetLastError());
+    uint32_t lv = 0;
+    unsigned long long found = 0;
+    for (uint32_t level = 1; level <= max_levels; ++level) {
+        int rc = k2t_spmv(t, dir, K2T_BOOLEAN, 1.0f, frontier, y, B, stream);
+        if (rc) return rc;
+        K2T_CUDA(cudaMemsetAsync(count, 0, sizeof(unsigned long long), st));
+        msbfs_mark_kernel<<<grid, 256, 0, st>>>(y, visited, frontier, dist, n, B, mask, (int32_t)level, count);
+        K2T_CUDA(cudaMemcpyAsync(&found, count, sizeof(found), cudaMemcpyDeviceToHost, st));
+        K2T_CUDA(cudaStreamSynchronize(st));
+        lv = level;
+        if (!found) break;
+    }
+    *levels = lv;
     return K2T_OK;
 }
 

@@ -30,7 +30,8 @@ EXPORTED = ["k2t_default_opts", "k2t_build", "k2t_workspace_bytes", "k2t_upload"
             "k2t_spmv_marked",
             "k2t_spmv_host", "k2t_stats_get", "k2t_level_signatures", "k2t_device_level",
             "k2t_decode", "k2t_free", "k2t_strerror", "k2t_last_cuda_error",
-            "k2t_spmv_noalloc", "k2t_noalloc_scratch_limit", "k2t_probe"]
+            "k2t_spmv_noalloc", "k2t_noalloc_scratch_limit", "k2t_probe", "k2t_msbfs",
+            "k2t_msbfs_work_bytes"]
 
 
 class Opts(ctypes.Structure):
@@ -89,6 +90,10 @@ def load() -> ctypes.CDLL:
         lib.k2t_spmv_noalloc.restype = ctypes.c_int
         lib.k2t_noalloc_scratch_limit.argtypes = []
         lib.k2t_noalloc_scratch_limit.restype = U64
+        lib.k2t_msbfs.argtypes = [P, I32, P, U32, P, P, U32, ctypes.POINTER(U32), P]
+        lib.k2t_msbfs.restype = ctypes.c_int
+        lib.k2t_msbfs_work_bytes.argtypes = [P]
+        lib.k2t_msbfs_work_bytes.restype = U64
         lib.k2t_probe.argtypes = [I32, P, P, U64, U64, P]
         lib.k2t_probe.restype = ctypes.c_int
         lib.k2t_spmv_host.argtypes = [P, I32, I32, ctypes.c_float, P, P, U32, P]
@@ -224,6 +229,18 @@ class Tree:
         _check("k2t_spmv_noalloc", load().k2t_spmv_noalloc(self._h, direction, semiring, ctypes.c_float(w),
                                                            _dev_ptr(x), _dev_ptr(y), B, _stream_ptr(stream)))
         return y
+
+    def msbfs(self, direction: int, sources, dist, work, max_levels: int = 1 << 30, stream=None) -> int:
+        """Multi-source BFS (k2t_msbfs): dist (CUDA int32, n x B) and work (CUDA
+        buffer of msbfs_work_bytes()) are the caller's; returns the levels run."""
+        src = np.ascontiguousarray(sources, dtype=np.uint32)
+        lv = ctypes.c_uint32()
+        _check("k2t_msbfs", load().k2t_msbfs(self._h, direction, src.ctypes.data, src.size, _dev_ptr(dist),
+                                             _dev_ptr(work), max_levels, ctypes.byref(lv), _stream_ptr(stream)))
+        return int(lv.value)
+
+    def msbfs_work_bytes(self) -> int:
+        return int(load().k2t_msbfs_work_bytes(self._h))
 
     def spmv_host(self, direction: int, semiring: int, x: np.ndarray, y: np.ndarray, B: int = 1,
                   w: float = 1.0, stream=None):

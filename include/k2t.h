@@ -217,6 +217,28 @@ int k2t_spmv_noalloc(k2t_tree *t, int32_t dir, int32_t semiring, float w,
 /* Size in bytes of the device array k2t_spmv_noalloc works in. */
 uint64_t k2t_noalloc_scratch_limit(void);
 
+/* Multi-source breadth-first search to the fixed point (section 5.8): hop
+ * distances from B <= 32 sources at once, one batched Boolean product per
+ * level, with a mark kernel over dense n x B tables.  dir K2T_RIGHT: vertex i
+ * is reached from j when A_ij = 1 (the product y = A x over the frontier);
+ * K2T_LEFT: vertex j is reached from i when A_ij = 1 (y^T = x^T A).  The
+ * matrix must be square.
+ *   sources   host array of B vertex ids (< n)
+ *   dist      device int32 array, n x B row-major: the level at which vertex v
+ *             is first reached from source b, or -1 if never (within
+ *             max_levels); dist[s_b][b] = 0
+ *   work      device buffer of k2t_msbfs_work_bytes(t) bytes (frontier,
+ *             visited, product output, counter), owned by the caller
+ *   levels    out: levels run (the last one reached no new vertex, or the cap)
+ * Synchronises the stream once per level (to read the new-vertex count).
+ * Errors: ESTATE (not uploaded), EINVAL (non-square, bad dir, null),
+ * ERANGE (B = 0 or > 32, a source >= n), ECUDA. */
+int k2t_msbfs(k2t_tree *t, int32_t dir, const uint32_t *sources, uint32_t B, int32_t *dist, void *work,
+              uint32_t max_levels, uint32_t *levels, void *stream);
+
+/* Bytes of the work buffer k2t_msbfs needs for this tree. */
+uint64_t k2t_msbfs_work_bytes(const k2t_tree *t);
+
 /* Memory-system ceilings for the leaf step's access patterns (the
  * microbenchmark of section 5.6, re-measured on this device; instrumentation,
  * not part of a product).  Launches one pass on `stream`; the caller times it.

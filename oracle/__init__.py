@@ -290,3 +290,35 @@ def rows_product(rows, cols, n_rows: int, n_cols: int, direction: int, semiring:
 def plus_times_tolerance(scale: np.ndarray) -> np.ndarray:
     """|y - y_ref| <= 1e-5 * sum_j |A_ij x_j| + 1e-6 (the stated fp32 bound)."""
     return 1e-5 * scale + 1e-6
+
+
+def msbfs(rows, cols, n: int, sources, direction: int, max_levels: int | None = None) -> np.ndarray:
+    """Hop distances from each source by level-synchronous search to the fixed
+    point (the multi-source search of section 5.8 of "A GPU Engine for Sparse
+    Matrix-Vector Products on k^2-Tree-Compressed Graphs"): level k+1 holds the
+    vertices reached in one step from level k and not reached before.  RIGHT:
+    vertex i is reached from j when A_ij = 1; LEFT: j is reached from i.  The
+    step is a scipy sparse matrix-vector product.  Returns int32 n x B, -1 for
+    vertices never reached (within max_levels)."""
+    import scipy.sparse as sp
+    r, c = dedup_edges(rows, cols)
+    A = sp.csr_matrix((np.ones(r.size, np.int32), (r.astype(np.int64), c.astype(np.int64))), shape=(n, n))
+    M = A if direction == RIGHT else A.T.tocsr()
+    sources = [int(s) for s in sources]
+    dist = np.full((n, len(sources)), -1, np.int32)
+    for b, s in enumerate(sources):
+        dist[s, b] = 0
+        frontier = np.zeros(n, bool)
+        frontier[s] = True
+        visited = frontier.copy()
+        level = 0
+        while max_levels is None or level < max_levels:
+            level += 1
+            nxt = (M @ frontier.astype(np.int32)) > 0
+            nxt &= ~visited
+            if not nxt.any():
+                break
+            dist[nxt, b] = level
+            visited |= nxt
+            frontier = nxt
+    return dist
