@@ -305,6 +305,9 @@ def run_ours(args):
     if args.engine is not None:
         opts["engine"] = args.engine
         opts["cache_last_internal"] = int(args.engine in (3, 4))
+    for kv in args.opt:
+        k, v = kv.split("=", 1)
+        opts[k] = int(v, 0)
     t_build = time.perf_counter()
     tree = K.Tree(wl.rows, wl.cols, wl.n_rows, wl.n_cols, **opts)
     t_build = time.perf_counter() - t_build
@@ -454,6 +457,7 @@ def run_ours(args):
            "warmup": args.warmup, "ms_per_step": float(step_ms.mean()), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": dtype_name(wl), "data": "synthetic",
            "config": {"workload": wl.name, "nnz": m, "n": wl.n_rows, "levels": int(st.levels), "d0": int(st.d0),
+                      "options": {k: v for k, v in opts.items() if k not in ("host_vectors", "max_batch")},
                       "engine": ["auto", "fused", "levelsync", "cached", "banded"][int(st.engine)],
                       "products": [list(p) for p in products],
                       "l2": "flushed between steps" if flush is not None else "inputs larger than L2",
@@ -503,6 +507,40 @@ def run_ceilings(args):
     print(json.dumps(out))
 
 
+def run_msbfs(args):
+    """Multi-source search to the fixed point on the workload's graph (section
+    5.8 analogue): B sources, both directions, cached engine."""
+    import torch
+    from compressed_graph_spmv_gb300 import k2t as K
+    import oracle
+    wl, wopts, _ = make_workload(args.workload)
+    n = wl.n_rows
+    B = args.bfs_sources
+    tree = K.Tree(wl.rows, wl.cols, n, wl.n_cols, **dict(wopts, cache_last_internal=1))
+    tree.upload()
+    rng = np.random.default_rng(7)
+    sources = rng.choice(n, size=B, replace=False)
+    dist = torch.empty(n * B, dtype=torch.int32, device="cuda")
+    work = torch.empty(tree.msbfs_work_bytes(), dtype=torch.uint8, device="cuda")
+    out = {"kind": "msbfs", "workload": wl.name, "sources": B, "nnz": int(tree.stats().nnz)}
+    for d, name in ((K.RIGHT, "right"), (K.LEFT, "left")):
+        tree.msbfs(d, sources, dist, work, max_levels=args.bfs_levels)  # warm-up
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        levels = tree.msbfs(d, sources, dist, work, max_levels=args.bfs_levels)
+        torch.cuda.synchronize()
+        sec = time.perf_counter() - t0
+        got = dist.cpu().numpy().reshape(n, B)
+        res = {"levels": levels, "seconds": sec, "reached": int((got >= 0).sum())}
+        if not args.no_parity:
+            check = list(range(min(B, 2)))
+            want = oracle.msbfs(wl.rows, wl.cols, n, sources[check], d, max_levels=args.bfs_levels)
+            res["parity_sources_checked"] = len(check)
+            res["parity_ok"] = bool(np.array_equal(got[:, check], want))
+        out[name] = res
+    print(json.dumps(out))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -511,17 +549,24 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="rmat27")
     ap.add_argument("--engine", type=int, default=None)
+    ap.add_argument("--opt", action="append", default=[],
+                    help="library option override, e.g. --opt tile_m=65536 (repeatable)")
     ap.add_argument("--products", default=None,
                     help="override the products of a step, e.g. 0:1,1:1 (direction:batch)")
     ap.add_argument("--oracle-edges", type=int, default=1_500_000)
     ap.add_argument("--no-parity", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ceilings", action="store_true", help="measure the leaf step's memory ceilings and exit")
+    ap.add_argument("--msbfs", action="store_true", help="time a multi-source search on the workload and exit")
+    ap.add_argument("--bfs-sources", type=int, default=16)
+    ap.add_argument("--bfs-levels", type=int, default=32)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.ceilings:
         run_ceilings(args)
+    elif args.msbfs:
+        run_msbfs(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
