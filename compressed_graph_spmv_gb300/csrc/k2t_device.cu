@@ -47,6 +47,21 @@ __global__ void __launch_bounds__(256) fill_kernel(uint32_t *y, uint64_t words, 
     for (uint64_t k = tail + i; k < words; k += stride) y[k] = pattern;
 }
 
+// fp64 outputs of a plus-times product: output list[i] of vector k receives
+// its fp64 sum acc[i * B + k], rounded to fp32 once.  The product sends every
+// term of such an output to acc, so y holds the fill's zero there; adding it
+// keeps the result right even if it did not.
+__global__ void __launch_bounds__(256) heavy_finish_kernel(const double *acc, const uint32_t *list, uint32_t h,
+                                                           uint32_t B, float *y)
+{
+    const uint64_t n = (uint64_t)h * B;
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+        float *p = y + (uint64_t)__ldg(list + i / B) * B + i % B;
+        *p = __double2float_rn(acc[i] + (double)*p);
+    }
+}
+
 // Algorithm 1, lines 5-10, for one tile: the frontier entries of nodes
 // [a, a+count) (read from src at index t - src_base) expand into their
 // children's entries, written at dst[child - dst_base].
@@ -212,7 +227,9 @@ int enqueue_product(k2t_tree *t, int32_t dir, int32_t semiring, float w, const v
     va.mask = B >= 32 ? 0xffffffffu : ((1u << B) - 1u);
     va.n_out = n_out;
     va.n_in = dir == K2T_RIGHT ? t->n_cols : t->n_rows;
+    const bool heavy = heavy_begin(t, d, dir, semiring, va, st);
     pick(t->engine, semiring, dir, vw)(t, d, va, st);
+    if (heavy) heavy_end(t, d, dir, va, st);
     return K2T_OK;
 }
 
@@ -282,6 +299,16 @@ int k2t_upload(k2t_tree *t, void *arena, uint64_t arena_bytes, void *stream)
         d->scan_prefix = d->scan_sums + L.scan_bytes / 8;
     }
     if (L.vec_bytes) { d->vec[0] = at<void>(d->arena, L.vec_off[0]); d->vec[1] = at<void>(d->arena, L.vec_off[1]); }
+    for (int dd = 0; dd < 2; ++dd) {
+        if (!L.hflag_bytes[dd]) continue;
+        d->hflag[dd] = at<uint32_t>(d->arena, L.hflag_off[dd]);
+        d->hent[dd] = at<uint32_t>(d->arena, L.hent_off[dd]);
+        d->hlist[dd] = at<uint32_t>(d->arena, L.hlist_off[dd]);
+        if ((e = put(L.hflag_off[dd], L.hflag_bytes[dd], t->hflag[dd].data()))) return fail(e);
+        if ((e = put(L.hent_off[dd], L.hent_bytes[dd], t->hent[dd].data()))) return fail(e);
+        if ((e = put(L.hlist_off[dd], L.hlist_bytes[dd], t->hlist[dd].data()))) return fail(e);
+    }
+    if (L.acc_bytes) d->acc = at<double>(d->arena, L.acc_off);
     if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return fail(e);
     return K2T_OK;
 }
@@ -295,6 +322,7 @@ int k2t_spmv_marked(k2t_tree *t, int32_t dir, int32_t semiring, float w, const v
     if (semiring < K2T_PLUS_TIMES || semiring > K2T_MIN_PLUS) return K2T_EINVAL;
     if (!x || !y || B == 0) return K2T_EINVAL;
     if (B > K2T_MAX_BATCH) return K2T_ERANGE;
+    if (semiring == K2T_PLUS_TIMES && t->dev->hflag[dir] && B > t->opts.max_batch) return K2T_ERANGE;
     if (((uintptr_t)x | (uintptr_t)y) & 3u) return K2T_EINVAL;
     const uint64_t n_in = dir == K2T_RIGHT ? t->n_cols : t->n_rows;
     const uint64_t n_out = dir == K2T_RIGHT ? t->n_rows : t->n_cols;

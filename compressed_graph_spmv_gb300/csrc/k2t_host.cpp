@@ -426,6 +426,63 @@ void plan_bands(k2t_tree *t, int nt)
         }
 }
 
+// Plus-times outputs with more than `limit` non-zeros, counted over the input
+// list (a repeated pair counts each time, so a count never falls short), for
+// the n outputs indexed by ids[]: fills the ascending list and the per-32
+// table (mask of fp64 outputs, fp64 outputs before the group).  A count stops
+// growing once it passes the limit, so it cannot wrap.
+void heavy_outputs(const uint32_t *ids, uint64_t nnz, uint64_t n, uint32_t limit, int nt,
+                   std::vector<uint32_t> &list, std::vector<uint32_t> &ent)
+{
+    list.clear();
+    ent.clear();
+    if (limit == 0xffffffffu || nnz <= limit) return;
+    std::vector<uint32_t> cnt(n, 0);
+    uint32_t *c = cnt.data();
+    parallel_for(nt, [&](int th) {
+        uint64_t lo = nnz * th / nt, hi = nnz * (th + 1) / nt;
+        for (uint64_t i = lo; i < hi; ++i) {
+            uint32_t *p = c + ids[i];
+            if (__atomic_load_n(p, __ATOMIC_RELAXED) <= limit) __atomic_fetch_add(p, 1u, __ATOMIC_RELAXED);
+        }
+    });
+    for (uint64_t i = 0; i < n; ++i)
+        if (cnt[i] > limit) list.push_back((uint32_t)i);
+    if (list.empty()) return;
+    const uint64_t groups = (n + 31) / 32;
+    ent.assign(2 * groups, 0);
+    for (uint32_t v : list) ent[2 * (v / 32)] |= 1u << (v % 32);
+    uint32_t run = 0;
+    for (uint64_t g = 0; g < groups; ++g) {
+        ent[2 * g + 1] = run;
+        run += (uint32_t)popc64(ent[2 * g]);
+    }
+}
+
+// Leaf flags of one direction: bit i set when leaf i (level order; block
+// origin (2 q.r, 2 q.c)) has an fp64 output among its two rows (dir 0) or
+// columns (dir 1).  prefixes[i] is leaf i's path prefix.
+void heavy_leaf_flags(k2t_tree *t, int dir, const uint64_t *prefixes, uint64_t nl, int nt)
+{
+    const std::vector<uint32_t> &ent = t->hent[dir];
+    std::vector<uint32_t> &fl = t->hflag[dir];
+    fl.assign((nl + 31) / 32 + 1, 0);
+    const int d = t->levels - 1;
+    const uint64_t words = (nl + 31) / 32;
+    parallel_for(nt, [&](int th) {
+        uint64_t lo = words * th / nt, hi = words * (th + 1) / nt;
+        for (uint64_t w = lo; w < hi; ++w) {
+            uint32_t v = 0;
+            for (uint64_t i = 32 * w; i < std::min<uint64_t>(32 * w + 32, nl); ++i) {
+                Coord q = prefix_coord(prefixes[i], d, t->n_k4);
+                uint64_t o = 2ull * (dir == 0 ? q.r : q.c);  // even: o and o + 1 share a group
+                if (((ent[2 * (o / 32)] >> (o % 32)) & 3u) != 0) v |= 1u << (i % 32);
+            }
+            fl[w] = v;
+        }
+    });
+}
+
 }  // namespace
 
 void compute_layout(k2t_tree *t)
@@ -499,6 +556,23 @@ void compute_layout(k2t_tree *t)
             }
         }
     }
+    if (!t->empty) {
+        uint64_t hmax = 0;
+        for (int dd = 0; dd < 2; ++dd) {
+            if (t->hlist[dd].empty()) continue;
+            L.hflag_bytes[dd] = t->hflag[dd].size() * sizeof(uint32_t);
+            L.hflag_off[dd] = take(L.hflag_bytes[dd]);
+            L.hent_bytes[dd] = t->hent[dd].size() * sizeof(uint32_t);
+            L.hent_off[dd] = take(L.hent_bytes[dd]);
+            L.hlist_bytes[dd] = t->hlist[dd].size() * sizeof(uint32_t);
+            L.hlist_off[dd] = take(L.hlist_bytes[dd]);
+            hmax = std::max<uint64_t>(hmax, t->hlist[dd].size());
+        }
+        if (hmax) {
+            L.acc_bytes = hmax * (uint64_t)t->opts.max_batch * sizeof(double);
+            L.acc_off = take(L.acc_bytes);
+        }
+    }
     if (t->opts.host_vectors) {
         uint64_t n = std::max(t->n_rows, t->n_cols);
         L.vec_bytes = n * (uint64_t)t->opts.max_batch * 4u;
@@ -531,6 +605,7 @@ void k2t_default_opts(k2t_opts *o)
     o->threads = 0;
     o->band_rows = 4096;
     o->band_cols = 1u << 23;
+    o->heavy_terms = 2048;
 }
 
 int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
@@ -546,6 +621,7 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
     if (o.band_rows < 16 || o.band_rows > 65536 || (o.band_rows & (o.band_rows - 1))) return K2T_EINVAL;
     if (o.band_cols && (o.band_cols < 16 || (o.band_cols & (o.band_cols - 1)))) return K2T_EINVAL;
     if (!o.band_cols) o.band_cols = 1u << 31;
+    if (!o.heavy_terms) o.heavy_terms = 2048;
     if (o.chunk_cap < 4 || o.chunk_cap > kMaxChunkCap || o.tile_m < 4) return K2T_EINVAL;
     if (o.max_batch < 1 || o.max_batch > K2T_MAX_BATCH) return K2T_ERANGE;
     if (o.host_top_max_nodes < 1) return K2T_EINVAL;
@@ -582,6 +658,10 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
                 if (rows[i] >= n_rows || cols[i] >= n_cols) { bad[(size_t)th] = 1; break; }
         });
         for (int b : bad) if (b) { delete t; return K2T_ERANGE; }
+        heavy_outputs(rows, nnz, n_rows, o.heavy_terms, nt, t->hlist[0], t->hent[0]);
+        heavy_outputs(cols, nnz, n_cols, o.heavy_terms, nt, t->hlist[1], t->hent[1]);
+        for (int dd = 0; dd < 2; ++dd)
+            if (t->hlist[dd].size() >= (1u << 30)) { delete t; return K2T_ERANGE; }
 
         t->nodes.assign((size_t)l, 0);
         t->sig.assign((size_t)l, std::vector<uint64_t>());
@@ -601,6 +681,7 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
 
         if (m == 0) {
             t->empty = true;
+            for (int dd = 0; dd < 2; ++dd) { t->hlist[dd].clear(); t->hent[dd].clear(); }
             t->nodes[0] = 1;
             t->sig[0].assign(2, 0);
             for (int d = 1; d < l; ++d) t->sig[(size_t)d].assign(1, 0);
@@ -618,6 +699,9 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
                 if (nn >= (1ull << 32)) { delete t; return K2T_ERANGE; }
                 t->nodes[(size_t)d] = nn;
                 pack_level(t, d, sg.data(), nn, nt);
+                if (d == l - 1)
+                    for (int dd = 0; dd < 2; ++dd)
+                        if (!t->hlist[dd].empty()) heavy_leaf_flags(t, dd, nxt, nn, nt);
                 if (d == l - 2 && (t->engine == K2T_ENGINE_CACHED || t->engine == K2T_ENGINE_BANDED)) {
                     t->cached.resize(nn);
                     parallel_for(nt, [&](int th) {
@@ -753,6 +837,11 @@ int k2t_stats_get(const k2t_tree *t, k2t_stats *s)
     s->engine = t->engine;
     s->offsets = t->opts.offsets;
     s->uploaded = t->dev != nullptr;
+    s->heavy_rows = (uint32_t)t->hlist[0].size();
+    s->heavy_cols = (uint32_t)t->hlist[1].size();
+    uint64_t hb = L.acc_bytes;
+    for (int dd = 0; dd < 2; ++dd) hb += L.hflag_bytes[dd] + L.hent_bytes[dd] + L.hlist_bytes[dd];
+    s->heavy_kib = (uint32_t)((hb + 1023) / 1024);
     return K2T_OK;
 }
 

@@ -35,6 +35,10 @@ struct VecArgs {
     uint32_t mask;   // Boolean: bits of the batch
     uint64_t n_out;  // entries (vertices) of y
     uint64_t n_in;   // entries (vertices) of x
+    // Plus-times outputs summed in fp64 (null hflag: none in this product)
+    const uint32_t *hflag;  // bit j: leaf j (level order) has an fp64 output
+    const uint32_t *hent;   // per 32 outputs: mask of fp64 outputs, fp64 outputs before the group
+    double *acc;            // fp64 sums, [index in the fp64 list][B]
 };
 
 __device__ __forceinline__ uint32_t nibble_at(const uint8_t *sig, uint32_t t)
@@ -135,6 +139,36 @@ __device__ __forceinline__ bool is_noop_word(uint32_t v)
     else return v == 0x7f800000u;
 }
 
+// ---- fp64 outputs (plus-times) -------------------------------------------------
+// An output with more non-zeros than the fp32 bound allows is summed in fp64.
+// heavy_leaf: leaf li has such an output.  heavy_word: for the outputs out
+// (even) and out + 1 of a leaf, (id << 2) | mask, where mask bit q is set when
+// out + q is summed in fp64 and id is out's index in the fp64 list (out + 1
+// has id + (mask & 1)); 0 when neither is.
+__device__ __forceinline__ uint32_t heavy_leaf(const VecArgs &va, uint32_t li)
+{
+    return (__ldg(va.hflag + (li >> 5)) >> (li & 31u)) & 1u;
+}
+
+__device__ __forceinline__ uint32_t heavy_word(const VecArgs &va, uint32_t out)
+{
+    const uint2 e = __ldg(reinterpret_cast<const uint2 *>(va.hent) + (out >> 5));
+    const uint32_t sh = out & 31u;
+    const uint32_t m = (e.x >> sh) & 3u;
+    if (!m) return 0u;
+    return ((e.y + (uint32_t)__popc(e.x & ((1u << sh) - 1u))) << 2) | m;
+}
+
+// Add the VW-wide slice k of output out + q (hv from heavy_word) to its fp64 sum.
+template <int VW>
+__device__ __forceinline__ void heavy_add(const VecArgs &va, uint32_t hv, int q, uint32_t k, const float (&v)[VW])
+{
+    const uint32_t id = (hv >> 2) + (q ? (hv & 1u) : 0u);
+    double *a = va.acc + (size_t)id * va.B + k;
+#pragma unroll
+    for (int i = 0; i < VW; ++i) atomicAdd(a + i, (double)v[i]);
+}
+
 template <int VW> struct VecLoad;
 template <> struct VecLoad<1> {
     static __device__ __forceinline__ void load(const float *p, float (&v)[1]) { v[0] = __ldg(p); }
@@ -162,10 +196,11 @@ template <> struct VecLoad<4> {
 //   right: output r gets bits 0 (input c) and 1 (input c+1); output r+1 bits 2, 3
 //   left:  output c gets bits 0 (input r) and 2 (input r+1); output c+1 bits 1, 3
 // win != null: updates go to the shared-memory window win[(out - lo) * width + k]
-// instead of y (width = B words, 1 for Boolean).
+// instead of y (width = B words, 1 for Boolean).  Bit u of fl (plus-times):
+// leaf u has fp64 outputs; those go to their fp64 sums instead.
 template <int SR, int DIR, int VW, int U>
 __device__ __forceinline__ void leaf_group(const uint32_t (&lam)[U], const uint32_t (&r)[U], const uint32_t (&c)[U],
-                                           const VecArgs &a, uint32_t *win, uint32_t lo)
+                                           uint32_t fl, const VecArgs &a, uint32_t *win, uint32_t lo)
 {
     bool a0[U], a1[U], b0[U], b1[U];
     uint32_t in[U], out[U];
@@ -235,8 +270,15 @@ __device__ __forceinline__ void leaf_group(const uint32_t (&lam)[U], const uint3
                             if (!S::skip(v1[q])) smem_update<SR>(w1 + q, __float_as_uint(v1[q]));
                     }
                 } else {
-                    if (a0[u] || a1[u]) S::update(y + (size_t)out[u] * B + k, v0);
-                    if (b0[u] || b1[u]) S::update(y + (size_t)(out[u] + 1) * B + k, v1);
+                    const uint32_t h = SR == K2T_PLUS_TIMES && ((fl >> u) & 1u) ? heavy_word(a, out[u]) : 0u;
+                    if (a0[u] || a1[u]) {
+                        if (h & 1u) heavy_add<VW>(a, h, 0, k, v0);
+                        else S::update(y + (size_t)out[u] * B + k, v0);
+                    }
+                    if (b0[u] || b1[u]) {
+                        if (h & 2u) heavy_add<VW>(a, h, 1, k, v1);
+                        else S::update(y + (size_t)(out[u] + 1) * B + k, v1);
+                    }
                 }
             }
         }
@@ -271,6 +313,7 @@ constexpr uint32_t kFusedSolo = 256;  // levels this narrow are expanded by one 
 
 // Kernels without template parameters, defined in k2t_device.cu.
 __global__ void fill_kernel(uint32_t *y, uint64_t words, uint32_t pattern);
+__global__ void heavy_finish_kernel(const double *acc, const uint32_t *list, uint32_t h, uint32_t B, float *y);
 __global__ void ls_expand_kernel(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix, uint32_t a,
                                  uint32_t count, const Coord *src, uint32_t src_base, Coord *dst, uint32_t dst_base);
 __global__ void ls_block_sums_kernel(const uint8_t *sig, uint32_t a, uint32_t count, uint32_t *sums);
@@ -371,7 +414,8 @@ template <int SR, int DIR>
 __device__ __forceinline__ void node_leaves_spec(uint32_t sg, uint32_t off, Coord p, const uint8_t *leaf,
                                                  const VecArgs &va)
 {
-    uint32_t lam[4], xin[4], xo[4][2];
+    uint32_t lam[4], xin[4], xo[4][2], fl = 0u;
+    const bool heavy = SR == K2T_PLUS_TIMES && va.hflag != nullptr;
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
         const uint32_t r = 4u * p.r + 2u * (uint32_t)(b >> 1);
@@ -381,10 +425,12 @@ __device__ __forceinline__ void node_leaves_spec(uint32_t sg, uint32_t off, Coor
         xo[b][0] = 0u;
         xo[b][1] = 0u;
         if (sg & (1u << b)) {
-            lam[b] = nibble_at(leaf, off + (uint32_t)__popc(sg & ((1u << b) - 1u)));
+            const uint32_t li = off + (uint32_t)__popc(sg & ((1u << b) - 1u));
+            lam[b] = nibble_at(leaf, li);
             const uint32_t *x = static_cast<const uint32_t *>(va.x);
             xo[b][0] = __ldg(x + xin[b]);
             if (xin[b] + 1u < va.n_in) xo[b][1] = __ldg(x + xin[b] + 1u);
+            if (heavy) fl |= heavy_leaf(va, li) << b;
         }
     }
 #pragma unroll
@@ -407,13 +453,16 @@ __device__ __forceinline__ void node_leaves_spec(uint32_t sg, uint32_t off, Coor
             float *y = static_cast<float *>(va.y);
             const float c0 = S::contrib(__uint_as_float(xo[b][0]), va.w);
             const float c1 = S::contrib(__uint_as_float(xo[b][1]), va.w);
+            const uint32_t h = SR == K2T_PLUS_TIMES && ((fl >> b) & 1u) ? heavy_word(va, out) : 0u;
             if (a0 || a1) {
                 const float v[1] = {a0 ? (a1 ? S::plus(c0, c1) : c0) : c1};
-                if (!S::skip(v[0])) S::update(y + out, v);
+                if (h & 1u) heavy_add<1>(va, h, 0, 0u, v);
+                else if (!S::skip(v[0])) S::update(y + out, v);
             }
             if (b0 || b1) {
                 const float v[1] = {b0 ? (b1 ? S::plus(c0, c1) : c0) : c1};
-                if (!S::skip(v[0])) S::update(y + out + 1, v);
+                if (h & 2u) heavy_add<1>(va, h, 1, 0u, v);
+                else if (!S::skip(v[0])) S::update(y + out + 1, v);
             }
         }
     }
@@ -450,24 +499,30 @@ flat_leaf_kernel(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix
         node_leaves_spec<SR, DIR>(sg, off, p, leaf, va);
         return;
     }
-    uint32_t lam[4], r[4], c[4];
+    uint32_t lam[4], r[4], c[4], fl = 0u;
+    const bool heavy = SR == K2T_PLUS_TIMES && va.hflag != nullptr;
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
         lam[b] = 0u;
         r[b] = 4u * p.r + 2u * (uint32_t)(b >> 1);
         c[b] = 4u * p.c + 2u * (uint32_t)(b & 1);
-        if (sg & (1u << b)) lam[b] = nibble_at(leaf, off + (uint32_t)__popc(sg & ((1u << b) - 1u)));
+        if (sg & (1u << b)) {
+            const uint32_t li = off + (uint32_t)__popc(sg & ((1u << b) - 1u));
+            lam[b] = nibble_at(leaf, li);
+            if (heavy) fl |= heavy_leaf(va, li) << b;
+        }
     }
-    leaf_group<SR, DIR, VW, 4>(lam, r, c, va, nullptr, 0u);
+    leaf_group<SR, DIR, VW, 4>(lam, r, c, fl, va, nullptr, 0u);
 }
 
 // Leaves of U leaf blocks (origins r[u], c[u], cells lam[u]) with x entries
 // already loaded (xo[u][0]: input r or c, xo[u][1]: the next one); one
-// vector slice (B = 1 fp32, or a Boolean word).
+// vector slice (B = 1 fp32, or a Boolean word).  Bit u of fl (plus-times):
+// leaf u has fp64 outputs; those go to their fp64 sums, window or not.
 template <int SR, int DIR, int U>
 __device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint32_t (&out)[U],
-                                            const uint32_t (&xo)[U][2], const VecArgs &va, uint32_t *win = nullptr,
-                                            uint32_t lo = 0u)
+                                            const uint32_t (&xo)[U][2], uint32_t fl, const VecArgs &va,
+                                            uint32_t *win, uint32_t lo)
 {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -493,16 +548,19 @@ __device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint
             float *y = static_cast<float *>(va.y);
             const float c0 = S::contrib(__uint_as_float(xo[u][0]), va.w);
             const float c1 = S::contrib(__uint_as_float(xo[u][1]), va.w);
+            const uint32_t h = SR == K2T_PLUS_TIMES && ((fl >> u) & 1u) ? heavy_word(va, out[u]) : 0u;
             if (a0 || a1) {
                 const float v[1] = {a0 ? (a1 ? S::plus(c0, c1) : c0) : c1};
-                if (!S::skip(v[0])) {
+                if (h & 1u) heavy_add<1>(va, h, 0, 0u, v);
+                else if (!S::skip(v[0])) {
                     if (win) smem_update<SR>(win + (out[u] - lo), __float_as_uint(v[0]));
                     else S::update(y + out[u], v);
                 }
             }
             if (b0 || b1) {
                 const float v[1] = {b0 ? (b1 ? S::plus(c0, c1) : c0) : c1};
-                if (!S::skip(v[0])) {
+                if (h & 2u) heavy_add<1>(va, h, 1, 0u, v);
+                else if (!S::skip(v[0])) {
                     if (win) smem_update<SR>(win + (out[u] + 1 - lo), __float_as_uint(v[0]));
                     else S::update(y + out[u] + 1, v);
                 }
@@ -570,8 +628,8 @@ __device__ __forceinline__ void warp_window_flush(const uint32_t *win, uint32_t 
 // One VW-wide vector slice k of one leaf (origin r, c; cells lam): gathers the
 // slice of the inputs it needs, combines per output, updates y or the window.
 template <int SR, int DIR, int VW>
-__device__ __forceinline__ void leaf_slice(uint32_t lam, uint32_t r, uint32_t c, uint32_t k, const VecArgs &va,
-                                           uint32_t *win, uint32_t lo)
+__device__ __forceinline__ void leaf_slice(uint32_t lam, uint32_t r, uint32_t c, uint32_t k, uint32_t hv,
+                                           const VecArgs &va, uint32_t *win, uint32_t lo)
 {
     using S = Fp32Sem<SR>;
     const uint32_t in = DIR == K2T_RIGHT ? c : r;
@@ -594,15 +652,23 @@ __device__ __forceinline__ void leaf_slice(uint32_t lam, uint32_t r, uint32_t c,
         v0[q] = a0 ? (a1 ? S::plus(c0, c1) : c0) : c1;
         v1[q] = b0 ? (b1 ? S::plus(c0, c1) : c0) : c1;
     }
+    const uint32_t h = SR == K2T_PLUS_TIMES ? hv : 0u;
+    const bool ya = (a0 || a1) && !(h & 1u), yb = (b0 || b1) && !(h & 2u);
+    if (h & 1u) {
+        if (a0 || a1) heavy_add<VW>(va, h, 0, k, v0);
+    }
+    if (h & 2u) {
+        if (b0 || b1) heavy_add<VW>(va, h, 1, k, v1);
+    }
     if (win) {
 #pragma unroll
         for (int q = 0; q < VW; ++q) {
-            if ((a0 || a1) && !S::skip(v0[q])) smem_update<SR>(win + (size_t)(out - lo) * B + k + q, __float_as_uint(v0[q]));
-            if ((b0 || b1) && !S::skip(v1[q])) smem_update<SR>(win + (size_t)(out + 1 - lo) * B + k + q, __float_as_uint(v1[q]));
+            if (ya && !S::skip(v0[q])) smem_update<SR>(win + (size_t)(out - lo) * B + k + q, __float_as_uint(v0[q]));
+            if (yb && !S::skip(v1[q])) smem_update<SR>(win + (size_t)(out + 1 - lo) * B + k + q, __float_as_uint(v1[q]));
         }
     } else {
-        if (a0 || a1) S::update(y + (size_t)out * B + k, v0);
-        if (b0 || b1) S::update(y + (size_t)(out + 1) * B + k, v1);
+        if (ya) S::update(y + (size_t)out * B + k, v0);
+        if (yb) S::update(y + (size_t)(out + 1) * B + k, v1);
     }
 }
 
@@ -625,15 +691,20 @@ __device__ __forceinline__ void warp_leaf_rounds(uint32_t jb, uint32_t je, LeafA
         constexpr int U = kLeafU;
         const uint32_t *x = static_cast<const uint32_t *>(va.x);
         const bool x8 = ((uintptr_t)x & 7u) == 0;
+        const bool heavy = SR == K2T_PLUS_TIMES && va.hflag != nullptr;
         for (uint32_t j0 = jb; j0 < je; j0 += 32u * U) {
-            uint32_t lam[U], r[U], c[U];
+            uint32_t lam[U], r[U], c[U], fl = 0u;
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const uint32_t j = j0 + 32u * u + lane;
                 lam[u] = 0u;
                 r[u] = 0u;
                 c[u] = 0u;
-                if (j < je) leaf_at(j, lam[u], r[u], c[u]);
+                uint32_t li = 0u;
+                if (j < je) {
+                    leaf_at(j, lam[u], r[u], c[u], li);
+                    if (heavy) fl |= heavy_leaf(va, li) << u;
+                }
             }
             uint32_t xo[U][2], out[U];
 #pragma unroll
@@ -653,7 +724,7 @@ __device__ __forceinline__ void warp_leaf_rounds(uint32_t jb, uint32_t je, LeafA
                     }
                 }
             }
-            leaf_apply1<SR, DIR, U>(lam, out, xo, va, win, lo);
+            leaf_apply1<SR, DIR, U>(lam, out, xo, fl, va, win, lo);
         }
         return;
     }
@@ -664,21 +735,27 @@ __device__ __forceinline__ void warp_leaf_rounds(uint32_t jb, uint32_t je, LeafA
         const uint32_t groups = G <= 32u ? G : 32u;      // lanes that own a slice per round
         const uint32_t slot = lane / groups, sub = lane % groups;
         const bool active = slot < per;
+        const bool heavy = SR == K2T_PLUS_TIMES && va.hflag != nullptr;
         for (uint32_t j0 = jb; j0 < je; j0 += per * U) {
-            uint32_t lam[U], r[U], c[U];
+            uint32_t lam[U], r[U], c[U], hv[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const uint32_t j = j0 + (uint32_t)u * per + slot;
                 lam[u] = 0u;
                 r[u] = 0u;
                 c[u] = 0u;
-                if (active && j < je) leaf_at(j, lam[u], r[u], c[u]);
+                hv[u] = 0u;
+                uint32_t li = 0u;
+                if (active && j < je) {
+                    leaf_at(j, lam[u], r[u], c[u], li);
+                    if (heavy && heavy_leaf(va, li)) hv[u] = heavy_word(va, DIR == K2T_RIGHT ? r[u] : c[u]);
+                }
             }
             // a group of G lanes covers the row; rows wider than 32 slices loop
             for (uint32_t k = sub * VW; k < va.B; k += groups * VW) {
 #pragma unroll
                 for (int u = 0; u < U; ++u)
-                    if (lam[u]) leaf_slice<SR, DIR, VW>(lam[u], r[u], c[u], k, va, win, lo);
+                    if (lam[u]) leaf_slice<SR, DIR, VW>(lam[u], r[u], c[u], k, hv[u], va, win, lo);
             }
         }
     }
@@ -742,13 +819,14 @@ cached_block_kernel(const uint8_t *sig, const uint32_t *dir, uint32_t n, const C
     uint32_t lo, span;
     uint32_t *win = warp_window_begin<SR>(mn, mx, 4u, width, wins[warp], lo, span);
     __syncwarp();
-    warp_leaf_rounds<SR, DIR, VW>(0u, total, [&](uint32_t j, uint32_t &lam, uint32_t &r, uint32_t &c) {
+    warp_leaf_rounds<SR, DIR, VW>(0u, total, [&](uint32_t j, uint32_t &lam, uint32_t &r, uint32_t &c, uint32_t &li) {
         const uint32_t e = sl[j];
         const Coord p = cw[e >> 2];
         const uint32_t b = e & 3u;
         r = 4u * p.r + 2u * (b >> 1);
         c = 4u * p.c + 2u * (b & 1u);
-        lam = nibble_at(leaf, base + j);
+        li = base + j;
+        lam = nibble_at(leaf, li);
     }, va, win, lo);
     if (win) warp_window_flush<SR>(win, lo, span, width, va);
 }
@@ -825,13 +903,14 @@ banded_kernel(const uint32_t *chunks, const Coord *coords, const uint32_t *bleaf
                 if (sg & (1u << b)) sl[pos++] = (uint16_t)(((8u * lane + k) << 4) | (b << 2) | rank++);
         }
         __syncwarp();
-        warp_leaf_rounds<SR, DIR, VW>(0u, total, [&](uint32_t j, uint32_t &lam, uint32_t &r, uint32_t &c) {
+        warp_leaf_rounds<SR, DIR, VW>(0u, total, [&](uint32_t j, uint32_t &lam, uint32_t &r, uint32_t &c, uint32_t &li) {
             const uint32_t e = sl[j];
             const uint32_t node = e >> 4, b = (e >> 2) & 3u;
             const Coord p = cw[node];
             r = 4u * p.r + 2u * (b >> 1);
             c = 4u * p.c + 2u * (b & 1u);
-            lam = nibble_at(leaf, lw[node] + (e & 3u));
+            li = lw[node] + (e & 3u);
+            lam = nibble_at(leaf, li);
         }, va, windowed ? win : nullptr, (uint32_t)band_lo);
         __syncwarp();
     }
@@ -1122,10 +1201,12 @@ fused_kernel(DevTree tr, const uint32_t *chunks, uint32_t stride, const Coord *r
     if (2u * cap >= kFusedWarps * kWarpWindow)  // the free buffer holds every warp's window
         win = warp_window_begin<SR>(wmn, wmx, 2u, width, reinterpret_cast<uint32_t *>(nxt) + warp * kWarpWindow,
                                     lo, span);
-    warp_leaf_rounds<SR, DIR, VW>(jb, je, [&](uint32_t j, uint32_t &lam, uint32_t &r, uint32_t &c) {
+    const uint32_t leaf0 = rng[2 * (l - 1 - d0)];  // the chunk's first leaf (level order)
+    warp_leaf_rounds<SR, DIR, VW>(jb, je, [&](uint32_t j, uint32_t &lam, uint32_t &r, uint32_t &c, uint32_t &li) {
         const Coord q = cur[j];
         r = 2u * q.r;
         c = 2u * q.c;
+        li = leaf0 + j;
         lam = snib(lsig, lnb + j);
     }, va, win, lo);
     if (win) warp_window_flush<SR>(win, lo, span, width, va);
@@ -1178,6 +1259,10 @@ struct DeviceState {
     uint32_t *scan_prefix = nullptr;
     uint32_t *err = nullptr;
     void *vec[2] = {nullptr, nullptr};
+    const uint32_t *hflag[2] = {nullptr, nullptr};  // fp64 outputs, per direction (null: none)
+    const uint32_t *hent[2] = {nullptr, nullptr};
+    const uint32_t *hlist[2] = {nullptr, nullptr};
+    double *acc = nullptr;
     cudaStream_t cap_stream = nullptr;
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t gexec = nullptr;
@@ -1270,6 +1355,33 @@ void launch_ls(const k2t_tree *t, const DeviceState *d, const VecArgs &va, cudaS
 }
 
 using LaunchFn = void (*)(const k2t_tree *, const DeviceState *, const VecArgs &, cudaStream_t);
+
+// Plus-times products of a direction with fp64 outputs.  heavy_begin points
+// va at the direction's tables and zeroes the fp64 sums of the B vectors
+// (queued after the fill of y); heavy_end rounds each sum to fp32 into its
+// output (queued after the product).  Other semirings: va gets no tables.
+inline bool heavy_begin(const k2t_tree *t, const DeviceState *d, int dir, int semiring, VecArgs &va, cudaStream_t st)
+{
+    va.hflag = nullptr;
+    va.hent = nullptr;
+    va.acc = nullptr;
+    if (semiring != K2T_PLUS_TIMES || !d->hflag[dir]) return false;
+    va.hflag = d->hflag[dir];
+    va.hent = d->hent[dir];
+    va.acc = d->acc;
+    const uint64_t words = 2ull * t->hlist[dir].size() * va.B;
+    const uint64_t blocks = std::min<uint64_t>((words / 4 + 255) / 256 + 1, 152ull * 8);
+    fill_kernel<<<(unsigned)blocks, 256, 0, st>>>(reinterpret_cast<uint32_t *>(d->acc), words, 0u);
+    return true;
+}
+
+inline void heavy_end(const k2t_tree *t, const DeviceState *d, int dir, const VecArgs &va, cudaStream_t st)
+{
+    const uint32_t h = (uint32_t)t->hlist[dir].size();
+    const uint64_t n = (uint64_t)h * va.B;
+    const uint64_t blocks = std::min<uint64_t>((n + 255) / 256, 152ull * 8);
+    heavy_finish_kernel<<<(unsigned)blocks, 256, 0, st>>>(d->acc, d->hlist[dir], h, va.B, static_cast<float *>(va.y));
+}
 
 template <int SR, int DIR, int VW>
 LaunchFn pick_engine(uint32_t engine)

@@ -41,7 +41,8 @@ class Opts(ctypes.Structure):
                 ("tile_m", ctypes.c_uint64), ("max_batch", ctypes.c_uint32),
                 ("host_vectors", ctypes.c_uint32), ("use_graph", ctypes.c_uint32),
                 ("threads", ctypes.c_uint32), ("band_rows", ctypes.c_uint32),
-                ("band_cols", ctypes.c_uint32), ("reserved", ctypes.c_uint32 * 6)]
+                ("band_cols", ctypes.c_uint32), ("heavy_terms", ctypes.c_uint32),
+                ("reserved", ctypes.c_uint32 * 5)]
 
 
 class Stats(ctypes.Structure):
@@ -55,7 +56,9 @@ class Stats(ctypes.Structure):
                 ("scratch_bytes", ctypes.c_uint64), ("vector_bytes", ctypes.c_uint64),
                 ("workspace_bytes", ctypes.c_uint64), ("n_chunks", ctypes.c_uint64),
                 ("n_steps", ctypes.c_uint64), ("engine", ctypes.c_uint32), ("offsets", ctypes.c_uint32),
-                ("uploaded", ctypes.c_uint32), ("reserved", ctypes.c_uint32 * 5)]
+                ("uploaded", ctypes.c_uint32), ("heavy_rows", ctypes.c_uint32),
+                ("heavy_cols", ctypes.c_uint32), ("heavy_kib", ctypes.c_uint32),
+                ("reserved", ctypes.c_uint32 * 2)]
 
 
 class K2TError(RuntimeError):

@@ -102,7 +102,12 @@ typedef struct {
     uint32_t band_rows;           /* BANDED: rows per band (power of two, 16..65536); default 4096 */
     uint32_t band_cols;           /* BANDED: columns per tile (power of two >= 16); default 2^23;
                                      0 = one column band                                             */
-    uint32_t reserved[6];
+    uint32_t heavy_terms;         /* plus-times: an output with more than this many non-zeros in
+                                     its row (right) or column (left), counted over the input list,
+                                     is summed in fp64 and rounded to fp32 once; every other output
+                                     is summed in fp32.  Default 2048; 0 = default; 0xffffffff =
+                                     never.  See "Accumulation precision" below.                     */
+    uint32_t reserved[5];
 } k2t_opts;
 
 /* ---- statistics -------------------------------------------------------- */
@@ -130,7 +135,11 @@ typedef struct {
     uint32_t engine;              /* resolved engine                               */
     uint32_t offsets;
     uint32_t uploaded;            /* 1 after k2t_upload                            */
-    uint32_t reserved[5];
+    uint32_t heavy_rows;          /* outputs of right products summed in fp64      */
+    uint32_t heavy_cols;          /* outputs of left products summed in fp64       */
+    uint32_t heavy_kib;           /* device KiB of the fp64 path's tables and
+                                     accumulators (part of workspace_bytes)        */
+    uint32_t reserved[2];
 } k2t_stats;
 
 /* Fill *o with the defaults: k = 2, tree-only FUSED engine (AUTO), directory
@@ -151,7 +160,8 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
               uint64_t n_rows, uint64_t n_cols, const k2t_opts *opts, k2t_tree **out);
 
 /* Exact device bytes k2t_upload places in its arena (tree, directory, top,
- * cached level, plan, scratch, optional host-product vectors), known before
+ * cached level, plan, scratch, the fp64 path's tables and accumulators,
+ * optional host-product vectors), known before
  * any kernel runs (section 1, "Our approach").  Dense x and y of device
  * products are the caller's and not included. */
 int k2t_workspace_bytes(const k2t_tree *t, uint64_t *bytes);
@@ -167,12 +177,19 @@ int k2t_upload(k2t_tree *t, void *arena, uint64_t arena_bytes, void *stream);
  * weight w (Table 1: plus-times w = 1, tropical w = 1 for hop counts; the
  * Boolean semiring ignores w), for B vectors, on device buffers, queued on
  * `stream`.  y is overwritten with the semiring zero first (Algorithm 1,
- * line 1).  Plus-times sums in fp32 in no fixed order; Boolean and tropical
- * results are exact and deterministic.  Tropical minima follow the IEEE
- * total order without NaN (-0 < +0); NaN inputs give unspecified values.
+ * line 1).  Boolean and tropical results are exact and deterministic.
+ * Tropical minima follow the IEEE total order without NaN (-0 < +0); NaN
+ * inputs give unspecified values.
+ * Accumulation precision (plus-times): sums run in no fixed order.  An
+ * output with at most opts.heavy_terms non-zeros is summed in fp32, so its
+ * rounding error stays that of an fp32 sum of at most that many terms; an
+ * output with more is summed in fp64 (each term w*x_j formed in fp32, the
+ * two terms of a leaf row added in fp32) and rounded to fp32 once, at the
+ * end of the product.  The fp64 sums need B <= opts.max_batch.
  * x and y must be 4-byte aligned (16-byte alignment enables vector access).
  * Errors: ESTATE (not uploaded), EINVAL (bad dir/semiring, null, B = 0,
- * overlap), ERANGE (B > 32), ECUDA (launch failure). */
+ * overlap), ERANGE (B > 32; plus-times with fp64 outputs and
+ * B > opts.max_batch), ECUDA (launch failure). */
 int k2t_spmv(k2t_tree *t, int32_t dir, int32_t semiring, float w,
              const void *x, void *y, uint32_t B, void *stream);
 

@@ -64,8 +64,9 @@ def test_random_ragged(seed):
     rows, cols, _ = synth.random_small(seed, nr, nc, float(rng.choice([0.002, 0.02, 0.2])))
     ot = oracle.OracleTree(rows, cols, nr, nc, n_k4=n_k4)
     top = int(rng.choice([1, 16, 65536]))
+    heavy = int(rng.choice([0, 3, 12]))  # small limits send most outputs to the fp64 sums
     for kw in ENGINES:
-        t = _tree(rows, cols, nr, nc, n_k4_levels=n_k4, host_top_max_nodes=top, **kw)
+        t = _tree(rows, cols, nr, nc, n_k4_levels=n_k4, host_top_max_nodes=top, heavy_terms=heavy, **kw)
         for semiring in (PLUS_TIMES, BOOLEAN, TROPICAL):
             for B in (1, 2, 3, 4, 8, 32):
                 if semiring == BOOLEAN and B not in (1, 3, 32):
@@ -76,7 +77,34 @@ def test_random_ragged(seed):
                 w = float(rng.choice([1.0, 0.5, 2.0])) if semiring != BOOLEAN else 1.0
                 ref = ot.spmv(d, semiring, x, B=B, w=w)
                 got = device_product(t, d, semiring, x, B, w=w)
-                assert_match(semiring, got, ref, "seed%d %s sr%d B%d d%d" % (seed, kw, semiring, B, d))
+                assert_match(semiring, got, ref, "seed%d %s h%d sr%d B%d d%d" % (seed, kw, heavy, semiring, B, d))
+
+
+@pytest.mark.parametrize("heavy_terms", [0, 4])
+def test_fp64_outputs_exact(heavy_terms):
+    """Row 0 and column 0 hold 5000 non-zeros, more than the fp64 limit
+    (default 2048, or 4): with x_0 = 2^24 and x_j = 1 for the other 4999,
+    the sum 2^24 + 4999 is exact in fp64 and rounds once to the nearest fp32,
+    whatever the order of the atomics.  An fp32 sum can lose each 1 against
+    2^24 (up to 4999 off, far beyond the plus-times bound).  Outputs 1..4999
+    hold the single term 2^24, the rest zero."""
+    n = 8192
+    j = np.arange(5000, dtype=np.uint32)
+    rows = np.concatenate([np.zeros(5000, np.uint32), j[1:]])
+    cols = np.concatenate([j, np.zeros(4999, np.uint32)])
+    want = np.zeros(n, np.float32)
+    want[0] = np.float32(np.float64(2 ** 24) + 4999.0)
+    want[1:5000] = np.float32(2 ** 24)
+    for kw in ENGINES:
+        t = _tree(rows, cols, n, n, heavy_terms=heavy_terms, host_top_max_nodes=16, **kw)
+        s = t.stats()
+        assert (s.heavy_rows, s.heavy_cols) == (1, 1)
+        for B in (1, 2, 3, 4, 16):
+            x = np.ones((n, B), np.float32)
+            x[0] = 2.0 ** 24
+            for d in (RIGHT, LEFT):
+                got = device_product(t, d, PLUS_TIMES, x, B)
+                assert np.array_equal(got, np.repeat(want[:, None], B, axis=1)), (kw, B, d, got[0])
 
 
 def test_uniform_1024_plus_times():

@@ -147,7 +147,9 @@ def test_options_struct_matches_header():
     """The binding's k2t_opts mirrors the header: defaults round-trip."""
     o = K.default_opts()
     assert o.band_rows == 4096 and o.chunk_cap == 2048 and o.tile_m == 1 << 20 and o.max_batch == 32
-    assert ctypes.sizeof(K.Opts) == 80  # 6 x u32, u64, 5 x u32, 7 reserved
+    assert o.heavy_terms == 2048
+    assert ctypes.sizeof(K.Opts) == 80  # 6 x u32, u64, 5 x u32, heavy_terms, 5 reserved
+    assert ctypes.sizeof(K.Stats) == 432
     with pytest.raises(K.K2TError):
         K.Tree(np.zeros(1, np.uint32), np.zeros(1, np.uint32), 8, 8, engine=4, cache_last_internal=1,
                band_rows=100)
@@ -182,3 +184,37 @@ def test_library_exports_every_declared_symbol():
     for name in declared:
         assert hasattr(lib, name), name
     assert declared == set(K.EXPORTED)
+
+
+@pytest.mark.parametrize("heavy_terms", [0, 5, 30, 0xFFFFFFFF])
+def test_heavy_outputs_stats(heavy_terms):
+    """Outputs summed in fp64 are those with more than heavy_terms non-zeros
+    in the input list (0 selects the default 2048); the fp64 tables take one
+    bit per leaf, two words per 32 outputs and one word per fp64 output per
+    direction, plus max_batch fp64 sums per fp64 output of the wider side."""
+    rng = np.random.default_rng(21)
+    nr, nc = 300, 200
+    rows, cols, _ = synth.random_small(3, nr, nc, 0.05)
+    hub_r = np.full(150, 7, np.uint32)
+    hub_c = rng.integers(0, nc, size=150).astype(np.uint32)
+    rows = np.concatenate([rows, hub_r, rng.integers(0, nr, size=120).astype(np.uint32)])
+    cols = np.concatenate([cols, hub_c, np.full(120, 11, np.uint32)])
+    t = K.Tree(rows, cols, nr, nc, heavy_terms=heavy_terms, max_batch=4)
+    s = t.stats()
+    lim = 2048 if heavy_terms == 0 else heavy_terms
+    hr = int((np.bincount(rows, minlength=nr) > lim).sum()) if rows.size > lim else 0
+    hc = int((np.bincount(cols, minlength=nc) > lim).sum()) if rows.size > lim else 0
+    assert (s.heavy_rows, s.heavy_cols) == (hr, hc)
+    if heavy_terms == 5:
+        assert hr > 1 and hc > 1
+    if heavy_terms == 30:
+        assert hr >= 1 and hc >= 1
+    nl = int(s.level_nodes[s.levels - 1])
+    want = 0
+    for h, n in ((hr, nr), (hc, nc)):
+        if h:
+            want += ((nl + 31) // 32 + 1) * 4 + 2 * ((n + 31) // 32) * 4 + 4 * h
+    want += max(hr, hc) * 4 * 8
+    assert s.heavy_kib == (want + 1023) // 1024
+    base = K.Tree(rows, cols, nr, nc, heavy_terms=0xFFFFFFFF, max_batch=4).workspace_bytes()
+    assert want <= t.workspace_bytes() - base <= want + 7 * 256
