@@ -159,14 +159,19 @@ __device__ __forceinline__ uint32_t heavy_word(const VecArgs &va, uint32_t out)
     return ((e.y + (uint32_t)__popc(e.x & ((1u << sh) - 1u))) << 2) | m;
 }
 
-// Add the VW-wide slice k of output out + q (hv from heavy_word) to its fp64 sum.
+// Add the VW-wide slice k of output out + q (hv from heavy_word) to its fp64
+// sum: the leaf's cells in that output contribute w*xa (when ua) and w*xb
+// (when ub), each formed in fp32 and added in fp64, where the sum of two
+// floats is exact.
 template <int VW>
-__device__ __forceinline__ void heavy_add(const VecArgs &va, uint32_t hv, int q, uint32_t k, const float (&v)[VW])
+__device__ __forceinline__ void heavy_add(const VecArgs &va, uint32_t hv, int q, uint32_t k, const float (&xa)[VW],
+                                          const float (&xb)[VW], bool ua, bool ub)
 {
     const uint32_t id = (hv >> 2) + (q ? (hv & 1u) : 0u);
     double *a = va.acc + (size_t)id * va.B + k;
 #pragma unroll
-    for (int i = 0; i < VW; ++i) atomicAdd(a + i, (double)v[i]);
+    for (int i = 0; i < VW; ++i)
+        atomicAdd(a + i, (ua ? (double)(va.w * xa[i]) : 0.0) + (ub ? (double)(va.w * xb[i]) : 0.0));
 }
 
 template <int VW> struct VecLoad;
@@ -272,11 +277,11 @@ __device__ __forceinline__ void leaf_group(const uint32_t (&lam)[U], const uint3
                 } else {
                     const uint32_t h = SR == K2T_PLUS_TIMES && ((fl >> u) & 1u) ? heavy_word(a, out[u]) : 0u;
                     if (a0[u] || a1[u]) {
-                        if (h & 1u) heavy_add<VW>(a, h, 0, k, v0);
+                        if (h & 1u) heavy_add<VW>(a, h, 0, k, x0[u], x1[u], a0[u], a1[u]);
                         else S::update(y + (size_t)out[u] * B + k, v0);
                     }
                     if (b0[u] || b1[u]) {
-                        if (h & 2u) heavy_add<VW>(a, h, 1, k, v1);
+                        if (h & 2u) heavy_add<VW>(a, h, 1, k, x0[u], x1[u], b0[u], b1[u]);
                         else S::update(y + (size_t)(out[u] + 1) * B + k, v1);
                     }
                 }
@@ -454,14 +459,15 @@ __device__ __forceinline__ void node_leaves_spec(uint32_t sg, uint32_t off, Coor
             const float c0 = S::contrib(__uint_as_float(xo[b][0]), va.w);
             const float c1 = S::contrib(__uint_as_float(xo[b][1]), va.w);
             const uint32_t h = SR == K2T_PLUS_TIMES && ((fl >> b) & 1u) ? heavy_word(va, out) : 0u;
+            const float xa[1] = {__uint_as_float(xo[b][0])}, xb[1] = {__uint_as_float(xo[b][1])};
             if (a0 || a1) {
                 const float v[1] = {a0 ? (a1 ? S::plus(c0, c1) : c0) : c1};
-                if (h & 1u) heavy_add<1>(va, h, 0, 0u, v);
+                if (h & 1u) heavy_add<1>(va, h, 0, 0u, xa, xb, a0, a1);
                 else if (!S::skip(v[0])) S::update(y + out, v);
             }
             if (b0 || b1) {
                 const float v[1] = {b0 ? (b1 ? S::plus(c0, c1) : c0) : c1};
-                if (h & 2u) heavy_add<1>(va, h, 1, 0u, v);
+                if (h & 2u) heavy_add<1>(va, h, 1, 0u, xa, xb, b0, b1);
                 else if (!S::skip(v[0])) S::update(y + out + 1, v);
             }
         }
@@ -549,9 +555,10 @@ __device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint
             const float c0 = S::contrib(__uint_as_float(xo[u][0]), va.w);
             const float c1 = S::contrib(__uint_as_float(xo[u][1]), va.w);
             const uint32_t h = SR == K2T_PLUS_TIMES && ((fl >> u) & 1u) ? heavy_word(va, out[u]) : 0u;
+            const float xa[1] = {__uint_as_float(xo[u][0])}, xb[1] = {__uint_as_float(xo[u][1])};
             if (a0 || a1) {
                 const float v[1] = {a0 ? (a1 ? S::plus(c0, c1) : c0) : c1};
-                if (h & 1u) heavy_add<1>(va, h, 0, 0u, v);
+                if (h & 1u) heavy_add<1>(va, h, 0, 0u, xa, xb, a0, a1);
                 else if (!S::skip(v[0])) {
                     if (win) smem_update<SR>(win + (out[u] - lo), __float_as_uint(v[0]));
                     else S::update(y + out[u], v);
@@ -559,7 +566,7 @@ __device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint
             }
             if (b0 || b1) {
                 const float v[1] = {b0 ? (b1 ? S::plus(c0, c1) : c0) : c1};
-                if (h & 2u) heavy_add<1>(va, h, 1, 0u, v);
+                if (h & 2u) heavy_add<1>(va, h, 1, 0u, xa, xb, b0, b1);
                 else if (!S::skip(v[0])) {
                     if (win) smem_update<SR>(win + (out[u] + 1 - lo), __float_as_uint(v[0]));
                     else S::update(y + out[u] + 1, v);
@@ -620,13 +627,9 @@ __device__ __forceinline__ void warp_window_flush(const uint32_t *win, uint32_t 
     }
 }
 
-// Leaves [jb, je) of a warp, dealt round-robin to its lanes, kLeafU per lane
-// per round.  leaf_at(j, lam, r, c) gives leaf j's cells and the origin of its
-// 2x2 block.  For one vector slice (B = 1 fp32, or a Boolean word) both input
-// entries of the block are read with one 8-byte load together with the leaf
-// signature; updates go to the window when there is one, else to y.
 // One VW-wide vector slice k of one leaf (origin r, c; cells lam): gathers the
-// slice of the inputs it needs, combines per output, updates y or the window.
+// slice of the inputs it needs, combines per output, updates y or the window;
+// outputs marked in hv (heavy_word) go to their fp64 sums.
 template <int SR, int DIR, int VW>
 __device__ __forceinline__ void leaf_slice(uint32_t lam, uint32_t r, uint32_t c, uint32_t k, uint32_t hv,
                                            const VecArgs &va, uint32_t *win, uint32_t lo)
@@ -644,36 +647,43 @@ __device__ __forceinline__ void leaf_slice(uint32_t lam, uint32_t r, uint32_t c,
     float x0[VW], x1[VW];
     if (a0 || b0) VecLoad<VW>::load(x + (size_t)in * B + k, x0);
     if (a1 || b1) VecLoad<VW>::load(x + (size_t)(in + 1) * B + k, x1);
-    float v0[VW], v1[VW];
-#pragma unroll
-    for (int q = 0; q < VW; ++q) {
-        const float c0 = (a0 || b0) ? S::contrib(x0[q], va.w) : S::zero();
-        const float c1 = (a1 || b1) ? S::contrib(x1[q], va.w) : S::zero();
-        v0[q] = a0 ? (a1 ? S::plus(c0, c1) : c0) : c1;
-        v1[q] = b0 ? (b1 ? S::plus(c0, c1) : c0) : c1;
-    }
-    const uint32_t h = SR == K2T_PLUS_TIMES ? hv : 0u;
-    const bool ya = (a0 || a1) && !(h & 1u), yb = (b0 || b1) && !(h & 2u);
-    if (h & 1u) {
-        if (a0 || a1) heavy_add<VW>(va, h, 0, k, v0);
-    }
-    if (h & 2u) {
-        if (b0 || b1) heavy_add<VW>(va, h, 1, k, v1);
-    }
-    if (win) {
+    // One output's update from x0, x1 (cells u0 on input in, u1 on in + 1).
+    auto put = [&](uint32_t o, bool u0, bool u1) {
+        float v[VW];
 #pragma unroll
         for (int q = 0; q < VW; ++q) {
-            if (ya && !S::skip(v0[q])) smem_update<SR>(win + (size_t)(out - lo) * B + k + q, __float_as_uint(v0[q]));
-            if (yb && !S::skip(v1[q])) smem_update<SR>(win + (size_t)(out + 1 - lo) * B + k + q, __float_as_uint(v1[q]));
+            const float c0 = u0 ? S::contrib(x0[q], va.w) : S::zero();
+            const float c1 = u1 ? S::contrib(x1[q], va.w) : S::zero();
+            v[q] = u0 ? (u1 ? S::plus(c0, c1) : c0) : c1;
         }
-    } else {
-        if (ya) S::update(y + (size_t)out * B + k, v0);
-        if (yb) S::update(y + (size_t)(out + 1) * B + k, v1);
+        if (win) {
+#pragma unroll
+            for (int q = 0; q < VW; ++q)
+                if (!S::skip(v[q])) smem_update<SR>(win + (size_t)(o - lo) * B + k + q, __float_as_uint(v[q]));
+        } else {
+            S::update(y + (size_t)o * B + k, v);
+        }
+    };
+    if (SR == K2T_PLUS_TIMES && hv) {
+        // a leaf with an fp64 output: separate branch, so the fp32 path below
+        // keeps its registers
+        if (a0 || a1) {
+            if (hv & 1u) heavy_add<VW>(va, hv, 0, k, x0, x1, a0, a1);
+            else put(out, a0, a1);
+        }
+        if (b0 || b1) {
+            if (hv & 2u) heavy_add<VW>(va, hv, 1, k, x0, x1, b0, b1);
+            else put(out + 1, b0, b1);
+        }
+        return;
     }
+    if (a0 || a1) put(out, a0, a1);
+    if (b0 || b1) put(out + 1, b0, b1);
 }
 
-// Leaves [jb, je) of a warp.  leaf_at(j, lam, r, c) gives leaf j's cells and
-// the origin of its 2x2 block.
+// Leaves [jb, je) of a warp.  leaf_at(j, lam, r, c, li) gives leaf j's cells,
+// the origin of its 2x2 block and its index in the leaf level (for the fp64
+// output flags).
 //  - One vector slice (B = 1 fp32, or a Boolean word): leaves dealt round-
 //    robin, kLeafU per lane per round; both input entries of a block come in
 //    one 8-byte load together with the leaf signature.

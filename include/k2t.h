@@ -183,9 +183,8 @@ int k2t_upload(k2t_tree *t, void *arena, uint64_t arena_bytes, void *stream);
  * Accumulation precision (plus-times): sums run in no fixed order.  An
  * output with at most opts.heavy_terms non-zeros is summed in fp32, so its
  * rounding error stays that of an fp32 sum of at most that many terms; an
- * output with more is summed in fp64 (each term w*x_j formed in fp32, the
- * two terms of a leaf row added in fp32) and rounded to fp32 once, at the
- * end of the product.  The fp64 sums need B <= opts.max_batch.
+ * output with more is summed in fp64 (each term w*x_j formed in fp32, then
+ * added in fp64) and rounded to fp32 once, at the end of the product.  The fp64 sums need B <= opts.max_batch.
  * x and y must be 4-byte aligned (16-byte alignment enables vector access).
  * Errors: ESTATE (not uploaded), EINVAL (bad dir/semiring, null, B = 0,
  * overlap), ERANGE (B > 32; plus-times with fp64 outputs and
