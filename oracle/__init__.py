@@ -50,7 +50,7 @@ def build() -> str:
 
 class _Tree(ctypes.Structure):
     _fields_ = [("levels", ctypes.c_int32), ("n_k4", ctypes.c_int32),
-                ("dim_bits", ctypes.c_int32), ("pad_", ctypes.c_int32),
+                ("dim_bits", ctypes.c_int32), ("leaf_k4", ctypes.c_int32),
                 ("nodes", ctypes.c_uint64 * _MAX_LEVELS),
                 ("start", ctypes.c_uint64 * (_MAX_LEVELS + 1)),
                 ("t_bits", ctypes.c_uint64), ("nwords", ctypes.c_uint64),
@@ -66,7 +66,7 @@ def _load():
         lib = ctypes.CDLL(build())
         P = ctypes.c_void_p
         lib.orc_build.argtypes = [P, P, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
-                                  ctypes.c_int32, ctypes.POINTER(_Tree)]
+                                  ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(_Tree)]
         lib.orc_build.restype = ctypes.c_int
         lib.orc_free.argtypes = [ctypes.POINTER(_Tree)]
         lib.orc_rank1.argtypes = [ctypes.POINTER(_Tree), ctypes.c_uint64]
@@ -103,16 +103,19 @@ class OracleResult:
 
 
 class OracleTree:
-    """k^2-tree of section 2.1 built by recursive subdivision (test oracle)."""
+    """k^2-tree of section 2.1 built by recursive subdivision (test oracle).
+    n_k4: leading levels with k = 4; leaf_k = 4: 4x4 leaf bitmaps (section 5.6)."""
 
-    def __init__(self, rows, cols, n_rows: int, n_cols: int, n_k4: int = 0):
+    def __init__(self, rows, cols, n_rows: int, n_cols: int, n_k4: int = 0, leaf_k: int = 2):
         lib = _load()
+        if leaf_k not in (2, 4):
+            raise ValueError("leaf_k must be 2 or 4")
         self.rows = np.ascontiguousarray(rows, dtype=np.uint32)
         self.cols = np.ascontiguousarray(cols, dtype=np.uint32)
         self.n_rows, self.n_cols = int(n_rows), int(n_cols)
         self._t = _Tree()
         rc = lib.orc_build(_ptr(self.rows), _ptr(self.cols), self.rows.size,
-                           self.n_rows, self.n_cols, int(n_k4), ctypes.byref(self._t))
+                           self.n_rows, self.n_cols, int(n_k4), int(leaf_k == 4), ctypes.byref(self._t))
         if rc != 0:
             raise ValueError("oracle build failed (%d)" % rc)
 
@@ -130,6 +133,10 @@ class OracleTree:
     @property
     def n_k4(self) -> int:
         return self._t.n_k4
+
+    @property
+    def leaf_k(self) -> int:
+        return 4 if self._t.leaf_k4 else 2
 
     @property
     def dim_bits(self) -> int:

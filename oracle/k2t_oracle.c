@@ -41,6 +41,9 @@
  * Hybrid trees: the first n_k4 levels may use k = 4 (16-bit signatures,
  * quadrant b = 4*br + bc in row-major order, which reduces to b = 2*b1 + b0
  * for k = 2).  The pages describe k = 2 only; this is the plainest extension.
+ * The leaf level may use k = 4 as well (leaf_k4 = 1): leaves are then 4x4
+ * bitmaps, cell (dr, dc) at bit 4*dr + dc, the "leaves larger than 2x2" the
+ * pages name as the next lever (section 5.6).  Every other level keeps k = 2.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -52,7 +55,7 @@ typedef struct {
     int32_t levels;                     /* number of levels; root = 0, leaves = levels-1 */
     int32_t n_k4;                       /* leading levels with k = 4 */
     int32_t dim_bits;                   /* padded side = 2^dim_bits */
-    int32_t pad_;
+    int32_t leaf_k4;                    /* 1: the leaf level has k = 4 */
     uint64_t nodes[ORC_MAX_LEVELS];     /* nodes per level */
     uint64_t start[ORC_MAX_LEVELS + 1]; /* bit offset of each level; start[levels] = total bits */
     uint64_t t_bits;                    /* bits in T (levels 0..levels-2) */
@@ -61,13 +64,18 @@ typedef struct {
     uint64_t *cum;                      /* cum[w] = set bits in words [0, w) */
 } orc_tree;
 
-static int level_k(const orc_tree *t, int d) { return d < t->n_k4 ? 4 : 2; }
+static int level_k(const orc_tree *t, int d)
+{
+    if (d < t->n_k4) return 4;
+    if (t->leaf_k4 && d == t->levels - 1) return 4;
+    return 2;
+}
 
 /* side of the square block covered by a node of level d */
 static uint64_t level_side(const orc_tree *t, int d)
 {
     int used = 0;
-    for (int e = 0; e < d; ++e) used += (e < t->n_k4) ? 2 : 1;
+    for (int e = 0; e < d; ++e) used += level_k(t, e) == 4 ? 2 : 1;
     return (uint64_t)1 << (t->dim_bits - used);
 }
 
@@ -91,23 +99,27 @@ void orc_free(orc_tree *t)
 
 typedef struct { uint64_t r0, c0; uint64_t lo, hi; } orc_node; /* block origin, edge range */
 
-/* Returns 0 on success, -1 on bad arguments, -2 on allocation failure. */
+/* Returns 0 on success, -1 on bad arguments, -2 on allocation failure.
+ * The side is padded to 2^bits with at least one k = 2 level below the k = 4
+ * top (so a last internal level with k = 2 exists): bits >= 2*n_k4 + 2, and
+ * with 4x4 leaves bits >= 2*n_k4 + 3. */
 int orc_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
-              uint64_t n_rows, uint64_t n_cols, int32_t n_k4, orc_tree *out)
+              uint64_t n_rows, uint64_t n_cols, int32_t n_k4, int32_t leaf_k4, orc_tree *out)
 {
     memset(out, 0, sizeof(*out));
-    if (n_rows == 0 || n_cols == 0 || n_k4 < 0) return -1;
+    if (n_rows == 0 || n_cols == 0 || n_k4 < 0 || leaf_k4 < 0 || leaf_k4 > 1) return -1;
     uint64_t n = n_rows > n_cols ? n_rows : n_cols;
     int bits = 0;
     while (((uint64_t)1 << bits) < n) ++bits;
     if (bits < 2) bits = 2;
-    if (bits < 2 * n_k4 + 2) bits = 2 * n_k4 + 2;
+    if (bits < 2 * n_k4 + 2 + leaf_k4) bits = 2 * n_k4 + 2 + leaf_k4;
     if (bits > 32) return -1;
     for (uint64_t i = 0; i < nnz; ++i)
         if (rows[i] >= n_rows || cols[i] >= n_cols) return -1;
     out->dim_bits = bits;
     out->n_k4 = n_k4;
-    out->levels = bits - n_k4;
+    out->leaf_k4 = leaf_k4;
+    out->levels = bits - n_k4 - leaf_k4;
 
     /* Edge indices, partitioned per node; two arrays alternate per level. */
     uint64_t *idx = (uint64_t *)malloc((nnz ? nnz : 1) * sizeof(uint64_t));

@@ -174,16 +174,18 @@ def _check_equal(semiring, got, want, scale=None):
         assert np.array_equal(np.asarray(got).view(np.uint32), np.asarray(want).view(np.uint32))
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", range(16))
 def test_brute_force_small(seed):
     rng = np.random.default_rng(1000 + seed)
     n_rows = int(rng.integers(1, 70))
     n_cols = int(rng.integers(1, 70))
     n_k4 = int(rng.integers(0, 3)) if max(n_rows, n_cols) > 4 else 0
+    leaf_k = 4 if seed % 2 else 2
     rows, cols, _ = synth.random_small(seed, n_rows, n_cols, float(rng.choice([0.01, 0.05, 0.3])))
     A = np.zeros((n_rows, n_cols), dtype=bool)
     A[rows, cols] = True
-    t = oracle.OracleTree(rows, cols, n_rows, n_cols, n_k4=n_k4)
+    t = oracle.OracleTree(rows, cols, n_rows, n_cols, n_k4=n_k4, leaf_k=leaf_k)
+    assert t.leaf_k == leaf_k
     for semiring in (PLUS_TIMES, BOOLEAN, TROPICAL):
         for B in (1, 3, 32):
             for direction in (RIGHT, LEFT):
@@ -206,10 +208,13 @@ def _level_side(dim_bits, n_k4, d):
     return 1 << (dim_bits - used)
 
 
-@pytest.mark.parametrize("n_k4", [0, 1, 2])
-def test_invariants(n_k4):
+@pytest.mark.parametrize("n_k4,leaf_k", [(0, 2), (1, 2), (2, 2), (0, 4), (1, 4), (2, 4)])
+def test_invariants(n_k4, leaf_k):
     rows, cols, _ = synth.random_small(7 + n_k4, 300, 200, 0.01)
-    t = oracle.OracleTree(rows, cols, 300, 200, n_k4=n_k4)
+    t = oracle.OracleTree(rows, cols, 300, 200, n_k4=n_k4, leaf_k=leaf_k)
+    # side 2^9 = 512; levels: n_k4 of k = 4, then k = 2, then the leaf level
+    assert t.dim_bits == 9 and t.levels == 9 - n_k4 - (leaf_k == 4)
+    assert _level_side(t.dim_bits, n_k4, t.levels - 1) == leaf_k
     bits = t.bits()
     start = t.level_start()
     nodes = t.level_nodes()
@@ -224,6 +229,28 @@ def test_invariants(n_k4):
     assert int(bits[start[t.levels - 1]:].sum()) == r.size          # popcount(L) = nnz
     dr, dc = t.decode()
     assert sorted(zip(dr.tolist(), dc.tolist())) == sorted(zip(r.tolist(), c.tolist()))
+
+
+def test_figure1_leaf4_by_hand():
+    """The Figure 1 matrix (8 x 8) with 4 x 4 leaves, derived by hand from its
+    twelve cells: the root's four quadrants of side 4 are all non-empty
+    (T = 1111), and each leaf lists its cells at bit 4*dr + dc:
+      rows 0-3, cols 0-3: (1,1)                   -> bit 5
+      rows 0-3, cols 4-7: (0,4) (1,5) (3,5)       -> bits 0, 5, 13
+      rows 4-7, cols 0-3: (5,1) (5,2) (6,1) (6,2) -> bits 5, 6, 9, 10
+      rows 4-7, cols 4-7: (6,6) (6,7) (7,6) (7,7) -> bits 10, 11, 14, 15"""
+    g = json.load(open(GOLDEN))
+    e = np.array(g["edges_decoded"], np.uint32)
+    t = oracle.OracleTree(e[:, 0], e[:, 1], 8, 8, leaf_k=4)
+    assert t.levels == 2 and t.level_nodes() == [1, 4]
+    assert t.bitstring(0) == "1111"
+    assert t.bitstring(1) == ("0000010000000000" "1000010000000100"
+                              "0000011001100000" "0000000000110011")
+    assert t.child_pos(0, 2) == 4 + 2 * 16  # third set bit of the root -> third leaf
+    x = np.arange(1, 9, dtype=np.float32).reshape(8, 1)
+    y = t.spmv(RIGHT, PLUS_TIMES, x).y[:, 0]
+    # x_c = c + 1 summed over each row's columns: row 6 has 1, 2, 6, 7 -> 2+3+7+8
+    assert y.tolist() == [5.0, 8.0, 0.0, 6.0, 0.0, 5.0, 20.0, 15.0]
 
 
 def test_left_equals_right_of_transpose():
