@@ -228,7 +228,7 @@ int enqueue_product(k2t_tree *t, int32_t dir, int32_t semiring, float w, const v
     va.n_out = n_out;
     va.n_in = dir == K2T_RIGHT ? t->n_cols : t->n_rows;
     const bool heavy = heavy_begin(t, d, dir, semiring, va, st);
-    pick(t->engine, semiring, dir, vw)(t, d, va, st);
+    pick(t->leaf_k4 ? kEngineCached4 : t->engine, semiring, dir, vw)(t, d, va, st);
     if (heavy) heavy_end(t, d, dir, va, st);
     return K2T_OK;
 }
@@ -271,7 +271,7 @@ int k2t_upload(k2t_tree *t, void *arena, uint64_t arena_bytes, void *stream)
         if (L.sig_bytes[lv]) {
             uint8_t *p = at<uint8_t>(d->arena, L.sig_off[lv]);
             d->tree.lv[lv].sig = p;
-            uint64_t bytes = (t->nodes[(size_t)lv] + 1) / 2;
+            uint64_t bytes = level_is_k4(t, lv) ? 2 * t->nodes[(size_t)lv] : (t->nodes[(size_t)lv] + 1) / 2;
             if (bytes && (e = cudaMemcpyAsync(p, t->sig[(size_t)lv].data(), bytes, cudaMemcpyHostToDevice, st)) != cudaSuccess)
                 return fail(e);
         }

@@ -59,17 +59,21 @@ inline uint64_t spread_bits(uint32_t v)
 }
 
 // Path key of cell (r, c): interleaved bits with the row bit first in every
-// pair (quadrant b = 2*b1 + b0), except that each of the first n_k4 nibbles is
-// reordered from (r1 c1 r0 c0) to the row-major k = 4 digit (r1 r0 c1 c0).
-inline uint64_t path_key(uint32_t r, uint32_t c, int dim_bits, int n_k4)
+// pair (quadrant b = 2*b1 + b0), except that each of the first n_k4 nibbles
+// (and the last nibble, for 4x4 leaves) is reordered from (r1 c1 r0 c0) to the
+// row-major k = 4 digit (r1 r0 c1 c0).
+inline uint64_t k4_digit(uint64_t m, int sh)
+{
+    uint64_t nib = (m >> sh) & 15u;
+    uint64_t dig = (nib & 9u) | ((nib & 4u) >> 1) | ((nib & 2u) << 1);
+    return (m & ~(15ull << sh)) | (dig << sh);
+}
+
+inline uint64_t path_key(uint32_t r, uint32_t c, int dim_bits, int n_k4, int leaf_k4)
 {
     uint64_t m = (spread_bits(r) << 1) | spread_bits(c);
-    for (int i = 0; i < n_k4; ++i) {
-        int sh = 2 * dim_bits - 4 * (i + 1);
-        uint64_t nib = (m >> sh) & 15u;
-        uint64_t dig = (nib & 9u) | ((nib & 4u) >> 1) | ((nib & 2u) << 1);
-        m = (m & ~(15ull << sh)) | (dig << sh);
-    }
+    for (int i = 0; i < n_k4; ++i) m = k4_digit(m, 2 * dim_bits - 4 * (i + 1));
+    if (leaf_k4) m = k4_digit(m, 0);
     return m;
 }
 
@@ -181,7 +185,7 @@ size_t group_level(const uint64_t *in, size_t n, int s, uint64_t *out_prefix, ui
 
 void pack_level(k2t_tree *t, int d, const uint16_t *sg, size_t n, int nt)
 {
-    bool k4 = d < t->n_k4;
+    bool k4 = level_is_k4(t, d);
     size_t per = k4 ? 4 : 16;
     size_t words = (n + per - 1) / per;
     std::vector<uint64_t> &out = t->sig[(size_t)d];
@@ -226,7 +230,7 @@ void build_directory(k2t_tree *t, int d, int nt)
 
 uint32_t level_sig(const k2t_tree *t, int d, uint64_t node)
 {
-    if (d < t->n_k4) return (uint32_t)((t->sig[(size_t)d][node / 4] >> (16 * (node % 4))) & 0xffffu);
+    if (level_is_k4(t, d)) return (uint32_t)((t->sig[(size_t)d][node / 4] >> (16 * (node % 4))) & 0xffffu);
     return (uint32_t)((t->sig[(size_t)d][node / 16] >> (4 * (node % 16))) & 15u);
 }
 
@@ -460,11 +464,12 @@ void heavy_outputs(const uint32_t *ids, uint64_t nnz, uint64_t n, uint32_t limit
 }
 
 // Leaf flags of one direction: bit i set when leaf i (level order; block
-// origin (2 q.r, 2 q.c)) has an fp64 output among its two rows (dir 0) or
-// columns (dir 1).  prefixes[i] is leaf i's path prefix.
+// origin (side*q.r, side*q.c), side 2 or 4) has an fp64 output among its rows
+// (dir 0) or columns (dir 1).  prefixes[i] is leaf i's path prefix.
 void heavy_leaf_flags(k2t_tree *t, int dir, const uint64_t *prefixes, uint64_t nl, int nt)
 {
     const std::vector<uint32_t> &ent = t->hent[dir];
+    const uint32_t side = t->leaf_k4 ? 4u : 2u, mask = t->leaf_k4 ? 15u : 3u;
     std::vector<uint32_t> &fl = t->hflag[dir];
     fl.assign((nl + 31) / 32 + 1, 0);
     const int d = t->levels - 1;
@@ -475,8 +480,9 @@ void heavy_leaf_flags(k2t_tree *t, int dir, const uint64_t *prefixes, uint64_t n
             uint32_t v = 0;
             for (uint64_t i = 32 * w; i < std::min<uint64_t>(32 * w + 32, nl); ++i) {
                 Coord q = prefix_coord(prefixes[i], d, t->n_k4);
-                uint64_t o = 2ull * (dir == 0 ? q.r : q.c);  // even: o and o + 1 share a group
-                if (((ent[2 * (o / 32)] >> (o % 32)) & 3u) != 0) v |= 1u << (i % 32);
+                // the leaf's outputs o .. o + side - 1 share a group of 32 (o is a multiple of the side)
+                uint64_t o = (uint64_t)side * (dir == 0 ? q.r : q.c);
+                if (((ent[2 * (o / 32)] >> (o % 32)) & mask) != 0) v |= 1u << (i % 32);
             }
             fl[w] = v;
         }
@@ -506,8 +512,8 @@ void compute_layout(k2t_tree *t)
         int first = cached ? l - 2 : t->d0;
         for (int d = first; d < l; ++d) {
             if (banded && d == l - 2) continue;  // signatures are kept in band order
-            // nibble bytes plus 16 bytes of slack for vector loads
-            L.sig_bytes[d] = (t->nodes[(size_t)d] + 1) / 2 + 16;
+            // nibble bytes (4x4 leaves: 2 bytes a node) plus 16 bytes of slack for vector loads
+            L.sig_bytes[d] = (t->leaf_k4 && d == l - 1 ? 2 * t->nodes[(size_t)d] : (t->nodes[(size_t)d] + 1) / 2) + 16;
             L.sig_off[d] = take(L.sig_bytes[d]);
         }
         bool want_dir = (ls && t->opts.offsets == K2T_OFFSETS_DIRECTORY);
@@ -606,6 +612,7 @@ void k2t_default_opts(k2t_opts *o)
     o->band_rows = 4096;
     o->band_cols = 1u << 23;
     o->heavy_terms = 2048;
+    o->leaf_k = 2;
 }
 
 int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
@@ -622,12 +629,17 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
     if (o.band_cols && (o.band_cols < 16 || (o.band_cols & (o.band_cols - 1)))) return K2T_EINVAL;
     if (!o.band_cols) o.band_cols = 1u << 31;
     if (!o.heavy_terms) o.heavy_terms = 2048;
+    if (!o.leaf_k) o.leaf_k = 2;
+    if (o.leaf_k != 2 && o.leaf_k != 4) return K2T_EINVAL;
     if (o.chunk_cap < 4 || o.chunk_cap > kMaxChunkCap || o.tile_m < 4) return K2T_EINVAL;
     if (o.max_batch < 1 || o.max_batch > K2T_MAX_BATCH) return K2T_ERANGE;
     if (o.host_top_max_nodes < 1) return K2T_EINVAL;
     if (o.n_k4_levels > 15) return K2T_EINVAL;
     if (n_rows > (1ull << 32) || n_cols > (1ull << 32)) return K2T_ERANGE;
     if ((o.engine == K2T_ENGINE_CACHED || o.engine == K2T_ENGINE_BANDED) && !o.cache_last_internal) return K2T_EINVAL;
+    // 4x4 leaves: the CACHED engine only
+    if (o.leaf_k == 4 && (!o.cache_last_internal || (o.engine != K2T_ENGINE_AUTO && o.engine != K2T_ENGINE_CACHED)))
+        return K2T_EINVAL;
 
     k2t_tree *t = new (std::nothrow) k2t_tree;
     if (!t) return K2T_ENOMEM;
@@ -639,11 +651,13 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
         int bits = 0;
         while ((1ull << bits) < n) ++bits;
         bits = std::max(bits, 2);
-        bits = std::max(bits, 2 * (int)o.n_k4_levels + 2);
+        const int leaf_k4 = o.leaf_k == 4 ? 1 : 0;
+        bits = std::max(bits, 2 * (int)o.n_k4_levels + 2 + leaf_k4);
         if (bits > 32) { delete t; return K2T_ERANGE; }
         t->dim_bits = bits;
         t->n_k4 = (int)o.n_k4_levels;
-        t->levels = bits - t->n_k4;
+        t->leaf_k4 = leaf_k4;
+        t->levels = bits - t->n_k4 - leaf_k4;
         const int l = t->levels;
         const int nt = thread_count(o);
         t->engine = o.engine == K2T_ENGINE_AUTO
@@ -661,7 +675,7 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
         heavy_outputs(rows, nnz, n_rows, o.heavy_terms, nt, t->hlist[0], t->hent[0]);
         heavy_outputs(cols, nnz, n_cols, o.heavy_terms, nt, t->hlist[1], t->hent[1]);
         for (int dd = 0; dd < 2; ++dd)
-            if (t->hlist[dd].size() >= (1u << 30)) { delete t; return K2T_ERANGE; }
+            if (t->hlist[dd].size() >= (1u << 28)) { delete t; return K2T_ERANGE; }
 
         t->nodes.assign((size_t)l, 0);
         t->sig.assign((size_t)l, std::vector<uint64_t>());
@@ -669,7 +683,7 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
         std::vector<uint64_t> keys(nnz), tmp;
         parallel_for(nt, [&](int th) {
             uint64_t lo = nnz * th / nt, hi = nnz * (th + 1) / nt;
-            for (uint64_t i = lo; i < hi; ++i) keys[i] = path_key(rows[i], cols[i], bits, t->n_k4);
+            for (uint64_t i = lo; i < hi; ++i) keys[i] = path_key(rows[i], cols[i], bits, t->n_k4, t->leaf_k4);
         });
         radix_sort(keys, tmp, 2 * bits, nt);
         tmp.resize(keys.size());
@@ -694,7 +708,7 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
             uint64_t *cur = keys.data(), *nxt = tmp.data();
             size_t ncur = m;
             for (int d = l - 1; d >= 0; --d) {
-                int s = d < t->n_k4 ? 4 : 2;
+                int s = level_is_k4(t, d) ? 4 : 2;
                 size_t nn = group_level(cur, ncur, s, nxt, sg.data(), nt);
                 if (nn >= (1ull << 32)) { delete t; return K2T_ERANGE; }
                 t->nodes[(size_t)d] = nn;
@@ -756,7 +770,7 @@ int k2t_level_signatures(const k2t_tree *t, uint32_t level, uint8_t *out, uint64
 {
     if (!t || !written || level >= (uint32_t)t->levels) return K2T_EINVAL;
     uint64_t n = t->nodes[level];
-    bool k4 = (int)level < t->n_k4;
+    bool k4 = level_is_k4(t, (int)level);
     uint64_t need = k4 ? 2 * n : n;
     *written = need;
     if (!out || cap < need) return K2T_ERANGE;
@@ -789,12 +803,13 @@ int k2t_decode(const k2t_tree *t, uint32_t *rows, uint32_t *cols, uint64_t cap, 
     }
     uint64_t w = 0;
     const int d = t->levels - 1;
+    const uint32_t k = t->leaf_k4 ? 4u : 2u;
     for (uint64_t i = 0; i < cur.size(); ++i) {
         uint32_t s = level_sig(t, d, i);
-        for (int b = 0; b < 4; ++b)
+        for (uint32_t b = 0; b < k * k; ++b)
             if (s & (1u << b)) {
-                rows[w] = 2 * cur[i].r + (uint32_t)(b >> 1);
-                cols[w] = 2 * cur[i].c + (uint32_t)(b & 1);
+                rows[w] = k * cur[i].r + b / k;
+                cols[w] = k * cur[i].c + b % k;
                 ++w;
             }
     }
@@ -815,7 +830,7 @@ int k2t_stats_get(const k2t_tree *t, k2t_stats *s)
     uint64_t bits = 0;
     for (int d = 0; d < t->levels; ++d) {
         s->level_nodes[d] = t->nodes[(size_t)d];
-        int k = d < t->n_k4 ? 4 : 2;
+        int k = level_is_k4(t, d) ? 4 : 2;
         bits += t->nodes[(size_t)d] * (uint64_t)(k * k);
     }
     s->tree_bits = bits;
@@ -842,6 +857,7 @@ int k2t_stats_get(const k2t_tree *t, k2t_stats *s)
     uint64_t hb = L.acc_bytes;
     for (int dd = 0; dd < 2; ++dd) hb += L.hflag_bytes[dd] + L.hent_bytes[dd] + L.hlist_bytes[dd];
     s->heavy_kib = (uint32_t)((hb + 1023) / 1024);
+    s->leaf_k = t->leaf_k4 ? 4u : 2u;
     return K2T_OK;
 }
 

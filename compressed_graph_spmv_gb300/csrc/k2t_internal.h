@@ -67,12 +67,14 @@ struct k2t_tree {
     k2t_opts opts;
     uint64_t n_rows = 0, n_cols = 0, nnz = 0;
     int dim_bits = 0, n_k4 = 0, levels = 0;
+    int leaf_k4 = 0;       // 1: the leaf level holds 4x4 bitmaps (16-bit signatures)
     int d0 = 0;
     uint32_t engine = 0;   // resolved engine
     bool empty = false;    // nnz == 0: a product is only the fill
     std::vector<uint64_t> nodes;                  // N_d
     // Signatures: k = 2 levels hold 16 nibbles per word (node t at bits
-    // 4*(t%16)); k = 4 levels hold 4 16-bit signatures per word.
+    // 4*(t%16)); k = 4 levels (the n_k4 top levels, and the leaf level when
+    // leaf_k4) hold 4 16-bit signatures per word.
     std::vector<std::vector<uint64_t>> sig;
     std::vector<std::vector<uint32_t>> dir;       // index d - d0, levels d0..l-2
     std::vector<k2t::Coord> top;                  // level d0
@@ -103,6 +105,7 @@ namespace k2t {
 // implemented in k2t_host.cpp
 uint64_t level_offset(const k2t_tree *t, int d, uint64_t node);  // first child of node (d0 <= d <= l-2)
 uint32_t level_sig(const k2t_tree *t, int d, uint64_t node);
+inline bool level_is_k4(const k2t_tree *t, int d) { return d < t->n_k4 || (t->leaf_k4 && d == t->levels - 1); }
 void compute_layout(k2t_tree *t);
 // implemented in k2t_device.cu
 void device_release(k2t_tree *t);

@@ -841,6 +841,315 @@ cached_block_kernel(const uint8_t *sig, const uint32_t *dir, uint32_t n, const C
     if (win) warp_window_flush<SR>(win, lo, span, width, va);
 }
 
+// ---- 4x4 leaves (leaf_k = 4) ------------------------------------------------------
+#ifndef K2T_LEAF4_U
+#define K2T_LEAF4_U 4
+#endif
+// The leaves the pages name as the next lever (section 5.6): a leaf is a 4x4
+// bitmap (16-bit signature, cell (dr, dc) at bit 4*dr + dc).  Its four inputs
+// are consecutive, so one vector load brings them; each of its (at most four)
+// outputs sums its row segment (right) or column segment (left) in registers
+// and updates y once.
+
+// Cells of output q of a leaf as a 4-bit set over its inputs: right products
+// take row q (bits 4q..4q+3), left products column q (bits q, q+4, q+8, q+12).
+template <int DIR>
+__device__ __forceinline__ uint32_t seg4(uint32_t lam, int q)
+{
+    if (DIR == K2T_RIGHT) return (lam >> (4 * q)) & 15u;
+    const uint32_t v = (lam >> q) & 0x1111u;
+    return (v | (v >> 3) | (v >> 6) | (v >> 9)) & 15u;
+}
+
+// Inputs a leaf reads: columns (right) or rows (left) holding a cell.
+template <int DIR>
+__device__ __forceinline__ uint32_t used4(uint32_t lam)
+{
+    if (DIR == K2T_RIGHT) return (lam | (lam >> 4) | (lam >> 8) | (lam >> 12)) & 15u;
+    return (uint32_t)((lam & 0xfu) != 0) | ((uint32_t)((lam & 0xf0u) != 0) << 1) |
+           ((uint32_t)((lam & 0xf00u) != 0) << 2) | ((uint32_t)((lam & 0xf000u) != 0) << 3);
+}
+
+// fp64 outputs among out .. out + 3 (out a multiple of 4): (id << 4) | mask,
+// mask bit q set when out + q is summed in fp64, id the fp64 index of the
+// first of them; output out + q has id + popc(mask & ((1 << q) - 1)).
+__device__ __forceinline__ uint32_t heavy_word4(const VecArgs &va, uint32_t out)
+{
+    const uint2 e = __ldg(reinterpret_cast<const uint2 *>(va.hent) + (out >> 5));
+    const uint32_t sh = out & 31u;
+    const uint32_t m = (e.x >> sh) & 15u;
+    if (!m) return 0u;
+    return ((e.y + (uint32_t)__popc(e.x & ((1u << sh) - 1u))) << 4) | m;
+}
+
+__device__ __forceinline__ double *heavy_slot4(const VecArgs &va, uint32_t hv, int q, uint32_t k)
+{
+    const uint32_t id = (hv >> 4) + (uint32_t)__popc(hv & 15u & ((1u << q) - 1u));
+    return va.acc + (size_t)id * va.B + k;
+}
+
+// One vector slice (B = 1 fp32, or a Boolean word) of U leaves whose inputs
+// xo[u][0..3] are loaded: every output with a cell gets its combined segment.
+template <int SR, int DIR, int U>
+__device__ __forceinline__ void leaf4_apply1(const uint32_t (&lam)[U], const uint32_t (&out)[U],
+                                             const uint32_t (&xo)[U][4], uint32_t fl, const VecArgs &va,
+                                             uint32_t *win, uint32_t lo)
+{
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const uint32_t l = lam[u];
+        if (!l) continue;
+        if constexpr (SR == K2T_BOOLEAN) {
+            uint32_t *y = static_cast<uint32_t *>(va.y);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t s = seg4<DIR>(l, q);
+                uint32_t v = 0u;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) v |= ((s >> i) & 1u) ? xo[u][i] : 0u;
+                v &= va.mask;
+                if (!v) continue;
+                if (win) atomicOr(win + (out[u] + q - lo), v);
+                else atomicOr(y + out[u] + q, v);
+            }
+        } else {
+            using S = Fp32Sem<SR>;
+            float *y = static_cast<float *>(va.y);
+            const uint32_t h = SR == K2T_PLUS_TIMES && ((fl >> u) & 1u) ? heavy_word4(va, out[u]) : 0u;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t s = seg4<DIR>(l, q);
+                if (!s) continue;
+                if (SR == K2T_PLUS_TIMES && ((h >> q) & 1u)) {
+                    double d = 0.0;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if ((s >> i) & 1u) d += (double)(va.w * __uint_as_float(xo[u][i]));
+                    atomicAdd(heavy_slot4(va, h, q, 0u), d);
+                    continue;
+                }
+                float v[1] = {S::zero()};
+                bool any = false;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if ((s >> i) & 1u) {
+                        const float c = S::contrib(__uint_as_float(xo[u][i]), va.w);
+                        v[0] = any ? S::plus(v[0], c) : c;
+                        any = true;
+                    }
+                if (S::skip(v[0])) continue;
+                if (win) smem_update<SR>(win + (out[u] + q - lo), __float_as_uint(v[0]));
+                else S::update(y + out[u] + q, v);
+            }
+        }
+    }
+}
+
+// One VW-wide slice k of one 4x4 leaf (origin r, c; cells lam) for batches.
+template <int SR, int DIR, int VW>
+__device__ __forceinline__ void leaf4_slice(uint32_t lam, uint32_t r, uint32_t c, uint32_t k, uint32_t hv,
+                                            const VecArgs &va, uint32_t *win, uint32_t lo)
+{
+    using S = Fp32Sem<SR>;
+    const uint32_t in = DIR == K2T_RIGHT ? c : r;
+    const uint32_t out = DIR == K2T_RIGHT ? r : c;
+    const uint32_t use = used4<DIR>(lam);
+    const float *x = static_cast<const float *>(va.x);
+    float *y = static_cast<float *>(va.y);
+    const size_t B = va.B;
+    float xv[4][VW];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        if ((use >> i) & 1u) VecLoad<VW>::load(x + (size_t)(in + i) * B + k, xv[i]);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t s = seg4<DIR>(lam, q);
+        if (!s) continue;
+        if (SR == K2T_PLUS_TIMES && ((hv >> q) & 1u)) {
+            double *a = heavy_slot4(va, hv, q, k);
+#pragma unroll
+            for (int e = 0; e < VW; ++e) {
+                double d = 0.0;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if ((s >> i) & 1u) d += (double)(va.w * xv[i][e]);
+                atomicAdd(a + e, d);
+            }
+            continue;
+        }
+        float v[VW];
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+            bool any = false;
+            v[e] = S::zero();
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if ((s >> i) & 1u) {
+                    const float cv = S::contrib(xv[i][e], va.w);
+                    v[e] = any ? S::plus(v[e], cv) : cv;
+                    any = true;
+                }
+        }
+        if (win) {
+#pragma unroll
+            for (int e = 0; e < VW; ++e)
+                if (!S::skip(v[e])) smem_update<SR>(win + (size_t)(out + q - lo) * B + k + e, __float_as_uint(v[e]));
+        } else {
+            S::update(y + (size_t)(out + q) * B + k, v);
+        }
+    }
+}
+
+// Leaves [jb, je) of a warp with 4x4 leaves; leaf_at(j, lam, r, c, li) as for
+// warp_leaf_rounds (lam a 16-bit bitmap, (r, c) its block's origin).
+//  - One vector slice: leaves dealt round-robin, four per lane per round; the
+//    four inputs of a block come in one 16-byte load when x allows it.
+//  - Batches: G = B/VW adjacent lanes share a leaf, each owning a VW slice.
+template <int SR, int DIR, int VW, class LeafAt>
+__device__ __forceinline__ void warp_leaf4_rounds(uint32_t jb, uint32_t je, LeafAt &&leaf_at, const VecArgs &va,
+                                                  uint32_t *win, uint32_t lo)
+{
+    const uint32_t lane = threadIdx.x & 31u;
+    const bool heavy = SR == K2T_PLUS_TIMES && va.hflag != nullptr;
+    if (SR == K2T_BOOLEAN || (VW == 1 && va.B == 1)) {
+        constexpr int U = K2T_LEAF4_U;
+        const uint32_t *x = static_cast<const uint32_t *>(va.x);
+        const bool x16 = ((uintptr_t)x & 15u) == 0;
+        for (uint32_t j0 = jb; j0 < je; j0 += 32u * U) {
+            uint32_t lam[U], r[U], c[U], fl = 0u;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const uint32_t j = j0 + 32u * u + lane;
+                lam[u] = 0u;
+                r[u] = 0u;
+                c[u] = 0u;
+                uint32_t li = 0u;
+                if (j < je) {
+                    leaf_at(j, lam[u], r[u], c[u], li);
+                    if (heavy) fl |= heavy_leaf(va, li) << u;
+                }
+            }
+            uint32_t xo[U][4], out[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const uint32_t in = DIR == K2T_RIGHT ? c[u] : r[u];  // a multiple of 4
+                out[u] = DIR == K2T_RIGHT ? r[u] : c[u];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) xo[u][i] = 0u;
+                if (lam[u]) {
+                    if (x16 && in + 3u < va.n_in) {
+                        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(x + in));
+                        xo[u][0] = v.x;
+                        xo[u][1] = v.y;
+                        xo[u][2] = v.z;
+                        xo[u][3] = v.w;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            if (in + (uint32_t)i < va.n_in) xo[u][i] = __ldg(x + in + i);
+                    }
+                }
+            }
+            leaf4_apply1<SR, DIR, U>(lam, out, xo, fl, va, win, lo);
+        }
+        return;
+    }
+    if constexpr (SR != K2T_BOOLEAN) {
+        constexpr int U = 2;
+        const uint32_t G = va.B / VW;
+        const uint32_t per = G <= 32u ? 32u / G : 1u;
+        const uint32_t groups = G <= 32u ? G : 32u;
+        const uint32_t slot = lane / groups, sub = lane % groups;
+        const bool active = slot < per;
+        for (uint32_t j0 = jb; j0 < je; j0 += per * U) {
+            uint32_t lam[U], r[U], c[U], hv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const uint32_t j = j0 + (uint32_t)u * per + slot;
+                lam[u] = 0u;
+                r[u] = 0u;
+                c[u] = 0u;
+                hv[u] = 0u;
+                uint32_t li = 0u;
+                if (active && j < je) {
+                    leaf_at(j, lam[u], r[u], c[u], li);
+                    if (heavy && heavy_leaf(va, li)) hv[u] = heavy_word4(va, DIR == K2T_RIGHT ? r[u] : c[u]);
+                }
+            }
+            for (uint32_t k = sub * VW; k < va.B; k += groups * VW) {
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (lam[u]) leaf4_slice<SR, DIR, VW>(lam[u], r[u], c[u], k, hv[u], va, win, lo);
+            }
+        }
+    }
+}
+
+// CACHED engine with 4x4 leaves: as cached_block_kernel (one warp per 256-node
+// directory block of the last internal level, leaf list built by a warp scan,
+// per-warp output window), with nodes covering 8x8 cells and 16-bit leaves.
+#ifndef K2T_LEAF4_MINB
+#define K2T_LEAF4_MINB 3
+#endif
+template <int SR, int DIR, int VW>
+__global__ void __launch_bounds__(32 * kCachedWarps, K2T_LEAF4_MINB)
+cached4_block_kernel(const uint8_t *sig, const uint32_t *dir, uint32_t n, const Coord *coords, const uint16_t *leaf,
+                     VecArgs va)
+{
+    __shared__ Coord cs[kCachedWarps][kDirS];
+    __shared__ uint16_t slots[kCachedWarps][4 * kDirS];
+    __shared__ uint32_t wins[kCachedWarps][kWarpWindow];
+    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+    const uint32_t g = blockIdx.x * kCachedWarps + warp;
+    const uint32_t s = g * kDirS;
+    if (s >= n) return;
+    const uint32_t cnt = min(n - s, kDirS);
+    Coord *cw = cs[warp];
+    uint16_t *sl = slots[warp];
+    uint32_t w = 0;
+    if (8u * lane < cnt) {
+        w = __ldg(reinterpret_cast<const uint32_t *>(sig + s / 2) + lane);
+        if (8u * lane + 8u > cnt) w &= (1u << (4u * (cnt - 8u * lane))) - 1u;
+    }
+    const uint32_t base = __ldg(dir + g);
+    uint32_t mn = 0xffffffffu, mx = 0u;
+#pragma unroll
+    for (uint32_t q = 0; q < kDirS / 32; ++q) {
+        const uint32_t i = 32u * q + lane;
+        if (i < cnt) {
+            const Coord p = coords[s + i];
+            cw[i] = p;
+            const uint32_t o = DIR == K2T_RIGHT ? p.r : p.c;
+            mn = min(mn, o);
+            mx = max(mx, o);
+        }
+    }
+    const uint32_t f = (uint32_t)__popc(w);
+    const uint32_t incl = warp_incl_scan(f);
+    const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+    uint32_t pos = incl - f;
+    uint32_t rest = w;
+    while (rest) {
+        const uint32_t bit = (uint32_t)(__ffs(rest) - 1);  // 4*k + b
+        rest &= rest - 1u;
+        sl[pos++] = (uint16_t)(((8u * lane + bit / 4u) << 2) | (bit & 3u));
+    }
+    const uint32_t width = SR == K2T_BOOLEAN ? 1u : va.B;
+    uint32_t lo, span;
+    uint32_t *win = warp_window_begin<SR>(mn, mx, 8u, width, wins[warp], lo, span);
+    __syncwarp();
+    warp_leaf4_rounds<SR, DIR, VW>(0u, total, [&](uint32_t j, uint32_t &lam, uint32_t &r, uint32_t &c, uint32_t &li) {
+        const uint32_t e = sl[j];
+        const Coord p = cw[e >> 2];
+        const uint32_t b = e & 3u;
+        r = 8u * p.r + 4u * (b >> 1);
+        c = 8u * p.c + 4u * (b & 1u);
+        li = base + j;
+        lam = __ldg(leaf + li);
+    }, va, win, lo);
+    if (win) warp_window_flush<SR>(win, lo, span, width, va);
+}
+
 // BANDED engine: the cached last internal level grouped by row band (band_rows
 // rows each; level order inside a band), one thread block per block of at most
 // kBandChunkNodes nodes of one band.  Warps take 256-node tiles: coordinates,
@@ -1321,6 +1630,18 @@ void launch_cached(const k2t_tree *t, const DeviceState *d, const VecArgs &va, c
 }
 
 template <int SR, int DIR, int VW>
+void launch_cached4(const k2t_tree *t, const DeviceState *d, const VecArgs &va, cudaStream_t st)
+{
+    const int l = t->levels;
+    const uint32_t n = (uint32_t)t->nodes[(size_t)l - 2];
+    const uint32_t blocks = (n + kDirS - 1) / kDirS;
+    const unsigned grid = (unsigned)((blocks + kCachedWarps - 1) / kCachedWarps);
+    cached4_block_kernel<SR, DIR, VW><<<grid, 32 * kCachedWarps, 0, st>>>(
+        d->tree.lv[l - 2].sig, d->tree.lv[l - 2].dir, n, d->cached,
+        reinterpret_cast<const uint16_t *>(d->tree.lv[l - 1].sig), va);
+}
+
+template <int SR, int DIR, int VW>
 void launch_banded(const k2t_tree *t, const DeviceState *d, const VecArgs &va, cudaStream_t st)
 {
     const int l = t->levels;
@@ -1366,6 +1687,9 @@ void launch_ls(const k2t_tree *t, const DeviceState *d, const VecArgs &va, cudaS
 
 using LaunchFn = void (*)(const k2t_tree *, const DeviceState *, const VecArgs &, cudaStream_t);
 
+// Internal engine id: the CACHED engine on a tree with 4x4 leaves.
+constexpr uint32_t kEngineCached4 = 100;
+
 // Plus-times products of a direction with fp64 outputs.  heavy_begin points
 // va at the direction's tables and zeroes the fp64 sums of the B vectors
 // (queued after the fill of y); heavy_end rounds each sum to fp32 into its
@@ -1400,6 +1724,7 @@ LaunchFn pick_engine(uint32_t engine)
     case K2T_ENGINE_FUSED: return launch_fused<SR, DIR, VW>;
     case K2T_ENGINE_CACHED: return launch_cached<SR, DIR, VW>;
     case K2T_ENGINE_BANDED: return launch_banded<SR, DIR, VW>;
+    case kEngineCached4: return launch_cached4<SR, DIR, VW>;
     default: return launch_ls<SR, DIR, VW>;
     }
 }

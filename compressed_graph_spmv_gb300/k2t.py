@@ -42,7 +42,7 @@ class Opts(ctypes.Structure):
                 ("host_vectors", ctypes.c_uint32), ("use_graph", ctypes.c_uint32),
                 ("threads", ctypes.c_uint32), ("band_rows", ctypes.c_uint32),
                 ("band_cols", ctypes.c_uint32), ("heavy_terms", ctypes.c_uint32),
-                ("reserved", ctypes.c_uint32 * 5)]
+                ("leaf_k", ctypes.c_uint32), ("reserved", ctypes.c_uint32 * 4)]
 
 
 class Stats(ctypes.Structure):
@@ -58,7 +58,7 @@ class Stats(ctypes.Structure):
                 ("n_steps", ctypes.c_uint64), ("engine", ctypes.c_uint32), ("offsets", ctypes.c_uint32),
                 ("uploaded", ctypes.c_uint32), ("heavy_rows", ctypes.c_uint32),
                 ("heavy_cols", ctypes.c_uint32), ("heavy_kib", ctypes.c_uint32),
-                ("reserved", ctypes.c_uint32 * 2)]
+                ("leaf_k", ctypes.c_uint32), ("reserved", ctypes.c_uint32 * 1)]
 
 
 class K2TError(RuntimeError):

@@ -107,7 +107,13 @@ typedef struct {
                                      is summed in fp64 and rounded to fp32 once; every other output
                                      is summed in fp32.  Default 2048; 0 = default; 0xffffffff =
                                      never.  See "Accumulation precision" below.                     */
-    uint32_t reserved[5];
+    uint32_t leaf_k;              /* side of a leaf block: 2 (default; 0 = default) or 4.  4: the
+                                     leaf level stores 4x4 bitmaps (16-bit signatures, cell
+                                     (dr, dc) at bit 4*dr + dc), the larger leaves of section 5.6;
+                                     every other level keeps k = 2 (or k = 4 on the n_k4 top
+                                     levels).  Needs the CACHED engine (cache_last_internal = 1,
+                                     engine AUTO or CACHED); other engines give EINVAL.              */
+    uint32_t reserved[4];
 } k2t_opts;
 
 /* ---- statistics -------------------------------------------------------- */
@@ -139,7 +145,8 @@ typedef struct {
     uint32_t heavy_cols;          /* outputs of left products summed in fp64       */
     uint32_t heavy_kib;           /* device KiB of the fp64 path's tables and
                                      accumulators (part of workspace_bytes)        */
-    uint32_t reserved[2];
+    uint32_t leaf_k;              /* side of a leaf block: 2 or 4                  */
+    uint32_t reserved[1];
 } k2t_stats;
 
 /* Fill *o with the defaults: k = 2, tree-only FUSED engine (AUTO), directory
@@ -150,7 +157,8 @@ void k2t_default_opts(k2t_opts *o);
 /* Build the tree of the n_rows x n_cols Boolean matrix whose non-zeros are
  * (rows[i], cols[i]), i < nnz, on the host (section 2.1; construction is the
  * host step of section 5.1).  Duplicated pairs count once.  The side is padded
- * to 2^l (at least 4, at least 2^(2*n_k4+2)).  The COO arrays are read, not
+ * to 2^b (at least 4, at least 2^(2*n_k4+2), with 4x4 leaves 2^(2*n_k4+3)),
+ * giving b - n_k4 levels (4x4 leaves: b - n_k4 - 1).  The COO arrays are read, not
  * kept.  opts may be NULL (defaults).  Plans the product as well: host-side
  * top (3.4), directories (3.2), chunk or tile plan (3.4), cached level (3.5).
  * Errors: EINVAL (null out/arrays with nnz > 0, zero side, bad option),

@@ -21,6 +21,11 @@ WORKLOADS = {
     "weblike22": (lambda: synth.weblike_c3(), dict(n_k4_levels=2), [(0, 32), (1, 32)]),
     "social24": (lambda: synth.social_c4(), dict(), [(0, 8)]),
     "rmat27": (lambda: synth.large_c5(B=16), dict(cache_last_internal=1), [(0, 1), (1, 1), (0, 16), (1, 16)]),
+    # 4x4 leaves (section 5.6) on the cached engine
+    "rmat20-leaf4": (lambda: synth.rmat_c2(), dict(cache_last_internal=1, leaf_k=4), [(0, 1), (1, 1)]),
+    "weblike22-leaf4": (lambda: synth.weblike_c3(), dict(n_k4_levels=2, cache_last_internal=1, leaf_k=4),
+                        [(0, 32), (1, 32)]),
+    "social24-leaf4": (lambda: synth.social_c4(), dict(cache_last_internal=1, leaf_k=4), [(0, 8)]),
 }
 
 

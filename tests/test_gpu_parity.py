@@ -26,6 +26,7 @@ ENGINES = [
     dict(engine=3, cache_last_internal=1),             # k^2+F
     dict(engine=4, cache_last_internal=1),             # k^2+F by row band
     dict(engine=4, cache_last_internal=1, band_rows=16),
+    dict(engine=3, cache_last_internal=1, leaf_k=4),   # k^2+F with 4x4 leaves (section 5.6)
 ]
 
 
@@ -140,7 +141,7 @@ def test_rmat_medium_all_semirings():
     rows, cols = synth.rmat(17, 0.57, 0.19, 0.19, 1 << 20, 12)
     n = 1 << 17
     rng = np.random.default_rng(12)
-    for kw in (ENGINES[0], ENGINES[2], ENGINES[3], ENGINES[5], ENGINES[6]):
+    for kw in (ENGINES[0], ENGINES[2], ENGINES[3], ENGINES[5], ENGINES[6], ENGINES[8]):
         t = _tree(rows, cols, n, n, **kw)
         for semiring, B in ((PLUS_TIMES, 1), (PLUS_TIMES, 16), (BOOLEAN, 32), (TROPICAL, 8)):
             for d in (RIGHT, LEFT):

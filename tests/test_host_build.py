@@ -20,25 +20,27 @@ from compressed_graph_spmv_gb300 import k2t as K  # noqa: E402
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def _lib_bits(tree, level, n_k4):
+def _lib_bits(tree, level, n_k4, leaf_k=2):
     sig = tree.level_signatures(level)
-    if level < n_k4:
+    if level < n_k4 or (leaf_k == 4 and level == tree.stats().levels - 1):
         s16 = sig.reshape(-1, 2).astype(np.uint16)
         s16 = s16[:, 0] | (s16[:, 1] << 8)
         return np.unpackbits(s16.view(np.uint8), bitorder="little")
     return np.unpackbits(sig, bitorder="little").reshape(-1, 8)[:, :4].reshape(-1)
 
 
-def _compare(rows, cols, n_rows, n_cols, n_k4=0, **kw):
-    ot = oracle.OracleTree(rows, cols, n_rows, n_cols, n_k4=n_k4)
+def _compare(rows, cols, n_rows, n_cols, n_k4=0, leaf_k=2, **kw):
+    ot = oracle.OracleTree(rows, cols, n_rows, n_cols, n_k4=n_k4, leaf_k=leaf_k)
+    if leaf_k == 4:
+        kw = dict(kw, leaf_k=4, cache_last_internal=1)
     lt = K.Tree(rows, cols, n_rows, n_cols, n_k4_levels=n_k4, **kw)
     s = lt.stats()
-    assert s.levels == ot.levels and s.dim_bits == ot.dim_bits
+    assert s.levels == ot.levels and s.dim_bits == ot.dim_bits and s.leaf_k == leaf_k
     bits = ot.bits()
     start = ot.level_start()
     for d in range(ot.levels):
         assert int(s.level_nodes[d]) == ot.level_nodes()[d]
-        assert np.array_equal(_lib_bits(lt, d, n_k4), bits[start[d]:start[d + 1]]), d
+        assert np.array_equal(_lib_bits(lt, d, n_k4, leaf_k), bits[start[d]:start[d + 1]]), d
     r, c = lt.decode()
     dr, dc = oracle.dedup_edges(rows, cols)
     assert sorted(zip(r.tolist(), c.tolist())) == sorted(zip(dr.tolist(), dc.tolist()))
@@ -54,14 +56,35 @@ def test_build_matches_oracle_random(seed):
     n_k4 = int(rng.integers(0, 3))
     rows, cols, _ = synth.random_small(seed, n_rows, n_cols, float(rng.choice([0.001, 0.01, 0.1])))
     _compare(rows, cols, n_rows, n_cols, n_k4=n_k4)
+    _compare(rows, cols, n_rows, n_cols, n_k4=n_k4, leaf_k=4)
 
 
-def test_build_matches_oracle_rmat_threads():
+@pytest.mark.parametrize("leaf_k", [2, 4])
+def test_build_matches_oracle_rmat_threads(leaf_k):
     rows, cols = synth.rmat(14, 0.57, 0.19, 0.19, 100000, 3)
-    a = _compare(rows, cols, 1 << 14, 1 << 14, threads=1)
-    b = _compare(rows, cols, 1 << 14, 1 << 14, threads=7)
+    a = _compare(rows, cols, 1 << 14, 1 << 14, leaf_k=leaf_k, threads=1)
+    b = _compare(rows, cols, 1 << 14, 1 << 14, leaf_k=leaf_k, threads=7)
     for d in range(a.stats().levels):
         assert np.array_equal(a.level_signatures(d), b.level_signatures(d))
+
+
+def test_build_figure1_leaf4():
+    """The Figure 1 matrix with 4 x 4 leaves: two levels, root 1111, four
+    16-bit leaves (the oracle's hand-derived pin), and the option errors."""
+    import json
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "figure1.json")))
+    e = np.array(g["edges_decoded"], np.uint32)
+    t = _compare(e[:, 0], e[:, 1], 8, 8, leaf_k=4)
+    s = t.stats()
+    assert s.levels == 2 and s.l_bytes_device == 2 * 4 + 16
+    assert t.level_signatures(1).view(np.uint16).tolist() == [1 << 5, 1 | 1 << 5 | 1 << 13,
+                                                              1 << 5 | 1 << 6 | 1 << 9 | 1 << 10,
+                                                              1 << 10 | 1 << 11 | 1 << 14 | 1 << 15]
+    for bad in (dict(leaf_k=3, cache_last_internal=1), dict(leaf_k=4), dict(leaf_k=4, engine=1),
+                dict(leaf_k=4, engine=2, cache_last_internal=1), dict(leaf_k=4, engine=4, cache_last_internal=1)):
+        with pytest.raises(K.K2TError) as err:
+            K.Tree(e[:, 0], e[:, 1], 8, 8, **bad)
+        assert err.value.status == -1, bad
 
 
 def test_build_figure1_and_top_level():
@@ -147,7 +170,7 @@ def test_options_struct_matches_header():
     """The binding's k2t_opts mirrors the header: defaults round-trip."""
     o = K.default_opts()
     assert o.band_rows == 4096 and o.chunk_cap == 2048 and o.tile_m == 1 << 20 and o.max_batch == 32
-    assert o.heavy_terms == 2048
+    assert o.heavy_terms == 2048 and o.leaf_k == 2
     assert ctypes.sizeof(K.Opts) == 80  # 6 x u32, u64, 5 x u32, heavy_terms, 5 reserved
     assert ctypes.sizeof(K.Stats) == 432
     with pytest.raises(K.K2TError):
