@@ -47,18 +47,27 @@ __global__ void __launch_bounds__(256) fill_kernel(uint32_t *y, uint64_t words, 
     for (uint64_t k = tail + i; k < words; k += stride) y[k] = pattern;
 }
 
-// fp64 outputs of a plus-times product: output list[i] of vector k receives
-// its fp64 sum acc[i * B + k], rounded to fp32 once.  The product sends every
-// term of such an output to acc, so y holds the fill's zero there; adding it
-// keeps the result right even if it did not.
-__global__ void __launch_bounds__(256) heavy_finish_kernel(const double *acc, const uint32_t *list, uint32_t h,
-                                                           uint32_t B, float *y)
+// Heavy outputs of a plus-times product: output list[i] of vector k receives
+// its sum, rounded to fp32 once: the fp64 sum acc[i * B + k] (hsplit 0), or
+// the hsplit fp32 partial sums acc[(i * hsplit + p) * B + k] added in fp64.
+// The product sends every term of such an output to acc, so y holds the
+// fill's zero there; adding it keeps the result right even if it did not.
+__global__ void __launch_bounds__(256) heavy_finish_kernel(const void *acc, uint32_t hsplit, const uint32_t *list,
+                                                           uint32_t h, uint32_t B, float *y)
 {
     const uint64_t n = (uint64_t)h * B;
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
     for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
-        float *p = y + (uint64_t)__ldg(list + i / B) * B + i % B;
-        *p = __double2float_rn(acc[i] + (double)*p);
+        const uint64_t o = i / B, k = i % B;
+        float *p = y + (uint64_t)__ldg(list + o) * B + k;
+        double s = (double)*p;
+        if (hsplit) {
+            const float *a = static_cast<const float *>(acc) + o * hsplit * B + k;
+            for (uint32_t q = 0; q < hsplit; ++q) s += (double)a[(uint64_t)q * B];
+        } else {
+            s += static_cast<const double *>(acc)[i];
+        }
+        *p = __double2float_rn(s);
     }
 }
 
@@ -308,7 +317,7 @@ int k2t_upload(k2t_tree *t, void *arena, uint64_t arena_bytes, void *stream)
         if ((e = put(L.hent_off[dd], L.hent_bytes[dd], t->hent[dd].data()))) return fail(e);
         if ((e = put(L.hlist_off[dd], L.hlist_bytes[dd], t->hlist[dd].data()))) return fail(e);
     }
-    if (L.acc_bytes) d->acc = at<double>(d->arena, L.acc_off);
+    if (L.acc_bytes) d->acc = at<void>(d->arena, L.acc_off);
     if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return fail(e);
     return K2T_OK;
 }

@@ -575,7 +575,8 @@ void compute_layout(k2t_tree *t)
             hmax = std::max<uint64_t>(hmax, t->hlist[dd].size());
         }
         if (hmax) {
-            L.acc_bytes = hmax * (uint64_t)t->opts.max_batch * sizeof(double);
+            L.acc_bytes = hmax * (uint64_t)t->opts.max_batch *
+                          (t->opts.heavy_mode ? sizeof(double) : kHeavySplit * sizeof(float));
             L.acc_off = take(L.acc_bytes);
         }
     }
@@ -630,6 +631,7 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
     if (!o.band_cols) o.band_cols = 1u << 31;
     if (!o.heavy_terms) o.heavy_terms = 2048;
     if (!o.leaf_k) o.leaf_k = 2;
+    if (o.heavy_mode > 1) return K2T_EINVAL;
     if (o.leaf_k != 2 && o.leaf_k != 4) return K2T_EINVAL;
     if (o.chunk_cap < 4 || o.chunk_cap > kMaxChunkCap || o.tile_m < 4) return K2T_EINVAL;
     if (o.max_batch < 1 || o.max_batch > K2T_MAX_BATCH) return K2T_ERANGE;

@@ -13,6 +13,7 @@ constexpr uint32_t kDirS = 256;        // directory sample period (section 3.2: 
 constexpr uint32_t kMaxChunkCap = 4096;
 constexpr uint32_t kArenaAlign = 256;
 constexpr uint32_t kBandChunkNodes = 16384;  // BANDED: nodes per thread block at most
+constexpr uint32_t kHeavySplit = 32;         // fp32 partial sums per heavy output (heavy_mode 0)
 
 // Coordinates of a node's block, in units of the block side at its level.
 // A frontier entry: (row, col) instead of the pages' Morton code; the two
@@ -55,7 +56,8 @@ struct ArenaLayout {
     uint64_t hflag_off[2], hflag_bytes[2];  // one bit per leaf: touches an fp64 output
     uint64_t hent_off[2], hent_bytes[2];    // per 32 outputs: (fp64 bits, fp64 outputs before)
     uint64_t hlist_off[2], hlist_bytes[2];  // the fp64 outputs, ascending
-    uint64_t acc_off, acc_bytes;            // fp64 sums [output][B], shared by both directions
+    uint64_t acc_off, acc_bytes;            // heavy sums, shared by both directions: fp64 [output][B]
+                                            // (heavy_mode 1) or fp32 [output][kHeavySplit][B]
     uint64_t total;
 };
 

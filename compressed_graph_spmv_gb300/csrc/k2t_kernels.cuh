@@ -37,8 +37,9 @@ struct VecArgs {
     uint64_t n_in;   // entries (vertices) of x
     // Plus-times outputs summed in fp64 (null hflag: none in this product)
     const uint32_t *hflag;  // bit j: leaf j (level order) has an fp64 output
-    const uint32_t *hent;   // per 32 outputs: mask of fp64 outputs, fp64 outputs before the group
-    double *acc;            // fp64 sums, [index in the fp64 list][B]
+    const uint32_t *hent;   // per 32 outputs: mask of such outputs, their count before the group
+    void *acc;              // their sums: hsplit == 0: fp64 [id][B]; else fp32 partial sums [id][hsplit][B]
+    uint32_t hsplit;        // fp32 partial sums per output (a power of two), or 0 for fp64 sums
 };
 
 __device__ __forceinline__ uint32_t nibble_at(const uint8_t *sig, uint32_t t)
@@ -159,16 +160,32 @@ __device__ __forceinline__ uint32_t heavy_word(const VecArgs &va, uint32_t out)
     return ((e.y + (uint32_t)__popc(e.x & ((1u << sh) - 1u))) << 2) | m;
 }
 
-// Add the VW-wide slice k of output out + q (hv from heavy_word) to its fp64
-// sum: the leaf's cells in that output contribute w*xa (when ua) and w*xb
-// (when ub), each formed in fp32 and added in fp64, where the sum of two
-// floats is exact.
-template <int VW>
-__device__ __forceinline__ void heavy_add(const VecArgs &va, uint32_t hv, int q, uint32_t k, const float (&xa)[VW],
-                                          const float (&xb)[VW], bool ua, bool ub)
+// Index in the heavy list of output out + q of a 2x2 leaf (hv from heavy_word).
+__device__ __forceinline__ uint32_t heavy_id2(uint32_t hv, int q) { return (hv >> 2) + (q ? (hv & 1u) : 0u); }
+
+// The fp32 partial sum of heavy output `id` (slice k) this warp adds to: the
+// warps of the grid take the hsplit partial sums in turn, so each holds about
+// 1/hsplit of the output's terms and the addresses a hub row's updates hit
+// are spread over hsplit lines.
+__device__ __forceinline__ float *heavy_part(const VecArgs &va, uint32_t id, uint32_t k)
 {
-    const uint32_t id = (hv >> 2) + (q ? (hv & 1u) : 0u);
-    double *a = va.acc + (size_t)id * va.B + k;
+    const uint32_t part = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) & (va.hsplit - 1u);
+    return static_cast<float *>(va.acc) + ((size_t)id * va.hsplit + part) * va.B + k;
+}
+
+// Update heavy output `id` (slice k) with a leaf's contribution: v is the
+// fp32 combination of its cells (split partial sums); in fp64 mode the cells
+// w*xa (when ua) and w*xb (when ub) are added in fp64, where the sum of two
+// floats is exact.
+template <int SR, int VW>
+__device__ __forceinline__ void heavy_put(const VecArgs &va, uint32_t id, uint32_t k, const float (&v)[VW],
+                                          const float (&xa)[VW], const float (&xb)[VW], bool ua, bool ub)
+{
+    if (va.hsplit) {
+        Fp32Sem<SR>::update(heavy_part(va, id, k), v);
+        return;
+    }
+    double *a = static_cast<double *>(va.acc) + (size_t)id * va.B + k;
 #pragma unroll
     for (int i = 0; i < VW; ++i)
         atomicAdd(a + i, (ua ? (double)(va.w * xa[i]) : 0.0) + (ub ? (double)(va.w * xb[i]) : 0.0));
@@ -277,11 +294,11 @@ __device__ __forceinline__ void leaf_group(const uint32_t (&lam)[U], const uint3
                 } else {
                     const uint32_t h = SR == K2T_PLUS_TIMES && ((fl >> u) & 1u) ? heavy_word(a, out[u]) : 0u;
                     if (a0[u] || a1[u]) {
-                        if (h & 1u) heavy_add<VW>(a, h, 0, k, x0[u], x1[u], a0[u], a1[u]);
+                        if (h & 1u) heavy_put<SR, VW>(a, heavy_id2(h, 0), k, v0, x0[u], x1[u], a0[u], a1[u]);
                         else S::update(y + (size_t)out[u] * B + k, v0);
                     }
                     if (b0[u] || b1[u]) {
-                        if (h & 2u) heavy_add<VW>(a, h, 1, k, x0[u], x1[u], b0[u], b1[u]);
+                        if (h & 2u) heavy_put<SR, VW>(a, heavy_id2(h, 1), k, v1, x0[u], x1[u], b0[u], b1[u]);
                         else S::update(y + (size_t)(out[u] + 1) * B + k, v1);
                     }
                 }
@@ -318,7 +335,8 @@ constexpr uint32_t kFusedSolo = 256;  // levels this narrow are expanded by one 
 
 // Kernels without template parameters, defined in k2t_device.cu.
 __global__ void fill_kernel(uint32_t *y, uint64_t words, uint32_t pattern);
-__global__ void heavy_finish_kernel(const double *acc, const uint32_t *list, uint32_t h, uint32_t B, float *y);
+__global__ void heavy_finish_kernel(const void *acc, uint32_t hsplit, const uint32_t *list, uint32_t h, uint32_t B,
+                                    float *y);
 __global__ void ls_expand_kernel(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix, uint32_t a,
                                  uint32_t count, const Coord *src, uint32_t src_base, Coord *dst, uint32_t dst_base);
 __global__ void ls_block_sums_kernel(const uint8_t *sig, uint32_t a, uint32_t count, uint32_t *sums);
@@ -462,12 +480,12 @@ __device__ __forceinline__ void node_leaves_spec(uint32_t sg, uint32_t off, Coor
             const float xa[1] = {__uint_as_float(xo[b][0])}, xb[1] = {__uint_as_float(xo[b][1])};
             if (a0 || a1) {
                 const float v[1] = {a0 ? (a1 ? S::plus(c0, c1) : c0) : c1};
-                if (h & 1u) heavy_add<1>(va, h, 0, 0u, xa, xb, a0, a1);
+                if (h & 1u) heavy_put<SR, 1>(va, heavy_id2(h, 0), 0u, v, xa, xb, a0, a1);
                 else if (!S::skip(v[0])) S::update(y + out, v);
             }
             if (b0 || b1) {
                 const float v[1] = {b0 ? (b1 ? S::plus(c0, c1) : c0) : c1};
-                if (h & 2u) heavy_add<1>(va, h, 1, 0u, xa, xb, b0, b1);
+                if (h & 2u) heavy_put<SR, 1>(va, heavy_id2(h, 1), 0u, v, xa, xb, b0, b1);
                 else if (!S::skip(v[0])) S::update(y + out + 1, v);
             }
         }
@@ -558,7 +576,7 @@ __device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint
             const float xa[1] = {__uint_as_float(xo[u][0])}, xb[1] = {__uint_as_float(xo[u][1])};
             if (a0 || a1) {
                 const float v[1] = {a0 ? (a1 ? S::plus(c0, c1) : c0) : c1};
-                if (h & 1u) heavy_add<1>(va, h, 0, 0u, xa, xb, a0, a1);
+                if (h & 1u) heavy_put<SR, 1>(va, heavy_id2(h, 0), 0u, v, xa, xb, a0, a1);
                 else if (!S::skip(v[0])) {
                     if (win) smem_update<SR>(win + (out[u] - lo), __float_as_uint(v[0]));
                     else S::update(y + out[u], v);
@@ -566,7 +584,7 @@ __device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint
             }
             if (b0 || b1) {
                 const float v[1] = {b0 ? (b1 ? S::plus(c0, c1) : c0) : c1};
-                if (h & 2u) heavy_add<1>(va, h, 1, 0u, xa, xb, b0, b1);
+                if (h & 2u) heavy_put<SR, 1>(va, heavy_id2(h, 1), 0u, v, xa, xb, b0, b1);
                 else if (!S::skip(v[0])) {
                     if (win) smem_update<SR>(win + (out[u] + 1 - lo), __float_as_uint(v[0]));
                     else S::update(y + out[u] + 1, v);
@@ -647,15 +665,19 @@ __device__ __forceinline__ void leaf_slice(uint32_t lam, uint32_t r, uint32_t c,
     float x0[VW], x1[VW];
     if (a0 || b0) VecLoad<VW>::load(x + (size_t)in * B + k, x0);
     if (a1 || b1) VecLoad<VW>::load(x + (size_t)(in + 1) * B + k, x1);
-    // One output's update from x0, x1 (cells u0 on input in, u1 on in + 1).
-    auto put = [&](uint32_t o, bool u0, bool u1) {
-        float v[VW];
+    // One output's combined contribution from x0, x1 (cells u0 on input in,
+    // u1 on in + 1), and its update of y or the window.
+    auto combine = [&](bool u0, bool u1, float (&v)[VW]) {
 #pragma unroll
         for (int q = 0; q < VW; ++q) {
             const float c0 = u0 ? S::contrib(x0[q], va.w) : S::zero();
             const float c1 = u1 ? S::contrib(x1[q], va.w) : S::zero();
             v[q] = u0 ? (u1 ? S::plus(c0, c1) : c0) : c1;
         }
+    };
+    auto put = [&](uint32_t o, bool u0, bool u1) {
+        float v[VW];
+        combine(u0, u1, v);
         if (win) {
 #pragma unroll
             for (int q = 0; q < VW; ++q)
@@ -668,12 +690,22 @@ __device__ __forceinline__ void leaf_slice(uint32_t lam, uint32_t r, uint32_t c,
         // a leaf with an fp64 output: separate branch, so the fp32 path below
         // keeps its registers
         if (a0 || a1) {
-            if (hv & 1u) heavy_add<VW>(va, hv, 0, k, x0, x1, a0, a1);
-            else put(out, a0, a1);
+            if (hv & 1u) {
+                float v[VW];
+                combine(a0, a1, v);
+                heavy_put<SR, VW>(va, heavy_id2(hv, 0), k, v, x0, x1, a0, a1);
+            } else {
+                put(out, a0, a1);
+            }
         }
         if (b0 || b1) {
-            if (hv & 2u) heavy_add<VW>(va, hv, 1, k, x0, x1, b0, b1);
-            else put(out + 1, b0, b1);
+            if (hv & 2u) {
+                float v[VW];
+                combine(b0, b1, v);
+                heavy_put<SR, VW>(va, heavy_id2(hv, 1), k, v, x0, x1, b0, b1);
+            } else {
+                put(out + 1, b0, b1);
+            }
         }
         return;
     }
@@ -882,10 +914,9 @@ __device__ __forceinline__ uint32_t heavy_word4(const VecArgs &va, uint32_t out)
     return ((e.y + (uint32_t)__popc(e.x & ((1u << sh) - 1u))) << 4) | m;
 }
 
-__device__ __forceinline__ double *heavy_slot4(const VecArgs &va, uint32_t hv, int q, uint32_t k)
+__device__ __forceinline__ uint32_t heavy_id4(uint32_t hv, int q)
 {
-    const uint32_t id = (hv >> 4) + (uint32_t)__popc(hv & 15u & ((1u << q) - 1u));
-    return va.acc + (size_t)id * va.B + k;
+    return (hv >> 4) + (uint32_t)__popc(hv & 15u & ((1u << q) - 1u));
 }
 
 // One vector slice (B = 1 fp32, or a Boolean word) of U leaves whose inputs
@@ -920,12 +951,12 @@ __device__ __forceinline__ void leaf4_apply1(const uint32_t (&lam)[U], const uin
             for (int q = 0; q < 4; ++q) {
                 const uint32_t s = seg4<DIR>(l, q);
                 if (!s) continue;
-                if (SR == K2T_PLUS_TIMES && ((h >> q) & 1u)) {
+                if (SR == K2T_PLUS_TIMES && ((h >> q) & 1u) && !va.hsplit) {
                     double d = 0.0;
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
                         if ((s >> i) & 1u) d += (double)(va.w * __uint_as_float(xo[u][i]));
-                    atomicAdd(heavy_slot4(va, h, q, 0u), d);
+                    atomicAdd(static_cast<double *>(va.acc) + heavy_id4(h, q), d);
                     continue;
                 }
                 float v[1] = {S::zero()};
@@ -937,6 +968,10 @@ __device__ __forceinline__ void leaf4_apply1(const uint32_t (&lam)[U], const uin
                         v[0] = any ? S::plus(v[0], c) : c;
                         any = true;
                     }
+                if (SR == K2T_PLUS_TIMES && ((h >> q) & 1u)) {
+                    S::update(heavy_part(va, heavy_id4(h, q), 0u), v);
+                    continue;
+                }
                 if (S::skip(v[0])) continue;
                 if (win) smem_update<SR>(win + (out[u] + q - lo), __float_as_uint(v[0]));
                 else S::update(y + out[u] + q, v);
@@ -965,8 +1000,8 @@ __device__ __forceinline__ void leaf4_slice(uint32_t lam, uint32_t r, uint32_t c
     for (int q = 0; q < 4; ++q) {
         const uint32_t s = seg4<DIR>(lam, q);
         if (!s) continue;
-        if (SR == K2T_PLUS_TIMES && ((hv >> q) & 1u)) {
-            double *a = heavy_slot4(va, hv, q, k);
+        if (SR == K2T_PLUS_TIMES && ((hv >> q) & 1u) && !va.hsplit) {
+            double *a = static_cast<double *>(va.acc) + (size_t)heavy_id4(hv, q) * va.B + k;
 #pragma unroll
             for (int e = 0; e < VW; ++e) {
                 double d = 0.0;
@@ -990,7 +1025,9 @@ __device__ __forceinline__ void leaf4_slice(uint32_t lam, uint32_t r, uint32_t c
                     any = true;
                 }
         }
-        if (win) {
+        if (SR == K2T_PLUS_TIMES && ((hv >> q) & 1u)) {
+            S::update(heavy_part(va, heavy_id4(hv, q), k), v);
+        } else if (win) {
 #pragma unroll
             for (int e = 0; e < VW; ++e)
                 if (!S::skip(v[e])) smem_update<SR>(win + (size_t)(out + q - lo) * B + k + e, __float_as_uint(v[e]));
@@ -1581,7 +1618,7 @@ struct DeviceState {
     const uint32_t *hflag[2] = {nullptr, nullptr};  // fp64 outputs, per direction (null: none)
     const uint32_t *hent[2] = {nullptr, nullptr};
     const uint32_t *hlist[2] = {nullptr, nullptr};
-    double *acc = nullptr;
+    void *acc = nullptr;
     cudaStream_t cap_stream = nullptr;
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t gexec = nullptr;
@@ -1690,20 +1727,23 @@ using LaunchFn = void (*)(const k2t_tree *, const DeviceState *, const VecArgs &
 // Internal engine id: the CACHED engine on a tree with 4x4 leaves.
 constexpr uint32_t kEngineCached4 = 100;
 
-// Plus-times products of a direction with fp64 outputs.  heavy_begin points
-// va at the direction's tables and zeroes the fp64 sums of the B vectors
-// (queued after the fill of y); heavy_end rounds each sum to fp32 into its
-// output (queued after the product).  Other semirings: va gets no tables.
+// Plus-times products of a direction with heavy outputs.  heavy_begin points
+// va at the direction's tables and zeroes their sums for the B vectors
+// (queued after the fill of y); heavy_end adds each output's sums in fp64 and
+// rounds the total into y once (queued after the product).  Other semirings:
+// va gets no tables.
 inline bool heavy_begin(const k2t_tree *t, const DeviceState *d, int dir, int semiring, VecArgs &va, cudaStream_t st)
 {
     va.hflag = nullptr;
     va.hent = nullptr;
     va.acc = nullptr;
+    va.hsplit = 0u;
     if (semiring != K2T_PLUS_TIMES || !d->hflag[dir]) return false;
     va.hflag = d->hflag[dir];
     va.hent = d->hent[dir];
     va.acc = d->acc;
-    const uint64_t words = 2ull * t->hlist[dir].size() * va.B;
+    va.hsplit = t->opts.heavy_mode == 0 ? kHeavySplit : 0u;
+    const uint64_t words = (va.hsplit ? (uint64_t)va.hsplit : 2ull) * t->hlist[dir].size() * va.B;
     const uint64_t blocks = std::min<uint64_t>((words / 4 + 255) / 256 + 1, 152ull * 8);
     fill_kernel<<<(unsigned)blocks, 256, 0, st>>>(reinterpret_cast<uint32_t *>(d->acc), words, 0u);
     return true;
@@ -1714,7 +1754,8 @@ inline void heavy_end(const k2t_tree *t, const DeviceState *d, int dir, const Ve
     const uint32_t h = (uint32_t)t->hlist[dir].size();
     const uint64_t n = (uint64_t)h * va.B;
     const uint64_t blocks = std::min<uint64_t>((n + 255) / 256, 152ull * 8);
-    heavy_finish_kernel<<<(unsigned)blocks, 256, 0, st>>>(d->acc, d->hlist[dir], h, va.B, static_cast<float *>(va.y));
+    heavy_finish_kernel<<<(unsigned)blocks, 256, 0, st>>>(d->acc, va.hsplit, d->hlist[dir], h, va.B,
+                                                          static_cast<float *>(va.y));
 }
 
 template <int SR, int DIR, int VW>

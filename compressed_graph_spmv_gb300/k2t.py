@@ -42,7 +42,8 @@ class Opts(ctypes.Structure):
                 ("host_vectors", ctypes.c_uint32), ("use_graph", ctypes.c_uint32),
                 ("threads", ctypes.c_uint32), ("band_rows", ctypes.c_uint32),
                 ("band_cols", ctypes.c_uint32), ("heavy_terms", ctypes.c_uint32),
-                ("leaf_k", ctypes.c_uint32), ("reserved", ctypes.c_uint32 * 4)]
+                ("heavy_mode", ctypes.c_uint32), ("leaf_k", ctypes.c_uint32),
+                ("reserved", ctypes.c_uint32 * 3)]
 
 
 class Stats(ctypes.Structure):

@@ -104,16 +104,20 @@ typedef struct {
                                      0 = one column band                                             */
     uint32_t heavy_terms;         /* plus-times: an output with more than this many non-zeros in
                                      its row (right) or column (left), counted over the input list,
-                                     is summed in fp64 and rounded to fp32 once; every other output
-                                     is summed in fp32.  Default 2048; 0 = default; 0xffffffff =
-                                     never.  See "Accumulation precision" below.                     */
+                                     is "heavy": summed as heavy_mode says and rounded to fp32 once;
+                                     every other output is one fp32 sum.  Default 2048; 0 = default;
+                                     0xffffffff = never.  See "Accumulation precision" below.        */
+    uint32_t heavy_mode;          /* how outputs above heavy_terms are summed: 0 (default) in 32
+                                     fp32 partial sums, taken by the grid's warps in turn, added in
+                                     fp64 at the end; 1 in fp64 (exact pair sums, fp64 atomics;
+                                     slower).  See "Accumulation precision" below.                  */
     uint32_t leaf_k;              /* side of a leaf block: 2 (default; 0 = default) or 4.  4: the
                                      leaf level stores 4x4 bitmaps (16-bit signatures, cell
                                      (dr, dc) at bit 4*dr + dc), the larger leaves of section 5.6;
                                      every other level keeps k = 2 (or k = 4 on the n_k4 top
                                      levels).  Needs the CACHED engine (cache_last_internal = 1,
                                      engine AUTO or CACHED); other engines give EINVAL.              */
-    uint32_t reserved[4];
+    uint32_t reserved[3];
 } k2t_opts;
 
 /* ---- statistics -------------------------------------------------------- */
@@ -141,10 +145,10 @@ typedef struct {
     uint32_t engine;              /* resolved engine                               */
     uint32_t offsets;
     uint32_t uploaded;            /* 1 after k2t_upload                            */
-    uint32_t heavy_rows;          /* outputs of right products summed in fp64      */
-    uint32_t heavy_cols;          /* outputs of left products summed in fp64       */
-    uint32_t heavy_kib;           /* device KiB of the fp64 path's tables and
-                                     accumulators (part of workspace_bytes)        */
+    uint32_t heavy_rows;          /* heavy outputs of right products               */
+    uint32_t heavy_cols;          /* heavy outputs of left products                */
+    uint32_t heavy_kib;           /* device KiB of the heavy outputs' tables and
+                                     sums (part of workspace_bytes)                */
     uint32_t leaf_k;              /* side of a leaf block: 2 or 4                  */
     uint32_t reserved[1];
 } k2t_stats;
@@ -168,7 +172,7 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
               uint64_t n_rows, uint64_t n_cols, const k2t_opts *opts, k2t_tree **out);
 
 /* Exact device bytes k2t_upload places in its arena (tree, directory, top,
- * cached level, plan, scratch, the fp64 path's tables and accumulators,
+ * cached level, plan, scratch, the heavy outputs' tables and sums,
  * optional host-product vectors), known before
  * any kernel runs (section 1, "Our approach").  Dense x and y of device
  * products are the caller's and not included. */
@@ -189,13 +193,15 @@ int k2t_upload(k2t_tree *t, void *arena, uint64_t arena_bytes, void *stream);
  * Tropical minima follow the IEEE total order without NaN (-0 < +0); NaN
  * inputs give unspecified values.
  * Accumulation precision (plus-times): sums run in no fixed order.  An
- * output with at most opts.heavy_terms non-zeros is summed in fp32, so its
- * rounding error stays that of an fp32 sum of at most that many terms; an
- * output with more is summed in fp64 (each term w*x_j formed in fp32, then
- * added in fp64) and rounded to fp32 once, at the end of the product.  The fp64 sums need B <= opts.max_batch.
+ * output with at most opts.heavy_terms non-zeros is one fp32 sum, so its
+ * rounding error stays that of an fp32 sum of at most that many terms.  An
+ * output with more is summed, per opts.heavy_mode, in 32 fp32 partial sums
+ * (each with about 1/32 of its terms) added in fp64 (mode 0), or in fp64 with
+ * each term w*x_j formed in fp32 (mode 1), and rounded to fp32 once, at the
+ * end of the product.  Heavy outputs need B <= opts.max_batch.
  * x and y must be 4-byte aligned (16-byte alignment enables vector access).
  * Errors: ESTATE (not uploaded), EINVAL (bad dir/semiring, null, B = 0,
- * overlap), ERANGE (B > 32; plus-times with fp64 outputs and
+ * overlap), ERANGE (B > 32; plus-times with heavy outputs and
  * B > opts.max_batch), ECUDA (launch failure). */
 int k2t_spmv(k2t_tree *t, int32_t dir, int32_t semiring, float w,
              const void *x, void *y, uint32_t B, void *stream);

@@ -81,23 +81,28 @@ def test_random_ragged(seed):
                 assert_match(semiring, got, ref, "seed%d %s h%d sr%d B%d d%d" % (seed, kw, heavy, semiring, B, d))
 
 
+@pytest.mark.parametrize("heavy_mode", [1, 0])
 @pytest.mark.parametrize("heavy_terms", [0, 4])
-def test_fp64_outputs_exact(heavy_terms):
-    """Row 0 and column 0 hold 5000 non-zeros, more than the fp64 limit
-    (default 2048, or 4): with x_0 = 2^24 and x_j = 1 for the other 4999,
-    the sum 2^24 + 4999 is exact in fp64 and rounds once to the nearest fp32,
-    whatever the order of the atomics.  An fp32 sum can lose each 1 against
-    2^24 (up to 4999 off, far beyond the plus-times bound).  Outputs 1..4999
-    hold the single term 2^24, the rest zero."""
+def test_heavy_outputs_hub_cancellation(heavy_terms, heavy_mode):
+    """Row 0 and column 0 hold 5000 non-zeros, more than the heavy limit
+    (default 2048, or 4): with x_0 = 2^24 and x_j = 1 for the other 4999, the
+    sum is 2^24 + 4999.  An fp32 sum can lose each 1 against 2^24 (up to 4999
+    off, far beyond the plus-times bound).  fp64 mode (1) sums exactly and
+    rounds once, so it matches bit for bit, whatever the order of the atomics;
+    split mode (0) keeps 32 fp32 partial sums, each with a share of the
+    terms, and must meet the bound.  Outputs 1..4999 hold the single term
+    2^24, the rest zero, in both modes."""
     n = 8192
     j = np.arange(5000, dtype=np.uint32)
     rows = np.concatenate([np.zeros(5000, np.uint32), j[1:]])
     cols = np.concatenate([j, np.zeros(4999, np.uint32)])
+    exact = np.float64(2 ** 24) + 4999.0
     want = np.zeros(n, np.float32)
-    want[0] = np.float32(np.float64(2 ** 24) + 4999.0)
+    want[0] = np.float32(exact)
     want[1:5000] = np.float32(2 ** 24)
+    tol0 = 1e-5 * exact + 1e-6
     for kw in ENGINES:
-        t = _tree(rows, cols, n, n, heavy_terms=heavy_terms, host_top_max_nodes=16, **kw)
+        t = _tree(rows, cols, n, n, heavy_terms=heavy_terms, heavy_mode=heavy_mode, host_top_max_nodes=16, **kw)
         s = t.stats()
         assert (s.heavy_rows, s.heavy_cols) == (1, 1)
         for B in (1, 2, 3, 4, 16):
@@ -105,7 +110,35 @@ def test_fp64_outputs_exact(heavy_terms):
             x[0] = 2.0 ** 24
             for d in (RIGHT, LEFT):
                 got = device_product(t, d, PLUS_TIMES, x, B)
-                assert np.array_equal(got, np.repeat(want[:, None], B, axis=1)), (kw, B, d, got[0])
+                if heavy_mode == 1:
+                    assert np.array_equal(got, np.repeat(want[:, None], B, axis=1)), (kw, B, d, got[0])
+                else:
+                    assert np.array_equal(got[1:], np.repeat(want[1:, None], B, axis=1)), (kw, B, d)
+                    assert np.all(np.abs(got[0].astype(np.float64) - exact) <= tol0), (kw, B, d, got[0])
+
+
+@pytest.mark.parametrize("heavy_mode", [0, 1])
+def test_heavy_outputs_large_hub(heavy_mode):
+    """A row and a column with 2^19 non-zeros each (x ~ U(0,1)), where a
+    single fp32 sum drifts to about the plus-times bound: both heavy modes
+    must meet it on every cached and tree-only engine, for B = 1 and 16."""
+    n = 1 << 19
+    rng = np.random.default_rng(31)
+    r0, c0, _ = synth.random_small(31, n, n, 2e-6)
+    a = np.arange(n, dtype=np.uint32)
+    rows, cols = oracle.dedup_edges(np.concatenate([r0, np.full(n, 7, np.uint32), a]),
+                                    np.concatenate([c0, a, np.full(n, 11, np.uint32)]))
+    for kw in (ENGINES[0], ENGINES[2], ENGINES[5], ENGINES[6], ENGINES[8]):
+        t = _tree(rows, cols, n, n, heavy_mode=heavy_mode, **kw)
+        assert t.stats().heavy_rows >= 1 and t.stats().heavy_cols >= 1
+        for B in (1, 16):
+            x = rng.random(size=(n, B), dtype=np.float32)
+            for d in (RIGHT, LEFT):
+                hub = 7 if d == RIGHT else 11
+                sample = np.unique(np.concatenate([[hub, 0, n - 1], rng.integers(0, n, size=200)]))
+                got = device_product(t, d, PLUS_TIMES, x, B)
+                ref = oracle.rows_product(rows, cols, n, n, d, PLUS_TIMES, x, sample, B=B)
+                assert_match(PLUS_TIMES, got[sample], ref, "%s mode%d B%d d%d" % (kw, heavy_mode, B, d))
 
 
 def test_uniform_1024_plus_times():

@@ -211,10 +211,11 @@ def test_library_exports_every_declared_symbol():
 
 @pytest.mark.parametrize("heavy_terms", [0, 5, 30, 0xFFFFFFFF])
 def test_heavy_outputs_stats(heavy_terms):
-    """Outputs summed in fp64 are those with more than heavy_terms non-zeros
-    in the input list (0 selects the default 2048); the fp64 tables take one
-    bit per leaf, two words per 32 outputs and one word per fp64 output per
-    direction, plus max_batch fp64 sums per fp64 output of the wider side."""
+    """Heavy outputs are those with more than heavy_terms non-zeros in the
+    input list (0 selects the default 2048); their tables take one bit per
+    leaf, two words per 32 outputs and one word per heavy output per
+    direction, plus, per heavy output of the wider side, max_batch x 32 fp32
+    partial sums (heavy_mode 0) or max_batch fp64 sums (heavy_mode 1)."""
     rng = np.random.default_rng(21)
     nr, nc = 300, 200
     rows, cols, _ = synth.random_small(3, nr, nc, 0.05)
@@ -237,7 +238,12 @@ def test_heavy_outputs_stats(heavy_terms):
     for h, n in ((hr, nr), (hc, nc)):
         if h:
             want += ((nl + 31) // 32 + 1) * 4 + 2 * ((n + 31) // 32) * 4 + 4 * h
-    want += max(hr, hc) * 4 * 8
+    tables = want
+    want = tables + max(hr, hc) * 4 * 32 * 4      # split mode: 32 fp32 partial sums per output
     assert s.heavy_kib == (want + 1023) // 1024
     base = K.Tree(rows, cols, nr, nc, heavy_terms=0xFFFFFFFF, max_batch=4).workspace_bytes()
     assert want <= t.workspace_bytes() - base <= want + 7 * 256
+    f64 = K.Tree(rows, cols, nr, nc, heavy_terms=heavy_terms, heavy_mode=1, max_batch=4).stats()
+    assert f64.heavy_kib == (tables + max(hr, hc) * 4 * 8 + 1023) // 1024   # fp64 mode: one double each
+    with pytest.raises(K.K2TError):
+        K.Tree(rows, cols, nr, nc, heavy_mode=2)
