@@ -329,3 +329,43 @@ def msbfs(rows, cols, n: int, sources, direction: int, max_levels: int | None = 
             visited |= nxt
             frontier = nxt
     return dist
+
+
+def bool_product(rows_a, cols_a, rows_b, cols_b, n: int, m: int, p: int):
+    """Boolean product C = A B of an n x m and an m x p Boolean matrix given as
+    edge lists: C_ij = OR_k (A_ik AND B_kj), the product of two trees the pages
+    name as the extension of the level-synchronous traversal (section 7 of "A
+    GPU Engine for Sparse Matrix-Vector Products on k^2-Tree-Compressed
+    Graphs").  A scipy sparse integer product (path counts) thresholded at 1.
+    Returns the distinct non-zeros (rows, cols) sorted by (row, col)."""
+    import scipy.sparse as sp
+    ra, ca = dedup_edges(rows_a, cols_a)
+    rb, cb = dedup_edges(rows_b, cols_b)
+    A = sp.csr_matrix((np.ones(ra.size, np.int64), (ra.astype(np.int64), ca.astype(np.int64))), shape=(n, m))
+    B = sp.csr_matrix((np.ones(rb.size, np.int64), (rb.astype(np.int64), cb.astype(np.int64))), shape=(m, p))
+    C = (A @ B).tocoo()
+    keep = C.data > 0
+    r = C.row[keep].astype(np.uint32)
+    c = C.col[keep].astype(np.uint32)
+    order = np.lexsort((c, r))
+    return r[order], c[order]
+
+
+def transitive_closure(rows, cols, n: int, max_iters: int = 64):
+    """A+ = A or A^2 or A^3 ... of an n x n Boolean matrix (pairs joined by a
+    path of one or more edges) by repeated squaring, C <- C or C C, until C
+    stops growing (section 7 of the same pages: "by repeated squaring the
+    transitive closure").  Returns (rows, cols, iterations): the distinct
+    non-zeros sorted by (row, col) and the number of squarings performed,
+    the last of which added nothing."""
+    r, c = dedup_edges(rows, cols)
+    it = 0
+    while it < max_iters:
+        it += 1
+        pr, pc = bool_product(r, c, r, c, n, n, n)
+        nr, nc = dedup_edges(np.concatenate([r, pr]), np.concatenate([c, pc]))
+        if nr.size == r.size:
+            break
+        r, c = nr, nc
+    order = np.lexsort((c, r))
+    return r[order], c[order], it
