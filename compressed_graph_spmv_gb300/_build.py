@@ -21,7 +21,7 @@ NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC,-O3", "-I" + os.path.join(ROOT, "include")]
 SOURCES = ["k2t_host.cpp", "k2t_device.cu", "k2t_sr_plus_times.cu", "k2t_sr_boolean.cu", "k2t_sr_min_plus.cu",
-           "k2t_static.cu", "k2t_probe.cu"]
+           "k2t_static.cu", "k2t_probe.cu", "k2t_product.cu"]
 HEADERS = ["k2t_internal.h", "k2t_kernels.cuh", os.path.join("..", "..", "include", "k2t.h")]
 
 

@@ -206,9 +206,17 @@ void pack_level(k2t_tree *t, int d, const uint16_t *sg, size_t n, int nt)
 
 void build_directory(k2t_tree *t, int d, int nt)
 {
+    level_directory(t, d, t->dir[(size_t)(d - t->d0)], nt);
+}
+
+}  // namespace
+
+// Directory of a k = 2 level d <= l-2: the first child of every 256-node
+// block (level-relative), then the level's child total (section 3.2).
+void level_directory(const k2t_tree *t, int d, std::vector<uint32_t> &dir, int nt)
+{
     uint64_t n = t->nodes[(size_t)d];
     uint64_t blocks = (n + kDirS - 1) / kDirS;
-    std::vector<uint32_t> &dir = t->dir[(size_t)(d - t->d0)];
     dir.assign(blocks + 1, 0);
     const std::vector<uint64_t> &w = t->sig[(size_t)d];
     std::vector<uint64_t> sums(blocks, 0);
@@ -225,8 +233,6 @@ void build_directory(k2t_tree *t, int d, int nt)
     for (uint64_t b = 0; b < blocks; ++b) { dir[b] = (uint32_t)run; run += sums[b]; }
     dir[blocks] = (uint32_t)run;
 }
-
-}  // namespace
 
 uint32_t level_sig(const k2t_tree *t, int d, uint64_t node)
 {

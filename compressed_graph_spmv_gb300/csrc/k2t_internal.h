@@ -109,6 +109,7 @@ uint64_t level_offset(const k2t_tree *t, int d, uint64_t node);  // first child 
 uint32_t level_sig(const k2t_tree *t, int d, uint64_t node);
 inline bool level_is_k4(const k2t_tree *t, int d) { return d < t->n_k4 || (t->leaf_k4 && d == t->levels - 1); }
 void compute_layout(k2t_tree *t);
+void level_directory(const k2t_tree *t, int d, std::vector<uint32_t> &dir, int nt);
 // implemented in k2t_device.cu
 void device_release(k2t_tree *t);
 }  // namespace k2t

@@ -31,7 +31,7 @@ EXPORTED = ["k2t_default_opts", "k2t_build", "k2t_workspace_bytes", "k2t_upload"
             "k2t_spmv_host", "k2t_stats_get", "k2t_level_signatures", "k2t_device_level",
             "k2t_decode", "k2t_free", "k2t_strerror", "k2t_last_cuda_error",
             "k2t_spmv_noalloc", "k2t_noalloc_scratch_limit", "k2t_probe", "k2t_msbfs",
-            "k2t_msbfs_work_bytes"]
+            "k2t_msbfs_work_bytes", "k2t_bool_product", "k2t_bool_closure"]
 
 
 class Opts(ctypes.Structure):
@@ -98,6 +98,10 @@ def load() -> ctypes.CDLL:
         lib.k2t_msbfs.restype = ctypes.c_int
         lib.k2t_msbfs_work_bytes.argtypes = [P]
         lib.k2t_msbfs_work_bytes.restype = U64
+        lib.k2t_bool_product.argtypes = [P, P, ctypes.POINTER(Opts), ctypes.POINTER(P), P]
+        lib.k2t_bool_product.restype = ctypes.c_int
+        lib.k2t_bool_closure.argtypes = [P, ctypes.POINTER(Opts), U32, ctypes.POINTER(P), ctypes.POINTER(U32), P]
+        lib.k2t_bool_closure.restype = ctypes.c_int
         lib.k2t_probe.argtypes = [I32, P, P, U64, U64, P]
         lib.k2t_probe.restype = ctypes.c_int
         lib.k2t_spmv_host.argtypes = [P, I32, I32, ctypes.c_float, P, P, U32, P]
@@ -242,6 +246,36 @@ class Tree:
         _check("k2t_msbfs", load().k2t_msbfs(self._h, direction, src.ctypes.data, src.size, _dev_ptr(dist),
                                              _dev_ptr(work), max_levels, ctypes.byref(lv), _stream_ptr(stream)))
         return int(lv.value)
+
+    @classmethod
+    def _adopt(cls, handle, n_rows: int, n_cols: int, opts: Opts) -> "Tree":
+        t = cls.__new__(cls)
+        t.opts = opts
+        t.n_rows, t.n_cols = int(n_rows), int(n_cols)
+        t._h = handle
+        t._arena = None
+        return t
+
+    def bool_product(self, other: "Tree", stream=None, opts: Opts | None = None, **kw) -> "Tree":
+        """Boolean C = self * other through k2t_bool_product; C is a new host
+        tree built with ``opts`` (or the given option keywords)."""
+        if opts is None:
+            opts = default_opts(**kw)
+        h = ctypes.c_void_p()
+        _check("k2t_bool_product", load().k2t_bool_product(self._h, other._h, ctypes.byref(opts), ctypes.byref(h),
+                                                           _stream_ptr(stream)))
+        return Tree._adopt(h, self.n_rows, other.n_cols, opts)
+
+    def bool_closure(self, max_iters: int = 64, stream=None, opts: Opts | None = None, **kw):
+        """Transitive closure by repeated squaring (k2t_bool_closure); returns
+        (tree, squarings run)."""
+        if opts is None:
+            opts = default_opts(**kw)
+        h = ctypes.c_void_p()
+        it = ctypes.c_uint32()
+        _check("k2t_bool_closure", load().k2t_bool_closure(self._h, ctypes.byref(opts), int(max_iters),
+                                                           ctypes.byref(h), ctypes.byref(it), _stream_ptr(stream)))
+        return Tree._adopt(h, self.n_rows, self.n_cols, opts), int(it.value)
 
     def msbfs_work_bytes(self) -> int:
         return int(load().k2t_msbfs_work_bytes(self._h))

@@ -247,6 +247,27 @@ int k2t_spmv_noalloc(k2t_tree *t, int32_t dir, int32_t semiring, float w,
 /* Size in bytes of the device array k2t_spmv_noalloc works in. */
 uint64_t k2t_noalloc_scratch_limit(void);
 
+/* Boolean product C = A B of two trees: A n x m, B m x p (a->n_cols ==
+ * b->n_rows), built with the same padded side and k = 2 on every level
+ * (n_k4_levels = 0, leaf_k = 2).  Section 7 of the pages: a level-synchronous
+ * descent over a frontier of node pairs (node of A, node of B, same level,
+ * matching inner block) expanding into the matching quadrant sub-products;
+ * at the leaves, 2x2 Boolean products.  Runs on the current device on
+ * `stream` (the trees need not be uploaded; the product copies every level's
+ * signatures and directory to memory it allocates and frees), then builds C
+ * on the host with k2t_build(opts) into *out (caller frees with k2t_free).
+ * Errors: EINVAL (null, shapes or tree kinds that do not match), ENOMEM,
+ * ECUDA, and k2t_build's errors. */
+int k2t_bool_product(const k2t_tree *a, const k2t_tree *b, const k2t_opts *opts, k2t_tree **out, void *stream);
+
+/* Transitive closure A+ (pairs joined by a path of one or more edges) of a
+ * square tree by repeated squaring, C <- C or C C (section 7), until C stops
+ * growing or max_iters squarings ran; *iters = squarings run.  *out is C's
+ * tree built with opts.  Errors as k2t_bool_product; EINVAL for a
+ * non-square tree. */
+int k2t_bool_closure(const k2t_tree *a, const k2t_opts *opts, uint32_t max_iters, k2t_tree **out,
+                     uint32_t *iters, void *stream);
+
 /* Multi-source breadth-first search to the fixed point (section 5.8): hop
  * distances from B <= 32 sources at once, one batched Boolean product per
  * level, with a mark kernel over dense n x B tables.  dir K2T_RIGHT: vertex i
