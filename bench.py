@@ -548,6 +548,38 @@ def run_msbfs(args):
     print(json.dumps(out))
 
 
+def run_bool_product(args):
+    """Boolean product of two trees, C = A A (section 7 analogue), on a local
+    web-like graph (n = 2^scale, Poisson(6) out-degree, targets within +-256
+    w.p. 0.8): the whole k2t_bool_product call (device pair descent, records
+    to the host, C's build) timed on the host clock, then the oracle's scipy
+    product of the edge lists for the same C."""
+    import torch
+    from compressed_graph_spmv_gb300 import k2t as K
+    import oracle
+    scale = args.bool_product
+    n = 1 << scale
+    rows, cols = synth.weblike(n, lam=6.0, seed=5)
+    a = K.Tree(rows, cols, n, n)
+    a.bool_product(a).close()   # warm-up (context, allocations)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    c = a.bool_product(a)
+    sec = time.perf_counter() - t0
+    st = c.stats()
+    out = {"kind": "bool_product", "workload": "local%d (weblike n=2^%d, lam 6)" % (scale, scale),
+           "nnz_a": int(a.stats().nnz), "nnz_c": int(st.nnz), "seconds": sec,
+           "c_nonzeros_per_s": st.nnz / sec}
+    t0 = time.perf_counter()
+    r, cc = oracle.bool_product(rows, cols, rows, cols, n, n, n)
+    out["oracle_seconds"] = time.perf_counter() - t0
+    if not args.no_parity:
+        gr, gc = c.decode()
+        order = np.lexsort((gc, gr))
+        out["parity_ok"] = bool(np.array_equal(gr[order], r) and np.array_equal(gc[order], cc))
+    print(json.dumps(out))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -567,6 +599,8 @@ def main():
     ap.add_argument("--msbfs", action="store_true", help="time a multi-source search on the workload and exit")
     ap.add_argument("--bfs-sources", type=int, default=16)
     ap.add_argument("--bfs-levels", type=int, default=32)
+    ap.add_argument("--bool-product", type=int, default=0, metavar="SCALE",
+                    help="time the Boolean product A A of a 2^SCALE local graph and exit")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
@@ -574,6 +608,8 @@ def main():
         run_ceilings(args)
     elif args.msbfs:
         run_msbfs(args)
+    elif args.bool_product:
+        run_bool_product(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
