@@ -163,13 +163,14 @@ __device__ __forceinline__ uint32_t heavy_word(const VecArgs &va, uint32_t out)
 // Index in the heavy list of output out + q of a 2x2 leaf (hv from heavy_word).
 __device__ __forceinline__ uint32_t heavy_id2(uint32_t hv, int q) { return (hv >> 2) + (q ? (hv & 1u) : 0u); }
 
-// The fp32 partial sum of heavy output `id` (slice k) this warp adds to: the
-// warps of the grid take the hsplit partial sums in turn, so each holds about
-// 1/hsplit of the output's terms and the addresses a hub row's updates hit
-// are spread over hsplit lines.
-__device__ __forceinline__ float *heavy_part(const VecArgs &va, uint32_t id, uint32_t k)
+// The fp32 partial sum of heavy output `id` (slice k) that a leaf with first
+// input `in` adds to: a multiplicative hash of the input index picks one of
+// the hsplit partial sums, so the terms of an output spread over them (about
+// 1/hsplit each, whatever the engine or launch shape) and concurrent updates
+// of a hub row hit hsplit different lines.
+__device__ __forceinline__ float *heavy_part(const VecArgs &va, uint32_t id, uint32_t in, uint32_t k)
 {
-    const uint32_t part = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) & (va.hsplit - 1u);
+    const uint32_t part = ((in * 2654435761u) >> 27) & (va.hsplit - 1u);
     return static_cast<float *>(va.acc) + ((size_t)id * va.hsplit + part) * va.B + k;
 }
 
@@ -178,11 +179,12 @@ __device__ __forceinline__ float *heavy_part(const VecArgs &va, uint32_t id, uin
 // w*xa (when ua) and w*xb (when ub) are added in fp64, where the sum of two
 // floats is exact.
 template <int SR, int VW>
-__device__ __forceinline__ void heavy_put(const VecArgs &va, uint32_t id, uint32_t k, const float (&v)[VW],
-                                          const float (&xa)[VW], const float (&xb)[VW], bool ua, bool ub)
+__device__ __forceinline__ void heavy_put(const VecArgs &va, uint32_t id, uint32_t in, uint32_t k,
+                                          const float (&v)[VW], const float (&xa)[VW], const float (&xb)[VW], bool ua,
+                                          bool ub)
 {
     if (va.hsplit) {
-        Fp32Sem<SR>::update(heavy_part(va, id, k), v);
+        Fp32Sem<SR>::update(heavy_part(va, id, in, k), v);
         return;
     }
     double *a = static_cast<double *>(va.acc) + (size_t)id * va.B + k;
@@ -294,11 +296,11 @@ __device__ __forceinline__ void leaf_group(const uint32_t (&lam)[U], const uint3
                 } else {
                     const uint32_t h = SR == K2T_PLUS_TIMES && ((fl >> u) & 1u) ? heavy_word(a, out[u]) : 0u;
                     if (a0[u] || a1[u]) {
-                        if (h & 1u) heavy_put<SR, VW>(a, heavy_id2(h, 0), k, v0, x0[u], x1[u], a0[u], a1[u]);
+                        if (h & 1u) heavy_put<SR, VW>(a, heavy_id2(h, 0), in[u], k, v0, x0[u], x1[u], a0[u], a1[u]);
                         else S::update(y + (size_t)out[u] * B + k, v0);
                     }
                     if (b0[u] || b1[u]) {
-                        if (h & 2u) heavy_put<SR, VW>(a, heavy_id2(h, 1), k, v1, x0[u], x1[u], b0[u], b1[u]);
+                        if (h & 2u) heavy_put<SR, VW>(a, heavy_id2(h, 1), in[u], k, v1, x0[u], x1[u], b0[u], b1[u]);
                         else S::update(y + (size_t)(out[u] + 1) * B + k, v1);
                     }
                 }
@@ -480,12 +482,12 @@ __device__ __forceinline__ void node_leaves_spec(uint32_t sg, uint32_t off, Coor
             const float xa[1] = {__uint_as_float(xo[b][0])}, xb[1] = {__uint_as_float(xo[b][1])};
             if (a0 || a1) {
                 const float v[1] = {a0 ? (a1 ? S::plus(c0, c1) : c0) : c1};
-                if (h & 1u) heavy_put<SR, 1>(va, heavy_id2(h, 0), 0u, v, xa, xb, a0, a1);
+                if (h & 1u) heavy_put<SR, 1>(va, heavy_id2(h, 0), xin[b], 0u, v, xa, xb, a0, a1);
                 else if (!S::skip(v[0])) S::update(y + out, v);
             }
             if (b0 || b1) {
                 const float v[1] = {b0 ? (b1 ? S::plus(c0, c1) : c0) : c1};
-                if (h & 2u) heavy_put<SR, 1>(va, heavy_id2(h, 1), 0u, v, xa, xb, b0, b1);
+                if (h & 2u) heavy_put<SR, 1>(va, heavy_id2(h, 1), xin[b], 0u, v, xa, xb, b0, b1);
                 else if (!S::skip(v[0])) S::update(y + out + 1, v);
             }
         }
@@ -493,7 +495,7 @@ __device__ __forceinline__ void node_leaves_spec(uint32_t sg, uint32_t off, Coor
 }
 
 template <int SR, int DIR, int VW>
-__global__ void __launch_bounds__(kFlatThreads)
+__global__ void __launch_bounds__(kFlatThreads, 3)
 flat_leaf_kernel(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix, uint32_t leaf_base, uint32_t a,
                  uint32_t count, const Coord *src, const uint8_t *leaf, VecArgs va)
 {
@@ -543,8 +545,8 @@ flat_leaf_kernel(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix
 // already loaded (xo[u][0]: input r or c, xo[u][1]: the next one); one
 // vector slice (B = 1 fp32, or a Boolean word).  Bit u of fl (plus-times):
 // leaf u has fp64 outputs; those go to their fp64 sums, window or not.
-template <int SR, int DIR, int U>
-__device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint32_t (&out)[U],
+template <int SR, int DIR, int U, class InOf>
+__device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint32_t (&out)[U], InOf &&in_of,
                                             const uint32_t (&xo)[U][2], uint32_t fl, const VecArgs &va,
                                             uint32_t *win, uint32_t lo)
 {
@@ -576,7 +578,7 @@ __device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint
             const float xa[1] = {__uint_as_float(xo[u][0])}, xb[1] = {__uint_as_float(xo[u][1])};
             if (a0 || a1) {
                 const float v[1] = {a0 ? (a1 ? S::plus(c0, c1) : c0) : c1};
-                if (h & 1u) heavy_put<SR, 1>(va, heavy_id2(h, 0), 0u, v, xa, xb, a0, a1);
+                if (h & 1u) heavy_put<SR, 1>(va, heavy_id2(h, 0), in_of(u), 0u, v, xa, xb, a0, a1);
                 else if (!S::skip(v[0])) {
                     if (win) smem_update<SR>(win + (out[u] - lo), __float_as_uint(v[0]));
                     else S::update(y + out[u], v);
@@ -584,7 +586,7 @@ __device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint
             }
             if (b0 || b1) {
                 const float v[1] = {b0 ? (b1 ? S::plus(c0, c1) : c0) : c1};
-                if (h & 2u) heavy_put<SR, 1>(va, heavy_id2(h, 1), 0u, v, xa, xb, b0, b1);
+                if (h & 2u) heavy_put<SR, 1>(va, heavy_id2(h, 1), in_of(u), 0u, v, xa, xb, b0, b1);
                 else if (!S::skip(v[0])) {
                     if (win) smem_update<SR>(win + (out[u] + 1 - lo), __float_as_uint(v[0]));
                     else S::update(y + out[u] + 1, v);
@@ -631,6 +633,13 @@ __device__ __forceinline__ uint32_t *warp_window_begin(uint32_t mn, uint32_t mx,
     return mem;
 }
 
+// Heavy outputs (plus-times, split partial sums) stay in a warp's window like
+// any other output: the window's fp32 sum of an output holds at most the
+// terms of one warp's leaves.  The flush adds it to one of the output's
+// partial sums (picked by a hash of the warp's position in the grid) instead
+// of y.  fp64 mode keeps heavy outputs out of windows altogether.
+__device__ __forceinline__ bool heavy_in_window(const VecArgs &va) { return va.hsplit != 0u; }
+
 template <int SR>
 __device__ __forceinline__ void warp_window_flush(const uint32_t *win, uint32_t lo, uint32_t span, uint32_t width,
                                                   const VecArgs &va)
@@ -639,9 +648,22 @@ __device__ __forceinline__ void warp_window_flush(const uint32_t *win, uint32_t 
     __syncwarp();
     uint32_t *y = static_cast<uint32_t *>(va.y) + (size_t)lo * width;
     const uint64_t limit = (va.n_out - lo) * width;
+    const bool heavy = SR == K2T_PLUS_TIMES && va.hflag != nullptr && heavy_in_window(va);
+    const uint32_t part = ((((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * 2654435761u) >> 27) & (va.hsplit - 1u);
     for (uint32_t i = lane; i < span * width; i += 32u) {
         const uint32_t v = win[i];
-        if (!is_noop_word<SR>(v) && i < limit) global_update_word<SR>(y + i, v);
+        if (is_noop_word<SR>(v) || i >= limit) continue;
+        if (heavy) {
+            const uint32_t o = lo + i / width;
+            const uint2 e = __ldg(reinterpret_cast<const uint2 *>(va.hent) + (o >> 5));
+            if ((e.x >> (o & 31u)) & 1u) {
+                const uint32_t id = e.y + (uint32_t)__popc(e.x & ((1u << (o & 31u)) - 1u));
+                float *dst = static_cast<float *>(va.acc) + ((size_t)id * va.hsplit + part) * width + i % width;
+                atomicAdd(dst, __uint_as_float(v));
+                continue;
+            }
+        }
+        global_update_word<SR>(y + i, v);
     }
 }
 
@@ -693,7 +715,7 @@ __device__ __forceinline__ void leaf_slice(uint32_t lam, uint32_t r, uint32_t c,
             if (hv & 1u) {
                 float v[VW];
                 combine(a0, a1, v);
-                heavy_put<SR, VW>(va, heavy_id2(hv, 0), k, v, x0, x1, a0, a1);
+                heavy_put<SR, VW>(va, heavy_id2(hv, 0), in, k, v, x0, x1, a0, a1);
             } else {
                 put(out, a0, a1);
             }
@@ -702,7 +724,7 @@ __device__ __forceinline__ void leaf_slice(uint32_t lam, uint32_t r, uint32_t c,
             if (hv & 2u) {
                 float v[VW];
                 combine(b0, b1, v);
-                heavy_put<SR, VW>(va, heavy_id2(hv, 1), k, v, x0, x1, b0, b1);
+                heavy_put<SR, VW>(va, heavy_id2(hv, 1), in, k, v, x0, x1, b0, b1);
             } else {
                 put(out + 1, b0, b1);
             }
@@ -724,16 +746,19 @@ __device__ __forceinline__ void leaf_slice(uint32_t lam, uint32_t r, uint32_t c,
 //    load and a row of y one coalesced vector reduction (the pages' B
 //    adjacent threads per node, section 3.6).
 // Updates go to the window when there is one, else to y.
+// warp_win: win is this warp's own window (flushed by warp_window_flush),
+// which may hold heavy outputs; a shared block window (BANDED) may not.
 template <int SR, int DIR, int VW, class LeafAt>
 __device__ __forceinline__ void warp_leaf_rounds(uint32_t jb, uint32_t je, LeafAt &&leaf_at, const VecArgs &va,
-                                                 uint32_t *win, uint32_t lo)
+                                                 uint32_t *win, uint32_t lo, bool warp_win = true)
 {
     const uint32_t lane = threadIdx.x & 31u;
+    // per-leaf heavy routing, unless every update of the warp goes to its window
+    const bool heavy = SR == K2T_PLUS_TIMES && va.hflag != nullptr && !(win && warp_win && heavy_in_window(va));
     if (SR == K2T_BOOLEAN || (VW == 1 && va.B == 1)) {
         constexpr int U = kLeafU;
         const uint32_t *x = static_cast<const uint32_t *>(va.x);
         const bool x8 = ((uintptr_t)x & 7u) == 0;
-        const bool heavy = SR == K2T_PLUS_TIMES && va.hflag != nullptr;
         for (uint32_t j0 = jb; j0 < je; j0 += 32u * U) {
             uint32_t lam[U], r[U], c[U], fl = 0u;
 #pragma unroll
@@ -766,7 +791,14 @@ __device__ __forceinline__ void warp_leaf_rounds(uint32_t jb, uint32_t je, LeafA
                     }
                 }
             }
-            leaf_apply1<SR, DIR, U>(lam, out, xo, fl, va, win, lo);
+            // the input index of leaf u, looked up again (only leaves with a
+            // heavy output outside a window need it)
+            auto in_of = [&](int u) {
+                uint32_t l2, r2, c2, li2;
+                leaf_at(j0 + 32u * (uint32_t)u + lane, l2, r2, c2, li2);
+                return DIR == K2T_RIGHT ? c2 : r2;
+            };
+            leaf_apply1<SR, DIR, U>(lam, out, in_of, xo, fl, va, win, lo);
         }
         return;
     }
@@ -777,7 +809,6 @@ __device__ __forceinline__ void warp_leaf_rounds(uint32_t jb, uint32_t je, LeafA
         const uint32_t groups = G <= 32u ? G : 32u;      // lanes that own a slice per round
         const uint32_t slot = lane / groups, sub = lane % groups;
         const bool active = slot < per;
-        const bool heavy = SR == K2T_PLUS_TIMES && va.hflag != nullptr;
         for (uint32_t j0 = jb; j0 < je; j0 += per * U) {
             uint32_t lam[U], r[U], c[U], hv[U];
 #pragma unroll
@@ -921,8 +952,8 @@ __device__ __forceinline__ uint32_t heavy_id4(uint32_t hv, int q)
 
 // One vector slice (B = 1 fp32, or a Boolean word) of U leaves whose inputs
 // xo[u][0..3] are loaded: every output with a cell gets its combined segment.
-template <int SR, int DIR, int U>
-__device__ __forceinline__ void leaf4_apply1(const uint32_t (&lam)[U], const uint32_t (&out)[U],
+template <int SR, int DIR, int U, class InOf>
+__device__ __forceinline__ void leaf4_apply1(const uint32_t (&lam)[U], const uint32_t (&out)[U], InOf &&in_of,
                                              const uint32_t (&xo)[U][4], uint32_t fl, const VecArgs &va,
                                              uint32_t *win, uint32_t lo)
 {
@@ -969,7 +1000,7 @@ __device__ __forceinline__ void leaf4_apply1(const uint32_t (&lam)[U], const uin
                         any = true;
                     }
                 if (SR == K2T_PLUS_TIMES && ((h >> q) & 1u)) {
-                    S::update(heavy_part(va, heavy_id4(h, q), 0u), v);
+                    S::update(heavy_part(va, heavy_id4(h, q), in_of(u), 0u), v);
                     continue;
                 }
                 if (S::skip(v[0])) continue;
@@ -1026,7 +1057,7 @@ __device__ __forceinline__ void leaf4_slice(uint32_t lam, uint32_t r, uint32_t c
                 }
         }
         if (SR == K2T_PLUS_TIMES && ((hv >> q) & 1u)) {
-            S::update(heavy_part(va, heavy_id4(hv, q), k), v);
+            S::update(heavy_part(va, heavy_id4(hv, q), in, k), v);
         } else if (win) {
 #pragma unroll
             for (int e = 0; e < VW; ++e)
@@ -1047,7 +1078,7 @@ __device__ __forceinline__ void warp_leaf4_rounds(uint32_t jb, uint32_t je, Leaf
                                                   uint32_t *win, uint32_t lo)
 {
     const uint32_t lane = threadIdx.x & 31u;
-    const bool heavy = SR == K2T_PLUS_TIMES && va.hflag != nullptr;
+    const bool heavy = SR == K2T_PLUS_TIMES && va.hflag != nullptr && !(win && heavy_in_window(va));
     if (SR == K2T_BOOLEAN || (VW == 1 && va.B == 1)) {
         constexpr int U = K2T_LEAF4_U;
         const uint32_t *x = static_cast<const uint32_t *>(va.x);
@@ -1087,7 +1118,12 @@ __device__ __forceinline__ void warp_leaf4_rounds(uint32_t jb, uint32_t je, Leaf
                     }
                 }
             }
-            leaf4_apply1<SR, DIR, U>(lam, out, xo, fl, va, win, lo);
+            auto in_of = [&](int u) {
+                uint32_t l2, r2, c2, li2;
+                leaf_at(j0 + 32u * (uint32_t)u + lane, l2, r2, c2, li2);
+                return DIR == K2T_RIGHT ? c2 : r2;
+            };
+            leaf4_apply1<SR, DIR, U>(lam, out, in_of, xo, fl, va, win, lo);
         }
         return;
     }
@@ -1267,7 +1303,7 @@ banded_kernel(const uint32_t *chunks, const Coord *coords, const uint32_t *bleaf
             c = 4u * p.c + 2u * (b & 1u);
             li = lw[node] + (e & 3u);
             lam = nibble_at(leaf, li);
-        }, va, windowed ? win : nullptr, (uint32_t)band_lo);
+        }, va, windowed ? win : nullptr, (uint32_t)band_lo, false);
         __syncwarp();
     }
     if (windowed) {
