@@ -54,6 +54,9 @@ def make_workload(name: str):
     if name == "social24":
         wl = synth.social_c4()
         return wl, dict(), [(0, 8)]
+    if name == "clustered22":
+        wl = synth.clustered()
+        return wl, dict(cache_last_internal=1), [(0, 1), (1, 1)]
     if name.startswith("rmat27"):
         wl = synth.large_c5(B=16)
         return wl, dict(cache_last_internal=1), [(0, 1), (1, 1), (0, 16), (1, 16)]

@@ -199,6 +199,22 @@ def large_c5(scale: int = 27, edges: int = 1_200_000_000, B: int = 1, seed: int 
                     cache_last_internal=True, xs={0: x, 1: x})
 
 
+def clustered(scale: int = 22, block: int = 16, per_row: int = 8, seed: int = 6):
+    """A clustered graph: every row i draws per_row distinct columns inside its
+    own block-aligned window [i - i % block, i - i % block + block), so the
+    matrix is block diagonal with blocks per_row/block full.  Dense leaves
+    (several non-zeros per 2x2 or 4x4 block), as on locality-ordered crawls.
+    x ~ U(0,1) fp32, plus-times, right and left, B = 1."""
+    n = 1 << scale
+    rng = np.random.default_rng(seed)
+    rows = np.repeat(np.arange(n, dtype=np.uint32), per_row)
+    offs = np.argsort(rng.random((n, block)), axis=1)[:, :per_row].astype(np.uint32).reshape(-1)
+    cols = (rows - rows % block) + offs
+    x = rng.random(size=(n, 1), dtype=np.float32)
+    return Workload("clustered%d-b%d-d%d" % (scale, block, per_row), rows, cols, n, n, PLUS_TIMES, 1, 1.0,
+                    cache_last_internal=True, xs={0: x, 1: x})
+
+
 def random_small(seed: int, n_rows: int, n_cols: int, density: float):
     """Small random Boolean matrix (with repeated coordinates) for exhaustive checks."""
     rng = np.random.default_rng(seed)
