@@ -906,7 +906,7 @@ cached_block_kernel(const uint8_t *sig, const uint32_t *dir, uint32_t n, const C
 
 // ---- 4x4 leaves (leaf_k = 4) ------------------------------------------------------
 #ifndef K2T_LEAF4_U
-#define K2T_LEAF4_U 4
+#define K2T_LEAF4_U 2
 #endif
 // The leaves the pages name as the next lever (section 5.6): a leaf is a 4x4
 // bitmap (16-bit signature, cell (dr, dc) at bit 4*dr + dc).  Its four inputs
@@ -1162,7 +1162,7 @@ __device__ __forceinline__ void warp_leaf4_rounds(uint32_t jb, uint32_t je, Leaf
 // directory block of the last internal level, leaf list built by a warp scan,
 // per-warp output window), with nodes covering 8x8 cells and 16-bit leaves.
 #ifndef K2T_LEAF4_MINB
-#define K2T_LEAF4_MINB 3
+#define K2T_LEAF4_MINB 4
 #endif
 template <int SR, int DIR, int VW>
 __global__ void __launch_bounds__(32 * kCachedWarps, K2T_LEAF4_MINB)
