@@ -188,6 +188,35 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
+# --- measured DRAM traffic ---------------------------------------------------------
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the product kernel,
+# from one ncu capture of the workload (the command is in
+# profiles/cached_block_kernel_rmat27.md).  The numbers hold only for the device
+# sources they were taken on: DEVICE_DIGEST is the SHA-256 of those sources, and
+# any later change to them makes roofline.traffic null until a new capture.
+MEASURED_TRAFFIC = {"digest": None, "rmat27-bfs-1200M": {}}
+
+
+def device_digest() -> str:
+    import hashlib
+    csrc = os.path.join(ROOT, "compressed_graph_spmv_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    with open(os.path.join(ROOT, "include", "k2t.h"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str, product: str):
+    table = MEASURED_TRAFFIC.get(workload, {})
+    if product not in table or MEASURED_TRAFFIC["digest"] != device_digest():
+        return None
+    return table[product]
+
+
 # --- byte accounting ------------------------------------------------------------
 def algorithmic_bytes(stats, semiring, direction, B):
     """Bytes a product kernel must move: the tree parts it reads, x once, y
@@ -414,7 +443,8 @@ def run_ours(args):
     peak, peak_kind = measured_peak()
     ach = per_kernel[dom]["achieved_gbs"]
     roofline = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
-                "traffic": None, "peak_source": peak_kind, "kernel": per_kernel[dom]["product"],
+                "traffic": measured_traffic(wl.name, per_kernel[dom]["product"]), "peak_source": peak_kind,
+                "kernel": per_kernel[dom]["product"],
                 "bytes_per_launch": per_kernel[dom]["algorithmic_bytes"]}
 
     # end to end through the C ABI with host buffers (copies inside the timed region)
