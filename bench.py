@@ -436,7 +436,9 @@ def run_ours(args):
     for i, (d, B) in enumerate(products):
         avg = float(main_ms[:, i].mean()) / 1e3
         byt = algorithmic_bytes(st, wl.semiring, d, B)
+        q1, med, q3 = (float(v) for v in np.percentile(main_ms[:, i], [25, 50, 75]))
         per_kernel.append({"product": "%s B=%d" % ("right" if d == 0 else "left", B), "avg_ms": avg * 1e3,
+                           "median_ms": med, "iqr_ms": q3 - q1,
                            "fill_ms": float((prod_ms[:, i] - main_ms[:, i]).mean()),
                            "algorithmic_bytes": byt, "achieved_gbs": byt / avg / 1e9,
                            "edges_per_s": m * B / avg})

@@ -247,3 +247,38 @@ def test_heavy_outputs_stats(heavy_terms):
     assert f64.heavy_kib == (tables + max(hr, hc) * 4 * 8 + 1023) // 1024   # fp64 mode: one double each
     with pytest.raises(K.K2TError):
         K.Tree(rows, cols, nr, nc, heavy_mode=2)
+
+
+def test_product_argument_errors_on_host():
+    """k2t_bool_product / k2t_bool_closure reject mismatched or unsupported
+    trees before touching the device (no GPU needed)."""
+    lib = K.load()
+    import ctypes
+    one = np.array([3], np.uint32)
+    a = K.Tree(one, one, 64, 64)
+    out = ctypes.c_void_p()
+    it = ctypes.c_uint32()
+    o = K.default_opts()
+    for bad in (K.Tree(one, one, 32, 64),                    # inner sizes differ
+                K.Tree(one, one, 64, 200),                    # padded sides differ
+                K.Tree(one, one, 64, 64, n_k4_levels=1),      # hybrid top
+                K.Tree(one, one, 64, 64, leaf_k=4, cache_last_internal=1)):
+        assert lib.k2t_bool_product(a.handle, bad.handle, ctypes.byref(o), ctypes.byref(out), None) == -1
+        assert not out.value
+    assert lib.k2t_bool_product(None, a.handle, ctypes.byref(o), ctypes.byref(out), None) == -1
+    rect = K.Tree(one, one, 64, 32)
+    assert lib.k2t_bool_closure(rect.handle, ctypes.byref(o), 8, ctypes.byref(out), ctypes.byref(it), None) == -1
+    assert lib.k2t_bool_closure(a.handle, ctypes.byref(o), 8, ctypes.byref(out), None, None) == -1
+
+
+def test_bench_traffic_follows_device_sources(monkeypatch):
+    """roofline.traffic is reported only while the device sources match the
+    digest the capture was taken on."""
+    import bench
+    table = bench.MEASURED_TRAFFIC
+    monkeypatch.setitem(table, "digest", bench.device_digest())
+    monkeypatch.setitem(table, "wl", {"right B=1": 123})
+    assert bench.measured_traffic("wl", "right B=1") == 123
+    assert bench.measured_traffic("wl", "left B=1") is None
+    monkeypatch.setitem(table, "digest", "0" * 64)
+    assert bench.measured_traffic("wl", "right B=1") is None
