@@ -844,8 +844,14 @@ __device__ __forceinline__ void warp_leaf_rounds(uint32_t jb, uint32_t je, LeafA
 // work per leaf, whatever the fan-out of its node.
 constexpr int kCachedWarps = 8;
 
+// Blocks per SM the kernel is compiled for: 5 for 4-wide batches (48
+// registers, no spills; 5% faster than 4 blocks on the 300M-edge R-MAT at
+// B = 16), 4 otherwise (at 5 the single-vector path spills and runs 13%
+// slower).
+template <int VW> constexpr int cached_min_blocks() { return VW == 4 ? 5 : 4; }
+
 template <int SR, int DIR, int VW>
-__global__ void __launch_bounds__(32 * kCachedWarps)
+__global__ void __launch_bounds__(32 * kCachedWarps, cached_min_blocks<VW>())
 cached_block_kernel(const uint8_t *sig, const uint32_t *dir, uint32_t n, const Coord *coords, const uint8_t *leaf,
                     VecArgs va)
 {
