@@ -198,16 +198,24 @@ MEASURED_TRAFFIC = {"digest": "ff24e30f4f27ec5dd71ed76b24900a0e837fe46675ef76fb1
                     "rmat27-bfs-1200M": {"right B=1": 14562798080, "left B=1": 14867702784, "right B=16": 68708074240, "left B=16": 76514040576}}
 
 
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source without comments and with whitespace runs collapsed
+    (the sources hold no string literal containing a comment marker)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def device_digest() -> str:
+    """SHA-256 of the device sources' code (comments and layout ignored)."""
     import hashlib
     csrc = os.path.join(ROOT, "compressed_graph_spmv_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
-    with open(os.path.join(ROOT, "include", "k2t.h"), "rb") as f:
-        h.update(f.read())
+    paths = [os.path.join(csrc, n) for n in sorted(os.listdir(csrc)) if n.endswith((".cu", ".cuh", ".h", ".cpp"))]
+    for path in paths + [os.path.join(ROOT, "include", "k2t.h")]:
+        with open(path) as f:
+            h.update(os.path.basename(path).encode() + b"\0" + _code_only(f.read()).encode())
     return h.hexdigest()
 
 
@@ -489,8 +497,8 @@ def run_ours(args):
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps}
 
     base_launches = 2 if st.engine != k2t.ENGINE_LEVELSYNC else 1 + int(st.n_steps) * (3 if st.offsets else 1)
-    # plus-times products of a direction with fp64 outputs add the zeroing of
-    # the fp64 sums and the final rounding pass
+    # plus-times products of a direction with heavy outputs add the zeroing of
+    # their sums and the final rounding pass
     launches_per_step = sum(base_launches + (2 if wl.semiring == synth.PLUS_TIMES and
                                              (st.heavy_rows if d == 0 else st.heavy_cols) else 0)
                             for d, _ in products)

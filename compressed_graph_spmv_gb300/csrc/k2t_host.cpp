@@ -439,7 +439,7 @@ void plan_bands(k2t_tree *t, int nt)
 // Plus-times outputs with more than `limit` non-zeros, counted over the input
 // list (a repeated pair counts each time, so a count never falls short), for
 // the n outputs indexed by ids[]: fills the ascending list and the per-32
-// table (mask of fp64 outputs, fp64 outputs before the group).  A count stops
+// table (mask of heavy outputs, heavy outputs before the group).  A count stops
 // growing once it passes the limit, so it cannot wrap.
 void heavy_outputs(const uint32_t *ids, uint64_t nnz, uint64_t n, uint32_t limit, int nt,
                    std::vector<uint32_t> &list, std::vector<uint32_t> &ent)
@@ -470,7 +470,7 @@ void heavy_outputs(const uint32_t *ids, uint64_t nnz, uint64_t n, uint32_t limit
 }
 
 // Leaf flags of one direction: bit i set when leaf i (level order; block
-// origin (side*q.r, side*q.c), side 2 or 4) has an fp64 output among its rows
+// origin (side*q.r, side*q.c), side 2 or 4) has a heavy output among its rows
 // (dir 0) or columns (dir 1).  prefixes[i] is leaf i's path prefix.
 void heavy_leaf_flags(k2t_tree *t, int dir, const uint64_t *prefixes, uint64_t nl, int nt)
 {

@@ -52,10 +52,10 @@ struct ArenaLayout {
     uint64_t scan_off, scan_bytes;      // LEVELSYNC scan space (block sums + prefixes)
     uint64_t err_off, err_bytes;        // device error word
     uint64_t vec_off[2], vec_bytes;     // host-product x and y
-    // fp64 outputs of plus-times products, per direction (0 right, 1 left)
-    uint64_t hflag_off[2], hflag_bytes[2];  // one bit per leaf: touches an fp64 output
-    uint64_t hent_off[2], hent_bytes[2];    // per 32 outputs: (fp64 bits, fp64 outputs before)
-    uint64_t hlist_off[2], hlist_bytes[2];  // the fp64 outputs, ascending
+    // heavy outputs of plus-times products, per direction (0 right, 1 left)
+    uint64_t hflag_off[2], hflag_bytes[2];  // one bit per leaf: touches a heavy output
+    uint64_t hent_off[2], hent_bytes[2];    // per 32 outputs: (heavy bits, heavy outputs before)
+    uint64_t hlist_off[2], hlist_bytes[2];  // the heavy outputs, ascending
     uint64_t acc_off, acc_bytes;            // heavy sums, shared by both directions: fp64 [output][B]
                                             // (heavy_mode 1) or fp32 [output][kHeavySplit][B]
     uint64_t total;
@@ -94,11 +94,11 @@ struct k2t_tree {
     // LEVELSYNC plan
     std::vector<k2t::LsStep> steps;
     uint64_t max_tile_nodes = 0;
-    // Plus-times outputs summed in fp64 (more than opts.heavy_terms non-zeros),
+    // Heavy plus-times outputs (more than opts.heavy_terms non-zeros),
     // per direction (0: rows, outputs of right products; 1: columns):
     std::vector<uint32_t> hlist[2];   // the outputs, ascending
     std::vector<uint32_t> hent[2];    // per group of 32 outputs: bit mask, then the count before it
-    std::vector<uint32_t> hflag[2];   // bit j: leaf j (level order) has an fp64 output
+    std::vector<uint32_t> hflag[2];   // bit j: leaf j (level order) has a heavy output
     k2t::ArenaLayout layout{};
     k2t::DeviceState *dev = nullptr;
 };

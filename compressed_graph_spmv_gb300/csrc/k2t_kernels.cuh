@@ -35,8 +35,8 @@ struct VecArgs {
     uint32_t mask;   // Boolean: bits of the batch
     uint64_t n_out;  // entries (vertices) of y
     uint64_t n_in;   // entries (vertices) of x
-    // Plus-times outputs summed in fp64 (null hflag: none in this product)
-    const uint32_t *hflag;  // bit j: leaf j (level order) has an fp64 output
+    // Heavy plus-times outputs (null hflag: none in this product)
+    const uint32_t *hflag;  // bit j: leaf j (level order) has a heavy output
     const uint32_t *hent;   // per 32 outputs: mask of such outputs, their count before the group
     void *acc;              // their sums: hsplit == 0: fp64 [id][B]; else fp32 partial sums [id][hsplit][B]
     uint32_t hsplit;        // fp32 partial sums per output (a power of two), or 0 for fp64 sums
@@ -140,12 +140,13 @@ __device__ __forceinline__ bool is_noop_word(uint32_t v)
     else return v == 0x7f800000u;
 }
 
-// ---- fp64 outputs (plus-times) -------------------------------------------------
-// An output with more non-zeros than the fp32 bound allows is summed in fp64.
+// ---- heavy outputs (plus-times) ------------------------------------------------
+// An output with more non-zeros than one fp32 sum can take within the bound
+// is "heavy": summed in 32 fp32 partial sums (hsplit) or in fp64.
 // heavy_leaf: leaf li has such an output.  heavy_word: for the outputs out
 // (even) and out + 1 of a leaf, (id << 2) | mask, where mask bit q is set when
-// out + q is summed in fp64 and id is out's index in the fp64 list (out + 1
-// has id + (mask & 1)); 0 when neither is.
+// out + q is heavy and id is out's index in the heavy list (out + 1 has
+// id + (mask & 1)); 0 when neither is.
 __device__ __forceinline__ uint32_t heavy_leaf(const VecArgs &va, uint32_t li)
 {
     return (__ldg(va.hflag + (li >> 5)) >> (li & 31u)) & 1u;
@@ -221,7 +222,7 @@ template <> struct VecLoad<4> {
 //   left:  output c gets bits 0 (input r) and 2 (input r+1); output c+1 bits 1, 3
 // win != null: updates go to the shared-memory window win[(out - lo) * width + k]
 // instead of y (width = B words, 1 for Boolean).  Bit u of fl (plus-times):
-// leaf u has fp64 outputs; those go to their fp64 sums instead.
+// leaf u has heavy outputs; those go to their heavy sums instead.
 template <int SR, int DIR, int VW, int U>
 __device__ __forceinline__ void leaf_group(const uint32_t (&lam)[U], const uint32_t (&r)[U], const uint32_t (&c)[U],
                                            uint32_t fl, const VecArgs &a, uint32_t *win, uint32_t lo)
@@ -544,7 +545,7 @@ flat_leaf_kernel(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix
 // Leaves of U leaf blocks (origins r[u], c[u], cells lam[u]) with x entries
 // already loaded (xo[u][0]: input r or c, xo[u][1]: the next one); one
 // vector slice (B = 1 fp32, or a Boolean word).  Bit u of fl (plus-times):
-// leaf u has fp64 outputs; those go to their fp64 sums, window or not.
+// leaf u has heavy outputs; outside a window those go to their heavy sums.
 template <int SR, int DIR, int U, class InOf>
 __device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint32_t (&out)[U], InOf &&in_of,
                                             const uint32_t (&xo)[U][2], uint32_t fl, const VecArgs &va,
@@ -669,7 +670,7 @@ __device__ __forceinline__ void warp_window_flush(const uint32_t *win, uint32_t 
 
 // One VW-wide vector slice k of one leaf (origin r, c; cells lam): gathers the
 // slice of the inputs it needs, combines per output, updates y or the window;
-// outputs marked in hv (heavy_word) go to their fp64 sums.
+// outputs marked in hv (heavy_word) go to their heavy sums.
 template <int SR, int DIR, int VW>
 __device__ __forceinline__ void leaf_slice(uint32_t lam, uint32_t r, uint32_t c, uint32_t k, uint32_t hv,
                                            const VecArgs &va, uint32_t *win, uint32_t lo)
@@ -709,7 +710,7 @@ __device__ __forceinline__ void leaf_slice(uint32_t lam, uint32_t r, uint32_t c,
         }
     };
     if (SR == K2T_PLUS_TIMES && hv) {
-        // a leaf with an fp64 output: separate branch, so the fp32 path below
+        // a leaf with a heavy output: separate branch, so the fp32 path below
         // keeps its registers
         if (a0 || a1) {
             if (hv & 1u) {
@@ -939,7 +940,7 @@ __device__ __forceinline__ uint32_t used4(uint32_t lam)
            ((uint32_t)((lam & 0xf00u) != 0) << 2) | ((uint32_t)((lam & 0xf000u) != 0) << 3);
 }
 
-// fp64 outputs among out .. out + 3 (out a multiple of 4): (id << 4) | mask,
+// Heavy outputs among out .. out + 3 (out a multiple of 4): (id << 4) | mask,
 // mask bit q set when out + q is summed in fp64, id the fp64 index of the
 // first of them; output out + q has id + popc(mask & ((1 << q) - 1)).
 __device__ __forceinline__ uint32_t heavy_word4(const VecArgs &va, uint32_t out)
@@ -1657,7 +1658,7 @@ struct DeviceState {
     uint32_t *scan_prefix = nullptr;
     uint32_t *err = nullptr;
     void *vec[2] = {nullptr, nullptr};
-    const uint32_t *hflag[2] = {nullptr, nullptr};  // fp64 outputs, per direction (null: none)
+    const uint32_t *hflag[2] = {nullptr, nullptr};  // heavy outputs, per direction (null: none)
     const uint32_t *hent[2] = {nullptr, nullptr};
     const uint32_t *hlist[2] = {nullptr, nullptr};
     void *acc = nullptr;
