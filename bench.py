@@ -194,8 +194,9 @@ def measured_peak():
 # profiles/cached_block_kernel_rmat27.md).  The numbers hold only for the device
 # sources they were taken on: DEVICE_DIGEST is the SHA-256 of those sources, and
 # any later change to them makes roofline.traffic null until a new capture.
-MEASURED_TRAFFIC = {"digest": "ff24e30f4f27ec5dd71ed76b24900a0e837fe46675ef76fb10c7f9f5c6318654",
-                    "rmat27-bfs-1200M": {"right B=1": 14562798080, "left B=1": 14867702784, "right B=16": 68708074240, "left B=16": 76514040576}}
+MEASURED_TRAFFIC = {"digest": "19bdf20d8d979c6d6f40b2fea0ef50e6e9fb283aaa645251bc878f5259b88b6a",
+                    "rmat27-bfs-1200M": {"right B=1": 14560415488, "left B=1": 14863264256,
+                                         "right B=16": 70346987264, "left B=16": 78223233024}}
 
 
 def _code_only(text: str) -> str:
