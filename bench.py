@@ -337,22 +337,33 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
-    t_gen = time.perf_counter()
-    wl, wopts, products = make_workload(args.workload)
-    if args.products:
-        products = [tuple(int(v) for v in p.split(":")) for p in args.products.split(",")]
-    t_gen = time.perf_counter() - t_gen
-    max_b = max(B for _, B in products)
-    opts = dict(wopts, host_vectors=1, max_batch=max_b)
-    if args.engine is not None:
-        opts["engine"] = args.engine
-        opts["cache_last_internal"] = int(args.engine in (3, 4))
-    for kv in args.opt:
-        k, v = kv.split("=", 1)
-        opts[k] = int(v, 0)
-    t_build = time.perf_counter()
-    tree = K.Tree(wl.rows, wl.cols, wl.n_rows, wl.n_cols, **opts)
-    t_build = time.perf_counter() - t_build
+    # Replicas generate and build in turn (a CPU-side barrier with a long
+    # timeout between turns): a builder's host peak (about 70 GB on the 1.2G
+    # edge graph) is then paid by one rank at a time.
+    turns = None
+    if world > 1:
+        import datetime
+        turns = dist.new_group(backend="gloo", timeout=datetime.timedelta(hours=3))
+    for turn in range(world):
+        if turn == rank:
+            t_gen = time.perf_counter()
+            wl, wopts, products = make_workload(args.workload)
+            if args.products:
+                products = [tuple(int(v) for v in p.split(":")) for p in args.products.split(",")]
+            t_gen = time.perf_counter() - t_gen
+            max_b = max(B for _, B in products)
+            opts = dict(wopts, host_vectors=1, max_batch=max_b)
+            if args.engine is not None:
+                opts["engine"] = args.engine
+                opts["cache_last_internal"] = int(args.engine in (3, 4))
+            for kv in args.opt:
+                k, v = kv.split("=", 1)
+                opts[k] = int(v, 0)
+            t_build = time.perf_counter()
+            tree = K.Tree(wl.rows, wl.cols, wl.n_rows, wl.n_cols, **opts)
+            t_build = time.perf_counter() - t_build
+        if turns is not None:
+            dist.barrier(group=turns)
     st = tree.stats()
     ws = tree.workspace_bytes()
     torch.cuda.synchronize()
