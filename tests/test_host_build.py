@@ -282,3 +282,17 @@ def test_bench_traffic_follows_device_sources(monkeypatch):
     assert bench.measured_traffic("wl", "left B=1") is None
     monkeypatch.setitem(table, "digest", "0" * 64)
     assert bench.measured_traffic("wl", "right B=1") is None
+
+
+def test_clustered_generator_shape():
+    """synth.clustered: every row holds exactly per_row distinct columns, all
+    inside its own block-aligned window (block-diagonal), seeded."""
+    wl = synth.clustered(scale=12, block=16, per_row=8, seed=3)
+    n = 1 << 12
+    assert wl.rows.size == 8 * n and wl.n_rows == n == wl.n_cols
+    assert np.all(wl.cols // 16 == wl.rows // 16)
+    r, c = oracle.dedup_edges(wl.rows, wl.cols)
+    assert r.size == wl.rows.size                                   # distinct per row
+    assert np.array_equal(np.bincount(r, minlength=n), np.full(n, 8))
+    again = synth.clustered(scale=12, block=16, per_row=8, seed=3)
+    assert np.array_equal(again.cols, wl.cols)
