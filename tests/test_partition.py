@@ -4,7 +4,8 @@ A k^2-tree product shards without a collective per product: rank r owns the
 rows [r*n/R, (r+1)*n/R) (right product) or the columns (left product), builds
 the tree of its band and computes its slice of y; an iterative user would
 all-gather the slices into the next x.  Checked here with two gloo ranks on
-CPU: the gathered band products equal the full product.
+CPU: the gathered band products equal the full product, and each rank's
+library-built band tree (host build, no GPU) decodes to its band's edges.
 """
 import os
 import socket
@@ -52,6 +53,21 @@ def _worker(rank, world, port, q):
             full = torch.cat(chunks).numpy()
             ref = oracle.spmv_edges(rows, cols, n, n, direction, oracle.PLUS_TIMES, x, B=2).y
             ok &= bool(np.allclose(full, ref, rtol=1e-12, atol=1e-12))
+            # the library's own host build of the band: it decodes to exactly
+            # the band's distinct edges, and the bands' non-zeros add up
+            from compressed_graph_spmv_gb300 import k2t as K
+            if direction == oracle.RIGHT:
+                band = K.Tree(r - lo, c, hi - lo, n, cache_last_internal=1)
+                want = oracle.dedup_edges(r - lo, c)
+            else:
+                band = K.Tree(r, c - lo, n, hi - lo, cache_last_internal=1)
+                want = oracle.dedup_edges(r, c - lo)
+            dr, dc = band.decode()
+            got = oracle.dedup_edges(dr, dc)
+            ok &= bool(np.array_equal(got[0], want[0]) and np.array_equal(got[1], want[1]))
+            cnt = torch.tensor([int(band.stats().nnz)], dtype=torch.int64)
+            dist.all_reduce(cnt)
+            ok &= int(cnt.item()) == int(oracle.dedup_edges(rows, cols)[0].size)
         q.put((rank, ok))
     finally:
         dist.destroy_process_group()
