@@ -29,6 +29,10 @@
  *     is vector b (B <= 32).  Right products read n_cols entries and write
  *     n_rows; left products the reverse.  x and y must not overlap.
  *   - Host calls are thread-compatible: one thread at a time per tree.
+ *   - Products of one tree must not overlap on the GPU: the tree's arena
+ *     holds per-product scratch (level-synchronous frontier buffers, the
+ *     sums of heavy plus-times outputs).  Queue them on one stream, or order
+ *     the streams.  Different trees are independent.
  */
 #ifndef K2T_H
 #define K2T_H
