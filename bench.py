@@ -311,7 +311,8 @@ def run_reference(args):
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
            "dtype": dtype_name(wl), "data": "synthetic",
-           "config": {"workload": wl.name, "products": [list(p) for p in products]},
+           "config": {"workload": wl.name, "nnz": int(wl.rows.size), "n": int(wl.n_rows),
+                      "products": [list(p) for p in products], "parallelism": "single"},
            "cpu_baseline": {"value": value, "unit": "edges/s", "cores": 1, "kind": "oracle",
                             "sample": desc},
            "e2e": {"value": value, "unit": "edges/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
