@@ -608,8 +608,8 @@ constexpr int kLeafU = K2T_LEAF_U;                  // leaves per lane per round
 constexpr uint32_t kWarpWindow = K2T_WARP_WINDOW;   // words of a warp's output window
 
 // Per-warp segmented scatter.  [mn, mx] bounds the warp's output coordinates
-// in units of `unit` cells (4 for nodes of the last internal level, 2 for
-// leaves).  When the outputs fit the warp's window (kWarpWindow words), the
+// in units of `unit` cells (4 or 8 for nodes of the last internal level with
+// 2x2 or 4x4 leaves, 2 for 2x2 leaves).  When the outputs fit the warp's window (kWarpWindow words), the
 // window is cleared and returned; updates are then reduced there and each
 // touched entry reaches y once (warp_window_flush).  Hub rows of power-law
 // graphs then cost one global atomic per warp instead of one per non-zero.
@@ -737,7 +737,7 @@ __device__ __forceinline__ void leaf_slice(uint32_t lam, uint32_t r, uint32_t c,
 }
 
 // Leaves [jb, je) of a warp.  leaf_at(j, lam, r, c, li) gives leaf j's cells,
-// the origin of its 2x2 block and its index in the leaf level (for the fp64
+// the origin of its 2x2 block and its index in the leaf level (for the heavy
 // output flags).
 //  - One vector slice (B = 1 fp32, or a Boolean word): leaves dealt round-
 //    robin, kLeafU per lane per round; both input entries of a block come in
