@@ -310,14 +310,16 @@ int k2t_stats_get(const k2t_tree *t, k2t_stats *s);
 
 /* Signatures of one level as one byte per node (low 4 bits for k = 2 levels;
  * low 8 bits of the 16-bit signature in out[2i], high 8 bits in out[2i+1]
- * for k = 4 levels).  cap is the capacity of out in bytes; *written is the
+ * for k = 4 levels: the n_k4 top levels, and the leaf level of a tree with
+ * leaf_k = 4).  cap is the capacity of out in bytes; *written is the
  * number of bytes the level needs.  ERANGE if cap is too small. */
 int k2t_level_signatures(const k2t_tree *t, uint32_t level, uint8_t *out, uint64_t cap,
                          uint64_t *written);
 
 /* Device pointers of the uploaded image, for instrumentation: the signature
- * bytes of a level (nibble t of the level at byte t/2, low nibble first) and
- * its directory (NULL where absent). */
+ * bytes of a level (nibble t of the level at byte t/2, low nibble first; the
+ * 16-bit signature of node t at bytes 2t, 2t+1 for a leaf level with
+ * leaf_k = 4) and its directory (NULL where absent). */
 int k2t_device_level(const k2t_tree *t, uint32_t level, const void **sig, const void **dir);
 
 /* The cells of the matrix, decoded from the tree on the host, in level order
