@@ -16,6 +16,7 @@
 #include <cstdint>
 #include <cstring>
 #include <functional>
+#include <cstdlib>
 #include <thread>
 #include <vector>
 
@@ -34,8 +35,14 @@ inline uint64_t draw(uint64_t seed, uint64_t stream, uint64_t index)
     return splitmix(splitmix(seed ^ (stream * 0xd1b54a32d192ed03ull)) + index * 0x9e3779b97f4a7c15ull);
 }
 
+// All hardware threads, or K2T_SYNTH_THREADS when set (the output does not
+// depend on it; tests vary it to check that).
 int nthreads()
 {
+    if (const char *e = std::getenv("K2T_SYNTH_THREADS")) {
+        int v = std::atoi(e);
+        if (v > 0) return v;
+    }
     unsigned h = std::thread::hardware_concurrency();
     return h ? (int)h : 4;
 }
