@@ -296,3 +296,19 @@ def test_clustered_generator_shape():
     assert np.array_equal(np.bincount(r, minlength=n), np.full(n, 8))
     again = synth.clustered(scale=12, block=16, per_row=8, seed=3)
     assert np.array_equal(again.cols, wl.cols)
+
+
+@pytest.mark.parametrize("leaf_k", [2, 4])
+def test_largest_side(leaf_k):
+    """n = 2^32 (the largest side): 32 levels (31 with 4x4 leaves), cells at
+    the four corners and near the middle decode back, and match the oracle's
+    tree bit for bit."""
+    top = (1 << 32) - 1
+    rows = np.array([0, top, 0, top, 1 << 31, 12345], np.uint32)
+    cols = np.array([0, 0, top, top, (1 << 31) - 1, 1 << 30], np.uint32)
+    t = _compare(rows, cols, 1 << 32, 1 << 32, leaf_k=leaf_k)
+    s = t.stats()
+    assert s.dim_bits == 32 and s.levels == 32 - (leaf_k == 4) and s.nnz == 6
+    with pytest.raises(K.K2TError) as e:
+        K.Tree(rows, cols, (1 << 32) + 1, 4)
+    assert e.value.status == -2
