@@ -506,7 +506,7 @@ flat_leaf_kernel(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix
     const uint32_t t0 = a + rel0;
     const uint32_t t = t0 + lane;
     const bool valid = rel0 + lane < count;
-    // round 1: all independent loads
+    // first memory round trip: all independent loads
     const uint32_t sg = valid ? nibble_at(sig, t) : 0u;
     Coord p{0u, 0u};
     if (valid) p = src[rel0 + lane];
