@@ -460,6 +460,7 @@ def run_ours(args):
         q1, med, q3 = (float(v) for v in np.percentile(main_ms[:, i], [25, 50, 75]))
         per_kernel.append({"product": "%s B=%d" % ("right" if d == 0 else "left", B), "avg_ms": avg * 1e3,
                            "median_ms": med, "iqr_ms": q3 - q1,
+                           "leaves_per_s": float(st.level_nodes[st.levels - 1]) / avg,
                            "fill_ms": float((prod_ms[:, i] - main_ms[:, i]).mean()),
                            "algorithmic_bytes": byt, "achieved_gbs": byt / avg / 1e9,
                            "edges_per_s": m * B / avg})
@@ -470,6 +471,20 @@ def run_ours(args):
                 "traffic": measured_traffic(wl.name, per_kernel[dom]["product"]), "peak_source": peak_kind,
                 "kernel": per_kernel[dom]["product"],
                 "bytes_per_launch": per_kernel[dom]["algorithmic_bytes"]}
+
+    # The single-vector leaf step's own bound: a leaf costs one scattered gather
+    # (its two inputs) and about one scattered reduction; with the L2-resident
+    # rates of `bench.py --ceilings` on this GPU (profiles/k2t_probe_ceilings.md)
+    # that allows 1 / (1/313.3G + 1/211.2G) leaves per second.
+    b1 = [k for k, (d, B) in zip(per_kernel, products) if B == 1 and wl.semiring != synth.BOOLEAN]
+    scatter_model = None
+    if b1:
+        ceil_lps = 1.0 / (1.0 / 313.3e9 + 1.0 / 211.2e9)
+        best = max(k["leaves_per_s"] for k in b1)
+        scatter_model = {"model": "1 scattered gather + 1 scattered reduction per leaf, L2-resident rates",
+                         "gather_per_s": 313.3e9, "reduction_per_s": 211.2e9,
+                         "ceiling_leaves_per_s": ceil_lps, "achieved_leaves_per_s": best,
+                         "frac": best / ceil_lps, "source": "profiles/k2t_probe_ceilings.md"}
 
     # end to end through the C ABI with host buffers (copies inside the timed region)
     # pinned staging: one input and one output buffer per batch width, filled
@@ -524,7 +539,7 @@ def run_ours(args):
                       "products": [list(p) for p in products],
                       "l2": "flushed between steps" if flush is not None else "inputs larger than L2",
                       "parallelism": "replicas" if world > 1 else "single"},
-           "roofline": roofline, "kernels": per_kernel,
+           "roofline": roofline, "scatter_bound": scatter_model, "kernels": per_kernel,
            "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clk,
            "parity": parity,
            "footprint": {"predicted_bytes": ws, "measured_bytes": int(footprint),
