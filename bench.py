@@ -323,6 +323,19 @@ def dtype_name(wl):
     return "u32" if wl.semiring == synth.BOOLEAN else "f32"
 
 
+def one_at_a_time(rank: int, world: int, group, fn):
+    """Run fn on every rank, one rank after the other (rank 0 first), with a
+    barrier of `group` between turns; returns this rank's result."""
+    import torch.distributed as dist
+    out = None
+    for turn in range(world):
+        if turn == rank:
+            out = fn()
+        if group is not None:
+            dist.barrier(group=group)
+    return out
+
+
 # --- the GPU arm ------------------------------------------------------------------
 def run_ours(args):
     import torch
@@ -345,26 +358,27 @@ def run_ours(args):
     if world > 1:
         import datetime
         turns = dist.new_group(backend="gloo", timeout=datetime.timedelta(hours=3))
-    for turn in range(world):
-        if turn == rank:
-            t_gen = time.perf_counter()
-            wl, wopts, products = make_workload(args.workload)
-            if args.products:
-                products = [tuple(int(v) for v in p.split(":")) for p in args.products.split(",")]
-            t_gen = time.perf_counter() - t_gen
-            max_b = max(B for _, B in products)
-            opts = dict(wopts, host_vectors=1, max_batch=max_b)
-            if args.engine is not None:
-                opts["engine"] = args.engine
-                opts["cache_last_internal"] = int(args.engine in (3, 4))
-            for kv in args.opt:
-                k, v = kv.split("=", 1)
-                opts[k] = int(v, 0)
-            t_build = time.perf_counter()
-            tree = K.Tree(wl.rows, wl.cols, wl.n_rows, wl.n_cols, **opts)
-            t_build = time.perf_counter() - t_build
-        if turns is not None:
-            dist.barrier(group=turns)
+
+    def prepare():
+        t_gen = time.perf_counter()
+        wl, wopts, products = make_workload(args.workload)
+        if args.products:
+            products = [tuple(int(v) for v in p.split(":")) for p in args.products.split(",")]
+        t_gen = time.perf_counter() - t_gen
+        max_b = max(B for _, B in products)
+        opts = dict(wopts, host_vectors=1, max_batch=max_b)
+        if args.engine is not None:
+            opts["engine"] = args.engine
+            opts["cache_last_internal"] = int(args.engine in (3, 4))
+        for kv in args.opt:
+            k, v = kv.split("=", 1)
+            opts[k] = int(v, 0)
+        t_build = time.perf_counter()
+        tree = K.Tree(wl.rows, wl.cols, wl.n_rows, wl.n_cols, **opts)
+        t_build = time.perf_counter() - t_build
+        return wl, products, opts, tree, t_gen, t_build
+
+    wl, products, opts, tree, t_gen, t_build = one_at_a_time(rank, world, turns, prepare)
     st = tree.stats()
     ws = tree.workspace_bytes()
     torch.cuda.synchronize()

@@ -86,3 +86,39 @@ def test_band_partition_two_ranks():
     results = dict(q.get(timeout=5) for _ in procs)
     assert all(p.exitcode == 0 for p in procs)
     assert results == {0: True, 1: True}
+
+
+def _turns_worker(rank, world, port, q):
+    import sys
+    import time
+    import torch.distributed as dist
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        def work():
+            t0 = time.time()
+            time.sleep(0.3)
+            return (t0, time.time())
+        q.put((rank, bench.one_at_a_time(rank, world, dist.group.WORLD, work)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_replicas_prepare_one_at_a_time():
+    """bench.py's replicas generate and build in turn: rank r's turn starts
+    only after rank r-1's has ended (two gloo ranks on CPU)."""
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_turns_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+    spans = dict(q.get(timeout=5) for _ in procs)
+    assert all(p.exitcode == 0 for p in procs)
+    assert spans[0][1] <= spans[1][0]
