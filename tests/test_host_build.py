@@ -312,3 +312,13 @@ def test_largest_side(leaf_k):
     with pytest.raises(K.K2TError) as e:
         K.Tree(rows, cols, (1 << 32) + 1, 4)
     assert e.value.status == -2
+
+
+def test_device_digest_ignores_comments_only():
+    """The digest keying roofline.traffic changes with code, not with comments
+    or layout."""
+    import bench
+    a = bench._code_only("int f(int x) { // add one\n  return x + 1; /* done */ }\n")
+    b = bench._code_only("int f(int x)\n{\n    return x + 1;\n}")
+    c = bench._code_only("int f(int x) { return x + 2; }")
+    assert a == b != c
