@@ -190,13 +190,15 @@ def measured_peak():
 
 # --- measured DRAM traffic ---------------------------------------------------------
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the product kernel,
-# from one ncu capture of the workload (the command is in
-# profiles/cached_block_kernel_rmat27.md).  The numbers hold only for the device
-# sources they were taken on: DEVICE_DIGEST is the SHA-256 of those sources, and
-# any later change to them makes roofline.traffic null until a new capture.
-MEASURED_TRAFFIC = {"digest": "19bdf20d8d979c6d6f40b2fea0ef50e6e9fb283aaa645251bc878f5259b88b6a",
-                    "rmat27-bfs-1200M": {"right B=1": 14560415488, "left B=1": 14863264256,
-                                         "right B=16": 70346987264, "left B=16": 78223233024}}
+# from one ncu capture of a smaller workload of the same recipe (R-MAT, ids
+# permuted then BFS-ordered, the cached engine; the capture command is in the
+# profile summary of the cached kernel).  A workload of the same recipe takes
+# the captured bytes scaled by its non-zeros (traffic grows in proportion to
+# the edges: the tree, the cached level and the scattered x / y accesses all
+# do).  The numbers hold only for the device sources they were taken on:
+# "digest" is the SHA-256 of those sources, and any later change to them
+# makes roofline.traffic null until a new capture.
+MEASURED_TRAFFIC = {"digest": None, "workload": None, "nnz": None, "bytes": {}}
 
 
 def _code_only(text: str) -> str:
@@ -220,11 +222,19 @@ def device_digest() -> str:
     return h.hexdigest()
 
 
-def measured_traffic(workload: str, product: str):
-    table = MEASURED_TRAFFIC.get(workload, {})
-    if product not in table or MEASURED_TRAFFIC["digest"] != device_digest():
-        return None
-    return table[product]
+def measured_traffic(wl_name: str, nnz: int, product: str):
+    """(bytes per launch, source) for a product of an R-MAT workload, scaled
+    from the recorded capture by non-zeros; (None, why) when there is no
+    capture of the current device code."""
+    t = MEASURED_TRAFFIC
+    if not t["digest"] or product not in t["bytes"]:
+        return None, "no capture recorded"
+    if not wl_name.startswith("rmat") or "bfs" not in wl_name:
+        return None, "no capture of this recipe"
+    if t["digest"] != device_digest():
+        return None, "device code changed since the capture"
+    scale = nnz / t["nnz"]
+    return int(t["bytes"][product] * scale), "ncu on %s, scaled by non-zeros x%.3f" % (t["workload"], scale)
 
 
 # --- byte accounting ------------------------------------------------------------
@@ -263,48 +273,79 @@ def parity_sample(wl, got: dict, n_sample: int = 2048, seed: int = 99):
 
 
 # --- CPU oracle on a bounded sample ------------------------------------------------
-def oracle_sample(wl, target_edges: int):
-    """Edges of the leading rows holding about target_edges non-zeros."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def oracle_sample(wl, target_edges: int, band_bits: int = 10, seed: int = 17):
+    """Edges of uniformly random aligned row bands of 2^band_bits rows, drawn
+    until about target_edges are kept.  Inside a band every non-zero of its
+    rows is kept, so the subtrees below the band's level have the full
+    matrix's shape there; the bands spread over the whole id range, so the
+    sample mixes hub rows and sparse rows as the matrix does."""
     m = wl.rows.size
     if m <= target_edges:
-        return wl.rows, wl.cols, wl.n_rows, "all %d edges" % m
-    order = np.bincount(wl.rows, minlength=wl.n_rows).cumsum()
-    R = int(np.searchsorted(order, target_edges)) + 1
-    sel = wl.rows < R
-    return wl.rows[sel], wl.cols[sel], R, "rows [0, %d): %d of %d edges" % (R, int(sel.sum()), m)
+        return wl.rows, wl.cols, "all %d edges" % m
+    nb = max(1, (wl.n_rows + (1 << band_bits) - 1) >> band_bits)
+    per_band = np.bincount(wl.rows >> band_bits, minlength=nb)
+    order = np.random.default_rng(seed).permutation(nb)
+    take = int(np.searchsorted(np.cumsum(per_band[order]), target_edges)) + 1
+    keep = np.zeros(nb, bool)
+    keep[order[:take]] = True
+    sel = keep[wl.rows >> band_bits]
+    return wl.rows[sel], wl.cols[sel], ("%d random row bands of %d rows (of %d): %d of %d edges"
+                                        % (take, 1 << band_bits, nb, int(sel.sum()), m))
 
 
-def time_oracle(wl, products, target_edges: int, steps: int = 1, warmup: int = 0):
-    """Rank-based recursive descent of the oracle (single thread), right and
-    left over the sample; returns (edges/s, description, per-step seconds)."""
+def time_oracle(wl, products, target_edges: int, steps: int = 1, warmup: int = 0, threads: int = 1):
+    """The oracle's rank-based recursive descent over the sample, right and
+    left, single-threaded (threads 1) or shared among host threads by row /
+    column bands (threads 0: one per core); returns (edges/s, description,
+    per-step seconds, units per step, threads used)."""
     import oracle
-    r, c, R, desc = oracle_sample(wl, target_edges)
-    t = oracle.OracleTree(r, c, R, wl.n_cols, n_k4=0)
+    r, c, desc = oracle_sample(wl, target_edges)
+    t = oracle.OracleTree(r, c, wl.n_rows, wl.n_cols, n_k4=0)
     m = int(oracle.dedup_edges(r, c)[0].size)
     times = []
     for it in range(warmup + steps):
         t0 = time.perf_counter()
         units = 0
         for (d, B) in products:
-            x = vector(wl, d, B)
-            if d == 1:
-                x = x[:R]
-            t.spmv(d, wl.semiring, x, B=B, w=wl.w)
+            t.spmv(d, wl.semiring, vector(wl, d, B), B=B, w=wl.w, threads=threads)
             units += m * B
         dt = time.perf_counter() - t0
         if it >= warmup:
             times.append(dt)
-    return units / statistics.median(times), desc, times, units
+    return units / statistics.median(times), desc, times, units, t.threads_used
 
 
 def run_reference(args):
+    """The reference arm: the oracle's descent on all host cores (row / column
+    bands), on a bounded sample of the workload, as edges/s."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     wl, _, products = make_workload(args.workload)
     if args.products:
         products = [tuple(int(v) for v in p.split(":")) for p in args.products.split(",")]
-    eps, desc, times, units = time_oracle(wl, products, args.oracle_edges, steps=args.steps, warmup=args.warmup)
+    eps, desc, times, units, used = time_oracle(wl, products, args.oracle_edges, steps=args.steps,
+                                                warmup=args.warmup, threads=0)
     total = sum(times)
     value = units * len(times) / total
     out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "edges/s", "n_gpus": args.gpus,
@@ -312,9 +353,9 @@ def run_reference(args):
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
            "dtype": dtype_name(wl), "data": "synthetic",
            "config": {"workload": wl.name, "nnz": int(wl.rows.size), "n": int(wl.n_rows),
-                      "products": [list(p) for p in products], "parallelism": "single"},
-           "cpu_baseline": {"value": value, "unit": "edges/s", "cores": 1, "kind": "oracle",
-                            "sample": desc},
+                      "products": [list(p) for p in products], "parallelism": "host threads"},
+           "cpu_baseline": {"value": value, "unit": "edges/s", "cores": used, "threads": used,
+                            "kind": "oracle", "cpu_model": cpu_model(), "sample": desc},
            "e2e": {"value": value, "unit": "edges/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out))
 
@@ -478,27 +519,51 @@ def run_ours(args):
                            "fill_ms": float((prod_ms[:, i] - main_ms[:, i]).mean()),
                            "algorithmic_bytes": byt, "achieved_gbs": byt / avg / 1e9,
                            "edges_per_s": m * B / avg})
+    # warm and cold times of each product (fill + kernel): warm right after
+    # the same product, cold right after writing a buffer of twice L2
+    flush2 = flush if flush is not None else torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device="cuda")
+    for i, p in enumerate(products):
+        warm, cold = [], []
+        for _ in range(3):
+            for kind in ("cold", "warm"):
+                if kind == "cold":
+                    flush2.add_(1.0)
+                e0, e1 = rev.create(), rev.create()
+                rev.record(e0, sh)
+                product(p)
+                rev.record(e1, sh)
+                torch.cuda.synchronize()
+                (cold if kind == "cold" else warm).append(rev.ms(e0, e1))
+                rev.destroy(e0)
+                rev.destroy(e1)
+        per_kernel[i]["warm_ms"] = float(np.median(warm))
+        per_kernel[i]["cold_ms"] = float(np.median(cold))
+    if flush is None:
+        del flush2
     dom = max(range(nprod), key=lambda i: per_kernel[i]["avg_ms"])
     peak, peak_kind = measured_peak()
     ach = per_kernel[dom]["achieved_gbs"]
+    traffic, traffic_src = measured_traffic(wl.name, m, per_kernel[dom]["product"])
     roofline = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
-                "traffic": measured_traffic(wl.name, per_kernel[dom]["product"]), "peak_source": peak_kind,
+                "traffic": traffic, "traffic_source": traffic_src, "peak_source": peak_kind,
                 "kernel": per_kernel[dom]["product"],
                 "bytes_per_launch": per_kernel[dom]["algorithmic_bytes"]}
 
     # The single-vector leaf step's own bound: a leaf costs one scattered gather
-    # (its two inputs) and about one scattered reduction; with the L2-resident
-    # rates of `bench.py --ceilings` on this GPU (profiles/k2t_probe_ceilings.md)
-    # that allows 1 / (1/313.3G + 1/211.2G) leaves per second.
+    # (its two inputs) and about one scattered reduction.  Their rates on this
+    # GPU, measured now with L2-resident arrays (the probe library), allow
+    # 1 / (1/gather + 1/reduction) leaves per second.
     b1 = [k for k, (d, B) in zip(per_kernel, products) if B == 1 and wl.semiring != synth.BOOLEAN]
     scatter_model = None
-    if b1:
-        ceil_lps = 1.0 / (1.0 / 313.3e9 + 1.0 / 211.2e9)
+    if b1 and not args.no_ceilings:
+        ceil = measure_ceilings(rev, stream, [("l2_resident_16MB", 1 << 22)])["l2_resident_16MB"]
+        g, r = ceil["gather8_Gops"] * 1e9, ceil["red_scattered_Gops"] * 1e9
+        ceil_lps = 1.0 / (1.0 / g + 1.0 / r)
         best = max(k["leaves_per_s"] for k in b1)
         scatter_model = {"model": "1 scattered gather + 1 scattered reduction per leaf, L2-resident rates",
-                         "gather_per_s": 313.3e9, "reduction_per_s": 211.2e9,
+                         "gather_per_s": g, "reduction_per_s": r, "measured": "this run",
                          "ceiling_leaves_per_s": ceil_lps, "achieved_leaves_per_s": best,
-                         "frac": best / ceil_lps, "source": "profiles/k2t_probe_ceilings.md"}
+                         "frac": best / ceil_lps}
 
     # end to end through the C ABI with host buffers (copies inside the timed region)
     # pinned staging: one input and one output buffer per batch width, filled
@@ -557,46 +622,67 @@ def run_ours(args):
            "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clk,
            "parity": parity,
            "footprint": {"predicted_bytes": ws, "measured_bytes": int(footprint),
+                         "host_vector_staging_bytes": int(st.vector_bytes),
+                         "product_bytes": int(ws - st.vector_bytes),
                          "tree_bits_per_edge": st.tree_bits / max(1, m),
-                         "fp64_outputs": {"rows": int(st.heavy_rows), "cols": int(st.heavy_cols),
-                                          "table_bytes": int(st.heavy_kib) * 1024}},
+                         "heavy_outputs": {"rows": int(st.heavy_rows), "cols": int(st.heavy_cols),
+                                           "fp32_partial_sums": [int(v) for v in st.heavy_partials],
+                                           "fp64_outputs": [int(v) for v in st.heavy_fp64],
+                                           "most_terms_per_fp32_sum": [int(v) for v in st.heavy_max_terms],
+                                           "table_and_sum_bytes": int(st.heavy_kib) * 1024}},
            "wall_ms_per_step": 1e3 * wall / args.steps,
            "host_seconds": {"generate": t_gen, "build": t_build},
            "host_peak_rss_gb": resource.getrusage(resource.RUSAGE_SELF).ru_maxrss / 1e6}
     if rank == 0 and not args.no_cpu_baseline:
-        eps, desc, _, _ = time_oracle(wl, products, args.oracle_edges)
-        out["cpu_baseline"] = {"value": eps, "unit": "edges/s", "cores": 1, "kind": "oracle", "sample": desc}
+        eps1, desc, _, _, _ = time_oracle(wl, products, args.oracle_edges)
+        epsn, _, _, _, used = time_oracle(wl, products, args.oracle_edges, threads=0)
+        out["cpu_baseline"] = {"value": epsn, "unit": "edges/s", "cores": used, "threads": used, "kind": "oracle",
+                               "cpu_model": cpu_model(), "sample": desc,
+                               "single_thread": {"value": eps1, "unit": "edges/s", "cores": 1}}
     if rank == 0:
         print(json.dumps(out))
     if dist:
         dist.destroy_process_group()
 
 
-def run_ceilings(args):
-    """Rates of the leaf step's memory patterns on this GPU (section 5.6 analogue)."""
+def measure_ceilings(rev, stream, sizes):
+    """Rates of the leaf step's memory patterns on this GPU (section 5.6
+    analogue), from the probe library: per array size, copy GB/s and
+    scattered gathers / reductions in G operations per second."""
     import torch
     from compressed_graph_spmv_gb300 import k2t as K
-    out = {"kind": "ceilings"}
-    rev = RawEvents()
-    sh = torch.cuda.current_stream().cuda_stream
-    for label, n in (("l2_resident_16MB", 1 << 22), ("hbm_2GB", 1 << 29)):
+    sh = stream.cuda_stream
+    out = {}
+    for label, n in sizes:
         x = torch.rand(n, device="cuda")
         y = torch.zeros(n, device="cuda")
         res = {}
         for kind, name, m in ((0, "copy_GBps", n), (1, "gather4_Gops", 1 << 28), (2, "gather8_Gops", 1 << 28),
-                              (3, "red_consecutive_Gops", 1 << 28), (4, "red_scattered_Gops", 1 << 28)):
+                              (3, "red_consecutive_Gops", 1 << 28), (4, "red_scattered_Gops", 1 << 28),
+                              (5, "smem_red_fp32_Gops", 1 << 30), (6, "smem_red_fp64_Gops", 1 << 30)):
             for _ in range(2):
-                K.probe(kind, x, y, n, m)
+                K.probe(kind, x, y, n, m, stream=stream)
             e0, e1 = rev.create(), rev.create()
             rev.record(e0, sh)
             for _ in range(5):
-                K.probe(kind, x, y, n, m)
+                K.probe(kind, x, y, n, m, stream=stream)
             rev.record(e1, sh)
             torch.cuda.synchronize()
             ms = rev.ms(e0, e1) / 5
+            rev.destroy(e0)
+            rev.destroy(e1)
             res[name] = (8.0 * n / (ms * 1e6)) if kind == 0 else (m / (ms * 1e6))
         out[label] = res
         del x, y
+    return out
+
+
+def run_ceilings(args):
+    """Rates of the leaf step's memory patterns on this GPU (section 5.6 analogue)."""
+    import torch
+    out = {"kind": "ceilings"}
+    out.update(measure_ceilings(RawEvents(), torch.cuda.current_stream(),
+                                [("l2_resident_16MB", 1 << 22), ("hbm_2GB", 1 << 29)]))
     print(json.dumps(out))
 
 
@@ -678,9 +764,10 @@ def main():
                     help="library option override, e.g. --opt tile_m=65536 (repeatable)")
     ap.add_argument("--products", default=None,
                     help="override the products of a step, e.g. 0:1,1:1 (direction:batch)")
-    ap.add_argument("--oracle-edges", type=int, default=1_500_000)
+    ap.add_argument("--oracle-edges", type=int, default=4_000_000)
     ap.add_argument("--no-parity", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-ceilings", action="store_true", help="skip the in-run scattered-access probe")
     ap.add_argument("--ceilings", action="store_true", help="measure the leaf step's memory ceilings and exit")
     ap.add_argument("--msbfs", action="store_true", help="time a multi-source search on the workload and exit")
     ap.add_argument("--bfs-sources", type=int, default=16)

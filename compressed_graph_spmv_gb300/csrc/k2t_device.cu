@@ -47,27 +47,42 @@ __global__ void __launch_bounds__(256) fill_kernel(uint32_t *y, uint64_t words, 
     for (uint64_t k = tail + i; k < words; k += stride) y[k] = pattern;
 }
 
-// Heavy outputs of a plus-times product: output list[i] of vector k receives
-// its sum, rounded to fp32 once: the fp64 sum acc[i * B + k] (hsplit 0), or
-// the hsplit fp32 partial sums acc[(i * hsplit + p) * B + k] added in fp64.
-// The product sends every term of such an output to acc, so y holds the
-// fill's zero there; adding it keeps the result right even if it did not.
-__global__ void __launch_bounds__(256) heavy_finish_kernel(const void *acc, uint32_t hsplit, const uint32_t *list,
-                                                           uint32_t h, uint32_t B, float *y)
+// Heavy outputs of a plus-times product, one warp per output: output list[i]
+// of vector k receives its sum, rounded to fp32 once: its fp64 slot
+// acc64[slot * B + k], or its 2^bits fp32 partial sums acc[(first + p) * B + k]
+// added in fp64 (rec[i] = (first partial or slot, bits)).  The product sends
+// every term of such an output there, so y holds the fill's zero; adding it
+// keeps the result right even if it did not.
+__global__ void __launch_bounds__(256) heavy_finish_kernel(const float *acc, const double *acc64, const uint2 *rec,
+                                                           const uint32_t *list, uint32_t h, uint32_t B, float *y)
 {
-    const uint64_t n = (uint64_t)h * B;
-    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
-    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
-        const uint64_t o = i / B, k = i % B;
-        float *p = y + (uint64_t)__ldg(list + o) * B + k;
-        double s = (double)*p;
-        if (hsplit) {
-            const float *a = static_cast<const float *>(acc) + o * hsplit * B + k;
-            for (uint32_t q = 0; q < hsplit; ++q) s += (double)a[(uint64_t)q * B];
-        } else {
-            s += static_cast<const double *>(acc)[i];
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x >> 5);
+    for (uint64_t id = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); id < h; id += warps) {
+        const uint2 r = __ldg(rec + id);
+        float *yo = y + (uint64_t)__ldg(list + id) * B;
+        if (r.y == kHeavyFp64) {
+            const double *a = acc64 + (uint64_t)r.x * B;
+            for (uint32_t k = lane; k < B; k += 32u) yo[k] = __double2float_rn(a[k] + (double)yo[k]);
+            continue;
         }
-        *p = __double2float_rn(s);
+        const uint64_t words = ((uint64_t)1 << r.y) * B;
+        const float *a = acc + (uint64_t)r.x * B;
+        if (32u % B == 0) {
+            // lane l always reads slice l % B: sum, then fold the lanes of one slice
+            double s = 0.0;
+            for (uint64_t e = lane; e < words; e += 32u) s += (double)a[e];
+            for (uint32_t o = 16; o >= B; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (lane < B) yo[lane] = __double2float_rn(s + (double)yo[lane]);
+        } else {
+            for (uint32_t k = 0; k < B; ++k) {
+                double s = 0.0;
+                for (uint64_t e = k + (uint64_t)lane * B; e < words; e += 32ull * B) s += (double)a[e];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+                if (lane == 0) yo[k] = __double2float_rn(s + (double)yo[k]);
+            }
+        }
     }
 }
 
@@ -200,11 +215,36 @@ void device_release(k2t_tree *t)
 
 namespace {
 
+// Map a status word to a status code: bit 0 a wait that ran out, any other
+// bit a failed device-side check.
+int status_code(uint32_t w)
+{
+    if (!w) return K2T_OK;
+    return (w & K2T_STATUS_WAIT_TIMEOUT) ? K2T_ETIMEOUT : K2T_EDEVICE;
+}
+
+// Wait for `st`, then read the tree's status word (with the work queued
+// before it) and map it.
+int read_status(const DeviceState *d, cudaStream_t st)
+{
+    uint32_t w = 0;
+    K2T_CUDA(cudaMemcpyAsync(&w, d->err, sizeof(w), cudaMemcpyDeviceToHost, st));
+    K2T_CUDA(cudaStreamSynchronize(st));
+    return status_code(w);
+}
+
 LaunchFn pick(uint32_t engine, int semiring, int dir, int vw)
 {
     if (semiring == K2T_PLUS_TIMES) return pick_plus_times(engine, dir, vw);
     if (semiring == K2T_BOOLEAN) return pick_boolean(engine, dir, vw);
     return pick_min_plus(engine, dir, vw);
+}
+
+// The CACHED engine runs fp32 batches of at least opts.coop_batch vectors
+// with one directory block per thread block (cached_coop_kernel).
+bool coop_batches(const k2t_tree *t, int semiring, uint32_t B)
+{
+    return semiring != K2T_BOOLEAN && B >= t->opts.coop_batch;
 }
 
 // Queue a whole product (fill + engine) on `st`.
@@ -237,7 +277,9 @@ int enqueue_product(k2t_tree *t, int32_t dir, int32_t semiring, float w, const v
     va.n_out = n_out;
     va.n_in = dir == K2T_RIGHT ? t->n_cols : t->n_rows;
     const bool heavy = heavy_begin(t, d, dir, semiring, va, st);
-    pick(t->leaf_k4 ? kEngineCached4 : t->engine, semiring, dir, vw)(t, d, va, st);
+    uint32_t engine = t->leaf_k4 ? kEngineCached4 : t->engine;
+    if (engine == K2T_ENGINE_CACHED && coop_batches(t, semiring, B)) engine = kEngineCachedCoop;
+    pick(engine, semiring, dir, vw)(t, d, va, st);
     if (heavy) heavy_end(t, d, dir, va, st);
     return K2T_OK;
 }
@@ -313,11 +355,14 @@ int k2t_upload(k2t_tree *t, void *arena, uint64_t arena_bytes, void *stream)
         d->hflag[dd] = at<uint32_t>(d->arena, L.hflag_off[dd]);
         d->hent[dd] = at<uint32_t>(d->arena, L.hent_off[dd]);
         d->hlist[dd] = at<uint32_t>(d->arena, L.hlist_off[dd]);
+        d->hrec[dd] = at<uint2>(d->arena, L.hrec_off[dd]);
+        if ((e = put(L.hrec_off[dd], L.hrec_bytes[dd], t->hrec[dd].data()))) return fail(e);
         if ((e = put(L.hflag_off[dd], L.hflag_bytes[dd], t->hflag[dd].data()))) return fail(e);
         if ((e = put(L.hent_off[dd], L.hent_bytes[dd], t->hent[dd].data()))) return fail(e);
         if ((e = put(L.hlist_off[dd], L.hlist_bytes[dd], t->hlist[dd].data()))) return fail(e);
     }
-    if (L.acc_bytes) d->acc = at<void>(d->arena, L.acc_off);
+    if (L.acc_bytes) d->acc = at<float>(d->arena, L.acc_off);
+    if (L.acc64_bytes) d->acc64 = at<double>(d->arena, L.acc64_off);
     if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return fail(e);
     return K2T_OK;
 }
@@ -338,6 +383,9 @@ int k2t_spmv_marked(k2t_tree *t, int32_t dir, int32_t semiring, float w, const v
     const uint64_t esz = semiring == K2T_BOOLEAN ? 4u : 4u * (uint64_t)B;
     uintptr_t xa = (uintptr_t)x, ya = (uintptr_t)y;
     if (xa < ya + n_out * esz && ya < xa + n_in * esz) return K2T_EINVAL;
+    int cur = -1;
+    K2T_CUDA(cudaGetDevice(&cur));
+    if (cur != t->dev->device) return K2T_ESTATE;   // the tree's arena lives on its own device
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     DeviceState *d = t->dev;
     const bool graph = t->engine == K2T_ENGINE_LEVELSYNC && t->opts.use_graph && !t->empty;
@@ -391,8 +439,7 @@ int k2t_spmv_host(k2t_tree *t, int32_t dir, int32_t semiring, float w, const voi
     int rc = k2t_spmv(t, dir, semiring, w, d->vec[0], d->vec[1], B, stream);
     if (rc) return rc;
     K2T_CUDA(cudaMemcpyAsync(y_host, d->vec[1], n_out * esz, cudaMemcpyDeviceToHost, st));
-    K2T_CUDA(cudaStreamSynchronize(st));
-    return K2T_OK;
+    return read_status(d, st);
 }
 
 uint64_t k2t_msbfs_work_bytes(const k2t_tree *t)
@@ -435,11 +482,24 @@ int k2t_msbfs(k2t_tree *t, int32_t dir, const uint32_t *sources, uint32_t B, int
         K2T_CUDA(cudaMemsetAsync(count, 0, sizeof(unsigned long long), st));
         msbfs_mark_kernel<<<grid, 256, 0, st>>>(y, visited, frontier, dist, n, B, mask, (int32_t)level, count);
         K2T_CUDA(cudaMemcpyAsync(&found, count, sizeof(found), cudaMemcpyDeviceToHost, st));
-        K2T_CUDA(cudaStreamSynchronize(st));
+        if ((rc = read_status(t->dev, st))) return rc;
         lv = level;
         if (!found) break;
     }
     *levels = lv;
+    return K2T_OK;
+}
+
+int k2t_status(k2t_tree *t, uint32_t *word, int32_t clear, void *stream)
+{
+    if (!t || !word) return K2T_EINVAL;
+    if (!t->dev) return K2T_ESTATE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t w = 0;
+    K2T_CUDA(cudaMemcpyAsync(&w, t->dev->err, sizeof(w), cudaMemcpyDeviceToHost, st));
+    if (clear) K2T_CUDA(cudaMemsetAsync(t->dev->err, 0, sizeof(w), st));
+    K2T_CUDA(cudaStreamSynchronize(st));
+    *word = w;
     return K2T_OK;
 }
 

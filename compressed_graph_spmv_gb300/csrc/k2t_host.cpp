@@ -20,6 +20,7 @@
 #include <cstring>
 #include <functional>
 #include <new>
+#include <stdexcept>
 #include <thread>
 #include <vector>
 
@@ -436,25 +437,41 @@ void plan_bands(k2t_tree *t, int nt)
         }
 }
 
-// Plus-times outputs with more than `limit` non-zeros, counted over the input
-// list (a repeated pair counts each time, so a count never falls short), for
-// the n outputs indexed by ids[]: fills the ascending list and the per-32
-// table (mask of heavy outputs, heavy outputs before the group).  A count stops
-// growing once it passes the limit, so it cannot wrap.
-void heavy_outputs(const uint32_t *ids, uint64_t nnz, uint64_t n, uint32_t limit, int nt,
-                   std::vector<uint32_t> &list, std::vector<uint32_t> &ent)
+// Heavy plus-times outputs of one direction: those with more than `limit`
+// non-zeros (counted over the input list: a repeated pair counts each time,
+// so a count never falls short).  Fills the ascending list, the per-32 table
+// (mask of heavy outputs, heavy outputs before the group) and one record per
+// heavy output saying where its terms are summed:
+//   - mode 1: in fp64 (slot = its index in the list);
+//   - mode 0: in 2^bits fp32 partial sums, a term going to partial
+//     heavy_partial(first input of its leaf, bits).  The builder counts the
+//     terms every partial receives and raises bits until none holds more
+//     than `limit`, so every fp32 sum the product forms, in whatever order
+//     its atomics land, has at most `limit` terms.  An output whose inputs
+//     still crowd one partial at kHeavyMaxBits (only possible for adversarial
+//     or heavily repeated input) is summed in fp64.
+// out_ids/in_ids: the output and input index of every input pair; side: 2
+// or 4 (leaf side; a leaf's first input is in & ~(side - 1)).
+void heavy_outputs(const uint32_t *out_ids, const uint32_t *in_ids, uint64_t nnz, uint64_t n, uint32_t limit,
+                   uint32_t side, uint32_t mode, int nt, k2t_tree *t, int dir)
 {
+    std::vector<uint32_t> &list = t->hlist[dir], &ent = t->hent[dir], &rec = t->hrec[dir];
     list.clear();
     ent.clear();
+    rec.clear();
+    t->hparts[dir] = 0;
+    t->hfp64[dir] = 0;
+    t->hmax_part[dir] = 0;
     if (limit == 0xffffffffu || nnz <= limit) return;
+    // saturating counts: a thread adds only below kSat, so nt racing adds stay below 2^32
+    constexpr uint32_t kSat = 0xfffff000u;
+    auto bump = [](uint32_t *p) {
+        if (__atomic_load_n(p, __ATOMIC_RELAXED) < kSat) __atomic_fetch_add(p, 1u, __ATOMIC_RELAXED);
+    };
     std::vector<uint32_t> cnt(n, 0);
-    uint32_t *c = cnt.data();
     parallel_for(nt, [&](int th) {
         uint64_t lo = nnz * th / nt, hi = nnz * (th + 1) / nt;
-        for (uint64_t i = lo; i < hi; ++i) {
-            uint32_t *p = c + ids[i];
-            if (__atomic_load_n(p, __ATOMIC_RELAXED) <= limit) __atomic_fetch_add(p, 1u, __ATOMIC_RELAXED);
-        }
+        for (uint64_t i = lo; i < hi; ++i) bump(cnt.data() + out_ids[i]);
     });
     for (uint64_t i = 0; i < n; ++i)
         if (cnt[i] > limit) list.push_back((uint32_t)i);
@@ -467,6 +484,78 @@ void heavy_outputs(const uint32_t *ids, uint64_t nnz, uint64_t n, uint32_t limit
         ent[2 * g + 1] = run;
         run += (uint32_t)popc64(ent[2 * g]);
     }
+    const size_t h = list.size();
+    rec.assign(2 * h, 0);
+    if (mode == 1) {
+        for (size_t id = 0; id < h; ++id) {
+            rec[2 * id] = (uint32_t)id;
+            rec[2 * id + 1] = kHeavyFp64;
+        }
+        t->hfp64[dir] = h;
+        return;
+    }
+    auto heavy_id = [&](uint32_t o) -> int64_t {
+        const uint32_t m = ent[2 * (o / 32)], sh = o % 32;
+        if (!((m >> sh) & 1u)) return -1;
+        return (int64_t)ent[2 * (o / 32) + 1] + popc64(m & ((1u << sh) - 1u));
+    };
+    // first guess: a mean of at most limit / 1.5 terms per partial
+    std::vector<uint32_t> bits(h);
+    for (size_t id = 0; id < h; ++id) {
+        const double want = 1.5 * (double)cnt[list[id]] / (double)limit;
+        uint32_t b = 1;
+        while (b < kHeavyMaxBits && (double)(1u << b) < want) ++b;
+        bits[id] = b;
+    }
+    std::vector<uint32_t>().swap(cnt);
+    const uint32_t in_mask = ~(side - 1u);
+    std::vector<uint8_t> todo(h, 1);
+    bool any = true;
+    while (any) {
+        // count the terms of every partial of the outputs still to check
+        std::vector<uint64_t> base(h, 0);
+        uint64_t total = 0;
+        for (size_t id = 0; id < h; ++id)
+            if (todo[id]) { base[id] = total; total += 1ull << bits[id]; }
+        std::vector<uint32_t> pc(total, 0);
+        parallel_for(nt, [&](int th) {
+            uint64_t lo = nnz * th / nt, hi = nnz * (th + 1) / nt;
+            for (uint64_t i = lo; i < hi; ++i) {
+                const int64_t id = heavy_id(out_ids[i]);
+                if (id < 0 || !todo[(size_t)id]) continue;
+                bump(pc.data() + base[(size_t)id] + heavy_partial(in_ids[i] & in_mask, bits[(size_t)id]));
+            }
+        });
+        any = false;
+        for (size_t id = 0; id < h; ++id) {
+            if (!todo[id]) continue;
+            uint32_t mx = 0;
+            for (uint64_t q = 0; q < (1ull << bits[id]); ++q) mx = std::max(mx, pc[base[id] + q]);
+            if (mx <= limit) {
+                todo[id] = 0;
+                t->hmax_part[dir] = std::max(t->hmax_part[dir], mx);
+            } else if (bits[id] < kHeavyMaxBits) {
+                ++bits[id];
+                any = true;
+            } else {
+                todo[id] = 0;
+                bits[id] = kHeavyFp64;
+            }
+        }
+    }
+    uint64_t parts = 0, slots = 0;
+    for (size_t id = 0; id < h; ++id) {
+        if (bits[id] == kHeavyFp64) {
+            rec[2 * id] = (uint32_t)slots++;
+        } else {
+            if (parts > 0xffffffffull - (1ull << bits[id])) throw std::length_error("heavy partial sums");
+            rec[2 * id] = (uint32_t)parts;
+            parts += 1ull << bits[id];
+        }
+        rec[2 * id + 1] = bits[id];
+    }
+    t->hparts[dir] = parts;
+    t->hfp64[dir] = slots;
 }
 
 // Leaf flags of one direction: bit i set when leaf i (level order; block
@@ -512,6 +601,7 @@ void compute_layout(k2t_tree *t)
     const bool ls = t->engine == K2T_ENGINE_LEVELSYNC;
     const bool banded = t->engine == K2T_ENGINE_BANDED;
     const bool cached = t->engine == K2T_ENGINE_CACHED || banded;
+    // the status word comes first: it is the arena's first 4 bytes (k2t.h)
     L.err_bytes = 64;
     L.err_off = take(L.err_bytes);
     if (!t->empty) {
@@ -569,7 +659,7 @@ void compute_layout(k2t_tree *t)
         }
     }
     if (!t->empty) {
-        uint64_t hmax = 0;
+        uint64_t parts = 0, slots = 0;
         for (int dd = 0; dd < 2; ++dd) {
             if (t->hlist[dd].empty()) continue;
             L.hflag_bytes[dd] = t->hflag[dd].size() * sizeof(uint32_t);
@@ -578,12 +668,18 @@ void compute_layout(k2t_tree *t)
             L.hent_off[dd] = take(L.hent_bytes[dd]);
             L.hlist_bytes[dd] = t->hlist[dd].size() * sizeof(uint32_t);
             L.hlist_off[dd] = take(L.hlist_bytes[dd]);
-            hmax = std::max<uint64_t>(hmax, t->hlist[dd].size());
+            L.hrec_bytes[dd] = t->hrec[dd].size() * sizeof(uint32_t);
+            L.hrec_off[dd] = take(L.hrec_bytes[dd]);
+            parts = std::max(parts, t->hparts[dd]);
+            slots = std::max(slots, t->hfp64[dd]);
         }
-        if (hmax) {
-            L.acc_bytes = hmax * (uint64_t)t->opts.max_batch *
-                          (t->opts.heavy_mode ? sizeof(double) : kHeavySplit * sizeof(float));
+        if (parts) {
+            L.acc_bytes = parts * (uint64_t)t->opts.max_batch * sizeof(float);
             L.acc_off = take(L.acc_bytes);
+        }
+        if (slots) {
+            L.acc64_bytes = slots * (uint64_t)t->opts.max_batch * sizeof(double);
+            L.acc64_off = take(L.acc64_bytes);
         }
     }
     if (t->opts.host_vectors) {
@@ -618,8 +714,9 @@ void k2t_default_opts(k2t_opts *o)
     o->threads = 0;
     o->band_rows = 4096;
     o->band_cols = 1u << 23;
-    o->heavy_terms = 2048;
+    o->heavy_terms = kDefaultHeavyTerms;
     o->leaf_k = 2;
+    o->coop_batch = 8;
 }
 
 int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
@@ -635,8 +732,9 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
     if (o.band_rows < 16 || o.band_rows > 65536 || (o.band_rows & (o.band_rows - 1))) return K2T_EINVAL;
     if (o.band_cols && (o.band_cols < 16 || (o.band_cols & (o.band_cols - 1)))) return K2T_EINVAL;
     if (!o.band_cols) o.band_cols = 1u << 31;
-    if (!o.heavy_terms) o.heavy_terms = 2048;
+    if (!o.heavy_terms) o.heavy_terms = kDefaultHeavyTerms;
     if (!o.leaf_k) o.leaf_k = 2;
+    if (!o.coop_batch) o.coop_batch = 8;
     if (o.heavy_mode > 1) return K2T_EINVAL;
     if (o.leaf_k != 2 && o.leaf_k != 4) return K2T_EINVAL;
     if (o.chunk_cap < 4 || o.chunk_cap > kMaxChunkCap || o.tile_m < 4) return K2T_EINVAL;
@@ -680,8 +778,8 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
                 if (rows[i] >= n_rows || cols[i] >= n_cols) { bad[(size_t)th] = 1; break; }
         });
         for (int b : bad) if (b) { delete t; return K2T_ERANGE; }
-        heavy_outputs(rows, nnz, n_rows, o.heavy_terms, nt, t->hlist[0], t->hent[0]);
-        heavy_outputs(cols, nnz, n_cols, o.heavy_terms, nt, t->hlist[1], t->hent[1]);
+        heavy_outputs(rows, cols, nnz, n_rows, o.heavy_terms, 2u << leaf_k4, o.heavy_mode, nt, t, 0);
+        heavy_outputs(cols, rows, nnz, n_cols, o.heavy_terms, 2u << leaf_k4, o.heavy_mode, nt, t, 1);
         for (int dd = 0; dd < 2; ++dd)
             if (t->hlist[dd].size() >= (1u << 28)) { delete t; return K2T_ERANGE; }
 
@@ -703,7 +801,12 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
 
         if (m == 0) {
             t->empty = true;
-            for (int dd = 0; dd < 2; ++dd) { t->hlist[dd].clear(); t->hent[dd].clear(); }
+            for (int dd = 0; dd < 2; ++dd) {
+                t->hlist[dd].clear();
+                t->hent[dd].clear();
+                t->hrec[dd].clear();
+                t->hparts[dd] = t->hfp64[dd] = 0;
+            }
             t->nodes[0] = 1;
             t->sig[0].assign(2, 0);
             for (int d = 1; d < l; ++d) t->sig[(size_t)d].assign(1, 0);
@@ -762,6 +865,9 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
     } catch (const std::bad_alloc &) {
         delete t;
         return K2T_ENOMEM;
+    } catch (const std::length_error &) {
+        delete t;
+        return K2T_ERANGE;
     }
     *out = t;
     return K2T_OK;
@@ -862,10 +968,15 @@ int k2t_stats_get(const k2t_tree *t, k2t_stats *s)
     s->uploaded = t->dev != nullptr;
     s->heavy_rows = (uint32_t)t->hlist[0].size();
     s->heavy_cols = (uint32_t)t->hlist[1].size();
-    uint64_t hb = L.acc_bytes;
-    for (int dd = 0; dd < 2; ++dd) hb += L.hflag_bytes[dd] + L.hent_bytes[dd] + L.hlist_bytes[dd];
+    uint64_t hb = L.acc_bytes + L.acc64_bytes;
+    for (int dd = 0; dd < 2; ++dd) hb += L.hflag_bytes[dd] + L.hent_bytes[dd] + L.hlist_bytes[dd] + L.hrec_bytes[dd];
     s->heavy_kib = (uint32_t)((hb + 1023) / 1024);
     s->leaf_k = t->leaf_k4 ? 4u : 2u;
+    for (int dd = 0; dd < 2; ++dd) {
+        s->heavy_partials[dd] = t->hparts[dd];
+        s->heavy_fp64[dd] = (uint32_t)t->hfp64[dd];
+        s->heavy_max_terms[dd] = t->hmax_part[dd];
+    }
     return K2T_OK;
 }
 
@@ -886,6 +997,7 @@ const char *k2t_strerror(int status)
     case K2T_ECUDA: return "CUDA runtime error";
     case K2T_ESTATE: return "call out of order";
     case K2T_EDEVICE: return "device-side check failed";
+    case K2T_ETIMEOUT: return "device-side wait ran out";
     default: return "unknown status";
     }
 }

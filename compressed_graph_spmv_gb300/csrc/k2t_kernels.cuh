@@ -38,8 +38,9 @@ struct VecArgs {
     // Heavy plus-times outputs (null hflag: none in this product)
     const uint32_t *hflag;  // bit j: leaf j (level order) has a heavy output
     const uint32_t *hent;   // per 32 outputs: mask of such outputs, their count before the group
-    void *acc;              // their sums: hsplit == 0: fp64 [id][B]; else fp32 partial sums [id][hsplit][B]
-    uint32_t hsplit;        // fp32 partial sums per output (a power of two), or 0 for fp64 sums
+    const uint2 *hrec;      // per heavy output: (first partial sum or fp64 slot, bits)
+    float *acc;             // fp32 partial sums [partial][B]
+    double *acc64;          // fp64 sums [slot][B]
 };
 
 __device__ __forceinline__ uint32_t nibble_at(const uint8_t *sig, uint32_t t)
@@ -142,7 +143,8 @@ __device__ __forceinline__ bool is_noop_word(uint32_t v)
 
 // ---- heavy outputs (plus-times) ------------------------------------------------
 // An output with more non-zeros than one fp32 sum can take within the bound
-// is "heavy": summed in 32 fp32 partial sums (hsplit) or in fp64.
+// is "heavy": summed in fp32 partial sums of bounded size or in fp64, never
+// in a warp window (a window's sum of an output would mix partial sums).
 // heavy_leaf: leaf li has such an output.  heavy_word: for the outputs out
 // (even) and out + 1 of a leaf, (id << 2) | mask, where mask bit q is set when
 // out + q is heavy and id is out's index in the heavy list (out + 1 has
@@ -164,34 +166,38 @@ __device__ __forceinline__ uint32_t heavy_word(const VecArgs &va, uint32_t out)
 // Index in the heavy list of output out + q of a 2x2 leaf (hv from heavy_word).
 __device__ __forceinline__ uint32_t heavy_id2(uint32_t hv, int q) { return (hv >> 2) + (q ? (hv & 1u) : 0u); }
 
-// The fp32 partial sum of heavy output `id` (slice k) that a leaf with first
-// input `in` adds to: a multiplicative hash of the input index picks one of
-// the hsplit partial sums, so the terms of an output spread over them (about
-// 1/hsplit each, whatever the engine or launch shape) and concurrent updates
-// of a hub row hit hsplit different lines.
-__device__ __forceinline__ float *heavy_part(const VecArgs &va, uint32_t id, uint32_t in, uint32_t k)
+// Where heavy output `id` (slice k) sums the terms of a leaf with first input
+// `in`: the fp32 partial sum heavy_partial(in, bits) of its record, or (null
+// p32) its fp64 slot.
+struct HeavyDst {
+    float *p32;
+    double *p64;
+};
+
+__device__ __forceinline__ HeavyDst heavy_dst(const VecArgs &va, uint32_t id, uint32_t in, uint32_t k)
 {
-    const uint32_t part = ((in * 2654435761u) >> 27) & (va.hsplit - 1u);
-    return static_cast<float *>(va.acc) + ((size_t)id * va.hsplit + part) * va.B + k;
+    const uint2 rec = __ldg(va.hrec + id);
+    if (rec.y == kHeavyFp64) return HeavyDst{nullptr, va.acc64 + (size_t)rec.x * va.B + k};
+    return HeavyDst{va.acc + ((size_t)rec.x + heavy_partial(in, rec.y)) * va.B + k, nullptr};
 }
 
 // Update heavy output `id` (slice k) with a leaf's contribution: v is the
-// fp32 combination of its cells (split partial sums); in fp64 mode the cells
-// w*xa (when ua) and w*xb (when ub) are added in fp64, where the sum of two
-// floats is exact.
+// fp32 combination of its cells (one term of an fp32 partial sum); for an
+// fp64 output the cells w*xa (when ua) and w*xb (when ub) are added in fp64,
+// where the sum of two floats is exact.
 template <int SR, int VW>
 __device__ __forceinline__ void heavy_put(const VecArgs &va, uint32_t id, uint32_t in, uint32_t k,
                                           const float (&v)[VW], const float (&xa)[VW], const float (&xb)[VW], bool ua,
                                           bool ub)
 {
-    if (va.hsplit) {
-        Fp32Sem<SR>::update(heavy_part(va, id, in, k), v);
+    const HeavyDst dst = heavy_dst(va, id, in, k);
+    if (dst.p32) {
+        Fp32Sem<SR>::update(dst.p32, v);
         return;
     }
-    double *a = static_cast<double *>(va.acc) + (size_t)id * va.B + k;
 #pragma unroll
     for (int i = 0; i < VW; ++i)
-        atomicAdd(a + i, (ua ? (double)(va.w * xa[i]) : 0.0) + (ub ? (double)(va.w * xb[i]) : 0.0));
+        atomicAdd(dst.p64 + i, (ua ? (double)(va.w * xa[i]) : 0.0) + (ub ? (double)(va.w * xb[i]) : 0.0));
 }
 
 template <int VW> struct VecLoad;
@@ -338,8 +344,8 @@ constexpr uint32_t kFusedSolo = 256;  // levels this narrow are expanded by one 
 
 // Kernels without template parameters, defined in k2t_device.cu.
 __global__ void fill_kernel(uint32_t *y, uint64_t words, uint32_t pattern);
-__global__ void heavy_finish_kernel(const void *acc, uint32_t hsplit, const uint32_t *list, uint32_t h, uint32_t B,
-                                    float *y);
+__global__ void heavy_finish_kernel(const float *acc, const double *acc64, const uint2 *rec, const uint32_t *list,
+                                    uint32_t h, uint32_t B, float *y);
 __global__ void ls_expand_kernel(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix, uint32_t a,
                                  uint32_t count, const Coord *src, uint32_t src_base, Coord *dst, uint32_t dst_base);
 __global__ void ls_block_sums_kernel(const uint8_t *sig, uint32_t a, uint32_t count, uint32_t *sums);
@@ -634,13 +640,6 @@ __device__ __forceinline__ uint32_t *warp_window_begin(uint32_t mn, uint32_t mx,
     return mem;
 }
 
-// Heavy outputs (plus-times, split partial sums) stay in a warp's window like
-// any other output: the window's fp32 sum of an output holds at most the
-// terms of one warp's leaves.  The flush adds it to one of the output's
-// partial sums (picked by a hash of the warp's position in the grid) instead
-// of y.  fp64 mode keeps heavy outputs out of windows altogether.
-__device__ __forceinline__ bool heavy_in_window(const VecArgs &va) { return va.hsplit != 0u; }
-
 template <int SR>
 __device__ __forceinline__ void warp_window_flush(const uint32_t *win, uint32_t lo, uint32_t span, uint32_t width,
                                                   const VecArgs &va)
@@ -649,21 +648,9 @@ __device__ __forceinline__ void warp_window_flush(const uint32_t *win, uint32_t 
     __syncwarp();
     uint32_t *y = static_cast<uint32_t *>(va.y) + (size_t)lo * width;
     const uint64_t limit = (va.n_out - lo) * width;
-    const bool heavy = SR == K2T_PLUS_TIMES && va.hflag != nullptr && heavy_in_window(va);
-    const uint32_t part = ((((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * 2654435761u) >> 27) & (va.hsplit - 1u);
     for (uint32_t i = lane; i < span * width; i += 32u) {
         const uint32_t v = win[i];
         if (is_noop_word<SR>(v) || i >= limit) continue;
-        if (heavy) {
-            const uint32_t o = lo + i / width;
-            const uint2 e = __ldg(reinterpret_cast<const uint2 *>(va.hent) + (o >> 5));
-            if ((e.x >> (o & 31u)) & 1u) {
-                const uint32_t id = e.y + (uint32_t)__popc(e.x & ((1u << (o & 31u)) - 1u));
-                float *dst = static_cast<float *>(va.acc) + ((size_t)id * va.hsplit + part) * width + i % width;
-                atomicAdd(dst, __uint_as_float(v));
-                continue;
-            }
-        }
         global_update_word<SR>(y + i, v);
     }
 }
@@ -746,16 +733,14 @@ __device__ __forceinline__ void leaf_slice(uint32_t lam, uint32_t r, uint32_t c,
 //    the VW-wide slice g of every vector row, so a row of x is one coalesced
 //    load and a row of y one coalesced vector reduction (the pages' B
 //    adjacent threads per node, section 3.6).
-// Updates go to the window when there is one, else to y.
-// warp_win: win is this warp's own window (flushed by warp_window_flush),
-// which may hold heavy outputs; a shared block window (BANDED) may not.
+// Updates of heavy outputs go to their sums; the others go to the window
+// when there is one, else to y.
 template <int SR, int DIR, int VW, class LeafAt>
 __device__ __forceinline__ void warp_leaf_rounds(uint32_t jb, uint32_t je, LeafAt &&leaf_at, const VecArgs &va,
-                                                 uint32_t *win, uint32_t lo, bool warp_win = true)
+                                                 uint32_t *win, uint32_t lo)
 {
     const uint32_t lane = threadIdx.x & 31u;
-    // per-leaf heavy routing, unless every update of the warp goes to its window
-    const bool heavy = SR == K2T_PLUS_TIMES && va.hflag != nullptr && !(win && warp_win && heavy_in_window(va));
+    const bool heavy = SR == K2T_PLUS_TIMES && va.hflag != nullptr;
     if (SR == K2T_BOOLEAN || (VW == 1 && va.B == 1)) {
         constexpr int U = kLeafU;
         const uint32_t *x = static_cast<const uint32_t *>(va.x);
@@ -911,6 +896,79 @@ cached_block_kernel(const uint8_t *sig, const uint32_t *dir, uint32_t n, const C
     if (win) warp_window_flush<SR>(win, lo, span, width, va);
 }
 
+// k^2+F engine for batches: the thread block's 8 warps share one 256-node
+// directory block instead of taking one each.  Warp 0 turns the block's
+// signatures into the leaf list (warp scan), every thread loads one node's
+// coordinates, and warp w then takes the w-th eighth of the leaves, with its
+// own output window over the outputs of its slice.  A batch row of x or y is
+// B * 4 bytes, so the rows a wave of warps touches at once are what L2 must
+// hold: with one directory block per thread block the Z-order window in
+// flight is 8 times narrower than with one per warp, and x and y rows are
+// reused from L2 while the block's leaves need them.
+template <int SR, int DIR, int VW>
+__global__ void __launch_bounds__(32 * kCachedWarps, cached_min_blocks<VW>())
+cached_coop_kernel(const uint8_t *sig, const uint32_t *dir, uint32_t n, const Coord *coords, const uint8_t *leaf,
+                   VecArgs va)
+{
+    __shared__ Coord cw[kDirS];
+    __shared__ uint16_t sl[4 * kDirS];
+    __shared__ uint32_t wins[kCachedWarps][kWarpWindow];
+    __shared__ uint32_t total_s;
+    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+    const uint32_t g = blockIdx.x;
+    const uint32_t s = g * kDirS;
+    if (s >= n) return;
+    const uint32_t cnt = min(n - s, kDirS);
+    if (threadIdx.x < cnt) cw[threadIdx.x] = coords[s + threadIdx.x];
+    if (warp == 0) {
+        uint32_t w = 0;
+        if (8u * lane < cnt) {
+            w = __ldg(reinterpret_cast<const uint32_t *>(sig + s / 2) + lane);
+            if (8u * lane + 8u > cnt) w &= (1u << (4u * (cnt - 8u * lane))) - 1u;
+        }
+        const uint32_t f = (uint32_t)__popc(w);
+        const uint32_t incl = warp_incl_scan(f);
+        if (lane == 31) total_s = incl;
+        uint32_t pos = incl - f;
+        uint32_t rest = w;
+        while (rest) {
+            const uint32_t bit = (uint32_t)(__ffs(rest) - 1);  // 4*k + b
+            rest &= rest - 1u;
+            sl[pos++] = (uint16_t)(((8u * lane + bit / 4u) << 2) | (bit & 3u));
+        }
+    }
+    __syncthreads();
+    const uint32_t total = total_s;
+    const uint32_t base = __ldg(dir + g);
+    const uint32_t jb = (uint32_t)(((uint64_t)total * warp) / kCachedWarps);
+    const uint32_t je = (uint32_t)(((uint64_t)total * (warp + 1)) / kCachedWarps);
+    auto leaf_at = [&](uint32_t j, uint32_t &lam, uint32_t &r, uint32_t &c, uint32_t &li) {
+        const uint32_t e = sl[j];
+        const Coord p = cw[e >> 2];
+        const uint32_t b = e & 3u;
+        r = 4u * p.r + 2u * (b >> 1);
+        c = 4u * p.c + 2u * (b & 1u);
+        li = base + j;
+        lam = nibble_at(leaf, li);
+    };
+    // the warp's output span, in units of leaf blocks (2 outputs)
+    uint32_t mn = 0xffffffffu, mx = 0u;
+    for (uint32_t j = jb + lane; j < je; j += 32u) {
+        const uint32_t e = sl[j];
+        const Coord p = cw[e >> 2];
+        const uint32_t b = e & 3u;
+        const uint32_t o = DIR == K2T_RIGHT ? 2u * p.r + (b >> 1) : 2u * p.c + (b & 1u);
+        mn = min(mn, o);
+        mx = max(mx, o);
+    }
+    const uint32_t width = SR == K2T_BOOLEAN ? 1u : va.B;
+    uint32_t lo, span;
+    uint32_t *win = warp_window_begin<SR>(mn, mx, 2u, width, wins[warp], lo, span);
+    __syncwarp();
+    warp_leaf_rounds<SR, DIR, VW>(jb, je, leaf_at, va, win, lo);
+    if (win) warp_window_flush<SR>(win, lo, span, width, va);
+}
+
 // ---- 4x4 leaves (leaf_k = 4) ------------------------------------------------------
 #ifndef K2T_LEAF4_U
 #define K2T_LEAF4_U 2
@@ -941,8 +999,8 @@ __device__ __forceinline__ uint32_t used4(uint32_t lam)
 }
 
 // Heavy outputs among out .. out + 3 (out a multiple of 4): (id << 4) | mask,
-// mask bit q set when out + q is summed in fp64, id the fp64 index of the
-// first of them; output out + q has id + popc(mask & ((1 << q) - 1)).
+// mask bit q set when out + q is heavy, id the heavy-list index of the first
+// of them; output out + q has id + popc(mask & ((1 << q) - 1)).
 __device__ __forceinline__ uint32_t heavy_word4(const VecArgs &va, uint32_t out)
 {
     const uint2 e = __ldg(reinterpret_cast<const uint2 *>(va.hent) + (out >> 5));
@@ -989,13 +1047,17 @@ __device__ __forceinline__ void leaf4_apply1(const uint32_t (&lam)[U], const uin
             for (int q = 0; q < 4; ++q) {
                 const uint32_t s = seg4<DIR>(l, q);
                 if (!s) continue;
-                if (SR == K2T_PLUS_TIMES && ((h >> q) & 1u) && !va.hsplit) {
-                    double d = 0.0;
+                HeavyDst hd{nullptr, nullptr};
+                if (SR == K2T_PLUS_TIMES && ((h >> q) & 1u)) {
+                    hd = heavy_dst(va, heavy_id4(h, q), in_of(u), 0u);
+                    if (!hd.p32) {
+                        double d = 0.0;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        if ((s >> i) & 1u) d += (double)(va.w * __uint_as_float(xo[u][i]));
-                    atomicAdd(static_cast<double *>(va.acc) + heavy_id4(h, q), d);
-                    continue;
+                        for (int i = 0; i < 4; ++i)
+                            if ((s >> i) & 1u) d += (double)(va.w * __uint_as_float(xo[u][i]));
+                        atomicAdd(hd.p64, d);
+                        continue;
+                    }
                 }
                 float v[1] = {S::zero()};
                 bool any = false;
@@ -1006,8 +1068,8 @@ __device__ __forceinline__ void leaf4_apply1(const uint32_t (&lam)[U], const uin
                         v[0] = any ? S::plus(v[0], c) : c;
                         any = true;
                     }
-                if (SR == K2T_PLUS_TIMES && ((h >> q) & 1u)) {
-                    S::update(heavy_part(va, heavy_id4(h, q), in_of(u), 0u), v);
+                if (hd.p32) {
+                    S::update(hd.p32, v);
                     continue;
                 }
                 if (S::skip(v[0])) continue;
@@ -1038,17 +1100,20 @@ __device__ __forceinline__ void leaf4_slice(uint32_t lam, uint32_t r, uint32_t c
     for (int q = 0; q < 4; ++q) {
         const uint32_t s = seg4<DIR>(lam, q);
         if (!s) continue;
-        if (SR == K2T_PLUS_TIMES && ((hv >> q) & 1u) && !va.hsplit) {
-            double *a = static_cast<double *>(va.acc) + (size_t)heavy_id4(hv, q) * va.B + k;
+        HeavyDst hd{nullptr, nullptr};
+        if (SR == K2T_PLUS_TIMES && ((hv >> q) & 1u)) {
+            hd = heavy_dst(va, heavy_id4(hv, q), in, k);
+            if (!hd.p32) {
 #pragma unroll
-            for (int e = 0; e < VW; ++e) {
-                double d = 0.0;
+                for (int e = 0; e < VW; ++e) {
+                    double d = 0.0;
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    if ((s >> i) & 1u) d += (double)(va.w * xv[i][e]);
-                atomicAdd(a + e, d);
+                    for (int i = 0; i < 4; ++i)
+                        if ((s >> i) & 1u) d += (double)(va.w * xv[i][e]);
+                    atomicAdd(hd.p64 + e, d);
+                }
+                continue;
             }
-            continue;
         }
         float v[VW];
 #pragma unroll
@@ -1063,8 +1128,8 @@ __device__ __forceinline__ void leaf4_slice(uint32_t lam, uint32_t r, uint32_t c
                     any = true;
                 }
         }
-        if (SR == K2T_PLUS_TIMES && ((hv >> q) & 1u)) {
-            S::update(heavy_part(va, heavy_id4(hv, q), in, k), v);
+        if (hd.p32) {
+            S::update(hd.p32, v);
         } else if (win) {
 #pragma unroll
             for (int e = 0; e < VW; ++e)
@@ -1085,7 +1150,7 @@ __device__ __forceinline__ void warp_leaf4_rounds(uint32_t jb, uint32_t je, Leaf
                                                   uint32_t *win, uint32_t lo)
 {
     const uint32_t lane = threadIdx.x & 31u;
-    const bool heavy = SR == K2T_PLUS_TIMES && va.hflag != nullptr && !(win && heavy_in_window(va));
+    const bool heavy = SR == K2T_PLUS_TIMES && va.hflag != nullptr;
     if (SR == K2T_BOOLEAN || (VW == 1 && va.B == 1)) {
         constexpr int U = K2T_LEAF4_U;
         const uint32_t *x = static_cast<const uint32_t *>(va.x);
@@ -1310,7 +1375,7 @@ banded_kernel(const uint32_t *chunks, const Coord *coords, const uint32_t *bleaf
             c = 4u * p.c + 2u * (b & 1u);
             li = lw[node] + (e & 3u);
             lam = nibble_at(leaf, li);
-        }, va, windowed ? win : nullptr, (uint32_t)band_lo, false);
+        }, va, windowed ? win : nullptr, (uint32_t)band_lo);
         __syncwarp();
     }
     if (windowed) {
@@ -1661,7 +1726,9 @@ struct DeviceState {
     const uint32_t *hflag[2] = {nullptr, nullptr};  // heavy outputs, per direction (null: none)
     const uint32_t *hent[2] = {nullptr, nullptr};
     const uint32_t *hlist[2] = {nullptr, nullptr};
-    void *acc = nullptr;
+    const uint2 *hrec[2] = {nullptr, nullptr};
+    float *acc = nullptr;
+    double *acc64 = nullptr;
     cudaStream_t cap_stream = nullptr;
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t gexec = nullptr;
@@ -1710,6 +1777,16 @@ void launch_cached(const k2t_tree *t, const DeviceState *d, const VecArgs &va, c
 }
 
 template <int SR, int DIR, int VW>
+void launch_cached_coop(const k2t_tree *t, const DeviceState *d, const VecArgs &va, cudaStream_t st)
+{
+    const int l = t->levels;
+    const uint32_t n = (uint32_t)t->nodes[(size_t)l - 2];
+    const unsigned grid = (n + kDirS - 1) / kDirS;
+    cached_coop_kernel<SR, DIR, VW><<<grid, 32 * kCachedWarps, 0, st>>>(
+        d->tree.lv[l - 2].sig, d->tree.lv[l - 2].dir, n, d->cached, d->tree.lv[l - 1].sig, va);
+}
+
+template <int SR, int DIR, int VW>
 void launch_cached4(const k2t_tree *t, const DeviceState *d, const VecArgs &va, cudaStream_t st)
 {
     const int l = t->levels;
@@ -1736,27 +1813,37 @@ void launch_banded(const k2t_tree *t, const DeviceState *d, const VecArgs &va, c
                                                                           d->tree.lv[l - 1].sig, t->opts.band_rows, va);
 }
 
+// Scratch of one level-synchronous product: a frontier buffer per expanded
+// level and, for scan offsets, the block sums and their prefixes.  k2t_spmv
+// takes them from the tree's arena, k2t_spmv_noalloc from its static array.
+struct LsBufs {
+    Coord *buf[K2T_MAX_LEVELS];
+    uint32_t *sums;
+    uint32_t *prefix;
+};
+
+// The planned launch sequence of the level-synchronous engine (section 3.4).
 template <int SR, int DIR, int VW>
-void launch_ls(const k2t_tree *t, const DeviceState *d, const VecArgs &va, cudaStream_t st)
+void run_ls(const k2t_tree *t, const DeviceState *d, const LsBufs &sb, const VecArgs &va, cudaStream_t st)
 {
     const bool scan = t->opts.offsets == K2T_OFFSETS_SCAN;
     const int l = t->levels;
     for (const LsStep &s : t->steps) {
         const int lv = s.level;
-        const Coord *src = s.src == 0xff ? d->top : d->buf[s.src];
+        const Coord *src = s.src == 0xff ? d->top : sb.buf[s.src];
         const uint8_t *sig = d->tree.lv[lv].sig;
         const uint32_t *dir = d->tree.lv[lv].dir;
         const uint64_t blocks = scan ? (s.count + 255u) / 256u
                                      : ((uint64_t)s.a + s.count + kDirS - 1) / kDirS - s.a / kDirS;
         const uint32_t *prefix = nullptr;
         if (scan) {
-            ls_block_sums_kernel<<<grid_for_blocks(blocks), kWalkThreads, 0, st>>>(sig, s.a, s.count, d->scan_sums);
-            ls_scan_kernel<<<1, 1024, 0, st>>>(d->scan_sums, (uint32_t)blocks, d->scan_prefix);
-            prefix = d->scan_prefix;
+            ls_block_sums_kernel<<<grid_for_blocks(blocks), kWalkThreads, 0, st>>>(sig, s.a, s.count, sb.sums);
+            ls_scan_kernel<<<1, 1024, 0, st>>>(sb.sums, (uint32_t)blocks, sb.prefix);
+            prefix = sb.prefix;
         }
         if (s.kind == 0) {
             ls_expand_kernel<<<grid_for_blocks(blocks), kWalkThreads, 0, st>>>(
-                sig, dir, prefix, s.a, s.count, src, s.src_base, d->buf[lv + 1], s.dst_base);
+                sig, dir, prefix, s.a, s.count, src, s.src_base, sb.buf[lv + 1], s.dst_base);
         } else {
             const uint32_t base = scan ? (uint32_t)level_offset(t, lv, s.a) : 0u;
             launch_flat<SR, DIR, VW>(sig, scan ? nullptr : dir, prefix, base, s.a, s.count,
@@ -1765,10 +1852,22 @@ void launch_ls(const k2t_tree *t, const DeviceState *d, const VecArgs &va, cudaS
     }
 }
 
+template <int SR, int DIR, int VW>
+void launch_ls(const k2t_tree *t, const DeviceState *d, const VecArgs &va, cudaStream_t st)
+{
+    LsBufs sb{};
+    for (int lv = 0; lv < K2T_MAX_LEVELS; ++lv) sb.buf[lv] = d->buf[lv];
+    sb.sums = d->scan_sums;
+    sb.prefix = d->scan_prefix;
+    run_ls<SR, DIR, VW>(t, d, sb, va, st);
+}
+
 using LaunchFn = void (*)(const k2t_tree *, const DeviceState *, const VecArgs &, cudaStream_t);
 
-// Internal engine id: the CACHED engine on a tree with 4x4 leaves.
+// Internal engine ids: the CACHED engine on a tree with 4x4 leaves, and its
+// block-cooperative form for batches.
 constexpr uint32_t kEngineCached4 = 100;
+constexpr uint32_t kEngineCachedCoop = 101;
 
 // Plus-times products of a direction with heavy outputs.  heavy_begin points
 // va at the direction's tables and zeroes their sums for the B vectors
@@ -1779,25 +1878,30 @@ inline bool heavy_begin(const k2t_tree *t, const DeviceState *d, int dir, int se
 {
     va.hflag = nullptr;
     va.hent = nullptr;
+    va.hrec = nullptr;
     va.acc = nullptr;
-    va.hsplit = 0u;
+    va.acc64 = nullptr;
     if (semiring != K2T_PLUS_TIMES || !d->hflag[dir]) return false;
     va.hflag = d->hflag[dir];
     va.hent = d->hent[dir];
+    va.hrec = d->hrec[dir];
     va.acc = d->acc;
-    va.hsplit = t->opts.heavy_mode == 0 ? kHeavySplit : 0u;
-    const uint64_t words = (va.hsplit ? (uint64_t)va.hsplit : 2ull) * t->hlist[dir].size() * va.B;
-    const uint64_t blocks = std::min<uint64_t>((words / 4 + 255) / 256 + 1, 152ull * 8);
-    fill_kernel<<<(unsigned)blocks, 256, 0, st>>>(reinterpret_cast<uint32_t *>(d->acc), words, 0u);
+    va.acc64 = d->acc64;
+    auto zero = [&](void *p, uint64_t words) {
+        if (!words) return;
+        const uint64_t blocks = std::min<uint64_t>((words / 4 + 255) / 256 + 1, 152ull * 8);
+        fill_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<uint32_t *>(p), words, 0u);
+    };
+    zero(d->acc, t->hparts[dir] * va.B);
+    zero(d->acc64, 2 * t->hfp64[dir] * va.B);
     return true;
 }
 
 inline void heavy_end(const k2t_tree *t, const DeviceState *d, int dir, const VecArgs &va, cudaStream_t st)
 {
     const uint32_t h = (uint32_t)t->hlist[dir].size();
-    const uint64_t n = (uint64_t)h * va.B;
-    const uint64_t blocks = std::min<uint64_t>((n + 255) / 256, 152ull * 8);
-    heavy_finish_kernel<<<(unsigned)blocks, 256, 0, st>>>(d->acc, va.hsplit, d->hlist[dir], h, va.B,
+    const uint64_t blocks = std::min<uint64_t>(((uint64_t)h + 7) / 8, 152ull * 16);
+    heavy_finish_kernel<<<(unsigned)blocks, 256, 0, st>>>(d->acc, d->acc64, d->hrec[dir], d->hlist[dir], h, va.B,
                                                           static_cast<float *>(va.y));
 }
 
@@ -1809,6 +1913,7 @@ LaunchFn pick_engine(uint32_t engine)
     case K2T_ENGINE_CACHED: return launch_cached<SR, DIR, VW>;
     case K2T_ENGINE_BANDED: return launch_banded<SR, DIR, VW>;
     case kEngineCached4: return launch_cached4<SR, DIR, VW>;
+    case kEngineCachedCoop: return launch_cached_coop<SR, DIR, VW>;
     default: return launch_ls<SR, DIR, VW>;
     }
 }

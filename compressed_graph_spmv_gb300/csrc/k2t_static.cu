@@ -33,17 +33,15 @@ namespace {
 std::mutex g_static_mutex;
 void *g_static_ptr[kStaticMaxDevices] = {};
 
-// Device address of the scratch array on the current device (looked up once).
-int static_scratch(void **out)
+// Device address of the scratch array on device `dev`, which is current
+// (looked up once per device).
+int static_scratch(int dev, void **out)
 {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) { g_last_cuda = (int)e; return K2T_ECUDA; }
     if (dev < 0 || dev >= kStaticMaxDevices) return K2T_ERANGE;
     std::lock_guard<std::mutex> lock(g_static_mutex);
     if (!g_static_ptr[dev]) {
         void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_static_scratch);
+        cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
         if (e != cudaSuccess || !p) { g_last_cuda = (int)e; return K2T_ECUDA; }
         g_static_ptr[dev] = p;
     }
@@ -51,53 +49,18 @@ int static_scratch(void **out)
     return K2T_OK;
 }
 
-struct StaticBufs {
-    Coord *buf[K2T_MAX_LEVELS];
-    uint32_t *sums;
-    uint32_t *prefix;
-};
-
-template <int SR, int DIR, int VW>
-void run_static(const k2t_tree *t, const DeviceState *d, const StaticBufs &sb, const VecArgs &va, cudaStream_t st)
-{
-    const bool scan = t->opts.offsets == K2T_OFFSETS_SCAN;
-    const int l = t->levels;
-    for (const LsStep &s : t->steps) {
-        const int lv = s.level;
-        const Coord *src = s.src == 0xff ? d->top : sb.buf[s.src];
-        const uint8_t *sig = d->tree.lv[lv].sig;
-        const uint32_t *dir = d->tree.lv[lv].dir;
-        const uint64_t blocks = scan ? (s.count + 255u) / 256u
-                                     : ((uint64_t)s.a + s.count + kDirS - 1) / kDirS - s.a / kDirS;
-        const uint32_t *prefix = nullptr;
-        if (scan) {
-            ls_block_sums_kernel<<<grid_for_blocks(blocks), kWalkThreads, 0, st>>>(sig, s.a, s.count, sb.sums);
-            ls_scan_kernel<<<1, 1024, 0, st>>>(sb.sums, (uint32_t)blocks, sb.prefix);
-            prefix = sb.prefix;
-        }
-        if (s.kind == 0) {
-            ls_expand_kernel<<<grid_for_blocks(blocks), kWalkThreads, 0, st>>>(
-                sig, dir, prefix, s.a, s.count, src, s.src_base, sb.buf[lv + 1], s.dst_base);
-        } else {
-            const uint32_t base = scan ? (uint32_t)level_offset(t, lv, s.a) : 0u;
-            launch_flat<SR, DIR, VW>(sig, scan ? nullptr : dir, prefix, base, s.a, s.count,
-                                     src + (s.a - s.src_base), d->tree.lv[l - 1].sig, va, st);
-        }
-    }
-}
-
-using StaticFn = void (*)(const k2t_tree *, const DeviceState *, const StaticBufs &, const VecArgs &, cudaStream_t);
+using StaticFn = void (*)(const k2t_tree *, const DeviceState *, const LsBufs &, const VecArgs &, cudaStream_t);
 
 template <int SR, int DIR>
 StaticFn pick_static_vw(int vw)
 {
     if constexpr (SR == K2T_BOOLEAN) {
         (void)vw;
-        return run_static<SR, DIR, 1>;
+        return run_ls<SR, DIR, 1>;
     } else {
-        if (vw == 4) return run_static<SR, DIR, 4>;
-        if (vw == 2) return run_static<SR, DIR, 2>;
-        return run_static<SR, DIR, 1>;
+        if (vw == 4) return run_ls<SR, DIR, 4>;
+        if (vw == 2) return run_ls<SR, DIR, 2>;
+        return run_ls<SR, DIR, 1>;
     }
 }
 
@@ -136,15 +99,20 @@ int k2t_spmv_noalloc(k2t_tree *t, int32_t dir, int32_t semiring, float w, const 
     const uint64_t esz = semiring == K2T_BOOLEAN ? 4u : 4u * (uint64_t)B;
     const uintptr_t xa = (uintptr_t)x, ya = (uintptr_t)y;
     if (xa < ya + n_out * esz && ya < xa + n_in * esz) return K2T_EINVAL;
+    // the array used must be the one on the tree's device
+    int cur = -1;
+    cudaError_t ce = cudaGetDevice(&cur);
+    if (ce != cudaSuccess) { g_last_cuda = (int)ce; return K2T_ECUDA; }
+    if (cur != t->dev->device) return K2T_ESTATE;
 
     // scratch this tree needs: one frontier buffer per expanded level, plus
     // the scan space when offsets come from a scan
     const ArenaLayout &L = t->layout;
     const int l = t->levels;
     uint64_t need = 0;
-    StaticBufs sb{};
+    LsBufs sb{};
     void *base = nullptr;
-    int rc = static_scratch(&base);
+    int rc = static_scratch(cur, &base);
     if (rc) return rc;
     uint8_t *p = static_cast<uint8_t *>(base);
     for (int lv = t->d0 + 1; lv <= l - 2; ++lv) {

@@ -1,5 +1,7 @@
 // k2t_probe.cu -- memory-system ceilings for the access patterns of the leaf
-// step, measured on the device the library runs on (the microbenchmark of
+// step, measured on the device the library runs on: instrumentation for the
+// benchmark, built into its own libk2t_probe.so, outside the product
+// library and its ABI (the microbenchmark of
 // section 5.6 of "A GPU Engine for Sparse Matrix-Vector Products on
 // k^2-Tree-Compressed Graphs": copy bandwidth and the rates of consecutive and
 // scattered vector updates y_o += x_i, re-measured here with gathers added).
@@ -9,7 +11,7 @@
 
 #include <cstdint>
 
-#include "../../include/k2t.h"
+#include "../../../include/k2t.h"
 
 namespace {
 
@@ -53,9 +55,27 @@ __global__ void probe_red(float *y, uint64_t mask, uint64_t m, uint32_t scattere
         atomicAdd(y + ((scattered ? scramble(i) : i) & mask), 1.0f);
 }
 
+// m shared-memory reductions per grid into a 2048-entry table per block, at
+// hashed slots: fp32 (kind 5) or fp64 (kind 6) atomicAdd; the table is
+// added to y once per block so the work stays live
+template <class T>
+__global__ void probe_smem_red(float *y, uint64_t m)
+{
+    __shared__ T tab[2048];
+    for (uint32_t i = threadIdx.x; i < 2048; i += blockDim.x) tab[i] = (T)0;
+    __syncthreads();
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < m; i += stride)
+        atomicAdd(&tab[scramble(i) & 2047u], (T)1);
+    __syncthreads();
+    if (threadIdx.x == 0) atomicAdd(y + (blockIdx.x & 1023u), (float)tab[blockIdx.x & 2047u]);
+}
+
 }  // namespace
 
 extern "C" {
+
+int k2t_probe(int32_t kind, const void *x, void *y, uint64_t n, uint64_t m, void *stream);
 
 /* Launch one probe pass on `stream` (the caller times it):
  *   kind 0: copy n floats x -> y (n a multiple of 4)
@@ -63,6 +83,9 @@ extern "C" {
  *   kind 2: m scattered 8-byte gathers (pairs) from x[0..n)
  *   kind 3: m consecutive reductions y[i mod n] += 1
  *   kind 4: m scattered reductions y[h(i) mod n] += 1
+ *   kind 5: m fp32 shared-memory reductions at hashed slots of a 2048-entry
+ *           table per block (y: at least 1024 floats)
+ *   kind 6: the same with fp64 shared-memory reductions
  * n must be a power of two for kinds 1-4.  Returns K2T_OK or K2T_EINVAL /
  * K2T_ECUDA. */
 int k2t_probe(int32_t kind, const void *x, void *y, uint64_t n, uint64_t m, void *stream)
@@ -87,6 +110,14 @@ int k2t_probe(int32_t kind, const void *x, void *y, uint64_t n, uint64_t m, void
     case 3:
     case 4:
         probe_red<<<grid, block, 0, st>>>(static_cast<float *>(y), n - 1, m, kind == 4);
+        break;
+    case 5:
+        if (n < 1024) return K2T_EINVAL;
+        probe_smem_red<float><<<grid, block, 0, st>>>(static_cast<float *>(y), m);
+        break;
+    case 6:
+        if (n < 1024) return K2T_EINVAL;
+        probe_smem_red<double><<<grid, block, 0, st>>>(static_cast<float *>(y), m);
         break;
     default:
         return K2T_EINVAL;

@@ -15,6 +15,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libk2t.so")
+PROBE_LIB_PATH = os.path.join(_HERE, "libk2t_probe.so")   # benchmark instrumentation
 
 RIGHT, LEFT = 0, 1
 PLUS_TIMES, BOOLEAN, MIN_PLUS = 0, 1, 2
@@ -24,14 +25,15 @@ MAX_LEVELS = 33
 MAX_BATCH = 32
 
 STATUS = {0: "K2T_OK", -1: "K2T_EINVAL", -2: "K2T_ERANGE", -3: "K2T_ENOMEM",
-          -4: "K2T_ECUDA", -5: "K2T_ESTATE", -6: "K2T_EDEVICE"}
+          -4: "K2T_ECUDA", -5: "K2T_ESTATE", -6: "K2T_EDEVICE", -7: "K2T_ETIMEOUT"}
+STATUS_WAIT_TIMEOUT, STATUS_OUT_OF_RANGE = 1, 2
 
 EXPORTED = ["k2t_default_opts", "k2t_build", "k2t_workspace_bytes", "k2t_upload", "k2t_spmv",
             "k2t_spmv_marked",
             "k2t_spmv_host", "k2t_stats_get", "k2t_level_signatures", "k2t_device_level",
             "k2t_decode", "k2t_free", "k2t_strerror", "k2t_last_cuda_error",
-            "k2t_spmv_noalloc", "k2t_noalloc_scratch_limit", "k2t_probe", "k2t_msbfs",
-            "k2t_msbfs_work_bytes", "k2t_bool_product", "k2t_bool_closure"]
+            "k2t_spmv_noalloc", "k2t_noalloc_scratch_limit", "k2t_msbfs",
+            "k2t_msbfs_work_bytes", "k2t_bool_product", "k2t_bool_closure", "k2t_status"]
 
 
 class Opts(ctypes.Structure):
@@ -43,7 +45,7 @@ class Opts(ctypes.Structure):
                 ("threads", ctypes.c_uint32), ("band_rows", ctypes.c_uint32),
                 ("band_cols", ctypes.c_uint32), ("heavy_terms", ctypes.c_uint32),
                 ("heavy_mode", ctypes.c_uint32), ("leaf_k", ctypes.c_uint32),
-                ("reserved", ctypes.c_uint32 * 3)]
+                ("coop_batch", ctypes.c_uint32), ("reserved", ctypes.c_uint32 * 2)]
 
 
 class Stats(ctypes.Structure):
@@ -59,7 +61,9 @@ class Stats(ctypes.Structure):
                 ("n_steps", ctypes.c_uint64), ("engine", ctypes.c_uint32), ("offsets", ctypes.c_uint32),
                 ("uploaded", ctypes.c_uint32), ("heavy_rows", ctypes.c_uint32),
                 ("heavy_cols", ctypes.c_uint32), ("heavy_kib", ctypes.c_uint32),
-                ("leaf_k", ctypes.c_uint32), ("reserved", ctypes.c_uint32 * 1)]
+                ("leaf_k", ctypes.c_uint32), ("heavy_fp64", ctypes.c_uint32 * 2),
+                ("heavy_max_terms", ctypes.c_uint32 * 2), ("pad", ctypes.c_uint32),
+                ("heavy_partials", ctypes.c_uint64 * 2)]
 
 
 class K2TError(RuntimeError):
@@ -102,8 +106,8 @@ def load() -> ctypes.CDLL:
         lib.k2t_bool_product.restype = ctypes.c_int
         lib.k2t_bool_closure.argtypes = [P, ctypes.POINTER(Opts), U32, ctypes.POINTER(P), ctypes.POINTER(U32), P]
         lib.k2t_bool_closure.restype = ctypes.c_int
-        lib.k2t_probe.argtypes = [I32, P, P, U64, U64, P]
-        lib.k2t_probe.restype = ctypes.c_int
+        lib.k2t_status.argtypes = [P, ctypes.POINTER(U32), I32, P]
+        lib.k2t_status.restype = ctypes.c_int
         lib.k2t_spmv_host.argtypes = [P, I32, I32, ctypes.c_float, P, P, U32, P]
         lib.k2t_stats_get.argtypes = [P, ctypes.POINTER(Stats)]
         lib.k2t_level_signatures.argtypes = [P, U32, P, U64, ctypes.POINTER(U64)]
@@ -238,6 +242,13 @@ class Tree:
                                                            _dev_ptr(x), _dev_ptr(y), B, _stream_ptr(stream)))
         return y
 
+    def status(self, clear: bool = False, stream=None) -> int:
+        """The tree's device status word (k2t_status): waits for the stream,
+        returns the word and, with clear, resets it."""
+        w = ctypes.c_uint32()
+        _check("k2t_status", load().k2t_status(self._h, ctypes.byref(w), int(bool(clear)), _stream_ptr(stream)))
+        return int(w.value)
+
     def msbfs(self, direction: int, sources, dist, work, max_levels: int = 1 << 30, stream=None) -> int:
         """Multi-source BFS (k2t_msbfs): dist (CUDA int32, n x B) and work (CUDA
         buffer of msbfs_work_bytes()) are the caller's; returns the levels run."""
@@ -315,10 +326,23 @@ class Tree:
         return r, c
 
 
+_probe_lib = None
+
+
 def probe(kind: int, x, y, n: int, m: int, stream=None):
-    """One pass of a memory-system ceiling probe (see k2t_probe in include/k2t.h)."""
-    _check("k2t_probe", load().k2t_probe(kind, _dev_ptr(x) if x is not None else None, _dev_ptr(y), n, m,
-                                         _stream_ptr(stream)))
+    """One pass of a memory-system ceiling probe of the benchmark's own
+    library libk2t_probe.so (kinds in csrc/probe/k2t_probe.cu)."""
+    global _probe_lib
+    if _probe_lib is None:
+        if not os.path.exists(PROBE_LIB_PATH):
+            raise RuntimeError("libk2t_probe.so is missing: run __graft_entry__.build() first")
+        lib = ctypes.CDLL(PROBE_LIB_PATH)
+        P, U64, I32 = ctypes.c_void_p, ctypes.c_uint64, ctypes.c_int32
+        lib.k2t_probe.argtypes = [I32, P, P, U64, U64, P]
+        lib.k2t_probe.restype = ctypes.c_int
+        _probe_lib = lib
+    _check("k2t_probe", _probe_lib.k2t_probe(kind, _dev_ptr(x) if x is not None else None, _dev_ptr(y), n, m,
+                                             _stream_ptr(stream)))
 
 
 @dataclass

@@ -51,6 +51,18 @@ extern "C" {
 #define K2T_ECUDA    (-4)  /* a CUDA runtime call failed (see k2t_last_cuda_error) */
 #define K2T_ESTATE   (-5)  /* wrong call order, e.g. a product before k2t_upload */
 #define K2T_EDEVICE  (-6)  /* a device-side consistency check failed */
+#define K2T_ETIMEOUT (-7)  /* a device-side wait ran out of iterations */
+
+/* Device status word.  The first 4 bytes of a tree's arena (k2t_upload)
+ * hold a word that kernels set instead of trapping: bit 0 when a bounded
+ * wait for a staged copy ran out (the block that waited left its outputs
+ * untouched), bit 1 when a checked build found an index out of range.
+ * Synchronising calls (k2t_spmv_host, k2t_msbfs) read it after their work
+ * and return K2T_ETIMEOUT (bit 0) or K2T_EDEVICE (other bits); the word is
+ * sticky until k2t_status() clears it.  Asynchronous calls leave the check
+ * to the caller (k2t_status after the stream's work). */
+#define K2T_STATUS_WAIT_TIMEOUT 1u
+#define K2T_STATUS_OUT_OF_RANGE 2u
 
 /* Opaque handle to one built tree (host image, plan and device image). */
 typedef struct k2t_tree k2t_tree;
@@ -106,22 +118,30 @@ typedef struct {
     uint32_t band_rows;           /* BANDED: rows per band (power of two, 16..65536); default 4096 */
     uint32_t band_cols;           /* BANDED: columns per tile (power of two >= 16); default 2^23;
                                      0 = one column band                                             */
-    uint32_t heavy_terms;         /* plus-times: an output with more than this many non-zeros in
-                                     its row (right) or column (left), counted over the input list,
-                                     is "heavy": summed as heavy_mode says and rounded to fp32 once;
-                                     every other output is one fp32 sum.  Default 2048; 0 = default;
-                                     0xffffffff = never.  See "Accumulation precision" below.        */
-    uint32_t heavy_mode;          /* how outputs above heavy_terms are summed: 0 (default) in 32
-                                     fp32 partial sums, taken by the grid's warps in turn, added in
-                                     fp64 at the end; 1 in fp64 (exact pair sums, fp64 atomics;
-                                     slower).  See "Accumulation precision" below.                  */
+    uint32_t heavy_terms;         /* plus-times: the most non-zeros one fp32 sum may hold.  An
+                                     output with more non-zeros in its row (right) or column
+                                     (left), counted over the input list, is "heavy": summed as
+                                     heavy_mode says and rounded to fp32 once.  Default 160 (0 =
+                                     default), the largest count for which an fp32 sum meets the
+                                     plus-times bound in any order; 0xffffffff = never (every
+                                     output one fp32 sum).  See "Accumulation precision" below.   */
+    uint32_t heavy_mode;          /* how heavy outputs are summed: 0 (default) in fp32 partial
+                                     sums of at most heavy_terms terms each (the builder picks
+                                     2^bits of them per output and checks the count of every
+                                     one), added in fp64 at the end; 1 in fp64 (fp64 atomics;
+                                     slower).  See "Accumulation precision" below.                */
     uint32_t leaf_k;              /* side of a leaf block: 2 (default; 0 = default) or 4.  4: the
                                      leaf level stores 4x4 bitmaps (16-bit signatures, cell
                                      (dr, dc) at bit 4*dr + dc), the larger leaves of section 5.6;
                                      every other level keeps k = 2 (or k = 4 on the n_k4 top
                                      levels).  Needs the CACHED engine (cache_last_internal = 1,
                                      engine AUTO or CACHED); other engines give EINVAL.              */
-    uint32_t reserved[3];
+    uint32_t coop_batch;          /* CACHED: fp32 batches of at least this many vectors run with
+                                     the 8 warps of a thread block sharing one 256-node directory
+                                     block (a narrower window of x and y rows in flight, so L2
+                                     keeps them); smaller batches give each warp its own block.
+                                     Default 8; 0 = default; 0xffffffff = never                    */
+    uint32_t reserved[2];
 } k2t_opts;
 
 /* ---- statistics -------------------------------------------------------- */
@@ -154,7 +174,12 @@ typedef struct {
     uint32_t heavy_kib;           /* device KiB of the heavy outputs' tables and
                                      sums (part of workspace_bytes)                */
     uint32_t leaf_k;              /* side of a leaf block: 2 or 4                  */
-    uint32_t reserved[1];
+    uint32_t heavy_fp64[2];       /* heavy outputs summed in fp64 (right, left)    */
+    uint32_t heavy_max_terms[2];  /* most terms one fp32 partial sum of a heavy
+                                     output receives (right, left)                 */
+    uint32_t pad;
+    uint64_t heavy_partials[2];   /* fp32 partial sums of the heavy outputs
+                                     (right, left)                                 */
 } k2t_stats;
 
 /* Fill *o with the defaults: k = 2, tree-only FUSED engine (AUTO), directory
@@ -196,17 +221,23 @@ int k2t_upload(k2t_tree *t, void *arena, uint64_t arena_bytes, void *stream);
  * line 1).  Boolean and tropical results are exact and deterministic.
  * Tropical minima follow the IEEE total order without NaN (-0 < +0); NaN
  * inputs give unspecified values.
- * Accumulation precision (plus-times): sums run in no fixed order.  An
- * output with at most opts.heavy_terms non-zeros is one fp32 sum, so its
- * rounding error stays that of an fp32 sum of at most that many terms.  An
- * output with more is summed, per opts.heavy_mode, in 32 fp32 partial sums
- * (each with about 1/32 of its terms) added in fp64 (mode 0), or in fp64 with
- * each term w*x_j formed in fp32 (mode 1), and rounded to fp32 once, at the
- * end of the product.  Heavy outputs need B <= opts.max_batch.
+ * Accumulation precision (plus-times): sums run in no fixed order, and
+ * every output meets |y - y_ref| <= 1e-5 * sum_j |w x_j| + 1e-6 (y_ref the
+ * exact sum) for any finite inputs whose partial sums stay in the fp32
+ * range.  An fp32 sum of N terms w*x_j (each rounded once), formed by any
+ * tree of additions, errs by at most N * 2^-24 * sum|w x_j| (to first
+ * order), which is within 1e-5 for N <= 167.  So an output with at most
+ * opts.heavy_terms (default 160) non-zeros is one fp32 sum, reduced in warp
+ * windows or in y; a heavy output (more non-zeros) is summed in fp32 partial
+ * sums of at most heavy_terms terms each (heavy_mode 0) or in fp64 (mode 1),
+ * then the partial sums are added in fp64 and rounded to fp32 once, at the
+ * end of the product: at most (heavy_terms + 1) * 2^-24 of the sum.
+ * Heavy outputs need B <= opts.max_batch.
  * x and y must be 4-byte aligned (16-byte alignment enables vector access).
- * Errors: ESTATE (not uploaded), EINVAL (bad dir/semiring, null, B = 0,
- * overlap), ERANGE (B > 32; plus-times with heavy outputs and
- * B > opts.max_batch), ECUDA (launch failure). */
+ * The tree's device (current at k2t_upload) must be the current device.
+ * Errors: ESTATE (not uploaded, or another device current), EINVAL (bad
+ * dir/semiring, null, B = 0, overlap), ERANGE (B > 32; plus-times with heavy
+ * outputs and B > opts.max_batch), ECUDA (launch failure). */
 int k2t_spmv(k2t_tree *t, int32_t dir, int32_t semiring, float w,
              const void *x, void *y, uint32_t B, void *stream);
 
@@ -221,7 +252,8 @@ int k2t_spmv_marked(k2t_tree *t, int32_t dir, int32_t semiring, float w,
 /* Same product on HOST buffers: copies x to the device vectors of the
  * workspace, runs k2t_spmv, copies y back, and synchronises the stream.
  * Needs opts.host_vectors = 1 and B <= opts.max_batch (else ESTATE/ERANGE).
- * Host buffers may be pageable; pinned buffers copy faster. */
+ * Host buffers may be pageable; pinned buffers copy faster.  After the copy
+ * back it reads the device status word: ETIMEOUT or EDEVICE if it is set. */
 int k2t_spmv_host(k2t_tree *t, int32_t dir, int32_t semiring, float w,
                   const void *x_host, void *y_host, uint32_t B, void *stream);
 
@@ -238,15 +270,26 @@ int k2t_spmv_host(k2t_tree *t, int32_t dir, int32_t semiring, float w,
  *   - The tree must use the LEVELSYNC engine (else ESTATE) and its frontier
  *     buffers plus scan space must fit the array (else ERANGE; lower
  *     opts.tile_m to fit).
+ *   - The tree's device (current at k2t_upload) must be current (else
+ *     ESTATE).
  *   - The first call on a device, with that device current, looks up the
  *     array's device address (cudaGetSymbolAddress); make that first call
  *     before any stream capture.
  *   - Every call shares the array.  Nothing in it needs to start at zero;
  *     calls whose work overlaps on the GPU race on it, so order them (one
  *     stream, or events).
+ *   - k2t_workspace_bytes still counts the level-synchronous scratch in the
+ *     tree's arena, which this call leaves unused: the device memory in use
+ *     is the workspace plus the 64 MiB array.
  *   - Other errors as k2t_spmv. */
 int k2t_spmv_noalloc(k2t_tree *t, int32_t dir, int32_t semiring, float w,
                      const void *x, void *y, uint32_t B, void *stream);
+
+/* Read the tree's device status word (see "Device status word"): waits for
+ * the work queued on `stream`, stores the word in *word and, if clear != 0,
+ * resets it to 0.  Returns K2T_OK, or ESTATE (not uploaded), EINVAL (null),
+ * ECUDA. */
+int k2t_status(k2t_tree *t, uint32_t *word, int32_t clear, void *stream);
 
 /* Size in bytes of the device array k2t_spmv_noalloc works in. */
 uint64_t k2t_noalloc_scratch_limit(void);
@@ -285,25 +328,16 @@ int k2t_bool_closure(const k2t_tree *a, const k2t_opts *opts, uint32_t max_iters
  *   work      device buffer of k2t_msbfs_work_bytes(t) bytes (frontier,
  *             visited, product output, counter), owned by the caller
  *   levels    out: levels run (the last one reached no new vertex, or the cap)
- * Synchronises the stream once per level (to read the new-vertex count).
+ * Synchronises the stream once per level (to read the new-vertex count and
+ * the device status word).
  * Errors: ESTATE (not uploaded), EINVAL (non-square, bad dir, null),
- * ERANGE (B = 0 or > 32, a source >= n), ECUDA. */
+ * ERANGE (B = 0 or > 32, a source >= n), ECUDA, ETIMEOUT / EDEVICE (status
+ * word set). */
 int k2t_msbfs(k2t_tree *t, int32_t dir, const uint32_t *sources, uint32_t B, int32_t *dist, void *work,
               uint32_t max_levels, uint32_t *levels, void *stream);
 
 /* Bytes of the work buffer k2t_msbfs needs for this tree. */
 uint64_t k2t_msbfs_work_bytes(const k2t_tree *t);
-
-/* Memory-system ceilings for the leaf step's access patterns (the
- * microbenchmark of section 5.6, re-measured on this device; instrumentation,
- * not part of a product).  Launches one pass on `stream`; the caller times it.
- *   kind 0: copy n floats x -> y (n a multiple of 4)
- *   kind 1: m scattered 4-byte gathers from x[0..n)
- *   kind 2: m scattered 8-byte gathers (adjacent pairs) from x[0..n)
- *   kind 3: m consecutive reductions y[i mod n] += 1
- *   kind 4: m scattered reductions y[h(i) mod n] += 1 (h a fixed hash)
- * n must be a power of two for kinds 1-4.  Errors: EINVAL, ECUDA. */
-int k2t_probe(int32_t kind, const void *x, void *y, uint64_t n, uint64_t m, void *stream);
 
 /* Shape, per-level sizes and the device footprint broken down by part. */
 int k2t_stats_get(const k2t_tree *t, k2t_stats *s);

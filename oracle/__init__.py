@@ -42,7 +42,7 @@ def build() -> str:
     """Compile the C oracle with gcc (no vector contraction: -ffp-contract=off)."""
     if (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + ".tmp%d" % os.getpid()
-        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared",
+        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-pthread",
                                "-ffp-contract=off", "-o", tmp, _SRC])
         os.replace(tmp, _LIB)
     return _LIB
@@ -77,6 +77,10 @@ def _load():
                                  ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_uint32,
                                  P, P, P]
         lib.orc_spmv.restype = ctypes.c_uint64
+        lib.orc_spmv_bands.argtypes = [ctypes.POINTER(_Tree), ctypes.c_uint64, ctypes.c_uint64,
+                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_uint32,
+                                       P, P, P, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]
+        lib.orc_spmv_bands.restype = ctypes.c_uint64
         lib.orc_decode.argtypes = [ctypes.POINTER(_Tree), P, P, ctypes.c_uint64]
         lib.orc_decode.restype = ctypes.c_uint64
         lib.orc_copy_bits.argtypes = [ctypes.POINTER(_Tree), P]
@@ -181,8 +185,12 @@ class OracleTree:
 
     # --- product -------------------------------------------------------
     def spmv(self, direction: int, semiring: int, x: np.ndarray, B: int = 1,
-             w: float | None = None) -> OracleResult:
-        """Product by recursive rank-based descent (see module docstring)."""
+             w: float | None = None, threads: int = 1, band_level: int = -1) -> OracleResult:
+        """Product by recursive rank-based descent (see module docstring).
+        threads != 1: the descent shared among threads by row bands (right)
+        or column bands (left) of the level-band_level subtrees (-1: picked
+        from the thread count; threads 0: one per core); the result is the
+        same, and ``threads_used`` records how many ran."""
         if w is None:
             w = 1.0
         n_in = self.n_cols if direction == RIGHT else self.n_rows
@@ -199,9 +207,19 @@ class OracleTree:
             x = np.ascontiguousarray(x, dtype=np.float32).reshape(n_in, B)
             y = np.zeros((n_out, B), dtype=np.float32)
             scale = None
-        cells = _load().orc_spmv(ctypes.byref(self._t), self.n_rows, self.n_cols, direction,
-                                 semiring, ctypes.c_float(w), B, _ptr(x), _ptr(y),
-                                 _ptr(scale) if scale is not None else None)
+        sc = _ptr(scale) if scale is not None else None
+        if threads == 1:
+            cells = _load().orc_spmv(ctypes.byref(self._t), self.n_rows, self.n_cols, direction,
+                                     semiring, ctypes.c_float(w), B, _ptr(x), _ptr(y), sc)
+            self.threads_used = 1
+        else:
+            used = ctypes.c_int32(0)
+            cells = _load().orc_spmv_bands(ctypes.byref(self._t), self.n_rows, self.n_cols, direction,
+                                           semiring, ctypes.c_float(w), B, _ptr(x), _ptr(y), sc,
+                                           int(band_level), int(threads), ctypes.byref(used))
+            if cells == (1 << 64) - 1:
+                raise MemoryError("oracle band descent ran out of memory")
+            self.threads_used = int(used.value)
         return OracleResult(y, scale, int(cells))
 
 

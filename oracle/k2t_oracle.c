@@ -22,6 +22,14 @@
  *                  the contribution w (x) x_j of Table 1 at every cell.
  *                  Right: y_r (+)= w (x) x_c.  Left (section 3.6): y_c (+)=
  *                  w (x) x_r.
+ *   orc_spmv_bands the same descent shared among POSIX threads: the subtrees
+ *                  of one level are grouped into row bands (right products)
+ *                  or column bands (left products), and the threads take
+ *                  whole bands, so no two threads write one output.  Every
+ *                  output receives its contributions in the order orc_spmv
+ *                  gives them, so the results are identical.  This is the
+ *                  multicore CPU descent the pages measure against (section
+ *                  4, "Baselines"), kept here as a timed baseline.
  *   orc_rows_product  the plain definition y_i = (+)_{j: A_ij = 1} w (x) x_j
  *                  (section 2.2) evaluated from the edge list, for a sample
  *                  of outputs only, in one pass over the edges.
@@ -45,9 +53,12 @@
  * bitmaps, cell (dr, dc) at bit 4*dr + dc, the "leaves larger than 2x2" the
  * pages name as the next lever (section 5.6).  Every other level keeps k = 2.
  */
+#define _POSIX_C_SOURCE 200809L
+#include <pthread.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#include <unistd.h>
 
 #define ORC_MAX_LEVELS 64
 
@@ -321,6 +332,142 @@ uint64_t orc_spmv(const orc_tree *t, uint64_t n_rows, uint64_t n_cols,
     }
     visit(t, &c, 0, 0, 0, 0);
     return c.cells;
+}
+
+/* --- the descent shared among threads by bands ------------------------- */
+typedef struct { uint64_t pos, r0, c0, band, seq; } orc_sub;  /* a level-bd node */
+typedef struct { orc_sub *v; uint64_t n, cap; int bd; int dir; } orc_subs;
+
+static int collect_visit(const orc_tree *t, orc_subs *s, int d, uint64_t pos, uint64_t r0, uint64_t c0)
+{
+    if (d == s->bd) {
+        if (s->n == s->cap) {
+            uint64_t ncap = s->cap ? 2 * s->cap : 1024;
+            orc_sub *nv = (orc_sub *)realloc(s->v, ncap * sizeof(orc_sub));
+            if (!nv) return -2;
+            s->v = nv;
+            s->cap = ncap;
+        }
+        orc_sub *e = &s->v[s->n];
+        e->pos = pos; e->r0 = r0; e->c0 = c0; e->seq = s->n;
+        e->band = (s->dir == 0 ? r0 : c0) / level_side(t, d);
+        s->n++;
+        return 0;
+    }
+    int k = level_k(t, d);
+    uint64_t sub = level_side(t, d) / (uint64_t)k;
+    for (int b = 0; b < k * k; ++b) {
+        if (!get_bit(t, pos + (uint64_t)b)) continue;
+        uint64_t r = r0 + (uint64_t)(b / k) * sub;
+        uint64_t col = c0 + (uint64_t)(b % k) * sub;
+        int rc = collect_visit(t, s, d + 1, orc_child_pos(t, d, pos + (uint64_t)b), r, col);
+        if (rc) return rc;
+    }
+    return 0;
+}
+
+static int sub_cmp(const void *a, const void *b)
+{
+    const orc_sub *x = (const orc_sub *)a, *y = (const orc_sub *)b;
+    if (x->band != y->band) return x->band < y->band ? -1 : 1;
+    return x->seq < y->seq ? -1 : (x->seq > y->seq ? 1 : 0);
+}
+
+typedef struct {
+    const orc_tree *t;
+    const orc_subs *subs;
+    const uint64_t *group;   /* group g = subs [group[g], group[g+1]) */
+    uint64_t ngroups;
+    uint64_t next;           /* next group to take (atomic) */
+    orc_ctx proto;
+} orc_shared;
+
+typedef struct { orc_shared *sh; uint64_t cells; } orc_worker;
+
+static void *band_worker(void *arg)
+{
+    orc_worker *w = (orc_worker *)arg;
+    orc_shared *sh = w->sh;
+    orc_ctx c = sh->proto;
+    c.cells = 0;
+    for (;;) {
+        uint64_t g = __atomic_fetch_add(&sh->next, 1, __ATOMIC_RELAXED);
+        if (g >= sh->ngroups) break;
+        for (uint64_t i = sh->group[g]; i < sh->group[g + 1]; ++i) {
+            const orc_sub *e = &sh->subs->v[i];
+            visit(sh->t, &c, sh->subs->bd, e->pos, e->r0, e->c0);
+        }
+    }
+    w->cells = c.cells;
+    return NULL;
+}
+
+/*
+ * orc_spmv with the level-bd subtrees grouped into bands of their node row
+ * (dir 0) or column (dir 1) and the bands shared among `threads` threads
+ * (0: one per online core).  bd < 0 picks the shallowest level with at least
+ * 8192 nodes per thread (at most the last internal level): enough bands to
+ * balance power-law rows, few enough that collecting them stays cheap.  *used receives the
+ * thread count.  Returns the cells visited, or (uint64_t)-1 if memory ran out.
+ */
+uint64_t orc_spmv_bands(const orc_tree *t, uint64_t n_rows, uint64_t n_cols,
+                        int32_t dir, int32_t semiring, float w, uint32_t B,
+                        const void *x, void *y, double *scale, int32_t bd, int32_t threads, int32_t *used)
+{
+    int nt = threads > 0 ? threads : (int)sysconf(_SC_NPROCESSORS_ONLN);
+    if (nt < 1) nt = 1;
+    if (bd < 0) {
+        bd = 0;
+        while (bd < t->levels - 2 && t->nodes[bd] < (uint64_t)8192 * (uint64_t)nt) ++bd;
+    }
+    if (bd > t->levels - 1) bd = t->levels - 1;
+    /* fill y and scale with the semiring zero, as orc_spmv does */
+    uint64_t n_out = dir == 0 ? n_rows : n_cols;
+    if (semiring == 0) {
+        double *yy = (double *)y;
+        for (uint64_t i = 0; i < n_out * B; ++i) yy[i] = 0.0;
+        if (scale) for (uint64_t i = 0; i < n_out * B; ++i) scale[i] = 0.0;
+    } else if (semiring == 1) {
+        memset(y, 0, n_out * sizeof(uint32_t));
+    } else {
+        orc_fu inf; inf.u = 0x7f800000u;
+        float *yy = (float *)y;
+        for (uint64_t i = 0; i < n_out * B; ++i) yy[i] = inf.f;
+    }
+    orc_subs subs;
+    memset(&subs, 0, sizeof(subs));
+    subs.bd = bd;
+    subs.dir = dir;
+    if (collect_visit(t, &subs, 0, 0, 0, 0)) { free(subs.v); return (uint64_t)-1; }
+    qsort(subs.v, subs.n, sizeof(orc_sub), sub_cmp);
+    uint64_t *group = (uint64_t *)malloc((subs.n + 1) * sizeof(uint64_t));
+    orc_worker *wk = (orc_worker *)calloc((size_t)nt, sizeof(orc_worker));
+    pthread_t *th = (pthread_t *)calloc((size_t)nt, sizeof(pthread_t));
+    if (!group || !wk || !th) { free(group); free(wk); free(th); free(subs.v); return (uint64_t)-1; }
+    uint64_t ng = 0;
+    for (uint64_t i = 0; i < subs.n; ++i)
+        if (i == 0 || subs.v[i].band != subs.v[i - 1].band) group[ng++] = i;
+    group[ng] = subs.n;
+    orc_shared sh;
+    sh.t = t; sh.subs = &subs; sh.group = group; sh.ngroups = ng; sh.next = 0;
+    sh.proto.dir = dir; sh.proto.semiring = semiring; sh.proto.w = w; sh.proto.B = B;
+    sh.proto.mask = (B >= 32) ? 0xffffffffu : ((1u << B) - 1u);
+    sh.proto.x = x; sh.proto.y = y; sh.proto.scale = scale; sh.proto.cells = 0;
+    int started = 0;
+    for (int i = 0; i < nt; ++i) {
+        wk[i].sh = &sh;
+        if (i > 0 && pthread_create(&th[i], NULL, band_worker, &wk[i]) == 0) ++started;
+        else if (i > 0) break;
+    }
+    band_worker(&wk[0]);
+    uint64_t cells = wk[0].cells;
+    for (int i = 1; i <= started; ++i) {
+        pthread_join(th[i], NULL);
+        cells += wk[i].cells;
+    }
+    if (used) *used = started + 1;
+    free(group); free(wk); free(th); free(subs.v);
+    return cells;
 }
 
 /* Decode the tree into its cells, in descent order.  Returns the number of

@@ -23,7 +23,8 @@ ENGINES = [
     dict(engine=2, offsets=0, tile_m=16),              # level-sync, directory, many tiles
     dict(engine=2, offsets=1, tile_m=16),              # level-sync, scan
     dict(engine=2, offsets=0, tile_m=1 << 20, use_graph=0),
-    dict(engine=3, cache_last_internal=1),             # k^2+F
+    dict(engine=3, cache_last_internal=1),             # k^2+F (fp32 batches of 8+: block-cooperative)
+    dict(engine=3, cache_last_internal=1, coop_batch=1),  # k^2+F, block-cooperative at every width
     dict(engine=4, cache_last_internal=1),             # k^2+F by row band
     dict(engine=4, cache_last_internal=1, band_rows=16),
     dict(engine=3, cache_last_internal=1, leaf_k=4),   # k^2+F with 4x4 leaves (section 5.6)
@@ -81,17 +82,97 @@ def test_random_ragged(seed):
                 assert_match(semiring, got, ref, "seed%d %s h%d sr%d B%d d%d" % (seed, kw, heavy, semiring, B, d))
 
 
+def _magnitude_mix(big_at_end: bool):
+    """A symmetric 4096 x 4096 matrix whose rows (and columns) 5, 6, 7, 8
+    hold 160, 2000, 161 and 100 non-zeros: one in column g (0, or 4095 when
+    big_at_end) and the rest spread over [16, 4095).  Row 9 holds one cell,
+    (9, 9), listed 300 times.  With x_g = 2^24 and every other x = 1 the exact sums
+    are 2^24 + (count - 1); an fp32 sum that adds 2^24 first loses every 1
+    after it, up to 1999 off against a bound of 1e-5 * (2^24 + 1999) ~ 168."""
+    n = 4096
+    g = n - 1 if big_at_end else 0
+    rng = np.random.default_rng(77 + int(big_at_end))
+    rows, cols = [], []
+    for r, cnt in ((5, 160), (6, 2000), (7, 161), (8, 100)):
+        others = rng.choice(np.arange(16, n - 1), size=cnt - 1, replace=False)
+        c = np.concatenate([[g], others]).astype(np.uint32)
+        rows.append(np.full(cnt, r, np.uint32))
+        cols.append(c)
+    r = np.concatenate(rows)
+    c = np.concatenate(cols)
+    rep = np.full(300, 9, np.uint32)
+    rows = np.concatenate([r, c, rep])
+    cols = np.concatenate([c, r, rep])
+    x = np.ones(n, np.float32)
+    x[g] = 2.0 ** 24
+    return rows, cols, n, x
+
+
+@pytest.mark.parametrize("big_at_end", [False, True])
+def test_plus_times_bound_default_options(big_at_end):
+    """Default heavy options (heavy_terms 160, bounded fp32 partial sums),
+    every engine, B = 1, 4, 16, right and left: the magnitude mix of
+    _magnitude_mix with the large input at the lowest column and again at
+    the highest (so the order in which the atomics meet it differs) meets
+    the plus-times bound on every output.  The 160-term rows stay one fp32
+    sum, the longer rows are split, and the repeated pair's row (300 listed
+    entries in one partial whatever the split) falls back to fp64."""
+    rows, cols, n, x1 = _magnitude_mix(big_at_end)
+    for kw in ENGINES:
+        t = _tree(rows, cols, n, n, **kw)
+        s = t.stats()
+        assert (s.heavy_rows, s.heavy_cols) == (3, 3)           # rows 6, 7 and the repeated pair's row 9
+        assert s.heavy_fp64[0] == 1 and s.heavy_fp64[1] == 1    # row 9 / column 9
+        assert 0 < s.heavy_max_terms[0] <= 160
+        for B in (1, 4, 16):
+            x = np.repeat(x1[:, None], B, axis=1)
+            for d in (RIGHT, LEFT):
+                ref = oracle.spmv_edges(rows, cols, n, n, d, PLUS_TIMES, x, B=B)
+                got = device_product(t, d, PLUS_TIMES, x, B)
+                assert_match(PLUS_TIMES, got, ref, "%s B%d d%d end%d" % (kw, B, d, big_at_end))
+                for r, cnt in ((5, 160), (6, 2000), (7, 161), (8, 100)):
+                    exact = 2.0 ** 24 + (cnt - 1)
+                    assert np.all(np.abs(got[r].astype(np.float64) - exact) <= 1e-5 * exact + 1e-6), (kw, B, d, r)
+
+
+def test_tropical_signed_zero_order():
+    """Tropical minima follow the IEEE total order with -0 < +0: with w = -0,
+    an input of -0 contributes -0 and one of +0 contributes +0, so an output
+    reaching both holds -0 (bit pattern 0x80000000); the oracle takes the
+    same order, and the comparison is bit for bit."""
+    n = 64
+    rows = np.array([1, 1, 2, 3, 3, 4], np.uint32)
+    cols = np.array([10, 11, 11, 12, 13, 10], np.uint32)
+    ot = oracle.OracleTree(rows, cols, n, n)
+    x = np.full((n, 2), np.inf, np.float32)
+    x[10] = [-0.0, 0.0]
+    x[11] = [0.0, -0.0]
+    x[12] = [-0.0, -0.0]
+    x[13] = [0.0, 0.0]
+    for kw in ENGINES:
+        t = _tree(rows, cols, n, n, host_top_max_nodes=1, **kw)
+        for d in (RIGHT, LEFT):
+            xd = x if d == RIGHT else np.full((n, 2), -0.0, np.float32)
+            ref = ot.spmv(d, TROPICAL, xd, B=2, w=-0.0)
+            got = device_product(t, d, TROPICAL, xd, 2, w=-0.0)
+            assert_match(TROPICAL, got, ref, "%s d%d" % (kw, d))
+            if d == RIGHT:
+                assert got[1].view(np.uint32).tolist() == [0x80000000, 0x80000000]
+                assert got[3].view(np.uint32).tolist() == [0x80000000, 0x80000000]
+                assert got[4].view(np.uint32).tolist() == [0x80000000, 0x00000000]
+
+
 @pytest.mark.parametrize("heavy_mode", [1, 0])
 @pytest.mark.parametrize("heavy_terms", [0, 4])
 def test_heavy_outputs_hub_cancellation(heavy_terms, heavy_mode):
     """Row 0 and column 0 hold 5000 non-zeros, more than the heavy limit
-    (default 2048, or 4): with x_0 = 2^24 and x_j = 1 for the other 4999, the
+    (default 160, or 4): with x_0 = 2^24 and x_j = 1 for the other 4999, the
     sum is 2^24 + 4999.  An fp32 sum can lose each 1 against 2^24 (up to 4999
     off, far beyond the plus-times bound).  fp64 mode (1) sums exactly and
     rounds once, so it matches bit for bit, whatever the order of the atomics;
-    split mode (0) keeps 32 fp32 partial sums, each with a share of the
-    terms, and must meet the bound.  Outputs 1..4999 hold the single term
-    2^24, the rest zero, in both modes."""
+    split mode (0) keeps fp32 partial sums of at most the limit's terms and
+    must meet the bound.  Outputs 1..4999 hold the single term 2^24, the rest
+    zero, in both modes."""
     n = 8192
     j = np.arange(5000, dtype=np.uint32)
     rows = np.concatenate([np.zeros(5000, np.uint32), j[1:]])
@@ -128,7 +209,7 @@ def test_heavy_outputs_large_hub(heavy_mode):
     a = np.arange(n, dtype=np.uint32)
     rows, cols = oracle.dedup_edges(np.concatenate([r0, np.full(n, 7, np.uint32), a]),
                                     np.concatenate([c0, a, np.full(n, 11, np.uint32)]))
-    for kw in (ENGINES[0], ENGINES[2], ENGINES[5], ENGINES[6], ENGINES[8]):
+    for kw in (ENGINES[0], ENGINES[2], ENGINES[5], ENGINES[6], ENGINES[7], ENGINES[9]):
         t = _tree(rows, cols, n, n, heavy_mode=heavy_mode, **kw)
         assert t.stats().heavy_rows >= 1 and t.stats().heavy_cols >= 1
         for B in (1, 16):
@@ -174,7 +255,7 @@ def test_rmat_medium_all_semirings():
     rows, cols = synth.rmat(17, 0.57, 0.19, 0.19, 1 << 20, 12)
     n = 1 << 17
     rng = np.random.default_rng(12)
-    for kw in (ENGINES[0], ENGINES[2], ENGINES[3], ENGINES[5], ENGINES[6], ENGINES[8]):
+    for kw in (ENGINES[0], ENGINES[2], ENGINES[3], ENGINES[5], ENGINES[6], ENGINES[7], ENGINES[9]):
         t = _tree(rows, cols, n, n, **kw)
         for semiring, B in ((PLUS_TIMES, 1), (PLUS_TIMES, 16), (BOOLEAN, 32), (TROPICAL, 8)):
             for d in (RIGHT, LEFT):

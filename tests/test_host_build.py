@@ -137,8 +137,11 @@ def test_errors():
 
 
 def _layout_parts(s):
+    """Sum of the parts the statistics list; the heavy outputs' tables and
+    sums are given in KiB (rounded up), so the sum may exceed the exact bytes
+    by under 1 KiB."""
     return (s.t_bytes_device + s.l_bytes_device + s.dir_bytes + s.top_bytes + s.cached_bytes +
-            s.plan_bytes + s.scratch_bytes + s.vector_bytes)
+            s.plan_bytes + s.scratch_bytes + s.vector_bytes + 1024 * s.heavy_kib)
 
 
 @pytest.mark.parametrize("engine", [1, 2, 3, 4])
@@ -152,8 +155,8 @@ def test_workspace_accounting(engine):
     parts = _layout_parts(s)
     # every part is placed at a 256-byte boundary: the total exceeds the sum of
     # the parts by the alignment padding only (plus the 64-byte status word)
-    nparts = 4 * s.levels + 10
-    assert parts <= ws <= parts + 256 * nparts + 256
+    nparts = 4 * s.levels + 20
+    assert parts - 1024 <= ws <= parts + 256 * nparts + 256
     assert s.vector_bytes == 2 * 4096 * 4 * 4
     if engine == 1:
         assert s.n_chunks > 1 and s.plan_bytes > 0 and s.scratch_bytes == 0
@@ -170,9 +173,24 @@ def test_options_struct_matches_header():
     """The binding's k2t_opts mirrors the header: defaults round-trip."""
     o = K.default_opts()
     assert o.band_rows == 4096 and o.chunk_cap == 2048 and o.tile_m == 1 << 20 and o.max_batch == 32
-    assert o.heavy_terms == 2048 and o.leaf_k == 2
-    assert ctypes.sizeof(K.Opts) == 80  # 6 x u32, u64, 5 x u32, heavy_terms, 5 reserved
-    assert ctypes.sizeof(K.Stats) == 432
+    assert o.heavy_terms == 160 and o.leaf_k == 2
+    # sizes and field offsets as a C compiler lays the header's structs out
+    import subprocess
+    import tempfile
+    probe = "\n".join([
+        "#include <stddef.h>", "#include <stdio.h>", "#include \"k2t.h\"",
+        "int main(void) {",
+        "  printf(\"%zu %zu %zu %zu %zu\\n\", sizeof(k2t_opts), sizeof(k2t_stats),",
+        "         offsetof(k2t_opts, leaf_k), offsetof(k2t_stats, leaf_k), offsetof(k2t_stats, heavy_partials));",
+        "  return 0; }"])
+    with tempfile.TemporaryDirectory() as d:
+        src, exe = os.path.join(d, "p.c"), os.path.join(d, "p")
+        with open(src, "w") as f:
+            f.write(probe)
+        subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), src, "-o", exe], check=True)
+        got = [int(v) for v in subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split()]
+    assert got == [ctypes.sizeof(K.Opts), ctypes.sizeof(K.Stats), K.Opts.leaf_k.offset, K.Stats.leaf_k.offset,
+                   K.Stats.heavy_partials.offset]
     with pytest.raises(K.K2TError):
         K.Tree(np.zeros(1, np.uint32), np.zeros(1, np.uint32), 8, 8, engine=4, cache_last_internal=1,
                band_rows=100)
@@ -212,10 +230,11 @@ def test_library_exports_every_declared_symbol():
 @pytest.mark.parametrize("heavy_terms", [0, 5, 30, 0xFFFFFFFF])
 def test_heavy_outputs_stats(heavy_terms):
     """Heavy outputs are those with more than heavy_terms non-zeros in the
-    input list (0 selects the default 2048); their tables take one bit per
-    leaf, two words per 32 outputs and one word per heavy output per
-    direction, plus, per heavy output of the wider side, max_batch x 32 fp32
-    partial sums (heavy_mode 0) or max_batch fp64 sums (heavy_mode 1)."""
+    input list (0 selects the default 160); their tables take one bit per
+    leaf, two words per 32 outputs, one word (list) and two words (record)
+    per heavy output per direction, plus max_batch fp32 words per partial sum
+    of the direction with more partial sums (heavy_mode 0) or max_batch fp64
+    sums per heavy output of the wider side (heavy_mode 1)."""
     rng = np.random.default_rng(21)
     nr, nc = 300, 200
     rows, cols, _ = synth.random_small(3, nr, nc, 0.05)
@@ -225,7 +244,7 @@ def test_heavy_outputs_stats(heavy_terms):
     cols = np.concatenate([cols, hub_c, np.full(120, 11, np.uint32)])
     t = K.Tree(rows, cols, nr, nc, heavy_terms=heavy_terms, max_batch=4)
     s = t.stats()
-    lim = 2048 if heavy_terms == 0 else heavy_terms
+    lim = 160 if heavy_terms == 0 else heavy_terms
     hr = int((np.bincount(rows, minlength=nr) > lim).sum()) if rows.size > lim else 0
     hc = int((np.bincount(cols, minlength=nc) > lim).sum()) if rows.size > lim else 0
     assert (s.heavy_rows, s.heavy_cols) == (hr, hc)
@@ -233,16 +252,20 @@ def test_heavy_outputs_stats(heavy_terms):
         assert hr > 1 and hc > 1
     if heavy_terms == 30:
         assert hr >= 1 and hc >= 1
+    if heavy_terms == 0:
+        assert hr == 1 and hc == 0   # the 150-entry hub row, with the random entries of row 7
     nl = int(s.level_nodes[s.levels - 1])
     want = 0
     for h, n in ((hr, nr), (hc, nc)):
         if h:
-            want += ((nl + 31) // 32 + 1) * 4 + 2 * ((n + 31) // 32) * 4 + 4 * h
+            want += ((nl + 31) // 32 + 1) * 4 + 2 * ((n + 31) // 32) * 4 + 4 * h + 8 * h
     tables = want
-    want = tables + max(hr, hc) * 4 * 32 * 4      # split mode: 32 fp32 partial sums per output
+    want = tables + max(s.heavy_partials[0], s.heavy_partials[1]) * 4 * 4
     assert s.heavy_kib == (want + 1023) // 1024
+    if hr:
+        assert s.heavy_partials[0] >= 2 * hr and 0 < s.heavy_max_terms[0] <= lim
     base = K.Tree(rows, cols, nr, nc, heavy_terms=0xFFFFFFFF, max_batch=4).workspace_bytes()
-    assert want <= t.workspace_bytes() - base <= want + 7 * 256
+    assert want <= t.workspace_bytes() - base <= want + 9 * 256
     f64 = K.Tree(rows, cols, nr, nc, heavy_terms=heavy_terms, heavy_mode=1, max_batch=4).stats()
     assert f64.heavy_kib == (tables + max(hr, hc) * 4 * 8 + 1023) // 1024   # fp64 mode: one double each
     with pytest.raises(K.K2TError):
@@ -277,11 +300,15 @@ def test_bench_traffic_follows_device_sources(monkeypatch):
     import bench
     table = bench.MEASURED_TRAFFIC
     monkeypatch.setitem(table, "digest", bench.device_digest())
-    monkeypatch.setitem(table, "wl", {"right B=1": 123})
-    assert bench.measured_traffic("wl", "right B=1") == 123
-    assert bench.measured_traffic("wl", "left B=1") is None
+    monkeypatch.setitem(table, "workload", "rmat24-bfs")
+    monkeypatch.setitem(table, "nnz", 1000)
+    monkeypatch.setitem(table, "bytes", {"right B=1": 123000})
+    # scaled by non-zeros to a workload of the same recipe
+    assert bench.measured_traffic("rmat27-bfs-1200M", 4000, "right B=1")[0] == 492000
+    assert bench.measured_traffic("rmat27-bfs-1200M", 4000, "left B=1")[0] is None
+    assert bench.measured_traffic("weblike22", 4000, "right B=1")[0] is None
     monkeypatch.setitem(table, "digest", "0" * 64)
-    assert bench.measured_traffic("wl", "right B=1") is None
+    assert bench.measured_traffic("rmat27-bfs-1200M", 4000, "right B=1")[0] is None
 
 
 def test_clustered_generator_shape():
@@ -322,3 +349,43 @@ def test_device_digest_ignores_comments_only():
     b = bench._code_only("int f(int x)\n{\n    return x + 1;\n}")
     c = bench._code_only("int f(int x) { return x + 2; }")
     assert a == b != c
+
+
+@pytest.mark.parametrize("leaf_k", [2, 4])
+def test_heavy_outputs_bounded_partials(leaf_k):
+    """Plus-times outputs with more than heavy_terms non-zeros (counted over
+    the input list) are heavy, and the builder splits each into fp32 partial
+    sums that receive at most heavy_terms terms: the largest count it found
+    is at most the limit, and the partials number at least the heavy terms
+    divided by the limit."""
+    rows, cols = synth.rmat(14, 0.57, 0.19, 0.19, 400000, 21)
+    n = 1 << 14
+    kw = dict(cache_last_internal=1, leaf_k=4) if leaf_k == 4 else {}
+    for limit in (160, 40):
+        t = K.Tree(rows, cols, n, n, heavy_terms=limit, **kw)
+        s = t.stats()
+        for d, ids in ((0, rows), (1, cols)):
+            cnt = np.bincount(ids, minlength=n)
+            heavy = cnt > limit
+            assert (s.heavy_rows, s.heavy_cols)[d] == int(heavy.sum())
+            assert s.heavy_fp64[d] == 0
+            assert 0 < s.heavy_max_terms[d] <= limit
+            assert s.heavy_partials[d] >= int(cnt[heavy].sum()) / limit
+    # fp64 mode: every heavy output has an fp64 slot and no partial sums
+    t = K.Tree(rows, cols, n, n, heavy_mode=1, **kw)
+    s = t.stats()
+    assert s.heavy_fp64[0] == s.heavy_rows > 0 and s.heavy_partials[0] == 0
+    # no heavy outputs at all
+    s = K.Tree(rows, cols, n, n, heavy_terms=0xffffffff, **kw).stats()
+    assert s.heavy_rows == s.heavy_cols == 0 and s.heavy_kib == 0
+
+
+def test_status_needs_upload():
+    """k2t_status on a tree that was never uploaded is out of order (no GPU
+    call is made)."""
+    rows, cols = synth.rmat(8, 0.57, 0.19, 0.19, 500, 42)
+    t = K.Tree(rows, cols, 256, 256)
+    with pytest.raises(K.K2TError) as e:
+        t.status()
+    assert e.value.status == -5
+    assert K.load().k2t_strerror(-7) == b"device-side wait ran out"

@@ -346,3 +346,38 @@ def test_medium_tree_matches_definition():
             _check_equal(semiring, a.y, b.y)
             if semiring == PLUS_TIMES:
                 assert np.allclose(a.scale, b.scale)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_band_parallel_descent_equals_serial(seed):
+    """The multicore descent (subtrees of one level grouped into row bands for
+    right products and column bands for left ones, bands shared among
+    threads) gives exactly the single-thread descent's result on every
+    semiring, at every band level and thread count: each output receives its
+    contributions in the same order, so even the fp64 plus-times sums and
+    their scales agree bit for bit, and a band never has two writers.  The
+    single-thread descent is itself pinned by brute force above."""
+    rng = np.random.default_rng(500 + seed)
+    nr, nc = int(rng.integers(300, 2000)), int(rng.integers(300, 2000))
+    rows, cols, _ = synth.random_small(50 + seed, nr, nc, 0.01)
+    hub = rng.integers(0, nr)
+    rows = np.concatenate([rows, np.full(nc // 2, hub, np.uint32)])
+    cols = np.concatenate([cols, rng.choice(nc, nc // 2, replace=False).astype(np.uint32)])
+    t = oracle.OracleTree(rows, cols, nr, nc, n_k4=seed % 2, leaf_k=4 if seed == 2 else 2)
+    for semiring, B in ((PLUS_TIMES, 3), (BOOLEAN, 32), (TROPICAL, 2)):
+        for d in (RIGHT, LEFT):
+            n_in = nc if d == RIGHT else nr
+            if semiring == BOOLEAN:
+                x = rng.integers(0, 2 ** 32, size=n_in, dtype=np.uint64).astype(np.uint32)
+            else:
+                x = rng.uniform(-3, 3, size=(n_in, B)).astype(np.float32)
+            want = t.spmv(d, semiring, x, B=B, w=0.75)
+            for level in (-1, 0, 2, t.levels - 2, t.levels - 1):
+                for th in (2, 5, 0):
+                    got = t.spmv(d, semiring, x, B=B, w=0.75, threads=th, band_level=level)
+                    assert got.cells == want.cells
+                    assert np.array_equal(np.ascontiguousarray(got.y).view(np.uint8),
+                                          np.ascontiguousarray(want.y).view(np.uint8)), (semiring, d, level, th)
+                    if semiring == PLUS_TIMES:
+                        assert np.array_equal(got.scale, want.scale)
+                    assert t.threads_used >= 1

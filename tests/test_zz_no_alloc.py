@@ -43,6 +43,19 @@ def _product(tree, fn, direction, semiring, x_np, B, n_in, n_out):
     return out.view(np.uint32) if semiring == oracle.BOOLEAN else out
 
 
+def _scribble(offsets):
+    """Run the allocation-free product on a tree of another shape (other
+    graph, other tile size, other offset source), so the static array holds
+    that tree's frontier coordinates and scan sums, not the ones the next
+    call needs."""
+    n = 1 << 13
+    r, c = synth.rmat(13, 0.45, 0.15, 0.15, 60000, 5)
+    other = K.Tree(r, c, n, n, engine=K.ENGINE_LEVELSYNC, offsets=1 - offsets, tile_m=64,
+                   host_top_max_nodes=16).upload()
+    x = np.random.default_rng(5).integers(0, 2 ** 32, size=n, dtype=np.uint64).astype(np.uint32)
+    _product(other, "spmv_noalloc", oracle.RIGHT, oracle.BOOLEAN, x, 32, n, n)
+
+
 @pytest.mark.parametrize("offsets", [0, 1])
 def test_noalloc_matches_spmv_twice(offsets):
     n = 1 << 14
@@ -57,6 +70,8 @@ def test_noalloc_matches_spmv_twice(offsets):
             ref = oracle.spmv_edges(rows, cols, n, n, direction, semiring, x, B=B)
             want = _product(tree, "spmv", direction, semiring, x, B, n, n)
             for call in range(2):
+                if call == 0:
+                    _scribble(offsets)
                 got = _product(tree, "spmv_noalloc", direction, semiring, x, B, n, n)
                 if semiring == oracle.PLUS_TIMES:
                     # both within the fp32 bound of the exact product
@@ -85,3 +100,10 @@ def test_noalloc_limits():
     fused = K.Tree(rows[:1000], cols[:1000], n, n).upload()
     assert lib.k2t_spmv_noalloc(fused.handle, 0, 0, ctypes.c_float(1.0), x.data_ptr(), y.data_ptr(), 1,
                                 None) == -5
+    # sizes past what the array holds are refused before any launch; a tree
+    # that fits still runs after the refusal
+    small = K.Tree(rows, cols, n, n, engine=K.ENGINE_LEVELSYNC, tile_m=1 << 16).upload()
+    assert small.stats().scratch_bytes <= limit
+    small.spmv_noalloc(0, 0, x, y)
+    torch.cuda.synchronize()
+    assert torch.isfinite(y).all()
