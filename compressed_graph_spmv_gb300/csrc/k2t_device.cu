@@ -48,39 +48,40 @@ __global__ void __launch_bounds__(256) fill_kernel(uint32_t *y, uint64_t words, 
 }
 
 // Heavy outputs of a plus-times product, one warp per output: output list[i]
-// of vector k receives its sum, rounded to fp32 once: its fp64 slot
-// acc64[slot * B + k], or its 2^bits fp32 partial sums acc[(first + p) * B + k]
-// added in fp64 (rec[i] = (first partial or slot, bits)).  The product sends
-// every term of such an output there, so y holds the fill's zero; adding it
-// keeps the result right even if it did not.
-__global__ void __launch_bounds__(256) heavy_finish_kernel(const float *acc, const double *acc64, const uint2 *rec,
+// of vector k receives its sum, rounded to fp32 once: the 2^bits fp32 partial
+// sums of its record (rows first .. first + 2^bits - 1 of acc) and its fp64
+// slot (the two rows after them, B doubles; for bits kHeavyFp64 the slot
+// alone), added in fp64.  The product sends every term of such an output
+// there, so y holds the fill's zero; adding it keeps the result right even if
+// it did not.
+__global__ void __launch_bounds__(256) heavy_finish_kernel(const float *acc, const uint32_t *hdir,
                                                            const uint32_t *list, uint32_t h, uint32_t B, float *y)
 {
     const uint32_t lane = threadIdx.x & 31u;
     const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x >> 5);
     for (uint64_t id = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); id < h; id += warps) {
-        const uint2 r = __ldg(rec + id);
-        float *yo = y + (uint64_t)__ldg(list + id) * B;
-        if (r.y == kHeavyFp64) {
-            const double *a = acc64 + (uint64_t)r.x * B;
-            for (uint32_t k = lane; k < B; k += 32u) yo[k] = __double2float_rn(a[k] + (double)yo[k]);
-            continue;
-        }
-        const uint64_t words = ((uint64_t)1 << r.y) * B;
-        const float *a = acc + (uint64_t)r.x * B;
+        const uint32_t o = __ldg(list + id);
+        const uint32_t rec = __ldg(hdir + o);
+        const uint32_t bits = rec & 31u;
+        const uint64_t first = rec >> 5;
+        const uint64_t parts = bits == kHeavyFp64 ? 0u : ((uint64_t)1 << bits);
+        const double *a64 = reinterpret_cast<const double *>(acc + (first + parts) * B);
+        float *yo = y + (uint64_t)o * B;
+        const uint64_t words = parts * B;
+        const float *a = acc + first * B;
         if (32u % B == 0) {
             // lane l always reads slice l % B: sum, then fold the lanes of one slice
             double s = 0.0;
             for (uint64_t e = lane; e < words; e += 32u) s += (double)a[e];
-            for (uint32_t o = 16; o >= B; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            if (lane < B) yo[lane] = __double2float_rn(s + (double)yo[lane]);
+            for (uint32_t f = 16; f >= B; f >>= 1) s += __shfl_xor_sync(0xffffffffu, s, f);
+            if (lane < B) yo[lane] = __double2float_rn(s + a64[lane] + (double)yo[lane]);
         } else {
             for (uint32_t k = 0; k < B; ++k) {
                 double s = 0.0;
                 for (uint64_t e = k + (uint64_t)lane * B; e < words; e += 32ull * B) s += (double)a[e];
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                if (lane == 0) yo[k] = __double2float_rn(s + (double)yo[k]);
+                for (int f = 16; f > 0; f >>= 1) s += __shfl_xor_sync(0xffffffffu, s, f);
+                if (lane == 0) yo[k] = __double2float_rn(s + a64[k] + (double)yo[k]);
             }
         }
     }
@@ -240,13 +241,6 @@ LaunchFn pick(uint32_t engine, int semiring, int dir, int vw)
     return pick_min_plus(engine, dir, vw);
 }
 
-// The CACHED engine runs fp32 batches of at least opts.coop_batch vectors
-// with one directory block per thread block (cached_coop_kernel).
-bool coop_batches(const k2t_tree *t, int semiring, uint32_t B)
-{
-    return semiring != K2T_BOOLEAN && B >= t->opts.coop_batch;
-}
-
 // Queue a whole product (fill + engine) on `st`.
 int enqueue_product(k2t_tree *t, int32_t dir, int32_t semiring, float w, const void *x, void *y, uint32_t B,
                     cudaStream_t st, cudaEvent_t marker)
@@ -277,8 +271,8 @@ int enqueue_product(k2t_tree *t, int32_t dir, int32_t semiring, float w, const v
     va.n_out = n_out;
     va.n_in = dir == K2T_RIGHT ? t->n_cols : t->n_rows;
     const bool heavy = heavy_begin(t, d, dir, semiring, va, st);
-    uint32_t engine = t->leaf_k4 ? kEngineCached4 : t->engine;
-    if (engine == K2T_ENGINE_CACHED && coop_batches(t, semiring, B)) engine = kEngineCachedCoop;
+    uint32_t engine = t->engine;
+    if (engine == K2T_ENGINE_CACHED && t->leaf_k4) engine = kEngineCached4;
     pick(engine, semiring, dir, vw)(t, d, va, st);
     if (heavy) heavy_end(t, d, dir, va, st);
     return K2T_OK;
@@ -353,16 +347,13 @@ int k2t_upload(k2t_tree *t, void *arena, uint64_t arena_bytes, void *stream)
     for (int dd = 0; dd < 2; ++dd) {
         if (!L.hflag_bytes[dd]) continue;
         d->hflag[dd] = at<uint32_t>(d->arena, L.hflag_off[dd]);
-        d->hent[dd] = at<uint32_t>(d->arena, L.hent_off[dd]);
+        d->hdir[dd] = at<uint32_t>(d->arena, L.hdir_off[dd]);
         d->hlist[dd] = at<uint32_t>(d->arena, L.hlist_off[dd]);
-        d->hrec[dd] = at<uint2>(d->arena, L.hrec_off[dd]);
-        if ((e = put(L.hrec_off[dd], L.hrec_bytes[dd], t->hrec[dd].data()))) return fail(e);
         if ((e = put(L.hflag_off[dd], L.hflag_bytes[dd], t->hflag[dd].data()))) return fail(e);
-        if ((e = put(L.hent_off[dd], L.hent_bytes[dd], t->hent[dd].data()))) return fail(e);
+        if ((e = put(L.hdir_off[dd], L.hdir_bytes[dd], t->hdir[dd].data()))) return fail(e);
         if ((e = put(L.hlist_off[dd], L.hlist_bytes[dd], t->hlist[dd].data()))) return fail(e);
     }
     if (L.acc_bytes) d->acc = at<float>(d->arena, L.acc_off);
-    if (L.acc64_bytes) d->acc64 = at<double>(d->arena, L.acc64_off);
     if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return fail(e);
     return K2T_OK;
 }

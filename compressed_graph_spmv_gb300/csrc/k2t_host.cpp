@@ -439,28 +439,26 @@ void plan_bands(k2t_tree *t, int nt)
 
 // Heavy plus-times outputs of one direction: those with more than `limit`
 // non-zeros (counted over the input list: a repeated pair counts each time,
-// so a count never falls short).  Fills the ascending list, the per-32 table
-// (mask of heavy outputs, heavy outputs before the group) and one record per
-// heavy output saying where its terms are summed:
-//   - mode 1: in fp64 (slot = its index in the list);
-//   - mode 0: in 2^bits fp32 partial sums, a term going to partial
-//     heavy_partial(first input of its leaf, bits).  The builder counts the
-//     terms every partial receives and raises bits until none holds more
+// so a count never falls short).  Fills the ascending list and the record of
+// every output up to the last heavy one (0 for the others), which says where
+// its terms are summed, in rows of max_batch fp32 words:
+//   - mode 1: in an fp64 slot of two rows (record bits kHeavyFp64);
+//   - mode 0: in 2^bits rows of fp32 partial sums, a term going to partial
+//     heavy_partial(its leaf's first input, bits), then the two rows of an
+//     fp64 slot (where warp windows hand over fp64 sums).  The builder counts
+//     the terms every partial receives and raises bits until none holds more
 //     than `limit`, so every fp32 sum the product forms, in whatever order
 //     its atomics land, has at most `limit` terms.  An output whose inputs
 //     still crowd one partial at kHeavyMaxBits (only possible for adversarial
-//     or heavily repeated input) is summed in fp64.
-// out_ids/in_ids: the output and input index of every input pair; side: 2
-// or 4 (leaf side; a leaf's first input is in & ~(side - 1)).
+//     or repeated input) is summed in its fp64 slot alone.
+// out_ids/in_ids: the output and input index of every input pair.
 void heavy_outputs(const uint32_t *out_ids, const uint32_t *in_ids, uint64_t nnz, uint64_t n, uint32_t limit,
-                   uint32_t side, uint32_t mode, int nt, k2t_tree *t, int dir)
+                   uint32_t mode, int nt, k2t_tree *t, int dir)
 {
-    std::vector<uint32_t> &list = t->hlist[dir], &ent = t->hent[dir], &rec = t->hrec[dir];
+    std::vector<uint32_t> &list = t->hlist[dir], &hdir = t->hdir[dir];
     list.clear();
-    ent.clear();
-    rec.clear();
-    t->hparts[dir] = 0;
-    t->hfp64[dir] = 0;
+    hdir.clear();
+    t->hrows[dir] = t->hparts[dir] = t->hfp64[dir] = 0;
     t->hmax_part[dir] = 0;
     if (limit == 0xffffffffu || nnz <= limit) return;
     // saturating counts: a thread adds only below kSat, so nt racing adds stay below 2^32
@@ -476,86 +474,70 @@ void heavy_outputs(const uint32_t *out_ids, const uint32_t *in_ids, uint64_t nnz
     for (uint64_t i = 0; i < n; ++i)
         if (cnt[i] > limit) list.push_back((uint32_t)i);
     if (list.empty()) return;
-    const uint64_t groups = (n + 31) / 32;
-    ent.assign(2 * groups, 0);
-    for (uint32_t v : list) ent[2 * (v / 32)] |= 1u << (v % 32);
-    uint32_t run = 0;
-    for (uint64_t g = 0; g < groups; ++g) {
-        ent[2 * g + 1] = run;
-        run += (uint32_t)popc64(ent[2 * g]);
-    }
     const size_t h = list.size();
-    rec.assign(2 * h, 0);
-    if (mode == 1) {
+    // records cover every output up to the last heavy one, plus room for the
+    // 16-byte read of a 4x4 leaf's four outputs
+    hdir.assign(((uint64_t)list.back() + 1 + 3) / 4 * 4 + 4, 0);
+    std::vector<uint32_t> bits(h, kHeavyFp64);
+    if (mode == 0) {
+        // ids during the count: hdir[o] = id + 1
+        for (size_t id = 0; id < h; ++id) hdir[list[id]] = (uint32_t)id + 1;
+        // first guess: a mean of at most limit / 1.5 terms per partial
         for (size_t id = 0; id < h; ++id) {
-            rec[2 * id] = (uint32_t)id;
-            rec[2 * id + 1] = kHeavyFp64;
+            const double want = 1.5 * (double)cnt[list[id]] / (double)limit;
+            uint32_t b = 1;
+            while (b < kHeavyMaxBits && (double)(1u << b) < want) ++b;
+            bits[id] = b;
         }
-        t->hfp64[dir] = h;
-        return;
-    }
-    auto heavy_id = [&](uint32_t o) -> int64_t {
-        const uint32_t m = ent[2 * (o / 32)], sh = o % 32;
-        if (!((m >> sh) & 1u)) return -1;
-        return (int64_t)ent[2 * (o / 32) + 1] + popc64(m & ((1u << sh) - 1u));
-    };
-    // first guess: a mean of at most limit / 1.5 terms per partial
-    std::vector<uint32_t> bits(h);
-    for (size_t id = 0; id < h; ++id) {
-        const double want = 1.5 * (double)cnt[list[id]] / (double)limit;
-        uint32_t b = 1;
-        while (b < kHeavyMaxBits && (double)(1u << b) < want) ++b;
-        bits[id] = b;
-    }
-    std::vector<uint32_t>().swap(cnt);
-    const uint32_t in_mask = ~(side - 1u);
-    std::vector<uint8_t> todo(h, 1);
-    bool any = true;
-    while (any) {
-        // count the terms of every partial of the outputs still to check
-        std::vector<uint64_t> base(h, 0);
-        uint64_t total = 0;
-        for (size_t id = 0; id < h; ++id)
-            if (todo[id]) { base[id] = total; total += 1ull << bits[id]; }
-        std::vector<uint32_t> pc(total, 0);
-        parallel_for(nt, [&](int th) {
-            uint64_t lo = nnz * th / nt, hi = nnz * (th + 1) / nt;
-            for (uint64_t i = lo; i < hi; ++i) {
-                const int64_t id = heavy_id(out_ids[i]);
-                if (id < 0 || !todo[(size_t)id]) continue;
-                bump(pc.data() + base[(size_t)id] + heavy_partial(in_ids[i] & in_mask, bits[(size_t)id]));
-            }
-        });
-        any = false;
-        for (size_t id = 0; id < h; ++id) {
-            if (!todo[id]) continue;
-            uint32_t mx = 0;
-            for (uint64_t q = 0; q < (1ull << bits[id]); ++q) mx = std::max(mx, pc[base[id] + q]);
-            if (mx <= limit) {
-                todo[id] = 0;
-                t->hmax_part[dir] = std::max(t->hmax_part[dir], mx);
-            } else if (bits[id] < kHeavyMaxBits) {
-                ++bits[id];
-                any = true;
-            } else {
-                todo[id] = 0;
-                bits[id] = kHeavyFp64;
+        std::vector<uint8_t> todo(h, 1);
+        bool any = true;
+        while (any) {
+            // count the terms of every partial of the outputs still to check
+            std::vector<uint64_t> base(h, 0);
+            uint64_t total = 0;
+            for (size_t id = 0; id < h; ++id)
+                if (todo[id]) { base[id] = total; total += 1ull << bits[id]; }
+            std::vector<uint32_t> pc(total, 0);
+            parallel_for(nt, [&](int th) {
+                uint64_t lo = nnz * th / nt, hi = nnz * (th + 1) / nt;
+                for (uint64_t i = lo; i < hi; ++i) {
+                    const uint32_t o = out_ids[i];
+                    if (o >= hdir.size() || !hdir[o]) continue;
+                    const size_t id = hdir[o] - 1;
+                    if (!todo[id]) continue;
+                    bump(pc.data() + base[id] + heavy_partial(in_ids[i], bits[id]));
+                }
+            });
+            any = false;
+            for (size_t id = 0; id < h; ++id) {
+                if (!todo[id]) continue;
+                uint32_t mx = 0;
+                for (uint64_t q = 0; q < (1ull << bits[id]); ++q) mx = std::max(mx, pc[base[id] + q]);
+                if (mx <= limit) {
+                    todo[id] = 0;
+                    t->hmax_part[dir] = std::max(t->hmax_part[dir], mx);
+                } else if (bits[id] < kHeavyMaxBits) {
+                    ++bits[id];
+                    any = true;
+                } else {
+                    todo[id] = 0;
+                    bits[id] = kHeavyFp64;
+                }
             }
         }
     }
-    uint64_t parts = 0, slots = 0;
+    // rows: the fp32 partial sums, then two rows (B doubles) of fp64 slot; the
+    // first row of every output is even, so every slot is 8-byte aligned
+    uint64_t rows = 0;
     for (size_t id = 0; id < h; ++id) {
-        if (bits[id] == kHeavyFp64) {
-            rec[2 * id] = (uint32_t)slots++;
-        } else {
-            if (parts > 0xffffffffull - (1ull << bits[id])) throw std::length_error("heavy partial sums");
-            rec[2 * id] = (uint32_t)parts;
-            parts += 1ull << bits[id];
-        }
-        rec[2 * id + 1] = bits[id];
+        const uint64_t parts = bits[id] == kHeavyFp64 ? 0 : (1ull << bits[id]);
+        if (rows + parts + 2 > kHeavyMaxRows) throw std::length_error("heavy partial sums");
+        hdir[list[id]] = (uint32_t)(rows << 5) | bits[id];
+        rows += parts + 2;
+        t->hparts[dir] += parts;
+        t->hfp64[dir] += parts ? 0 : 1;
     }
-    t->hparts[dir] = parts;
-    t->hfp64[dir] = slots;
+    t->hrows[dir] = rows;
 }
 
 // Leaf flags of one direction: bit i set when leaf i (level order; block
@@ -563,8 +545,8 @@ void heavy_outputs(const uint32_t *out_ids, const uint32_t *in_ids, uint64_t nnz
 // (dir 0) or columns (dir 1).  prefixes[i] is leaf i's path prefix.
 void heavy_leaf_flags(k2t_tree *t, int dir, const uint64_t *prefixes, uint64_t nl, int nt)
 {
-    const std::vector<uint32_t> &ent = t->hent[dir];
-    const uint32_t side = t->leaf_k4 ? 4u : 2u, mask = t->leaf_k4 ? 15u : 3u;
+    const std::vector<uint32_t> &hdir = t->hdir[dir];
+    const uint32_t side = t->leaf_k4 ? 4u : 2u;
     std::vector<uint32_t> &fl = t->hflag[dir];
     fl.assign((nl + 31) / 32 + 1, 0);
     const int d = t->levels - 1;
@@ -575,9 +557,9 @@ void heavy_leaf_flags(k2t_tree *t, int dir, const uint64_t *prefixes, uint64_t n
             uint32_t v = 0;
             for (uint64_t i = 32 * w; i < std::min<uint64_t>(32 * w + 32, nl); ++i) {
                 Coord q = prefix_coord(prefixes[i], d, t->n_k4);
-                // the leaf's outputs o .. o + side - 1 share a group of 32 (o is a multiple of the side)
                 uint64_t o = (uint64_t)side * (dir == 0 ? q.r : q.c);
-                if (((ent[2 * (o / 32)] >> (o % 32)) & mask) != 0) v |= 1u << (i % 32);
+                for (uint32_t k = 0; k < side; ++k)
+                    if (o + k < hdir.size() && hdir[o + k]) { v |= 1u << (i % 32); break; }
             }
             fl[w] = v;
         }
@@ -659,27 +641,20 @@ void compute_layout(k2t_tree *t)
         }
     }
     if (!t->empty) {
-        uint64_t parts = 0, slots = 0;
+        uint64_t rows = 0;
         for (int dd = 0; dd < 2; ++dd) {
             if (t->hlist[dd].empty()) continue;
             L.hflag_bytes[dd] = t->hflag[dd].size() * sizeof(uint32_t);
             L.hflag_off[dd] = take(L.hflag_bytes[dd]);
-            L.hent_bytes[dd] = t->hent[dd].size() * sizeof(uint32_t);
-            L.hent_off[dd] = take(L.hent_bytes[dd]);
+            L.hdir_bytes[dd] = t->hdir[dd].size() * sizeof(uint32_t);
+            L.hdir_off[dd] = take(L.hdir_bytes[dd]);
             L.hlist_bytes[dd] = t->hlist[dd].size() * sizeof(uint32_t);
             L.hlist_off[dd] = take(L.hlist_bytes[dd]);
-            L.hrec_bytes[dd] = t->hrec[dd].size() * sizeof(uint32_t);
-            L.hrec_off[dd] = take(L.hrec_bytes[dd]);
-            parts = std::max(parts, t->hparts[dd]);
-            slots = std::max(slots, t->hfp64[dd]);
+            rows = std::max(rows, t->hrows[dd]);
         }
-        if (parts) {
-            L.acc_bytes = parts * (uint64_t)t->opts.max_batch * sizeof(float);
+        if (rows) {
+            L.acc_bytes = rows * (uint64_t)t->opts.max_batch * sizeof(float);
             L.acc_off = take(L.acc_bytes);
-        }
-        if (slots) {
-            L.acc64_bytes = slots * (uint64_t)t->opts.max_batch * sizeof(double);
-            L.acc64_off = take(L.acc64_bytes);
         }
     }
     if (t->opts.host_vectors) {
@@ -715,8 +690,7 @@ void k2t_default_opts(k2t_opts *o)
     o->band_rows = 4096;
     o->band_cols = 1u << 23;
     o->heavy_terms = kDefaultHeavyTerms;
-    o->leaf_k = 2;
-    o->coop_batch = 8;
+    o->leaf_k = 0;
 }
 
 int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
@@ -733,19 +707,17 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
     if (o.band_cols && (o.band_cols < 16 || (o.band_cols & (o.band_cols - 1)))) return K2T_EINVAL;
     if (!o.band_cols) o.band_cols = 1u << 31;
     if (!o.heavy_terms) o.heavy_terms = kDefaultHeavyTerms;
-    if (!o.leaf_k) o.leaf_k = 2;
-    if (!o.coop_batch) o.coop_batch = 8;
     if (o.heavy_mode > 1) return K2T_EINVAL;
-    if (o.leaf_k != 2 && o.leaf_k != 4) return K2T_EINVAL;
+    if (o.leaf_k != 0 && o.leaf_k != 2 && o.leaf_k != 4) return K2T_EINVAL;
     if (o.chunk_cap < 4 || o.chunk_cap > kMaxChunkCap || o.tile_m < 4) return K2T_EINVAL;
     if (o.max_batch < 1 || o.max_batch > K2T_MAX_BATCH) return K2T_ERANGE;
     if (o.host_top_max_nodes < 1) return K2T_EINVAL;
     if (o.n_k4_levels > 15) return K2T_EINVAL;
     if (n_rows > (1ull << 32) || n_cols > (1ull << 32)) return K2T_ERANGE;
     if ((o.engine == K2T_ENGINE_CACHED || o.engine == K2T_ENGINE_BANDED) && !o.cache_last_internal) return K2T_EINVAL;
-    // 4x4 leaves: the CACHED engine only
-    if (o.leaf_k == 4 && (!o.cache_last_internal || (o.engine != K2T_ENGINE_AUTO && o.engine != K2T_ENGINE_CACHED)))
-        return K2T_EINVAL;
+    // 4x4 leaves: the CACHED and FUSED engines
+    const bool leaf4_ok = o.engine == K2T_ENGINE_AUTO || o.engine == K2T_ENGINE_CACHED || o.engine == K2T_ENGINE_FUSED;
+    if (o.leaf_k == 4 && !leaf4_ok) return K2T_EINVAL;
 
     k2t_tree *t = new (std::nothrow) k2t_tree;
     if (!t) return K2T_ENOMEM;
@@ -754,17 +726,11 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
         t->n_rows = n_rows;
         t->n_cols = n_cols;
         uint64_t n = std::max(n_rows, n_cols);
-        int bits = 0;
-        while ((1ull << bits) < n) ++bits;
-        bits = std::max(bits, 2);
-        const int leaf_k4 = o.leaf_k == 4 ? 1 : 0;
-        bits = std::max(bits, 2 * (int)o.n_k4_levels + 2 + leaf_k4);
-        if (bits > 32) { delete t; return K2T_ERANGE; }
-        t->dim_bits = bits;
+        int bits0 = 0;
+        while ((1ull << bits0) < n) ++bits0;
+        bits0 = std::max(bits0, 2);
+        if (std::max(bits0, 2 * (int)o.n_k4_levels + 2 + (o.leaf_k == 4 ? 1 : 0)) > 32) { delete t; return K2T_ERANGE; }
         t->n_k4 = (int)o.n_k4_levels;
-        t->leaf_k4 = leaf_k4;
-        t->levels = bits - t->n_k4 - leaf_k4;
-        const int l = t->levels;
         const int nt = thread_count(o);
         t->engine = o.engine == K2T_ENGINE_AUTO
                         ? (o.cache_last_internal ? K2T_ENGINE_CACHED : K2T_ENGINE_FUSED)
@@ -778,34 +744,65 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
                 if (rows[i] >= n_rows || cols[i] >= n_cols) { bad[(size_t)th] = 1; break; }
         });
         for (int b : bad) if (b) { delete t; return K2T_ERANGE; }
-        heavy_outputs(rows, cols, nnz, n_rows, o.heavy_terms, 2u << leaf_k4, o.heavy_mode, nt, t, 0);
-        heavy_outputs(cols, rows, nnz, n_cols, o.heavy_terms, 2u << leaf_k4, o.heavy_mode, nt, t, 1);
+
+        // Sorted distinct path keys of the cells for a leaf side.  With
+        // leaf_k 0 the side is chosen here: 4x4 leaves when the 2x2 leaves
+        // would hold at least kAutoLeaf4Density non-zeros each on average
+        // (the measured break-even of the two leaf sizes), 2x2 otherwise.
+        std::vector<uint64_t> keys(nnz), tmp;
+        int leaf_k4 = o.leaf_k == 4 ? 1 : 0, bits = 0;
+        size_t m = 0;
+        auto make_keys = [&](int l4) {
+            bits = std::max(bits0, 2 * (int)o.n_k4_levels + 2 + l4);
+            keys.resize(nnz);
+            parallel_for(nt, [&](int th) {
+                uint64_t lo = nnz * th / nt, hi = nnz * (th + 1) / nt;
+                for (uint64_t i = lo; i < hi; ++i) keys[i] = path_key(rows[i], cols[i], bits, t->n_k4, l4);
+            });
+            radix_sort(keys, tmp, 2 * bits, nt);
+            tmp.resize(keys.size());
+            m = unique_into(keys.data(), keys.size(), tmp.data(), nt);
+            keys.swap(tmp);
+            keys.resize(m);
+            tmp.resize(m);
+        };
+        make_keys(leaf_k4);
+        if (o.leaf_k == 0 && leaf4_ok && m > 0 && 2 * (int)o.n_k4_levels + 3 <= 32) {
+            // distinct 2x2 leaves: keys that differ above the leaf-cell digit
+            std::vector<uint64_t> part((size_t)nt, 0);
+            parallel_for(nt, [&](int th) {
+                size_t lo = m * th / nt, hi = m * (th + 1) / nt;
+                uint64_t c = 0;
+                for (size_t i = lo; i < hi; ++i) c += (i == 0 || (keys[i] >> 2) != (keys[i - 1] >> 2)) ? 1 : 0;
+                part[(size_t)th] = c;
+            });
+            uint64_t leaves = 0;
+            for (uint64_t c : part) leaves += c;
+            if ((double)m >= kAutoLeaf4Density * (double)leaves) {
+                leaf_k4 = 1;
+                make_keys(1);
+            }
+        }
+        t->opts.leaf_k = leaf_k4 ? 4u : 2u;
+        t->dim_bits = bits;
+        t->leaf_k4 = leaf_k4;
+        t->levels = bits - t->n_k4 - leaf_k4;
+        const int l = t->levels;
+        heavy_outputs(rows, cols, nnz, n_rows, o.heavy_terms, o.heavy_mode, nt, t, 0);
+        heavy_outputs(cols, rows, nnz, n_cols, o.heavy_terms, o.heavy_mode, nt, t, 1);
         for (int dd = 0; dd < 2; ++dd)
             if (t->hlist[dd].size() >= (1u << 28)) { delete t; return K2T_ERANGE; }
 
         t->nodes.assign((size_t)l, 0);
         t->sig.assign((size_t)l, std::vector<uint64_t>());
-
-        std::vector<uint64_t> keys(nnz), tmp;
-        parallel_for(nt, [&](int th) {
-            uint64_t lo = nnz * th / nt, hi = nnz * (th + 1) / nt;
-            for (uint64_t i = lo; i < hi; ++i) keys[i] = path_key(rows[i], cols[i], bits, t->n_k4, t->leaf_k4);
-        });
-        radix_sort(keys, tmp, 2 * bits, nt);
-        tmp.resize(keys.size());
-        size_t m = unique_into(keys.data(), keys.size(), tmp.data(), nt);
-        keys.swap(tmp);
-        keys.resize(m);
-        tmp.resize(m);
         t->nnz = m;
 
         if (m == 0) {
             t->empty = true;
             for (int dd = 0; dd < 2; ++dd) {
                 t->hlist[dd].clear();
-                t->hent[dd].clear();
-                t->hrec[dd].clear();
-                t->hparts[dd] = t->hfp64[dd] = 0;
+                t->hdir[dd].clear();
+                t->hrows[dd] = t->hparts[dd] = t->hfp64[dd] = 0;
             }
             t->nodes[0] = 1;
             t->sig[0].assign(2, 0);
@@ -968,8 +965,8 @@ int k2t_stats_get(const k2t_tree *t, k2t_stats *s)
     s->uploaded = t->dev != nullptr;
     s->heavy_rows = (uint32_t)t->hlist[0].size();
     s->heavy_cols = (uint32_t)t->hlist[1].size();
-    uint64_t hb = L.acc_bytes + L.acc64_bytes;
-    for (int dd = 0; dd < 2; ++dd) hb += L.hflag_bytes[dd] + L.hent_bytes[dd] + L.hlist_bytes[dd] + L.hrec_bytes[dd];
+    uint64_t hb = L.acc_bytes;
+    for (int dd = 0; dd < 2; ++dd) hb += L.hflag_bytes[dd] + L.hdir_bytes[dd] + L.hlist_bytes[dd];
     s->heavy_kib = (uint32_t)((hb + 1023) / 1024);
     s->leaf_k = t->leaf_k4 ? 4u : 2u;
     for (int dd = 0; dd < 2; ++dd) {

@@ -13,14 +13,20 @@ constexpr uint32_t kDirS = 256;        // directory sample period (section 3.2: 
 constexpr uint32_t kMaxChunkCap = 4096;
 constexpr uint32_t kArenaAlign = 256;
 constexpr uint32_t kBandChunkNodes = 16384;  // BANDED: nodes per thread block at most
+// leaf_k 0 (automatic): 4x4 leaves when 2x2 leaves would average at least this
+// many non-zeros (measured: 1.0-1.04 per 2x2 leaf favours 2x2, 2.1 favours 4x4)
+constexpr double kAutoLeaf4Density = 1.75;
 // Heavy plus-times outputs (more non-zeros than one fp32 sum may hold within
 // the bound |y - y_ref| <= 1e-5 * sum|w x| + 1e-6): each is summed in 2^bits
 // fp32 partial sums, a term going to the partial that a multiplicative hash
-// of its leaf's first input picks, or in fp64 (record bits = kHeavyFp64).
+// of its leaf's first input picks, plus an fp64 slot; or in the fp64 slot
+// alone (bits = kHeavyFp64).  Its record (one uint32 per output, 0 for the
+// others) is (first row << 5) | bits, rows of max_batch fp32 words.
 constexpr uint32_t kDefaultHeavyTerms = 160;
 constexpr uint32_t kHeavyHash = 2654435761u;
-constexpr uint32_t kHeavyFp64 = 0xffu;
+constexpr uint32_t kHeavyFp64 = 31u;
 constexpr uint32_t kHeavyMaxBits = 22;
+constexpr uint64_t kHeavyMaxRows = 1ull << 27;   // rows a record can address
 
 #ifdef __CUDACC__
 #define K2T_HD __host__ __device__
@@ -30,9 +36,17 @@ constexpr uint32_t kHeavyMaxBits = 22;
 
 // Partial sum (of 2^bits, 1 <= bits <= 31) of a heavy output that the terms of
 // a leaf whose first input (column for right products, row for left ones) is
-// `in` go to: the top bits of in * kHeavyHash.  The builder counts the terms
-// of every partial with this function, the kernels route with it.
-K2T_HD inline uint32_t heavy_partial(uint32_t in, uint32_t bits) { return (in * kHeavyHash) >> (32u - bits); }
+// `in` go to: the top bits of run * kHeavyHash, run = in >> kHeavyRunBits.
+// The inputs of one aligned run of 32 (a leaf never straddles two) share a
+// partial, so the terms a warp meets close together in Z-order land on few
+// partial sums, while the hash spreads the runs over all of them.  The builder
+// counts the terms of every partial with this function, the kernels route
+// with it.
+constexpr uint32_t kHeavyRunBits = 5;
+K2T_HD inline uint32_t heavy_partial(uint32_t in, uint32_t bits)
+{
+    return ((in >> kHeavyRunBits) * kHeavyHash) >> (32u - bits);
+}
 
 // Coordinates of a node's block, in units of the block side at its level.
 // A frontier entry: (row, col) instead of the pages' Morton code; the two
@@ -73,11 +87,9 @@ struct ArenaLayout {
     uint64_t vec_off[2], vec_bytes;     // host-product x and y
     // heavy outputs of plus-times products, per direction (0 right, 1 left)
     uint64_t hflag_off[2], hflag_bytes[2];  // one bit per leaf: touches a heavy output
-    uint64_t hent_off[2], hent_bytes[2];    // per 32 outputs: (heavy bits, heavy outputs before)
+    uint64_t hdir_off[2], hdir_bytes[2];    // per output up to the last heavy one: its record
     uint64_t hlist_off[2], hlist_bytes[2];  // the heavy outputs, ascending
-    uint64_t hrec_off[2], hrec_bytes[2];    // per heavy output: (first partial or fp64 slot, bits)
-    uint64_t acc_off, acc_bytes;            // fp32 partial sums [partial][B], shared by both directions
-    uint64_t acc64_off, acc64_bytes;        // fp64 sums [slot][B], shared by both directions
+    uint64_t acc_off, acc_bytes;            // rows of the heavy sums, shared by both directions
     uint64_t total;
 };
 
@@ -117,12 +129,11 @@ struct k2t_tree {
     // Heavy plus-times outputs (more than opts.heavy_terms non-zeros),
     // per direction (0: rows, outputs of right products; 1: columns):
     std::vector<uint32_t> hlist[2];   // the outputs, ascending
-    std::vector<uint32_t> hent[2];    // per group of 32 outputs: bit mask, then the count before it
     std::vector<uint32_t> hflag[2];   // bit j: leaf j (level order) has a heavy output
-    std::vector<uint32_t> hrec[2];    // per heavy output: first partial sum (or fp64 slot), then bits
-                                      // (2^bits fp32 partial sums, or kHeavyFp64)
+    std::vector<uint32_t> hdir[2];    // record of every output below the last heavy one + padding
+    uint64_t hrows[2] = {0, 0};       // accumulator rows of the direction
     uint64_t hparts[2] = {0, 0};      // fp32 partial sums of the direction
-    uint64_t hfp64[2] = {0, 0};       // outputs of the direction summed in fp64
+    uint64_t hfp64[2] = {0, 0};       // outputs of the direction summed in fp64 alone
     uint32_t hmax_part[2] = {0, 0};   // largest term count of one fp32 partial sum
     k2t::ArenaLayout layout{};
     k2t::DeviceState *dev = nullptr;

@@ -37,10 +37,9 @@ struct VecArgs {
     uint64_t n_in;   // entries (vertices) of x
     // Heavy plus-times outputs (null hflag: none in this product)
     const uint32_t *hflag;  // bit j: leaf j (level order) has a heavy output
-    const uint32_t *hent;   // per 32 outputs: mask of such outputs, their count before the group
-    const uint2 *hrec;      // per heavy output: (first partial sum or fp64 slot, bits)
-    float *acc;             // fp32 partial sums [partial][B]
-    double *acc64;          // fp64 sums [slot][B]
+    const uint32_t *hdir;   // per output below hdir_len: its record (heavy_record), 0 if not heavy
+    uint32_t hdir_len;
+    float *acc;             // rows of B fp32 words: partial sums and fp64 slots of heavy outputs
 };
 
 __device__ __forceinline__ uint32_t nibble_at(const uint8_t *sig, uint32_t t)
@@ -143,54 +142,57 @@ __device__ __forceinline__ bool is_noop_word(uint32_t v)
 
 // ---- heavy outputs (plus-times) ------------------------------------------------
 // An output with more non-zeros than one fp32 sum can take within the bound
-// is "heavy": summed in fp32 partial sums of bounded size or in fp64, never
-// in a warp window (a window's sum of an output would mix partial sums).
-// heavy_leaf: leaf li has such an output.  heavy_word: for the outputs out
-// (even) and out + 1 of a leaf, (id << 2) | mask, where mask bit q is set when
-// out + q is heavy and id is out's index in the heavy list (out + 1 has
-// id + (mask & 1)); 0 when neither is.
+// is "heavy".  Its record (heavy_record, built once per tree) names rows of
+// the accumulator array acc (B fp32 words a row): 2^bits fp32 partial sums,
+// each receiving at most heavy_terms terms, then an fp64 slot of two rows (B
+// doubles) for the sums fp64 warp windows hand over; or, bits kHeavyFp64, the
+// fp64 slot alone, which then takes every term.  heavy_leaf: leaf li has a
+// heavy output.  heavy_word: the records of a 2x2 leaf's outputs out (even)
+// and out + 1, read together (one 8-byte load); only called for flagged
+// leaves, whose outputs lie below hdir_len.
 __device__ __forceinline__ uint32_t heavy_leaf(const VecArgs &va, uint32_t li)
 {
     return (__ldg(va.hflag + (li >> 5)) >> (li & 31u)) & 1u;
 }
 
-__device__ __forceinline__ uint32_t heavy_word(const VecArgs &va, uint32_t out)
+__device__ __forceinline__ uint2 heavy_word(const VecArgs &va, uint32_t out)
 {
-    const uint2 e = __ldg(reinterpret_cast<const uint2 *>(va.hent) + (out >> 5));
-    const uint32_t sh = out & 31u;
-    const uint32_t m = (e.x >> sh) & 3u;
-    if (!m) return 0u;
-    return ((e.y + (uint32_t)__popc(e.x & ((1u << sh) - 1u))) << 2) | m;
+    return __ldg(reinterpret_cast<const uint2 *>(va.hdir + out));
 }
 
-// Index in the heavy list of output out + q of a 2x2 leaf (hv from heavy_word).
-__device__ __forceinline__ uint32_t heavy_id2(uint32_t hv, int q) { return (hv >> 2) + (q ? (hv & 1u) : 0u); }
+// fp64 slot (B doubles) of a heavy output's record.
+__device__ __forceinline__ double *heavy_slot64(const VecArgs &va, uint32_t rec)
+{
+    const uint32_t bits = rec & 31u;
+    const size_t row = (size_t)(rec >> 5) + (bits == kHeavyFp64 ? 0u : (1u << bits));
+    return reinterpret_cast<double *>(va.acc + row * va.B);
+}
 
-// Where heavy output `id` (slice k) sums the terms of a leaf with first input
-// `in`: the fp32 partial sum heavy_partial(in, bits) of its record, or (null
-// p32) its fp64 slot.
+// Where a heavy output (record rec, slice k) sums the terms of a leaf with
+// first input `in`: the fp32 partial sum heavy_partial(in, bits), or (null
+// p32, bits kHeavyFp64) its fp64 slot.
 struct HeavyDst {
     float *p32;
     double *p64;
 };
 
-__device__ __forceinline__ HeavyDst heavy_dst(const VecArgs &va, uint32_t id, uint32_t in, uint32_t k)
+__device__ __forceinline__ HeavyDst heavy_dst(const VecArgs &va, uint32_t rec, uint32_t in, uint32_t k)
 {
-    const uint2 rec = __ldg(va.hrec + id);
-    if (rec.y == kHeavyFp64) return HeavyDst{nullptr, va.acc64 + (size_t)rec.x * va.B + k};
-    return HeavyDst{va.acc + ((size_t)rec.x + heavy_partial(in, rec.y)) * va.B + k, nullptr};
+    const uint32_t bits = rec & 31u;
+    if (bits == kHeavyFp64) return HeavyDst{nullptr, heavy_slot64(va, rec) + k};
+    return HeavyDst{va.acc + ((size_t)(rec >> 5) + heavy_partial(in, bits)) * va.B + k, nullptr};
 }
 
-// Update heavy output `id` (slice k) with a leaf's contribution: v is the
-// fp32 combination of its cells (one term of an fp32 partial sum); for an
-// fp64 output the cells w*xa (when ua) and w*xb (when ub) are added in fp64,
-// where the sum of two floats is exact.
+// Update a heavy output (record rec, slice k) with a leaf's contribution: v
+// is the fp32 combination of its cells (one term of an fp32 partial sum); for
+// an fp64 output the cells w*xa (when ua) and w*xb (when ub) are added in
+// fp64, where the sum of two floats is exact.
 template <int SR, int VW>
-__device__ __forceinline__ void heavy_put(const VecArgs &va, uint32_t id, uint32_t in, uint32_t k,
+__device__ __forceinline__ void heavy_put(const VecArgs &va, uint32_t rec, uint32_t in, uint32_t k,
                                           const float (&v)[VW], const float (&xa)[VW], const float (&xb)[VW], bool ua,
                                           bool ub)
 {
-    const HeavyDst dst = heavy_dst(va, id, in, k);
+    const HeavyDst dst = heavy_dst(va, rec, in, k);
     if (dst.p32) {
         Fp32Sem<SR>::update(dst.p32, v);
         return;
@@ -301,13 +303,13 @@ __device__ __forceinline__ void leaf_group(const uint32_t (&lam)[U], const uint3
                             if (!S::skip(v1[q])) smem_update<SR>(w1 + q, __float_as_uint(v1[q]));
                     }
                 } else {
-                    const uint32_t h = SR == K2T_PLUS_TIMES && ((fl >> u) & 1u) ? heavy_word(a, out[u]) : 0u;
+                    const uint2 h = SR == K2T_PLUS_TIMES && ((fl >> u) & 1u) ? heavy_word(a, out[u]) : make_uint2(0u, 0u);
                     if (a0[u] || a1[u]) {
-                        if (h & 1u) heavy_put<SR, VW>(a, heavy_id2(h, 0), in[u], k, v0, x0[u], x1[u], a0[u], a1[u]);
+                        if (h.x) heavy_put<SR, VW>(a, h.x, in[u], k, v0, x0[u], x1[u], a0[u], a1[u]);
                         else S::update(y + (size_t)out[u] * B + k, v0);
                     }
                     if (b0[u] || b1[u]) {
-                        if (h & 2u) heavy_put<SR, VW>(a, heavy_id2(h, 1), in[u], k, v1, x0[u], x1[u], b0[u], b1[u]);
+                        if (h.y) heavy_put<SR, VW>(a, h.y, in[u], k, v1, x0[u], x1[u], b0[u], b1[u]);
                         else S::update(y + (size_t)(out[u] + 1) * B + k, v1);
                     }
                 }
@@ -344,8 +346,8 @@ constexpr uint32_t kFusedSolo = 256;  // levels this narrow are expanded by one 
 
 // Kernels without template parameters, defined in k2t_device.cu.
 __global__ void fill_kernel(uint32_t *y, uint64_t words, uint32_t pattern);
-__global__ void heavy_finish_kernel(const float *acc, const double *acc64, const uint2 *rec, const uint32_t *list,
-                                    uint32_t h, uint32_t B, float *y);
+__global__ void heavy_finish_kernel(const float *acc, const uint32_t *hdir, const uint32_t *list, uint32_t h,
+                                    uint32_t B, float *y);
 __global__ void ls_expand_kernel(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix, uint32_t a,
                                  uint32_t count, const Coord *src, uint32_t src_base, Coord *dst, uint32_t dst_base);
 __global__ void ls_block_sums_kernel(const uint8_t *sig, uint32_t a, uint32_t count, uint32_t *sums);
@@ -485,16 +487,16 @@ __device__ __forceinline__ void node_leaves_spec(uint32_t sg, uint32_t off, Coor
             float *y = static_cast<float *>(va.y);
             const float c0 = S::contrib(__uint_as_float(xo[b][0]), va.w);
             const float c1 = S::contrib(__uint_as_float(xo[b][1]), va.w);
-            const uint32_t h = SR == K2T_PLUS_TIMES && ((fl >> b) & 1u) ? heavy_word(va, out) : 0u;
+            const uint2 h = SR == K2T_PLUS_TIMES && ((fl >> b) & 1u) ? heavy_word(va, out) : make_uint2(0u, 0u);
             const float xa[1] = {__uint_as_float(xo[b][0])}, xb[1] = {__uint_as_float(xo[b][1])};
             if (a0 || a1) {
                 const float v[1] = {a0 ? (a1 ? S::plus(c0, c1) : c0) : c1};
-                if (h & 1u) heavy_put<SR, 1>(va, heavy_id2(h, 0), xin[b], 0u, v, xa, xb, a0, a1);
+                if (h.x) heavy_put<SR, 1>(va, h.x, xin[b], 0u, v, xa, xb, a0, a1);
                 else if (!S::skip(v[0])) S::update(y + out, v);
             }
             if (b0 || b1) {
                 const float v[1] = {b0 ? (b1 ? S::plus(c0, c1) : c0) : c1};
-                if (h & 2u) heavy_put<SR, 1>(va, heavy_id2(h, 1), xin[b], 0u, v, xa, xb, b0, b1);
+                if (h.y) heavy_put<SR, 1>(va, h.y, xin[b], 0u, v, xa, xb, b0, b1);
                 else if (!S::skip(v[0])) S::update(y + out + 1, v);
             }
         }
@@ -548,6 +550,21 @@ flat_leaf_kernel(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix
     leaf_group<SR, DIR, VW, 4>(lam, r, c, fl, va, nullptr, 0u);
 }
 
+// One single-slice update of a warp window entry: the semiring's shared
+// atomic on a 32-bit word, or (w64, plus-times) an fp64 add on entry i of a
+// window of doubles.
+template <int SR>
+__device__ __forceinline__ void window_put(uint32_t *win, uint32_t i, float v, bool w64)
+{
+    if constexpr (SR == K2T_PLUS_TIMES) {
+        if (w64) {
+            atomicAdd(reinterpret_cast<double *>(win) + i, (double)v);
+            return;
+        }
+    }
+    smem_update<SR>(win + i, __float_as_uint(v));
+}
+
 // Leaves of U leaf blocks (origins r[u], c[u], cells lam[u]) with x entries
 // already loaded (xo[u][0]: input r or c, xo[u][1]: the next one); one
 // vector slice (B = 1 fp32, or a Boolean word).  Bit u of fl (plus-times):
@@ -555,7 +572,7 @@ flat_leaf_kernel(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix
 template <int SR, int DIR, int U, class InOf>
 __device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint32_t (&out)[U], InOf &&in_of,
                                             const uint32_t (&xo)[U][2], uint32_t fl, const VecArgs &va,
-                                            uint32_t *win, uint32_t lo)
+                                            uint32_t *win, uint32_t lo, bool w64)
 {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -581,21 +598,21 @@ __device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint
             float *y = static_cast<float *>(va.y);
             const float c0 = S::contrib(__uint_as_float(xo[u][0]), va.w);
             const float c1 = S::contrib(__uint_as_float(xo[u][1]), va.w);
-            const uint32_t h = SR == K2T_PLUS_TIMES && ((fl >> u) & 1u) ? heavy_word(va, out[u]) : 0u;
+            const uint2 h = SR == K2T_PLUS_TIMES && ((fl >> u) & 1u) ? heavy_word(va, out[u]) : make_uint2(0u, 0u);
             const float xa[1] = {__uint_as_float(xo[u][0])}, xb[1] = {__uint_as_float(xo[u][1])};
             if (a0 || a1) {
                 const float v[1] = {a0 ? (a1 ? S::plus(c0, c1) : c0) : c1};
-                if (h & 1u) heavy_put<SR, 1>(va, heavy_id2(h, 0), in_of(u), 0u, v, xa, xb, a0, a1);
+                if (h.x) heavy_put<SR, 1>(va, h.x, in_of(u), 0u, v, xa, xb, a0, a1);
                 else if (!S::skip(v[0])) {
-                    if (win) smem_update<SR>(win + (out[u] - lo), __float_as_uint(v[0]));
+                    if (win) window_put<SR>(win, out[u] - lo, v[0], w64);
                     else S::update(y + out[u], v);
                 }
             }
             if (b0 || b1) {
                 const float v[1] = {b0 ? (b1 ? S::plus(c0, c1) : c0) : c1};
-                if (h & 2u) heavy_put<SR, 1>(va, heavy_id2(h, 1), in_of(u), 0u, v, xa, xb, b0, b1);
+                if (h.y) heavy_put<SR, 1>(va, h.y, in_of(u), 0u, v, xa, xb, b0, b1);
                 else if (!S::skip(v[0])) {
-                    if (win) smem_update<SR>(win + (out[u] + 1 - lo), __float_as_uint(v[0]));
+                    if (win) window_put<SR>(win, out[u] + 1 - lo, v[0], w64);
                     else S::update(y + out[u] + 1, v);
                 }
             }
@@ -615,13 +632,38 @@ constexpr uint32_t kWarpWindow = K2T_WARP_WINDOW;   // words of a warp's output 
 
 // Per-warp segmented scatter.  [mn, mx] bounds the warp's output coordinates
 // in units of `unit` cells (4 or 8 for nodes of the last internal level with
-// 2x2 or 4x4 leaves, 2 for 2x2 leaves).  When the outputs fit the warp's window (kWarpWindow words), the
-// window is cleared and returned; updates are then reduced there and each
-// touched entry reaches y once (warp_window_flush).  Hub rows of power-law
-// graphs then cost one global atomic per warp instead of one per non-zero.
+// 2x2 or 4x4 leaves, 2 or 4 for leaves).  When the outputs fit the warp's
+// window (kWarpWindow words), the window is cleared and returned; updates are
+// then reduced there and each touched entry reaches y once
+// (warp_window_flush).  Hub rows of power-law graphs then cost one global
+// atomic per warp instead of one per non-zero.
+//
+// Window modes (wmode):
+//   kWinF32     32-bit words, no heavy plus-times output among the window's
+//               outputs, so leaves need no heavy lookups;
+//   kWinF64     plus-times, single vectors, the span holds heavy outputs:
+//               entries are fp64 (half as many), every output in the span is
+//               summed there; the flush adds heavy outputs to their fp64
+//               slots and rounds the others to fp32 once into y;
+//   kWinShared  a block window that may hold heavy outputs (BANDED): heavy
+//               outputs are routed per leaf and never enter it.
+constexpr int kWinF32 = 0, kWinF64 = 1, kWinShared = 2;
+
+// Heavy plus-times outputs among [lo, lo + span) (span <= kWarpWindow), over
+// the warp: the lanes read the range's records (coalesced).
+__device__ __forceinline__ bool warp_span_has_heavy(const VecArgs &va, uint32_t lo, uint32_t span)
+{
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t hi = (uint32_t)min((uint64_t)lo + span, (uint64_t)va.hdir_len);   // exclusive
+    uint32_t any = 0u;
+    for (uint32_t o = lo + lane; o < hi; o += 32u) any |= __ldg(va.hdir + o);
+    return __any_sync(0xffffffffu, any != 0u);
+}
+
 template <int SR>
 __device__ __forceinline__ uint32_t *warp_window_begin(uint32_t mn, uint32_t mx, uint32_t unit, uint32_t width,
-                                                       uint32_t *mem, uint32_t &lo, uint32_t &span)
+                                                       uint32_t *mem, uint32_t &lo, uint32_t &span,
+                                                       const VecArgs &va, int &wmode)
 {
     const uint32_t lane = threadIdx.x & 31u;
 #pragma unroll
@@ -631,21 +673,43 @@ __device__ __forceinline__ uint32_t *warp_window_begin(uint32_t mn, uint32_t mx,
     }
     lo = unit * mn;
     span = 0;
+    wmode = kWinF32;
     if (mn > mx) return nullptr;
     const uint64_t span64 = (uint64_t)unit * ((uint64_t)mx - mn + 1u);
     if (span64 * width > kWarpWindow) return nullptr;
+    if (SR == K2T_PLUS_TIMES && va.hflag != nullptr && warp_span_has_heavy(va, lo, (uint32_t)span64)) {
+        if (width != 1u || 2u * span64 > kWarpWindow) return nullptr;
+        wmode = kWinF64;
+    }
     span = (uint32_t)span64;
-    for (uint32_t i = lane; i < span * width; i += 32u) mem[i] = zero_word<SR>();
+    const uint32_t words = wmode == kWinF64 ? 2u * span : span * width;
+    for (uint32_t i = lane; i < words; i += 32u) mem[i] = wmode == kWinF64 ? 0u : zero_word<SR>();
     __syncwarp();
     return mem;
 }
 
 template <int SR>
 __device__ __forceinline__ void warp_window_flush(const uint32_t *win, uint32_t lo, uint32_t span, uint32_t width,
-                                                  const VecArgs &va)
+                                                  const VecArgs &va, int wmode)
 {
     const uint32_t lane = threadIdx.x & 31u;
     __syncwarp();
+    if constexpr (SR == K2T_PLUS_TIMES) {
+        if (wmode == kWinF64) {   // single vectors: width 1
+            const double *w64 = reinterpret_cast<const double *>(win);
+            float *y = static_cast<float *>(va.y);
+            const uint64_t limit = va.n_out - lo;
+            for (uint32_t i = lane; i < span; i += 32u) {
+                const double v = w64[i];
+                if (v == 0.0 || i >= limit) continue;
+                const uint32_t o = lo + i;
+                const uint32_t rec = o < va.hdir_len ? __ldg(va.hdir + o) : 0u;
+                if (rec) atomicAdd(heavy_slot64(va, rec), v);
+                else atomicAdd(y + o, (float)v);
+            }
+            return;
+        }
+    }
     uint32_t *y = static_cast<uint32_t *>(va.y) + (size_t)lo * width;
     const uint64_t limit = (va.n_out - lo) * width;
     for (uint32_t i = lane; i < span * width; i += 32u) {
@@ -657,9 +721,9 @@ __device__ __forceinline__ void warp_window_flush(const uint32_t *win, uint32_t 
 
 // One VW-wide vector slice k of one leaf (origin r, c; cells lam): gathers the
 // slice of the inputs it needs, combines per output, updates y or the window;
-// outputs marked in hv (heavy_word) go to their heavy sums.
+// outputs with a record in hv (heavy_word) go to their heavy sums.
 template <int SR, int DIR, int VW>
-__device__ __forceinline__ void leaf_slice(uint32_t lam, uint32_t r, uint32_t c, uint32_t k, uint32_t hv,
+__device__ __forceinline__ void leaf_slice(uint32_t lam, uint32_t r, uint32_t c, uint32_t k, uint2 hv,
                                            const VecArgs &va, uint32_t *win, uint32_t lo)
 {
     using S = Fp32Sem<SR>;
@@ -696,23 +760,23 @@ __device__ __forceinline__ void leaf_slice(uint32_t lam, uint32_t r, uint32_t c,
             S::update(y + (size_t)o * B + k, v);
         }
     };
-    if (SR == K2T_PLUS_TIMES && hv) {
+    if (SR == K2T_PLUS_TIMES && (hv.x | hv.y)) {
         // a leaf with a heavy output: separate branch, so the fp32 path below
         // keeps its registers
         if (a0 || a1) {
-            if (hv & 1u) {
+            if (hv.x) {
                 float v[VW];
                 combine(a0, a1, v);
-                heavy_put<SR, VW>(va, heavy_id2(hv, 0), in, k, v, x0, x1, a0, a1);
+                heavy_put<SR, VW>(va, hv.x, in, k, v, x0, x1, a0, a1);
             } else {
                 put(out, a0, a1);
             }
         }
         if (b0 || b1) {
-            if (hv & 2u) {
+            if (hv.y) {
                 float v[VW];
                 combine(b0, b1, v);
-                heavy_put<SR, VW>(va, heavy_id2(hv, 1), in, k, v, x0, x1, b0, b1);
+                heavy_put<SR, VW>(va, hv.y, in, k, v, x0, x1, b0, b1);
             } else {
                 put(out + 1, b0, b1);
             }
@@ -733,14 +797,16 @@ __device__ __forceinline__ void leaf_slice(uint32_t lam, uint32_t r, uint32_t c,
 //    the VW-wide slice g of every vector row, so a row of x is one coalesced
 //    load and a row of y one coalesced vector reduction (the pages' B
 //    adjacent threads per node, section 3.6).
-// Updates of heavy outputs go to their sums; the others go to the window
-// when there is one, else to y.
+// Updates go to the window when there is one (wmode as warp_window_begin
+// says), else to y; heavy plus-times outputs outside a window go to their
+// partial sums.
 template <int SR, int DIR, int VW, class LeafAt>
 __device__ __forceinline__ void warp_leaf_rounds(uint32_t jb, uint32_t je, LeafAt &&leaf_at, const VecArgs &va,
-                                                 uint32_t *win, uint32_t lo)
+                                                 uint32_t *win, uint32_t lo, int wmode = kWinF32)
 {
     const uint32_t lane = threadIdx.x & 31u;
-    const bool heavy = SR == K2T_PLUS_TIMES && va.hflag != nullptr;
+    const bool heavy = SR == K2T_PLUS_TIMES && va.hflag != nullptr && (!win || wmode == kWinShared);
+    const bool w64 = win && wmode == kWinF64;
     if (SR == K2T_BOOLEAN || (VW == 1 && va.B == 1)) {
         constexpr int U = kLeafU;
         const uint32_t *x = static_cast<const uint32_t *>(va.x);
@@ -784,7 +850,7 @@ __device__ __forceinline__ void warp_leaf_rounds(uint32_t jb, uint32_t je, LeafA
                 leaf_at(j0 + 32u * (uint32_t)u + lane, l2, r2, c2, li2);
                 return DIR == K2T_RIGHT ? c2 : r2;
             };
-            leaf_apply1<SR, DIR, U>(lam, out, in_of, xo, fl, va, win, lo);
+            leaf_apply1<SR, DIR, U>(lam, out, in_of, xo, fl, va, win, lo, w64);
         }
         return;
     }
@@ -796,14 +862,15 @@ __device__ __forceinline__ void warp_leaf_rounds(uint32_t jb, uint32_t je, LeafA
         const uint32_t slot = lane / groups, sub = lane % groups;
         const bool active = slot < per;
         for (uint32_t j0 = jb; j0 < je; j0 += per * U) {
-            uint32_t lam[U], r[U], c[U], hv[U];
+            uint32_t lam[U], r[U], c[U];
+            uint2 hv[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const uint32_t j = j0 + (uint32_t)u * per + slot;
                 lam[u] = 0u;
                 r[u] = 0u;
                 c[u] = 0u;
-                hv[u] = 0u;
+                hv[u] = make_uint2(0u, 0u);
                 uint32_t li = 0u;
                 if (active && j < je) {
                     leaf_at(j, lam[u], r[u], c[u], li);
@@ -843,7 +910,7 @@ cached_block_kernel(const uint8_t *sig, const uint32_t *dir, uint32_t n, const C
 {
     __shared__ Coord cs[kCachedWarps][kDirS];
     __shared__ uint16_t slots[kCachedWarps][4 * kDirS];
-    __shared__ uint32_t wins[kCachedWarps][kWarpWindow];
+    __shared__ __align__(16) uint32_t wins[kCachedWarps][kWarpWindow];
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
     const uint32_t g = blockIdx.x * kCachedWarps + warp;
     const uint32_t s = g * kDirS;
@@ -882,7 +949,8 @@ cached_block_kernel(const uint8_t *sig, const uint32_t *dir, uint32_t n, const C
     }
     const uint32_t width = SR == K2T_BOOLEAN ? 1u : va.B;
     uint32_t lo, span;
-    uint32_t *win = warp_window_begin<SR>(mn, mx, 4u, width, wins[warp], lo, span);
+    int wmode;
+    uint32_t *win = warp_window_begin<SR>(mn, mx, 4u, width, wins[warp], lo, span, va, wmode);
     __syncwarp();
     warp_leaf_rounds<SR, DIR, VW>(0u, total, [&](uint32_t j, uint32_t &lam, uint32_t &r, uint32_t &c, uint32_t &li) {
         const uint32_t e = sl[j];
@@ -892,81 +960,8 @@ cached_block_kernel(const uint8_t *sig, const uint32_t *dir, uint32_t n, const C
         c = 4u * p.c + 2u * (b & 1u);
         li = base + j;
         lam = nibble_at(leaf, li);
-    }, va, win, lo);
-    if (win) warp_window_flush<SR>(win, lo, span, width, va);
-}
-
-// k^2+F engine for batches: the thread block's 8 warps share one 256-node
-// directory block instead of taking one each.  Warp 0 turns the block's
-// signatures into the leaf list (warp scan), every thread loads one node's
-// coordinates, and warp w then takes the w-th eighth of the leaves, with its
-// own output window over the outputs of its slice.  A batch row of x or y is
-// B * 4 bytes, so the rows a wave of warps touches at once are what L2 must
-// hold: with one directory block per thread block the Z-order window in
-// flight is 8 times narrower than with one per warp, and x and y rows are
-// reused from L2 while the block's leaves need them.
-template <int SR, int DIR, int VW>
-__global__ void __launch_bounds__(32 * kCachedWarps, cached_min_blocks<VW>())
-cached_coop_kernel(const uint8_t *sig, const uint32_t *dir, uint32_t n, const Coord *coords, const uint8_t *leaf,
-                   VecArgs va)
-{
-    __shared__ Coord cw[kDirS];
-    __shared__ uint16_t sl[4 * kDirS];
-    __shared__ uint32_t wins[kCachedWarps][kWarpWindow];
-    __shared__ uint32_t total_s;
-    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
-    const uint32_t g = blockIdx.x;
-    const uint32_t s = g * kDirS;
-    if (s >= n) return;
-    const uint32_t cnt = min(n - s, kDirS);
-    if (threadIdx.x < cnt) cw[threadIdx.x] = coords[s + threadIdx.x];
-    if (warp == 0) {
-        uint32_t w = 0;
-        if (8u * lane < cnt) {
-            w = __ldg(reinterpret_cast<const uint32_t *>(sig + s / 2) + lane);
-            if (8u * lane + 8u > cnt) w &= (1u << (4u * (cnt - 8u * lane))) - 1u;
-        }
-        const uint32_t f = (uint32_t)__popc(w);
-        const uint32_t incl = warp_incl_scan(f);
-        if (lane == 31) total_s = incl;
-        uint32_t pos = incl - f;
-        uint32_t rest = w;
-        while (rest) {
-            const uint32_t bit = (uint32_t)(__ffs(rest) - 1);  // 4*k + b
-            rest &= rest - 1u;
-            sl[pos++] = (uint16_t)(((8u * lane + bit / 4u) << 2) | (bit & 3u));
-        }
-    }
-    __syncthreads();
-    const uint32_t total = total_s;
-    const uint32_t base = __ldg(dir + g);
-    const uint32_t jb = (uint32_t)(((uint64_t)total * warp) / kCachedWarps);
-    const uint32_t je = (uint32_t)(((uint64_t)total * (warp + 1)) / kCachedWarps);
-    auto leaf_at = [&](uint32_t j, uint32_t &lam, uint32_t &r, uint32_t &c, uint32_t &li) {
-        const uint32_t e = sl[j];
-        const Coord p = cw[e >> 2];
-        const uint32_t b = e & 3u;
-        r = 4u * p.r + 2u * (b >> 1);
-        c = 4u * p.c + 2u * (b & 1u);
-        li = base + j;
-        lam = nibble_at(leaf, li);
-    };
-    // the warp's output span, in units of leaf blocks (2 outputs)
-    uint32_t mn = 0xffffffffu, mx = 0u;
-    for (uint32_t j = jb + lane; j < je; j += 32u) {
-        const uint32_t e = sl[j];
-        const Coord p = cw[e >> 2];
-        const uint32_t b = e & 3u;
-        const uint32_t o = DIR == K2T_RIGHT ? 2u * p.r + (b >> 1) : 2u * p.c + (b & 1u);
-        mn = min(mn, o);
-        mx = max(mx, o);
-    }
-    const uint32_t width = SR == K2T_BOOLEAN ? 1u : va.B;
-    uint32_t lo, span;
-    uint32_t *win = warp_window_begin<SR>(mn, mx, 2u, width, wins[warp], lo, span);
-    __syncwarp();
-    warp_leaf_rounds<SR, DIR, VW>(jb, je, leaf_at, va, win, lo);
-    if (win) warp_window_flush<SR>(win, lo, span, width, va);
+    }, va, win, lo, wmode);
+    if (win) warp_window_flush<SR>(win, lo, span, width, va, wmode);
 }
 
 // ---- 4x4 leaves (leaf_k = 4) ------------------------------------------------------
@@ -998,21 +993,16 @@ __device__ __forceinline__ uint32_t used4(uint32_t lam)
            ((uint32_t)((lam & 0xf00u) != 0) << 2) | ((uint32_t)((lam & 0xf000u) != 0) << 3);
 }
 
-// Heavy outputs among out .. out + 3 (out a multiple of 4): (id << 4) | mask,
-// mask bit q set when out + q is heavy, id the heavy-list index of the first
-// of them; output out + q has id + popc(mask & ((1 << q) - 1)).
-__device__ __forceinline__ uint32_t heavy_word4(const VecArgs &va, uint32_t out)
+// Records of the outputs out .. out + 3 of a 4x4 leaf (out a multiple of 4),
+// one 16-byte load; 0 where an output is not heavy.
+__device__ __forceinline__ uint4 heavy_word4(const VecArgs &va, uint32_t out)
 {
-    const uint2 e = __ldg(reinterpret_cast<const uint2 *>(va.hent) + (out >> 5));
-    const uint32_t sh = out & 31u;
-    const uint32_t m = (e.x >> sh) & 15u;
-    if (!m) return 0u;
-    return ((e.y + (uint32_t)__popc(e.x & ((1u << sh) - 1u))) << 4) | m;
+    return __ldg(reinterpret_cast<const uint4 *>(va.hdir + out));
 }
 
-__device__ __forceinline__ uint32_t heavy_id4(uint32_t hv, int q)
+__device__ __forceinline__ uint32_t rec_at(const uint4 &h, int q)
 {
-    return (hv >> 4) + (uint32_t)__popc(hv & 15u & ((1u << q) - 1u));
+    return q == 0 ? h.x : (q == 1 ? h.y : (q == 2 ? h.z : h.w));
 }
 
 // One vector slice (B = 1 fp32, or a Boolean word) of U leaves whose inputs
@@ -1020,7 +1010,7 @@ __device__ __forceinline__ uint32_t heavy_id4(uint32_t hv, int q)
 template <int SR, int DIR, int U, class InOf>
 __device__ __forceinline__ void leaf4_apply1(const uint32_t (&lam)[U], const uint32_t (&out)[U], InOf &&in_of,
                                              const uint32_t (&xo)[U][4], uint32_t fl, const VecArgs &va,
-                                             uint32_t *win, uint32_t lo)
+                                             uint32_t *win, uint32_t lo, bool w64)
 {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -1042,14 +1032,14 @@ __device__ __forceinline__ void leaf4_apply1(const uint32_t (&lam)[U], const uin
         } else {
             using S = Fp32Sem<SR>;
             float *y = static_cast<float *>(va.y);
-            const uint32_t h = SR == K2T_PLUS_TIMES && ((fl >> u) & 1u) ? heavy_word4(va, out[u]) : 0u;
+            const uint4 h = SR == K2T_PLUS_TIMES && ((fl >> u) & 1u) ? heavy_word4(va, out[u]) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const uint32_t s = seg4<DIR>(l, q);
                 if (!s) continue;
                 HeavyDst hd{nullptr, nullptr};
-                if (SR == K2T_PLUS_TIMES && ((h >> q) & 1u)) {
-                    hd = heavy_dst(va, heavy_id4(h, q), in_of(u), 0u);
+                if (SR == K2T_PLUS_TIMES && rec_at(h, q)) {
+                    hd = heavy_dst(va, rec_at(h, q), in_of(u), 0u);
                     if (!hd.p32) {
                         double d = 0.0;
 #pragma unroll
@@ -1073,7 +1063,7 @@ __device__ __forceinline__ void leaf4_apply1(const uint32_t (&lam)[U], const uin
                     continue;
                 }
                 if (S::skip(v[0])) continue;
-                if (win) smem_update<SR>(win + (out[u] + q - lo), __float_as_uint(v[0]));
+                if (win) window_put<SR>(win, out[u] + q - lo, v[0], w64);
                 else S::update(y + out[u] + q, v);
             }
         }
@@ -1082,7 +1072,7 @@ __device__ __forceinline__ void leaf4_apply1(const uint32_t (&lam)[U], const uin
 
 // One VW-wide slice k of one 4x4 leaf (origin r, c; cells lam) for batches.
 template <int SR, int DIR, int VW>
-__device__ __forceinline__ void leaf4_slice(uint32_t lam, uint32_t r, uint32_t c, uint32_t k, uint32_t hv,
+__device__ __forceinline__ void leaf4_slice(uint32_t lam, uint32_t r, uint32_t c, uint32_t k, uint4 hv,
                                             const VecArgs &va, uint32_t *win, uint32_t lo)
 {
     using S = Fp32Sem<SR>;
@@ -1101,8 +1091,8 @@ __device__ __forceinline__ void leaf4_slice(uint32_t lam, uint32_t r, uint32_t c
         const uint32_t s = seg4<DIR>(lam, q);
         if (!s) continue;
         HeavyDst hd{nullptr, nullptr};
-        if (SR == K2T_PLUS_TIMES && ((hv >> q) & 1u)) {
-            hd = heavy_dst(va, heavy_id4(hv, q), in, k);
+        if (SR == K2T_PLUS_TIMES && rec_at(hv, q)) {
+            hd = heavy_dst(va, rec_at(hv, q), in, k);
             if (!hd.p32) {
 #pragma unroll
                 for (int e = 0; e < VW; ++e) {
@@ -1147,10 +1137,11 @@ __device__ __forceinline__ void leaf4_slice(uint32_t lam, uint32_t r, uint32_t c
 //  - Batches: G = B/VW adjacent lanes share a leaf, each owning a VW slice.
 template <int SR, int DIR, int VW, class LeafAt>
 __device__ __forceinline__ void warp_leaf4_rounds(uint32_t jb, uint32_t je, LeafAt &&leaf_at, const VecArgs &va,
-                                                  uint32_t *win, uint32_t lo)
+                                                  uint32_t *win, uint32_t lo, int wmode = kWinF32)
 {
     const uint32_t lane = threadIdx.x & 31u;
-    const bool heavy = SR == K2T_PLUS_TIMES && va.hflag != nullptr;
+    const bool heavy = SR == K2T_PLUS_TIMES && va.hflag != nullptr && (!win || wmode == kWinShared);
+    const bool w64 = win && wmode == kWinF64;
     if (SR == K2T_BOOLEAN || (VW == 1 && va.B == 1)) {
         constexpr int U = K2T_LEAF4_U;
         const uint32_t *x = static_cast<const uint32_t *>(va.x);
@@ -1195,7 +1186,7 @@ __device__ __forceinline__ void warp_leaf4_rounds(uint32_t jb, uint32_t je, Leaf
                 leaf_at(j0 + 32u * (uint32_t)u + lane, l2, r2, c2, li2);
                 return DIR == K2T_RIGHT ? c2 : r2;
             };
-            leaf4_apply1<SR, DIR, U>(lam, out, in_of, xo, fl, va, win, lo);
+            leaf4_apply1<SR, DIR, U>(lam, out, in_of, xo, fl, va, win, lo, w64);
         }
         return;
     }
@@ -1207,14 +1198,15 @@ __device__ __forceinline__ void warp_leaf4_rounds(uint32_t jb, uint32_t je, Leaf
         const uint32_t slot = lane / groups, sub = lane % groups;
         const bool active = slot < per;
         for (uint32_t j0 = jb; j0 < je; j0 += per * U) {
-            uint32_t lam[U], r[U], c[U], hv[U];
+            uint32_t lam[U], r[U], c[U];
+            uint4 hv[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const uint32_t j = j0 + (uint32_t)u * per + slot;
                 lam[u] = 0u;
                 r[u] = 0u;
                 c[u] = 0u;
-                hv[u] = 0u;
+                hv[u] = make_uint4(0u, 0u, 0u, 0u);
                 uint32_t li = 0u;
                 if (active && j < je) {
                     leaf_at(j, lam[u], r[u], c[u], li);
@@ -1243,7 +1235,7 @@ cached4_block_kernel(const uint8_t *sig, const uint32_t *dir, uint32_t n, const 
 {
     __shared__ Coord cs[kCachedWarps][kDirS];
     __shared__ uint16_t slots[kCachedWarps][4 * kDirS];
-    __shared__ uint32_t wins[kCachedWarps][kWarpWindow];
+    __shared__ __align__(16) uint32_t wins[kCachedWarps][kWarpWindow];
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
     const uint32_t g = blockIdx.x * kCachedWarps + warp;
     const uint32_t s = g * kDirS;
@@ -1281,7 +1273,8 @@ cached4_block_kernel(const uint8_t *sig, const uint32_t *dir, uint32_t n, const 
     }
     const uint32_t width = SR == K2T_BOOLEAN ? 1u : va.B;
     uint32_t lo, span;
-    uint32_t *win = warp_window_begin<SR>(mn, mx, 8u, width, wins[warp], lo, span);
+    int wmode;
+    uint32_t *win = warp_window_begin<SR>(mn, mx, 8u, width, wins[warp], lo, span, va, wmode);
     __syncwarp();
     warp_leaf4_rounds<SR, DIR, VW>(0u, total, [&](uint32_t j, uint32_t &lam, uint32_t &r, uint32_t &c, uint32_t &li) {
         const uint32_t e = sl[j];
@@ -1291,8 +1284,8 @@ cached4_block_kernel(const uint8_t *sig, const uint32_t *dir, uint32_t n, const 
         c = 8u * p.c + 4u * (b & 1u);
         li = base + j;
         lam = __ldg(leaf + li);
-    }, va, win, lo);
-    if (win) warp_window_flush<SR>(win, lo, span, width, va);
+    }, va, win, lo, wmode);
+    if (win) warp_window_flush<SR>(win, lo, span, width, va, wmode);
 }
 
 // BANDED engine: the cached last internal level grouped by row band (band_rows
@@ -1375,7 +1368,7 @@ banded_kernel(const uint32_t *chunks, const Coord *coords, const uint32_t *bleaf
             c = 4u * p.c + 2u * (b & 1u);
             li = lw[node] + (e & 3u);
             lam = nibble_at(leaf, li);
-        }, va, windowed ? win : nullptr, (uint32_t)band_lo);
+        }, va, windowed ? win : nullptr, (uint32_t)band_lo, kWinShared);
         __syncwarp();
     }
     if (windowed) {
@@ -1563,6 +1556,14 @@ __device__ __forceinline__ void sliced_expand(const uint32_t *words, uint32_t nb
     warp_expand<DIR>(words, nb, a, b, cur, nxt, start, mn, mx);
 }
 
+// Bytes of one level's staging slot in fused_kernel: the nibbles (or, for a
+// 4x4 leaf level, the 16-bit signatures) of at most cap nodes, widened to
+// 16-byte boundaries at both ends.
+__host__ __device__ constexpr uint32_t fused_slot(uint32_t cap, bool wide)
+{
+    return ((wide ? 2u * cap : cap / 2u) + 48u + 15u) & ~15u;
+}
+
 // FUSED engine: thread block k descends chunk k, a run of whole subtrees
 // rooted at level d_c with at most `cap` leaves, from its roots to the
 // leaves.  The chunk record holds the index of its roots' coordinates and,
@@ -1572,20 +1573,21 @@ __device__ __forceinline__ void sliced_expand(const uint32_t *words, uint32_t nb
 // in shared memory: every warp takes an equal slice of the level, learns
 // where its children start from the other warps' fan-out totals (one block
 // barrier per level) and writes them with warp scans.  No global scratch.
-template <int SR, int DIR, int VW>
+// L4: the leaf level holds 4x4 bitmaps (16-bit signatures, section 5.6).
+template <int SR, int DIR, int VW, bool L4>
 __global__ void __launch_bounds__(kFusedThreads)
 fused_kernel(DevTree tr, const uint32_t *chunks, uint32_t stride, const Coord *roots, uint32_t cap, VecArgs va,
              uint32_t *status)
 {
     extern __shared__ __align__(16) uint8_t fsm[];
     const int d0 = tr.d0, l = tr.levels;
-    const uint32_t slot = (cap / 2 + 48 + 15) & ~15u;
+    const uint32_t slot = fused_slot(cap, false), lslot = fused_slot(cap, L4);
     uint64_t *bar = reinterpret_cast<uint64_t *>(fsm);
     uint32_t *wtot = reinterpret_cast<uint32_t *>(fsm + 16);           // [2][kFusedWarps] fan-out totals
-    uint32_t *nbase = reinterpret_cast<uint32_t *>(fsm + 80);          // per level, nibble base in its slot
+    uint32_t *nbase = reinterpret_cast<uint32_t *>(fsm + 80);          // per level, entry base in its slot
     uint8_t *stage = fsm + 80 + 4 * K2T_MAX_LEVELS;
     stage += (16 - ((uintptr_t)stage & 15)) & 15;
-    Coord *cur = reinterpret_cast<Coord *>(stage + (size_t)(l - d0) * slot);
+    Coord *cur = reinterpret_cast<Coord *>(stage + (size_t)(l - 1 - d0) * slot + lslot);
     Coord *nxt = cur + cap;
 
     const uint32_t *rec = chunks + (size_t)blockIdx.x * stride;
@@ -1597,8 +1599,13 @@ fused_kernel(DevTree tr, const uint32_t *chunks, uint32_t stride, const Coord *r
         StagePlan pl[K2T_MAX_LEVELS];
         for (int d = dc; d < l; ++d) {
             const uint32_t s = rng[2 * (d - d0)], n = rng[2 * (d - d0) + 1];
-            pl[d] = stage_plan(s >> 1, ((uint64_t)s + n + 1) >> 1);
-            nbase[d - d0] = 2u * pl[d].shift + (s & 1u);
+            if (L4 && d == l - 1) {   // 2 bytes a leaf
+                pl[d] = stage_plan(2ull * s, 2ull * ((uint64_t)s + n));
+                nbase[d - d0] = pl[d].shift / 2u;
+            } else {                  // a nibble a node
+                pl[d] = stage_plan(s >> 1, ((uint64_t)s + n + 1) >> 1);
+                nbase[d - d0] = 2u * pl[d].shift + (s & 1u);
+            }
             total += pl[d].bytes;
         }
         mbar_init(bar);
@@ -1658,30 +1665,46 @@ fused_kernel(DevTree tr, const uint32_t *chunks, uint32_t stride, const Coord *r
         wmx = max(wmx, o);
     }
     const uint32_t width = SR == K2T_BOOLEAN ? 1u : va.B;
+    constexpr uint32_t side = L4 ? 4u : 2u;
     uint32_t lo, span;
     uint32_t *win = nullptr;
+    int wmode = kWinF32;
     lo = 0u;
     span = 0u;
     if (2u * cap >= kFusedWarps * kWarpWindow)  // the free buffer holds every warp's window
-        win = warp_window_begin<SR>(wmn, wmx, 2u, width, reinterpret_cast<uint32_t *>(nxt) + warp * kWarpWindow,
-                                    lo, span);
+        win = warp_window_begin<SR>(wmn, wmx, side, width, reinterpret_cast<uint32_t *>(nxt) + warp * kWarpWindow,
+                                    lo, span, va, wmode);
     const uint32_t leaf0 = rng[2 * (l - 1 - d0)];  // the chunk's first leaf (level order)
-    warp_leaf_rounds<SR, DIR, VW>(jb, je, [&](uint32_t j, uint32_t &lam, uint32_t &r, uint32_t &c, uint32_t &li) {
-        const Coord q = cur[j];
-        r = 2u * q.r;
-        c = 2u * q.c;
-        li = leaf0 + j;
-        lam = snib(lsig, lnb + j);
-    }, va, win, lo);
-    if (win) warp_window_flush<SR>(win, lo, span, width, va);
+    if constexpr (L4) {
+        const uint16_t *lsig16 = reinterpret_cast<const uint16_t *>(lsig) + lnb;
+        warp_leaf4_rounds<SR, DIR, VW>(jb, je, [&](uint32_t j, uint32_t &lam, uint32_t &r, uint32_t &c, uint32_t &li) {
+            const Coord q = cur[j];
+            r = 4u * q.r;
+            c = 4u * q.c;
+            li = leaf0 + j;
+            lam = lsig16[j];
+        }, va, win, lo, wmode);
+    } else {
+        warp_leaf_rounds<SR, DIR, VW>(jb, je, [&](uint32_t j, uint32_t &lam, uint32_t &r, uint32_t &c, uint32_t &li) {
+            const Coord q = cur[j];
+            r = 2u * q.r;
+            c = 2u * q.c;
+            li = leaf0 + j;
+            lam = snib(lsig, lnb + j);
+        }, va, win, lo, wmode);
+    }
+    if (win) warp_window_flush<SR>(win, lo, span, width, va, wmode);
     (void)mn;
     (void)mx;
 }
 
-// Dynamic shared memory of fused_kernel for a tree.
-inline size_t fused_smem(int levels, int d0, uint32_t cap)
+// Dynamic shared memory of fused_kernel for a tree: header, one staging slot
+// per level (the leaf level's holds 2 bytes a leaf with 4x4 leaves), and two
+// coordinate buffers of cap entries.
+inline size_t fused_smem(int levels, int d0, uint32_t cap, bool l4)
 {
-    return 80 + 4 * K2T_MAX_LEVELS + 16 + (size_t)(levels - d0) * ((cap / 2 + 48 + 15) & ~15u) + 2 * (size_t)cap * 8;
+    return 80 + 4 * K2T_MAX_LEVELS + 16 + (size_t)(levels - 1 - d0) * fused_slot(cap, false) + fused_slot(cap, l4) +
+           2 * (size_t)cap * 8;
 }
 
 }  // namespace k2t
@@ -1724,11 +1747,9 @@ struct DeviceState {
     uint32_t *err = nullptr;
     void *vec[2] = {nullptr, nullptr};
     const uint32_t *hflag[2] = {nullptr, nullptr};  // heavy outputs, per direction (null: none)
-    const uint32_t *hent[2] = {nullptr, nullptr};
+    const uint32_t *hdir[2] = {nullptr, nullptr};
     const uint32_t *hlist[2] = {nullptr, nullptr};
-    const uint2 *hrec[2] = {nullptr, nullptr};
     float *acc = nullptr;
-    double *acc64 = nullptr;
     cudaStream_t cap_stream = nullptr;
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t gexec = nullptr;
@@ -1744,17 +1765,24 @@ inline int grid_for_blocks(uint64_t warps_needed)
 }
 
 // ---- per-(semiring, direction, vector width) launch tables --------------
+template <int SR, int DIR, int VW, bool L4>
+void launch_fused_k(const k2t_tree *t, const DeviceState *d, const VecArgs &va, cudaStream_t st)
+{
+    const size_t smem = fused_smem(t->levels, t->d0, t->opts.chunk_cap, L4);
+    static size_t configured = 0;
+    if (smem > configured) {
+        cudaFuncSetAttribute(fused_kernel<SR, DIR, VW, L4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        configured = smem;
+    }
+    fused_kernel<SR, DIR, VW, L4><<<(unsigned)t->n_chunks, kFusedThreads, smem, st>>>(
+        d->tree, d->chunks, t->chunk_stride, d->roots, t->opts.chunk_cap, va, d->err);
+}
+
 template <int SR, int DIR, int VW>
 void launch_fused(const k2t_tree *t, const DeviceState *d, const VecArgs &va, cudaStream_t st)
 {
-    const size_t smem = fused_smem(t->levels, t->d0, t->opts.chunk_cap);
-    static size_t configured = 0;
-    if (smem > configured) {
-        cudaFuncSetAttribute(fused_kernel<SR, DIR, VW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        configured = smem;
-    }
-    fused_kernel<SR, DIR, VW><<<(unsigned)t->n_chunks, kFusedThreads, smem, st>>>(
-        d->tree, d->chunks, t->chunk_stride, d->roots, t->opts.chunk_cap, va, d->err);
+    if (t->leaf_k4) launch_fused_k<SR, DIR, VW, true>(t, d, va, st);
+    else launch_fused_k<SR, DIR, VW, false>(t, d, va, st);
 }
 
 template <int SR, int DIR, int VW>
@@ -1773,16 +1801,6 @@ void launch_cached(const k2t_tree *t, const DeviceState *d, const VecArgs &va, c
     const uint32_t blocks = (n + kDirS - 1) / kDirS;
     const unsigned grid = (unsigned)((blocks + kCachedWarps - 1) / kCachedWarps);
     cached_block_kernel<SR, DIR, VW><<<grid, 32 * kCachedWarps, 0, st>>>(
-        d->tree.lv[l - 2].sig, d->tree.lv[l - 2].dir, n, d->cached, d->tree.lv[l - 1].sig, va);
-}
-
-template <int SR, int DIR, int VW>
-void launch_cached_coop(const k2t_tree *t, const DeviceState *d, const VecArgs &va, cudaStream_t st)
-{
-    const int l = t->levels;
-    const uint32_t n = (uint32_t)t->nodes[(size_t)l - 2];
-    const unsigned grid = (n + kDirS - 1) / kDirS;
-    cached_coop_kernel<SR, DIR, VW><<<grid, 32 * kCachedWarps, 0, st>>>(
         d->tree.lv[l - 2].sig, d->tree.lv[l - 2].dir, n, d->cached, d->tree.lv[l - 1].sig, va);
 }
 
@@ -1864,10 +1882,8 @@ void launch_ls(const k2t_tree *t, const DeviceState *d, const VecArgs &va, cudaS
 
 using LaunchFn = void (*)(const k2t_tree *, const DeviceState *, const VecArgs &, cudaStream_t);
 
-// Internal engine ids: the CACHED engine on a tree with 4x4 leaves, and its
-// block-cooperative form for batches.
+// Internal engine id: the CACHED engine on a tree with 4x4 leaves.
 constexpr uint32_t kEngineCached4 = 100;
-constexpr uint32_t kEngineCachedCoop = 101;
 
 // Plus-times products of a direction with heavy outputs.  heavy_begin points
 // va at the direction's tables and zeroes their sums for the B vectors
@@ -1877,23 +1893,17 @@ constexpr uint32_t kEngineCachedCoop = 101;
 inline bool heavy_begin(const k2t_tree *t, const DeviceState *d, int dir, int semiring, VecArgs &va, cudaStream_t st)
 {
     va.hflag = nullptr;
-    va.hent = nullptr;
-    va.hrec = nullptr;
+    va.hdir = nullptr;
+    va.hdir_len = 0u;
     va.acc = nullptr;
-    va.acc64 = nullptr;
     if (semiring != K2T_PLUS_TIMES || !d->hflag[dir]) return false;
     va.hflag = d->hflag[dir];
-    va.hent = d->hent[dir];
-    va.hrec = d->hrec[dir];
+    va.hdir = d->hdir[dir];
+    va.hdir_len = (uint32_t)t->hdir[dir].size();
     va.acc = d->acc;
-    va.acc64 = d->acc64;
-    auto zero = [&](void *p, uint64_t words) {
-        if (!words) return;
-        const uint64_t blocks = std::min<uint64_t>((words / 4 + 255) / 256 + 1, 152ull * 8);
-        fill_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<uint32_t *>(p), words, 0u);
-    };
-    zero(d->acc, t->hparts[dir] * va.B);
-    zero(d->acc64, 2 * t->hfp64[dir] * va.B);
+    const uint64_t words = t->hrows[dir] * va.B;
+    const uint64_t blocks = std::min<uint64_t>((words / 4 + 255) / 256 + 1, 152ull * 8);
+    fill_kernel<<<(unsigned)blocks, 256, 0, st>>>(reinterpret_cast<uint32_t *>(d->acc), words, 0u);
     return true;
 }
 
@@ -1901,7 +1911,7 @@ inline void heavy_end(const k2t_tree *t, const DeviceState *d, int dir, const Ve
 {
     const uint32_t h = (uint32_t)t->hlist[dir].size();
     const uint64_t blocks = std::min<uint64_t>(((uint64_t)h + 7) / 8, 152ull * 16);
-    heavy_finish_kernel<<<(unsigned)blocks, 256, 0, st>>>(d->acc, d->acc64, d->hrec[dir], d->hlist[dir], h, va.B,
+    heavy_finish_kernel<<<(unsigned)blocks, 256, 0, st>>>(d->acc, d->hdir[dir], d->hlist[dir], h, va.B,
                                                           static_cast<float *>(va.y));
 }
 
@@ -1913,7 +1923,6 @@ LaunchFn pick_engine(uint32_t engine)
     case K2T_ENGINE_CACHED: return launch_cached<SR, DIR, VW>;
     case K2T_ENGINE_BANDED: return launch_banded<SR, DIR, VW>;
     case kEngineCached4: return launch_cached4<SR, DIR, VW>;
-    case kEngineCachedCoop: return launch_cached_coop<SR, DIR, VW>;
     default: return launch_ls<SR, DIR, VW>;
     }
 }

@@ -412,6 +412,12 @@ int k2t_bool_closure(const k2t_tree *a, const k2t_opts *opts, uint32_t max_iters
     *out = nullptr;
     *iters = 0;
     if (a->n_rows != a->n_cols || !plain_k2(a)) return K2T_EINVAL;
+    // every squaring takes a tree with 2x2 leaves: an automatic leaf size
+    // resolves to 2 here (an explicit 4 fails in the first squaring)
+    k2t_opts wo;
+    if (opts) wo = *opts; else k2t_default_opts(&wo);
+    if (wo.leaf_k == 0) wo.leaf_k = 2;
+    opts = &wo;
     // C <- A, rebuilt with the caller's options
     std::vector<uint32_t> r(a->nnz), c(a->nnz);
     uint64_t got = 0;

@@ -45,7 +45,7 @@ class Opts(ctypes.Structure):
                 ("threads", ctypes.c_uint32), ("band_rows", ctypes.c_uint32),
                 ("band_cols", ctypes.c_uint32), ("heavy_terms", ctypes.c_uint32),
                 ("heavy_mode", ctypes.c_uint32), ("leaf_k", ctypes.c_uint32),
-                ("coop_batch", ctypes.c_uint32), ("reserved", ctypes.c_uint32 * 2)]
+                ("reserved", ctypes.c_uint32 * 3)]
 
 
 class Stats(ctypes.Structure):

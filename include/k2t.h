@@ -130,18 +130,15 @@ typedef struct {
                                      2^bits of them per output and checks the count of every
                                      one), added in fp64 at the end; 1 in fp64 (fp64 atomics;
                                      slower).  See "Accumulation precision" below.                */
-    uint32_t leaf_k;              /* side of a leaf block: 2 (default; 0 = default) or 4.  4: the
-                                     leaf level stores 4x4 bitmaps (16-bit signatures, cell
-                                     (dr, dc) at bit 4*dr + dc), the larger leaves of section 5.6;
-                                     every other level keeps k = 2 (or k = 4 on the n_k4 top
-                                     levels).  Needs the CACHED engine (cache_last_internal = 1,
-                                     engine AUTO or CACHED); other engines give EINVAL.              */
-    uint32_t coop_batch;          /* CACHED: fp32 batches of at least this many vectors run with
-                                     the 8 warps of a thread block sharing one 256-node directory
-                                     block (a narrower window of x and y rows in flight, so L2
-                                     keeps them); smaller batches give each warp its own block.
-                                     Default 8; 0 = default; 0xffffffff = never                    */
-    uint32_t reserved[2];
+    uint32_t leaf_k;              /* side of a leaf block: 0 (default: chosen by the build), 2 or
+                                     4.  4: the leaf level stores 4x4 bitmaps (16-bit signatures,
+                                     cell (dr, dc) at bit 4*dr + dc), the larger leaves of section
+                                     5.6; every other level keeps k = 2 (or k = 4 on the n_k4 top
+                                     levels).  0 picks 4 when 2x2 leaves would hold at least 1.75
+                                     non-zeros each on average, else 2.  4x4 leaves need the
+                                     FUSED or CACHED engine (AUTO resolves to one of them);
+                                     LEVELSYNC and BANDED give EINVAL for 4 and use 2 for 0.      */
+    uint32_t reserved[3];
 } k2t_opts;
 
 /* ---- statistics -------------------------------------------------------- */
@@ -184,7 +181,8 @@ typedef struct {
 
 /* Fill *o with the defaults: k = 2, tree-only FUSED engine (AUTO), directory
  * offsets, top of at most 2^16 nodes, chunk_cap 2048, tile_m 2^20,
- * max_batch 32, no host vectors, CUDA graph on, all host threads. */
+ * max_batch 32, no host vectors, CUDA graph on, all host threads, leaf size
+ * chosen by the build, heavy_terms 160 in fp32 partial sums. */
 void k2t_default_opts(k2t_opts *o);
 
 /* Build the tree of the n_rows x n_cols Boolean matrix whose non-zeros are
@@ -310,7 +308,8 @@ int k2t_bool_product(const k2t_tree *a, const k2t_tree *b, const k2t_opts *opts,
 /* Transitive closure A+ (pairs joined by a path of one or more edges) of a
  * square tree by repeated squaring, C <- C or C C (section 7), until C stops
  * growing or max_iters squarings ran; *iters = squarings run.  *out is C's
- * tree built with opts.  Errors as k2t_bool_product; EINVAL for a
+ * tree built with opts (an automatic leaf size resolves to 2x2 leaves, which
+ * every squaring needs).  Errors as k2t_bool_product; EINVAL for a
  * non-square tree. */
 int k2t_bool_closure(const k2t_tree *a, const k2t_opts *opts, uint32_t max_iters, k2t_tree **out,
                      uint32_t *iters, void *stream);

@@ -26,8 +26,11 @@ WORKLOADS = {
     "weblike22-leaf4": (lambda: synth.weblike_c3(), dict(n_k4_levels=2, cache_last_internal=1, leaf_k=4),
                         [(0, 32), (1, 32)]),
     "social24-leaf4": (lambda: synth.social_c4(), dict(cache_last_internal=1, leaf_k=4), [(0, 8)]),
-    "clustered22": (lambda: synth.clustered(), dict(cache_last_internal=1), [(0, 1), (1, 1)]),
+    "clustered22": (lambda: synth.clustered(), dict(cache_last_internal=1, leaf_k=2), [(0, 1), (1, 1)]),
     "clustered22-leaf4": (lambda: synth.clustered(), dict(cache_last_internal=1, leaf_k=4), [(0, 1), (1, 1)]),
+    # tree-only with the automatic leaf size: 4x4 leaves on the FUSED engine
+    "clustered22-fused-auto": (lambda: synth.clustered(), dict(), [(0, 1), (1, 1)]),
+    "rmat20-fused-leaf4": (lambda: synth.rmat_c2(), dict(leaf_k=4), [(0, 1), (1, 1)]),
 }
 
 

@@ -23,11 +23,12 @@ ENGINES = [
     dict(engine=2, offsets=0, tile_m=16),              # level-sync, directory, many tiles
     dict(engine=2, offsets=1, tile_m=16),              # level-sync, scan
     dict(engine=2, offsets=0, tile_m=1 << 20, use_graph=0),
-    dict(engine=3, cache_last_internal=1),             # k^2+F (fp32 batches of 8+: block-cooperative)
-    dict(engine=3, cache_last_internal=1, coop_batch=1),  # k^2+F, block-cooperative at every width
+    dict(engine=3, cache_last_internal=1),             # k^2+F
     dict(engine=4, cache_last_internal=1),             # k^2+F by row band
     dict(engine=4, cache_last_internal=1, band_rows=16),
     dict(engine=3, cache_last_internal=1, leaf_k=4),   # k^2+F with 4x4 leaves (section 5.6)
+    dict(engine=1, leaf_k=4),                          # tree-only with 4x4 leaves
+    dict(engine=1, leaf_k=4, chunk_cap=4),
 ]
 
 
@@ -209,7 +210,7 @@ def test_heavy_outputs_large_hub(heavy_mode):
     a = np.arange(n, dtype=np.uint32)
     rows, cols = oracle.dedup_edges(np.concatenate([r0, np.full(n, 7, np.uint32), a]),
                                     np.concatenate([c0, a, np.full(n, 11, np.uint32)]))
-    for kw in (ENGINES[0], ENGINES[2], ENGINES[5], ENGINES[6], ENGINES[7], ENGINES[9]):
+    for kw in (ENGINES[0], ENGINES[2], ENGINES[5], ENGINES[6], ENGINES[8], ENGINES[9]):
         t = _tree(rows, cols, n, n, heavy_mode=heavy_mode, **kw)
         assert t.stats().heavy_rows >= 1 and t.stats().heavy_cols >= 1
         for B in (1, 16):
@@ -255,7 +256,7 @@ def test_rmat_medium_all_semirings():
     rows, cols = synth.rmat(17, 0.57, 0.19, 0.19, 1 << 20, 12)
     n = 1 << 17
     rng = np.random.default_rng(12)
-    for kw in (ENGINES[0], ENGINES[2], ENGINES[3], ENGINES[5], ENGINES[6], ENGINES[7], ENGINES[9]):
+    for kw in (ENGINES[0], ENGINES[2], ENGINES[3], ENGINES[5], ENGINES[6], ENGINES[8], ENGINES[9]):
         t = _tree(rows, cols, n, n, **kw)
         for semiring, B in ((PLUS_TIMES, 1), (PLUS_TIMES, 16), (BOOLEAN, 32), (TROPICAL, 8)):
             for d in (RIGHT, LEFT):

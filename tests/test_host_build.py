@@ -80,11 +80,33 @@ def test_build_figure1_leaf4():
     assert t.level_signatures(1).view(np.uint16).tolist() == [1 << 5, 1 | 1 << 5 | 1 << 13,
                                                               1 << 5 | 1 << 6 | 1 << 9 | 1 << 10,
                                                               1 << 10 | 1 << 11 | 1 << 14 | 1 << 15]
-    for bad in (dict(leaf_k=3, cache_last_internal=1), dict(leaf_k=4), dict(leaf_k=4, engine=1),
+    for bad in (dict(leaf_k=3, cache_last_internal=1), dict(leaf_k=4, engine=2),
                 dict(leaf_k=4, engine=2, cache_last_internal=1), dict(leaf_k=4, engine=4, cache_last_internal=1)):
         with pytest.raises(K.K2TError) as err:
             K.Tree(e[:, 0], e[:, 1], 8, 8, **bad)
         assert err.value.status == -1, bad
+    # the tree-only FUSED engine takes 4x4 leaves as well
+    for ok in (dict(leaf_k=4), dict(leaf_k=4, engine=1)):
+        assert K.Tree(e[:, 0], e[:, 1], 8, 8, **ok).stats().leaf_k == 4
+
+
+def test_automatic_leaf_size():
+    """leaf_k 0 (the default) picks 4x4 leaves when the 2x2 leaves would hold
+    at least 1.75 non-zeros on average, on the engines that have them (FUSED,
+    CACHED); the tree then equals the one built with leaf_k 4 explicitly."""
+    wl = synth.clustered(scale=12, block=16, per_row=8, seed=3)    # 2x2 leaves hold ~2.1 non-zeros
+    r, c = wl.rows, wl.cols
+    n = 1 << 12
+    for kw in (dict(), dict(cache_last_internal=1)):
+        auto = K.Tree(r, c, n, n, **kw)
+        four = K.Tree(r, c, n, n, leaf_k=4, **kw)
+        assert auto.stats().leaf_k == 4 and auto.opts.leaf_k == 0
+        for d in range(four.stats().levels):
+            assert np.array_equal(auto.level_signatures(d), four.level_signatures(d))
+    assert K.Tree(r, c, n, n, engine=2).stats().leaf_k == 2          # LEVELSYNC: 2x2 only
+    assert K.Tree(r, c, n, n, leaf_k=2).stats().leaf_k == 2
+    rr, cc = synth.rmat(12, 0.57, 0.19, 0.19, 30000, 4)               # ~1.03 per 2x2 leaf
+    assert K.Tree(rr, cc, n, n).stats().leaf_k == 2
 
 
 def test_build_figure1_and_top_level():
@@ -173,7 +195,7 @@ def test_options_struct_matches_header():
     """The binding's k2t_opts mirrors the header: defaults round-trip."""
     o = K.default_opts()
     assert o.band_rows == 4096 and o.chunk_cap == 2048 and o.tile_m == 1 << 20 and o.max_batch == 32
-    assert o.heavy_terms == 160 and o.leaf_k == 2
+    assert o.heavy_terms == 160 and o.leaf_k == 0
     # sizes and field offsets as a C compiler lays the header's structs out
     import subprocess
     import tempfile
@@ -230,11 +252,12 @@ def test_library_exports_every_declared_symbol():
 @pytest.mark.parametrize("heavy_terms", [0, 5, 30, 0xFFFFFFFF])
 def test_heavy_outputs_stats(heavy_terms):
     """Heavy outputs are those with more than heavy_terms non-zeros in the
-    input list (0 selects the default 160); their tables take one bit per
-    leaf, two words per 32 outputs, one word (list) and two words (record)
-    per heavy output per direction, plus max_batch fp32 words per partial sum
-    of the direction with more partial sums (heavy_mode 0) or max_batch fp64
-    sums per heavy output of the wider side (heavy_mode 1)."""
+    input list (0 selects the default 160).  Per direction with any, their
+    tables take one bit per leaf, one word per heavy output (the list) and
+    one record word per output up to the last heavy one (padded for a 16-byte
+    read); the sums take, for the direction with more, rows of max_batch fp32
+    words: 2^bits partial sums and two rows of fp64 slot per heavy output (the
+    slot alone for an output summed in fp64)."""
     rng = np.random.default_rng(21)
     nr, nc = 300, 200
     rows, cols, _ = synth.random_small(3, nr, nc, 0.05)
@@ -245,8 +268,9 @@ def test_heavy_outputs_stats(heavy_terms):
     t = K.Tree(rows, cols, nr, nc, heavy_terms=heavy_terms, max_batch=4)
     s = t.stats()
     lim = 160 if heavy_terms == 0 else heavy_terms
-    hr = int((np.bincount(rows, minlength=nr) > lim).sum()) if rows.size > lim else 0
-    hc = int((np.bincount(cols, minlength=nc) > lim).sum()) if rows.size > lim else 0
+    cr, cc = np.bincount(rows, minlength=nr), np.bincount(cols, minlength=nc)
+    hr = int((cr > lim).sum()) if rows.size > lim else 0
+    hc = int((cc > lim).sum()) if rows.size > lim else 0
     assert (s.heavy_rows, s.heavy_cols) == (hr, hc)
     if heavy_terms == 5:
         assert hr > 1 and hc > 1
@@ -255,19 +279,27 @@ def test_heavy_outputs_stats(heavy_terms):
     if heavy_terms == 0:
         assert hr == 1 and hc == 0   # the 150-entry hub row, with the random entries of row 7
     nl = int(s.level_nodes[s.levels - 1])
-    want = 0
-    for h, n in ((hr, nr), (hc, nc)):
+    tables = 0
+    acc_rows = 0
+    for d, (h, cnt) in enumerate(((hr, cr), (hc, cc))):
         if h:
-            want += ((nl + 31) // 32 + 1) * 4 + 2 * ((n + 31) // 32) * 4 + 4 * h + 8 * h
-    tables = want
-    want = tables + max(s.heavy_partials[0], s.heavy_partials[1]) * 4 * 4
+            last = int(np.nonzero(cnt > lim)[0].max())
+            hdir = ((last + 1 + 3) // 4 * 4 + 4) * 4
+            tables += ((nl + 31) // 32 + 1) * 4 + 4 * h + hdir
+            acc_rows = max(acc_rows, int(s.heavy_partials[d]) + 2 * h)
+    want = tables + acc_rows * 4 * 4
     assert s.heavy_kib == (want + 1023) // 1024
     if hr:
-        assert s.heavy_partials[0] >= 2 * hr and 0 < s.heavy_max_terms[0] <= lim
+        # every heavy output is split into at least two partial sums of at most
+        # the limit's terms, or (when one run of 32 inputs already holds more)
+        # summed in fp64
+        assert s.heavy_partials[0] >= 2 * (hr - s.heavy_fp64[0])
+        assert s.heavy_max_terms[0] <= lim and (s.heavy_max_terms[0] > 0 or s.heavy_fp64[0] == hr)
     base = K.Tree(rows, cols, nr, nc, heavy_terms=0xFFFFFFFF, max_batch=4).workspace_bytes()
-    assert want <= t.workspace_bytes() - base <= want + 9 * 256
+    assert want <= t.workspace_bytes() - base <= want + 8 * 256
     f64 = K.Tree(rows, cols, nr, nc, heavy_terms=heavy_terms, heavy_mode=1, max_batch=4).stats()
-    assert f64.heavy_kib == (tables + max(hr, hc) * 4 * 8 + 1023) // 1024   # fp64 mode: one double each
+    assert list(f64.heavy_partials) == [0, 0] and list(f64.heavy_fp64) == [hr, hc]
+    assert f64.heavy_kib == (tables + 2 * max(hr, hc) * 4 * 4 + 1023) // 1024   # fp64 mode: two rows each
     with pytest.raises(K.K2TError):
         K.Tree(rows, cols, nr, nc, heavy_mode=2)
 
