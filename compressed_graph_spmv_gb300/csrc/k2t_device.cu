@@ -345,11 +345,9 @@ int k2t_upload(k2t_tree *t, void *arena, uint64_t arena_bytes, void *stream)
     }
     if (L.vec_bytes) { d->vec[0] = at<void>(d->arena, L.vec_off[0]); d->vec[1] = at<void>(d->arena, L.vec_off[1]); }
     for (int dd = 0; dd < 2; ++dd) {
-        if (!L.hflag_bytes[dd]) continue;
-        d->hflag[dd] = at<uint32_t>(d->arena, L.hflag_off[dd]);
+        if (!L.hdir_bytes[dd]) continue;
         d->hdir[dd] = at<uint32_t>(d->arena, L.hdir_off[dd]);
         d->hlist[dd] = at<uint32_t>(d->arena, L.hlist_off[dd]);
-        if ((e = put(L.hflag_off[dd], L.hflag_bytes[dd], t->hflag[dd].data()))) return fail(e);
         if ((e = put(L.hdir_off[dd], L.hdir_bytes[dd], t->hdir[dd].data()))) return fail(e);
         if ((e = put(L.hlist_off[dd], L.hlist_bytes[dd], t->hlist[dd].data()))) return fail(e);
     }
@@ -367,7 +365,7 @@ int k2t_spmv_marked(k2t_tree *t, int32_t dir, int32_t semiring, float w, const v
     if (semiring < K2T_PLUS_TIMES || semiring > K2T_MIN_PLUS) return K2T_EINVAL;
     if (!x || !y || B == 0) return K2T_EINVAL;
     if (B > K2T_MAX_BATCH) return K2T_ERANGE;
-    if (semiring == K2T_PLUS_TIMES && t->dev->hflag[dir] && B > t->opts.max_batch) return K2T_ERANGE;
+    if (semiring == K2T_PLUS_TIMES && t->dev->hdir[dir] && B > t->opts.max_batch) return K2T_ERANGE;
     if (((uintptr_t)x | (uintptr_t)y) & 3u) return K2T_EINVAL;
     const uint64_t n_in = dir == K2T_RIGHT ? t->n_cols : t->n_rows;
     const uint64_t n_out = dir == K2T_RIGHT ? t->n_rows : t->n_cols;

@@ -540,32 +540,6 @@ void heavy_outputs(const uint32_t *out_ids, const uint32_t *in_ids, uint64_t nnz
     t->hrows[dir] = rows;
 }
 
-// Leaf flags of one direction: bit i set when leaf i (level order; block
-// origin (side*q.r, side*q.c), side 2 or 4) has a heavy output among its rows
-// (dir 0) or columns (dir 1).  prefixes[i] is leaf i's path prefix.
-void heavy_leaf_flags(k2t_tree *t, int dir, const uint64_t *prefixes, uint64_t nl, int nt)
-{
-    const std::vector<uint32_t> &hdir = t->hdir[dir];
-    const uint32_t side = t->leaf_k4 ? 4u : 2u;
-    std::vector<uint32_t> &fl = t->hflag[dir];
-    fl.assign((nl + 31) / 32 + 1, 0);
-    const int d = t->levels - 1;
-    const uint64_t words = (nl + 31) / 32;
-    parallel_for(nt, [&](int th) {
-        uint64_t lo = words * th / nt, hi = words * (th + 1) / nt;
-        for (uint64_t w = lo; w < hi; ++w) {
-            uint32_t v = 0;
-            for (uint64_t i = 32 * w; i < std::min<uint64_t>(32 * w + 32, nl); ++i) {
-                Coord q = prefix_coord(prefixes[i], d, t->n_k4);
-                uint64_t o = (uint64_t)side * (dir == 0 ? q.r : q.c);
-                for (uint32_t k = 0; k < side; ++k)
-                    if (o + k < hdir.size() && hdir[o + k]) { v |= 1u << (i % 32); break; }
-            }
-            fl[w] = v;
-        }
-    });
-}
-
 }  // namespace
 
 void compute_layout(k2t_tree *t)
@@ -644,8 +618,6 @@ void compute_layout(k2t_tree *t)
         uint64_t rows = 0;
         for (int dd = 0; dd < 2; ++dd) {
             if (t->hlist[dd].empty()) continue;
-            L.hflag_bytes[dd] = t->hflag[dd].size() * sizeof(uint32_t);
-            L.hflag_off[dd] = take(L.hflag_bytes[dd]);
             L.hdir_bytes[dd] = t->hdir[dd].size() * sizeof(uint32_t);
             L.hdir_off[dd] = take(L.hdir_bytes[dd]);
             L.hlist_bytes[dd] = t->hlist[dd].size() * sizeof(uint32_t);
@@ -821,9 +793,6 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
                 if (nn >= (1ull << 32)) { delete t; return K2T_ERANGE; }
                 t->nodes[(size_t)d] = nn;
                 pack_level(t, d, sg.data(), nn, nt);
-                if (d == l - 1)
-                    for (int dd = 0; dd < 2; ++dd)
-                        if (!t->hlist[dd].empty()) heavy_leaf_flags(t, dd, nxt, nn, nt);
                 if (d == l - 2 && (t->engine == K2T_ENGINE_CACHED || t->engine == K2T_ENGINE_BANDED)) {
                     t->cached.resize(nn);
                     parallel_for(nt, [&](int th) {
@@ -966,7 +935,7 @@ int k2t_stats_get(const k2t_tree *t, k2t_stats *s)
     s->heavy_rows = (uint32_t)t->hlist[0].size();
     s->heavy_cols = (uint32_t)t->hlist[1].size();
     uint64_t hb = L.acc_bytes;
-    for (int dd = 0; dd < 2; ++dd) hb += L.hflag_bytes[dd] + L.hdir_bytes[dd] + L.hlist_bytes[dd];
+    for (int dd = 0; dd < 2; ++dd) hb += L.hdir_bytes[dd] + L.hlist_bytes[dd];
     s->heavy_kib = (uint32_t)((hb + 1023) / 1024);
     s->leaf_k = t->leaf_k4 ? 4u : 2u;
     for (int dd = 0; dd < 2; ++dd) {

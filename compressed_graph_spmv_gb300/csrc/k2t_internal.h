@@ -86,7 +86,6 @@ struct ArenaLayout {
     uint64_t err_off, err_bytes;        // device error word
     uint64_t vec_off[2], vec_bytes;     // host-product x and y
     // heavy outputs of plus-times products, per direction (0 right, 1 left)
-    uint64_t hflag_off[2], hflag_bytes[2];  // one bit per leaf: touches a heavy output
     uint64_t hdir_off[2], hdir_bytes[2];    // per output up to the last heavy one: its record
     uint64_t hlist_off[2], hlist_bytes[2];  // the heavy outputs, ascending
     uint64_t acc_off, acc_bytes;            // rows of the heavy sums, shared by both directions
@@ -129,7 +128,6 @@ struct k2t_tree {
     // Heavy plus-times outputs (more than opts.heavy_terms non-zeros),
     // per direction (0: rows, outputs of right products; 1: columns):
     std::vector<uint32_t> hlist[2];   // the outputs, ascending
-    std::vector<uint32_t> hflag[2];   // bit j: leaf j (level order) has a heavy output
     std::vector<uint32_t> hdir[2];    // record of every output below the last heavy one + padding
     uint64_t hrows[2] = {0, 0};       // accumulator rows of the direction
     uint64_t hparts[2] = {0, 0};      // fp32 partial sums of the direction

@@ -35,9 +35,8 @@ struct VecArgs {
     uint32_t mask;   // Boolean: bits of the batch
     uint64_t n_out;  // entries (vertices) of y
     uint64_t n_in;   // entries (vertices) of x
-    // Heavy plus-times outputs (null hflag: none in this product)
-    const uint32_t *hflag;  // bit j: leaf j (level order) has a heavy output
-    const uint32_t *hdir;   // per output below hdir_len: its record (heavy_record), 0 if not heavy
+    // Heavy plus-times outputs (null hdir: none in this product)
+    const uint32_t *hdir;   // per output below hdir_len: its record, 0 if not heavy
     uint32_t hdir_len;
     float *acc;             // rows of B fp32 words: partial sums and fp64 slots of heavy outputs
 };
@@ -142,17 +141,18 @@ __device__ __forceinline__ bool is_noop_word(uint32_t v)
 
 // ---- heavy outputs (plus-times) ------------------------------------------------
 // An output with more non-zeros than one fp32 sum can take within the bound
-// is "heavy".  Its record (heavy_record, built once per tree) names rows of
+// is "heavy".  Its record (one word per output, built once per tree) names rows of
 // the accumulator array acc (B fp32 words a row): 2^bits fp32 partial sums,
 // each receiving at most heavy_terms terms, then an fp64 slot of two rows (B
 // doubles) for the sums fp64 warp windows hand over; or, bits kHeavyFp64, the
-// fp64 slot alone, which then takes every term.  heavy_leaf: leaf li has a
-// heavy output.  heavy_word: the records of a 2x2 leaf's outputs out (even)
-// and out + 1, read together (one 8-byte load); only called for flagged
-// leaves, whose outputs lie below hdir_len.
-__device__ __forceinline__ uint32_t heavy_leaf(const VecArgs &va, uint32_t li)
+// fp64 slot alone, which then takes every term.  The records cover the
+// outputs below hdir_len (the last heavy output, rounded up to a multiple of
+// 4, plus 4): heavy_near(out) says whether a leaf with first output `out`
+// may have a heavy output; heavy_word: the records of a 2x2 leaf's outputs
+// out (even) and out + 1, read together (one 8-byte load), for such a leaf.
+__device__ __forceinline__ uint32_t heavy_near(const VecArgs &va, uint32_t out)
 {
-    return (__ldg(va.hflag + (li >> 5)) >> (li & 31u)) & 1u;
+    return out < va.hdir_len ? 1u : 0u;
 }
 
 __device__ __forceinline__ uint2 heavy_word(const VecArgs &va, uint32_t out)
@@ -220,103 +220,6 @@ template <> struct VecLoad<4> {
         v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
     }
 };
-
-// Cells of U leaves at once.  Leaf u is the 2x2 block with origin (r[u], c[u])
-// and set cells lam[u] (bit 2*dr + dc).  The two cells that share an output
-// are combined with the semiring's addition first, so a leaf issues at most two
-// atomics per vector slice.  All gathers of x for the U leaves are issued
-// before any atomic, so their latencies overlap.
-//   right: output r gets bits 0 (input c) and 1 (input c+1); output r+1 bits 2, 3
-//   left:  output c gets bits 0 (input r) and 2 (input r+1); output c+1 bits 1, 3
-// win != null: updates go to the shared-memory window win[(out - lo) * width + k]
-// instead of y (width = B words, 1 for Boolean).  Bit u of fl (plus-times):
-// leaf u has heavy outputs; those go to their heavy sums instead.
-template <int SR, int DIR, int VW, int U>
-__device__ __forceinline__ void leaf_group(const uint32_t (&lam)[U], const uint32_t (&r)[U], const uint32_t (&c)[U],
-                                           uint32_t fl, const VecArgs &a, uint32_t *win, uint32_t lo)
-{
-    bool a0[U], a1[U], b0[U], b1[U];
-    uint32_t in[U], out[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        in[u] = DIR == K2T_RIGHT ? c[u] : r[u];
-        out[u] = DIR == K2T_RIGHT ? r[u] : c[u];
-        a0[u] = lam[u] & 1u;
-        a1[u] = DIR == K2T_RIGHT ? (lam[u] & 2u) : (lam[u] & 4u);
-        b0[u] = DIR == K2T_RIGHT ? (lam[u] & 4u) : (lam[u] & 2u);
-        b1[u] = lam[u] & 8u;
-    }
-    if constexpr (SR == K2T_BOOLEAN) {
-        const uint32_t *x = static_cast<const uint32_t *>(a.x);
-        uint32_t *y = static_cast<uint32_t *>(a.y);
-        uint32_t x0[U], x1[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            x0[u] = (a0[u] || b0[u]) ? __ldg(x + in[u]) : 0u;
-            x1[u] = (a1[u] || b1[u]) ? __ldg(x + in[u] + 1) : 0u;
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            uint32_t v0 = ((a0[u] ? x0[u] : 0u) | (a1[u] ? x1[u] : 0u)) & a.mask;
-            uint32_t v1 = ((b0[u] ? x0[u] : 0u) | (b1[u] ? x1[u] : 0u)) & a.mask;
-            if (win) {
-                if (v0) atomicOr(win + (out[u] - lo), v0);
-                if (v1) atomicOr(win + (out[u] + 1 - lo), v1);
-            } else {
-                if (v0) atomicOr(y + out[u], v0);
-                if (v1) atomicOr(y + out[u] + 1, v1);
-            }
-        }
-    } else {
-        using S = Fp32Sem<SR>;
-        const float *x = static_cast<const float *>(a.x);
-        float *y = static_cast<float *>(a.y);
-        const size_t B = a.B;
-        for (uint32_t k = 0; k < a.B; k += VW) {
-            float x0[U][VW], x1[U][VW];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (a0[u] || b0[u]) VecLoad<VW>::load(x + (size_t)in[u] * B + k, x0[u]);
-                if (a1[u] || b1[u]) VecLoad<VW>::load(x + (size_t)(in[u] + 1) * B + k, x1[u]);
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                float v0[VW], v1[VW];
-#pragma unroll
-                for (int q = 0; q < VW; ++q) {
-                    float c0 = (a0[u] || b0[u]) ? S::contrib(x0[u][q], a.w) : S::zero();
-                    float c1 = (a1[u] || b1[u]) ? S::contrib(x1[u][q], a.w) : S::zero();
-                    v0[q] = a0[u] ? (a1[u] ? S::plus(c0, c1) : c0) : c1;
-                    v1[q] = b0[u] ? (b1[u] ? S::plus(c0, c1) : c0) : c1;
-                }
-                if (win) {
-                    if (a0[u] || a1[u]) {
-                        uint32_t *w0 = win + (size_t)(out[u] - lo) * B + k;
-#pragma unroll
-                        for (int q = 0; q < VW; ++q)
-                            if (!S::skip(v0[q])) smem_update<SR>(w0 + q, __float_as_uint(v0[q]));
-                    }
-                    if (b0[u] || b1[u]) {
-                        uint32_t *w1 = win + (size_t)(out[u] + 1 - lo) * B + k;
-#pragma unroll
-                        for (int q = 0; q < VW; ++q)
-                            if (!S::skip(v1[q])) smem_update<SR>(w1 + q, __float_as_uint(v1[q]));
-                    }
-                } else {
-                    const uint2 h = SR == K2T_PLUS_TIMES && ((fl >> u) & 1u) ? heavy_word(a, out[u]) : make_uint2(0u, 0u);
-                    if (a0[u] || a1[u]) {
-                        if (h.x) heavy_put<SR, VW>(a, h.x, in[u], k, v0, x0[u], x1[u], a0[u], a1[u]);
-                        else S::update(y + (size_t)out[u] * B + k, v0);
-                    }
-                    if (b0[u] || b1[u]) {
-                        if (h.y) heavy_put<SR, VW>(a, h.y, in[u], k, v1, x0[u], x1[u], b0[u], b1[u]);
-                        else S::update(y + (size_t)(out[u] + 1) * B + k, v1);
-                    }
-                }
-            }
-        }
-    }
-}
 
 __device__ __forceinline__ Coord child_of(Coord p, int b)
 {
@@ -428,137 +331,15 @@ __device__ __forceinline__ bool tile_block(const uint8_t *sig, const uint32_t *d
     return true;
 }
 
-// Flat leaf kernel: one thread per node of the last internal level, one warp
-// per 32 consecutive nodes, as in Algorithm 1, lines 12-20.  The warp's first
-// leaf comes from the directory sample of its 256-node block plus the fan-outs
-// before it in the block (or, in scan mode, from the tile's prefix sums); a
-// warp scan of the fan-outs places every node's leaves.  Each thread reads its
-// node's coordinates and leaf signatures, gathers all x entries its leaves
-// need, then applies the (at most 8) combined updates.
-//   nodes [a, a+count) of the level (level size n_level); src holds the
-//   coordinates of node a at index 0.
-constexpr int kFlatThreads = 256;
-
-// Single-slice fast path (B = 1 fp32, or any Boolean batch): the two input
-// entries of each child leaf block are adjacent, so both are loaded before the
-// leaf signatures are known (same sector, no extra traffic); the node then
-// costs two dependent memory round trips: (directory, signatures,
-// coordinates) and (leaf signatures, x).
-template <int SR, int DIR>
-__device__ __forceinline__ void node_leaves_spec(uint32_t sg, uint32_t off, Coord p, const uint8_t *leaf,
-                                                 const VecArgs &va)
-{
-    uint32_t lam[4], xin[4], xo[4][2], fl = 0u;
-    const bool heavy = SR == K2T_PLUS_TIMES && va.hflag != nullptr;
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        const uint32_t r = 4u * p.r + 2u * (uint32_t)(b >> 1);
-        const uint32_t c = 4u * p.c + 2u * (uint32_t)(b & 1);
-        xin[b] = DIR == K2T_RIGHT ? c : r;
-        lam[b] = 0u;
-        xo[b][0] = 0u;
-        xo[b][1] = 0u;
-        if (sg & (1u << b)) {
-            const uint32_t li = off + (uint32_t)__popc(sg & ((1u << b) - 1u));
-            lam[b] = nibble_at(leaf, li);
-            const uint32_t *x = static_cast<const uint32_t *>(va.x);
-            xo[b][0] = __ldg(x + xin[b]);
-            if (xin[b] + 1u < va.n_in) xo[b][1] = __ldg(x + xin[b] + 1u);
-            if (heavy) fl |= heavy_leaf(va, li) << b;
-        }
-    }
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        const uint32_t l = lam[b];
-        if (!l) continue;
-        const uint32_t out = DIR == K2T_RIGHT ? 4u * p.r + 2u * (uint32_t)(b >> 1) : 4u * p.c + 2u * (uint32_t)(b & 1);
-        const bool a0 = l & 1u;
-        const bool a1 = DIR == K2T_RIGHT ? (l & 2u) : (l & 4u);
-        const bool b0 = DIR == K2T_RIGHT ? (l & 4u) : (l & 2u);
-        const bool b1 = l & 8u;
-        if constexpr (SR == K2T_BOOLEAN) {
-            uint32_t *y = static_cast<uint32_t *>(va.y);
-            const uint32_t v0 = ((a0 ? xo[b][0] : 0u) | (a1 ? xo[b][1] : 0u)) & va.mask;
-            const uint32_t v1 = ((b0 ? xo[b][0] : 0u) | (b1 ? xo[b][1] : 0u)) & va.mask;
-            if (v0) atomicOr(y + out, v0);
-            if (v1) atomicOr(y + out + 1, v1);
-        } else {
-            using S = Fp32Sem<SR>;
-            float *y = static_cast<float *>(va.y);
-            const float c0 = S::contrib(__uint_as_float(xo[b][0]), va.w);
-            const float c1 = S::contrib(__uint_as_float(xo[b][1]), va.w);
-            const uint2 h = SR == K2T_PLUS_TIMES && ((fl >> b) & 1u) ? heavy_word(va, out) : make_uint2(0u, 0u);
-            const float xa[1] = {__uint_as_float(xo[b][0])}, xb[1] = {__uint_as_float(xo[b][1])};
-            if (a0 || a1) {
-                const float v[1] = {a0 ? (a1 ? S::plus(c0, c1) : c0) : c1};
-                if (h.x) heavy_put<SR, 1>(va, h.x, xin[b], 0u, v, xa, xb, a0, a1);
-                else if (!S::skip(v[0])) S::update(y + out, v);
-            }
-            if (b0 || b1) {
-                const float v[1] = {b0 ? (b1 ? S::plus(c0, c1) : c0) : c1};
-                if (h.y) heavy_put<SR, 1>(va, h.y, xin[b], 0u, v, xa, xb, b0, b1);
-                else if (!S::skip(v[0])) S::update(y + out + 1, v);
-            }
-        }
-    }
-}
-
-template <int SR, int DIR, int VW>
-__global__ void __launch_bounds__(kFlatThreads, 3)
-flat_leaf_kernel(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix, uint32_t leaf_base, uint32_t a,
-                 uint32_t count, const Coord *src, const uint8_t *leaf, VecArgs va)
-{
-    const uint32_t lane = threadIdx.x & 31u;
-    const uint32_t rel0 = blockIdx.x * kFlatThreads + (threadIdx.x & ~31u);  // warp's first node, tile-relative
-    if (rel0 >= count) return;
-    const uint32_t t0 = a + rel0;
-    const uint32_t t = t0 + lane;
-    const bool valid = rel0 + lane < count;
-    // first memory round trip: all independent loads
-    const uint32_t sg = valid ? nibble_at(sig, t) : 0u;
-    Coord p{0u, 0u};
-    if (valid) p = src[rel0 + lane];
-    uint32_t base;
-    if (dir) {
-        const uint32_t g = t0 / kDirS;
-        base = __ldg(dir + g) + (t0 > g * kDirS ? warp_popc_range(sig, g * kDirS, t0) : 0u);
-    } else {
-        const uint32_t j = rel0 / 256u;
-        const uint32_t bs = a + 256u * j;
-        base = leaf_base + __ldg(prefix + j) + (t0 > bs ? warp_popc_range(sig, bs, t0) : 0u);
-    }
-    const uint32_t f = (uint32_t)__popc(sg);
-    const uint32_t off = base + warp_incl_scan(f) - f;
-    if (!sg) return;
-    if (SR == K2T_BOOLEAN || (VW == 1 && va.B == 1)) {
-        node_leaves_spec<SR, DIR>(sg, off, p, leaf, va);
-        return;
-    }
-    uint32_t lam[4], r[4], c[4], fl = 0u;
-    const bool heavy = SR == K2T_PLUS_TIMES && va.hflag != nullptr;
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        lam[b] = 0u;
-        r[b] = 4u * p.r + 2u * (uint32_t)(b >> 1);
-        c[b] = 4u * p.c + 2u * (uint32_t)(b & 1);
-        if (sg & (1u << b)) {
-            const uint32_t li = off + (uint32_t)__popc(sg & ((1u << b) - 1u));
-            lam[b] = nibble_at(leaf, li);
-            if (heavy) fl |= heavy_leaf(va, li) << b;
-        }
-    }
-    leaf_group<SR, DIR, VW, 4>(lam, r, c, fl, va, nullptr, 0u);
-}
-
 // One single-slice update of a warp window entry: the semiring's shared
-// atomic on a 32-bit word, or (w64, plus-times) an fp64 add on entry i of a
-// window of doubles.
+// atomic on a 32-bit word, or (w64, plus-times) an fp64 add of d, the leaf's
+// cells w*x_j summed in fp64, on entry i of a window of doubles.
 template <int SR>
-__device__ __forceinline__ void window_put(uint32_t *win, uint32_t i, float v, bool w64)
+__device__ __forceinline__ void window_put(uint32_t *win, uint32_t i, float v, double d, bool w64)
 {
     if constexpr (SR == K2T_PLUS_TIMES) {
         if (w64) {
-            atomicAdd(reinterpret_cast<double *>(win) + i, (double)v);
+            atomicAdd(reinterpret_cast<double *>(win) + i, d);
             return;
         }
     }
@@ -604,7 +385,7 @@ __device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint
                 const float v[1] = {a0 ? (a1 ? S::plus(c0, c1) : c0) : c1};
                 if (h.x) heavy_put<SR, 1>(va, h.x, in_of(u), 0u, v, xa, xb, a0, a1);
                 else if (!S::skip(v[0])) {
-                    if (win) window_put<SR>(win, out[u] - lo, v[0], w64);
+                    if (win) window_put<SR>(win, out[u] - lo, v[0], (a0 ? (double)c0 : 0.0) + (a1 ? (double)c1 : 0.0), w64);
                     else S::update(y + out[u], v);
                 }
             }
@@ -612,7 +393,7 @@ __device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint
                 const float v[1] = {b0 ? (b1 ? S::plus(c0, c1) : c0) : c1};
                 if (h.y) heavy_put<SR, 1>(va, h.y, in_of(u), 0u, v, xa, xb, b0, b1);
                 else if (!S::skip(v[0])) {
-                    if (win) window_put<SR>(win, out[u] + 1 - lo, v[0], w64);
+                    if (win) window_put<SR>(win, out[u] + 1 - lo, v[0], (b0 ? (double)c0 : 0.0) + (b1 ? (double)c1 : 0.0), w64);
                     else S::update(y + out[u] + 1, v);
                 }
             }
@@ -628,6 +409,7 @@ __device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint
 #define K2T_WARP_WINDOW 256
 #endif
 constexpr int kLeafU = K2T_LEAF_U;                  // leaves per lane per round (one vector slice)
+constexpr int kBatchU = 2;                          // leaves per lane group per round (batches)
 constexpr uint32_t kWarpWindow = K2T_WARP_WINDOW;   // words of a warp's output window
 
 // Per-warp segmented scatter.  [mn, mx] bounds the warp's output coordinates
@@ -677,7 +459,7 @@ __device__ __forceinline__ uint32_t *warp_window_begin(uint32_t mn, uint32_t mx,
     if (mn > mx) return nullptr;
     const uint64_t span64 = (uint64_t)unit * ((uint64_t)mx - mn + 1u);
     if (span64 * width > kWarpWindow) return nullptr;
-    if (SR == K2T_PLUS_TIMES && va.hflag != nullptr && warp_span_has_heavy(va, lo, (uint32_t)span64)) {
+    if (SR == K2T_PLUS_TIMES && va.hdir != nullptr && warp_span_has_heavy(va, lo, (uint32_t)span64)) {
         if (width != 1u || 2u * span64 > kWarpWindow) return nullptr;
         wmode = kWinF64;
     }
@@ -799,13 +581,16 @@ __device__ __forceinline__ void leaf_slice(uint32_t lam, uint32_t r, uint32_t c,
 //    adjacent threads per node, section 3.6).
 // Updates go to the window when there is one (wmode as warp_window_begin
 // says), else to y; heavy plus-times outputs outside a window go to their
-// partial sums.
+// partial sums.  out_min: no output of the warp's leaves is below it (0 when
+// unknown); a warp whose outputs all lie past the last heavy one skips the
+// heavy lookups.
 template <int SR, int DIR, int VW, class LeafAt>
 __device__ __forceinline__ void warp_leaf_rounds(uint32_t jb, uint32_t je, LeafAt &&leaf_at, const VecArgs &va,
-                                                 uint32_t *win, uint32_t lo, int wmode = kWinF32)
+                                                 uint32_t *win, uint32_t lo, int wmode, uint32_t out_min)
 {
     const uint32_t lane = threadIdx.x & 31u;
-    const bool heavy = SR == K2T_PLUS_TIMES && va.hflag != nullptr && (!win || wmode == kWinShared);
+    const bool heavy = SR == K2T_PLUS_TIMES && va.hdir != nullptr && out_min < va.hdir_len &&
+                       (!win || wmode == kWinShared);
     const bool w64 = win && wmode == kWinF64;
     if (SR == K2T_BOOLEAN || (VW == 1 && va.B == 1)) {
         constexpr int U = kLeafU;
@@ -822,7 +607,7 @@ __device__ __forceinline__ void warp_leaf_rounds(uint32_t jb, uint32_t je, LeafA
                 uint32_t li = 0u;
                 if (j < je) {
                     leaf_at(j, lam[u], r[u], c[u], li);
-                    if (heavy) fl |= heavy_leaf(va, li) << u;
+                    if (heavy) fl |= heavy_near(va, DIR == K2T_RIGHT ? r[u] : c[u]) << u;
                 }
             }
             uint32_t xo[U][2], out[U];
@@ -855,7 +640,7 @@ __device__ __forceinline__ void warp_leaf_rounds(uint32_t jb, uint32_t je, LeafA
         return;
     }
     if constexpr (SR != K2T_BOOLEAN) {
-        constexpr int U = 2;
+        constexpr int U = kBatchU;
         const uint32_t G = va.B / VW;                    // lanes per leaf (B is a multiple of VW)
         const uint32_t per = G <= 32u ? 32u / G : 1u;    // leaves per lane-group round
         const uint32_t groups = G <= 32u ? G : 32u;      // lanes that own a slice per round
@@ -874,7 +659,8 @@ __device__ __forceinline__ void warp_leaf_rounds(uint32_t jb, uint32_t je, LeafA
                 uint32_t li = 0u;
                 if (active && j < je) {
                     leaf_at(j, lam[u], r[u], c[u], li);
-                    if (heavy && heavy_leaf(va, li)) hv[u] = heavy_word(va, DIR == K2T_RIGHT ? r[u] : c[u]);
+                    if (heavy && heavy_near(va, DIR == K2T_RIGHT ? r[u] : c[u]))
+                        hv[u] = heavy_word(va, DIR == K2T_RIGHT ? r[u] : c[u]);
                 }
             }
             // a group of G lanes covers the row; rows wider than 32 slices loop
@@ -887,50 +673,92 @@ __device__ __forceinline__ void warp_leaf_rounds(uint32_t jb, uint32_t je, LeafA
     }
 }
 
-// k^2+F engine (section 3.5): one warp per 256-node directory block of the
-// last internal level.  The warp reads the block's 128 bytes of signatures
-// (one word of 8 nibbles per lane), its directory sample and the cached
-// coordinates; a warp scan of the fan-outs turns the block into a list of its
-// leaves (node, quadrant) in shared memory.  The lanes then take the leaves
-// round-robin: leaf signature and the x entries of its two inputs are loaded
-// together, then the combined updates are applied.  Every lane does the same
-// work per leaf, whatever the fan-out of its node.
+// The nodes of one warp's block of the last internal level, within the tile
+// [a, a + count): block g of the tile (directory mode: the 256-node block of
+// the directory, clipped to the tile; scan mode, prefix != null: nodes
+// a + 256 g ..., the tile's g-th block of 256).  Sets the block's first node
+// blk, the tile-clipped range [s, e), the first leaf `base` of node s, and
+// lane's 8 nibbles (nodes blk + 8 lane ..., those outside [s, e) cleared);
+// false when the block lies past the tile.
+__device__ __forceinline__ bool tile_warp_block(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix,
+                                                uint32_t leaf_base, uint32_t a, uint32_t count, uint32_t g,
+                                                uint32_t &blk, uint32_t &s, uint32_t &e, uint32_t &base,
+                                                uint32_t &w)
+{
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t end = a + count;
+    if (prefix) {
+        blk = a + kDirS * g;
+        if (blk >= end) return false;
+        s = blk;
+        e = min(blk + kDirS, end);
+        base = leaf_base + __ldg(prefix + g);
+        const uint32_t t0 = blk + 8u * lane;
+        w = t0 < e ? load8(sig, t0, e) : 0u;
+        return true;
+    }
+    const uint32_t G = a / kDirS + g;
+    blk = G * kDirS;
+    if (blk >= end) return false;
+    s = max(blk, a);
+    e = min(blk + kDirS, end);
+    const uint32_t t0 = blk + 8u * lane;
+    w = 0u;
+    uint32_t pre = 0u;   // fan-outs of the block's nodes before s (the tile's start)
+    if (t0 < e) {
+        const uint32_t word = __ldg(reinterpret_cast<const uint32_t *>(sig + blk / 2) + lane);
+        const uint32_t lo = s > t0 ? min(s - t0, 8u) : 0u;          // nibbles before s
+        const uint32_t hi = min(e - t0, 8u);                          // nibbles before e
+        const uint32_t below_lo = lo == 8u ? 0xffffffffu : ((1u << (4u * lo)) - 1u);
+        const uint32_t below_hi = hi == 8u ? 0xffffffffu : ((1u << (4u * hi)) - 1u);
+        w = word & below_hi & ~below_lo;
+        pre = (uint32_t)__popc(word & below_lo);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) pre += __shfl_xor_sync(0xffffffffu, pre, o);
+    base = __ldg(dir + G) + pre;
+    return true;
+}
+
+// Leaf step over a tile [a, a + count) of the last internal level whose
+// coordinates are known (coords[i] = node a + i): the k^2+F engine (section
+// 3.5) over the whole cached level, and the leaf tiles of the level-
+// synchronous engine (section 3.4) over their frontier buffers.  One warp per
+// 256-node block: the warp reads the block's signatures (one word of 8
+// nibbles per lane), the first leaf from the directory (or the tile's scan),
+// and the coordinates; a warp scan of the fan-outs turns the block into a
+// list of its leaves (node, quadrant) in shared memory.  The lanes then take
+// the leaves round-robin: leaf signature and the x entries of its two inputs
+// are loaded together, then the combined updates are applied.  Every lane
+// does the same work per leaf, whatever the fan-out of its node.
 constexpr int kCachedWarps = 8;
 
 // Blocks per SM the kernel is compiled for: 5 for 4-wide batches (48
 // registers, no spills; 5% faster than 4 blocks on the 300M-edge R-MAT at
-// B = 16), 4 otherwise (at 5 the single-vector path spills and runs 13%
-// slower).
+// B = 16, and 3 or 4 leaves per lane group at 4 or 3 blocks are slower), 4
+// otherwise (at 5 the single-vector path spills and runs 13% slower).
 template <int VW> constexpr int cached_min_blocks() { return VW == 4 ? 5 : 4; }
 
 template <int SR, int DIR, int VW>
 __global__ void __launch_bounds__(32 * kCachedWarps, cached_min_blocks<VW>())
-cached_block_kernel(const uint8_t *sig, const uint32_t *dir, uint32_t n, const Coord *coords, const uint8_t *leaf,
-                    VecArgs va)
+cached_block_kernel(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix, uint32_t leaf_base, uint32_t a,
+                    uint32_t count, const Coord *coords, const uint8_t *leaf, VecArgs va)
 {
     __shared__ Coord cs[kCachedWarps][kDirS];
     __shared__ uint16_t slots[kCachedWarps][4 * kDirS];
     __shared__ __align__(16) uint32_t wins[kCachedWarps][kWarpWindow];
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
-    const uint32_t g = blockIdx.x * kCachedWarps + warp;
-    const uint32_t s = g * kDirS;
-    if (s >= n) return;
-    const uint32_t cnt = min(n - s, kDirS);
+    uint32_t blk, s, e, base, w;
+    if (!tile_warp_block(sig, dir, prefix, leaf_base, a, count, blockIdx.x * kCachedWarps + warp, blk, s, e, base, w))
+        return;
     Coord *cw = cs[warp];
     uint16_t *sl = slots[warp];
-    // signatures, directory sample, coordinates
-    uint32_t w = 0;
-    if (8u * lane < cnt) {
-        w = __ldg(reinterpret_cast<const uint32_t *>(sig + s / 2) + lane);
-        if (8u * lane + 8u > cnt) w &= (1u << (4u * (cnt - 8u * lane))) - 1u;
-    }
-    const uint32_t base = __ldg(dir + g);
     uint32_t mn = 0xffffffffu, mx = 0u;
 #pragma unroll
     for (uint32_t q = 0; q < kDirS / 32; ++q) {
-        const uint32_t i = 32u * q + lane;
-        if (i < cnt) {
-            const Coord p = coords[s + i];
+        const uint32_t i = 32u * q + lane;   // node blk + i
+        if (blk + i >= s && blk + i < e) {
+            const Coord p = coords[blk + i - a];
             cw[i] = p;
             const uint32_t o = DIR == K2T_RIGHT ? p.r : p.c;
             mn = min(mn, o);
@@ -953,14 +781,14 @@ cached_block_kernel(const uint8_t *sig, const uint32_t *dir, uint32_t n, const C
     uint32_t *win = warp_window_begin<SR>(mn, mx, 4u, width, wins[warp], lo, span, va, wmode);
     __syncwarp();
     warp_leaf_rounds<SR, DIR, VW>(0u, total, [&](uint32_t j, uint32_t &lam, uint32_t &r, uint32_t &c, uint32_t &li) {
-        const uint32_t e = sl[j];
-        const Coord p = cw[e >> 2];
-        const uint32_t b = e & 3u;
+        const uint32_t el = sl[j];
+        const Coord p = cw[el >> 2];
+        const uint32_t b = el & 3u;
         r = 4u * p.r + 2u * (b >> 1);
         c = 4u * p.c + 2u * (b & 1u);
         li = base + j;
         lam = nibble_at(leaf, li);
-    }, va, win, lo, wmode);
+    }, va, win, lo, wmode, lo);
     if (win) warp_window_flush<SR>(win, lo, span, width, va, wmode);
 }
 
@@ -1050,12 +878,14 @@ __device__ __forceinline__ void leaf4_apply1(const uint32_t (&lam)[U], const uin
                     }
                 }
                 float v[1] = {S::zero()};
+                double d = 0.0;
                 bool any = false;
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     if ((s >> i) & 1u) {
                         const float c = S::contrib(__uint_as_float(xo[u][i]), va.w);
                         v[0] = any ? S::plus(v[0], c) : c;
+                        if (SR == K2T_PLUS_TIMES && w64) d += (double)c;
                         any = true;
                     }
                 if (hd.p32) {
@@ -1063,7 +893,7 @@ __device__ __forceinline__ void leaf4_apply1(const uint32_t (&lam)[U], const uin
                     continue;
                 }
                 if (S::skip(v[0])) continue;
-                if (win) window_put<SR>(win, out[u] + q - lo, v[0], w64);
+                if (win) window_put<SR>(win, out[u] + q - lo, v[0], d, w64);
                 else S::update(y + out[u] + q, v);
             }
         }
@@ -1137,10 +967,11 @@ __device__ __forceinline__ void leaf4_slice(uint32_t lam, uint32_t r, uint32_t c
 //  - Batches: G = B/VW adjacent lanes share a leaf, each owning a VW slice.
 template <int SR, int DIR, int VW, class LeafAt>
 __device__ __forceinline__ void warp_leaf4_rounds(uint32_t jb, uint32_t je, LeafAt &&leaf_at, const VecArgs &va,
-                                                  uint32_t *win, uint32_t lo, int wmode = kWinF32)
+                                                  uint32_t *win, uint32_t lo, int wmode, uint32_t out_min)
 {
     const uint32_t lane = threadIdx.x & 31u;
-    const bool heavy = SR == K2T_PLUS_TIMES && va.hflag != nullptr && (!win || wmode == kWinShared);
+    const bool heavy = SR == K2T_PLUS_TIMES && va.hdir != nullptr && out_min < va.hdir_len &&
+                       (!win || wmode == kWinShared);
     const bool w64 = win && wmode == kWinF64;
     if (SR == K2T_BOOLEAN || (VW == 1 && va.B == 1)) {
         constexpr int U = K2T_LEAF4_U;
@@ -1157,7 +988,7 @@ __device__ __forceinline__ void warp_leaf4_rounds(uint32_t jb, uint32_t je, Leaf
                 uint32_t li = 0u;
                 if (j < je) {
                     leaf_at(j, lam[u], r[u], c[u], li);
-                    if (heavy) fl |= heavy_leaf(va, li) << u;
+                    if (heavy) fl |= heavy_near(va, DIR == K2T_RIGHT ? r[u] : c[u]) << u;
                 }
             }
             uint32_t xo[U][4], out[U];
@@ -1191,7 +1022,7 @@ __device__ __forceinline__ void warp_leaf4_rounds(uint32_t jb, uint32_t je, Leaf
         return;
     }
     if constexpr (SR != K2T_BOOLEAN) {
-        constexpr int U = 2;
+        constexpr int U = kBatchU;
         const uint32_t G = va.B / VW;
         const uint32_t per = G <= 32u ? 32u / G : 1u;
         const uint32_t groups = G <= 32u ? G : 32u;
@@ -1210,7 +1041,8 @@ __device__ __forceinline__ void warp_leaf4_rounds(uint32_t jb, uint32_t je, Leaf
                 uint32_t li = 0u;
                 if (active && j < je) {
                     leaf_at(j, lam[u], r[u], c[u], li);
-                    if (heavy && heavy_leaf(va, li)) hv[u] = heavy_word4(va, DIR == K2T_RIGHT ? r[u] : c[u]);
+                    if (heavy && heavy_near(va, DIR == K2T_RIGHT ? r[u] : c[u]))
+                        hv[u] = heavy_word4(va, DIR == K2T_RIGHT ? r[u] : c[u]);
                 }
             }
             for (uint32_t k = sub * VW; k < va.B; k += groups * VW) {
@@ -1284,7 +1116,7 @@ cached4_block_kernel(const uint8_t *sig, const uint32_t *dir, uint32_t n, const 
         c = 8u * p.c + 4u * (b & 1u);
         li = base + j;
         lam = __ldg(leaf + li);
-    }, va, win, lo, wmode);
+    }, va, win, lo, wmode, lo);
     if (win) warp_window_flush<SR>(win, lo, span, width, va, wmode);
 }
 
@@ -1368,7 +1200,7 @@ banded_kernel(const uint32_t *chunks, const Coord *coords, const uint32_t *bleaf
             c = 4u * p.c + 2u * (b & 1u);
             li = lw[node] + (e & 3u);
             lam = nibble_at(leaf, li);
-        }, va, windowed ? win : nullptr, (uint32_t)band_lo, kWinShared);
+        }, va, windowed ? win : nullptr, (uint32_t)band_lo, kWinShared, 0u);
         __syncwarp();
     }
     if (windowed) {
@@ -1674,6 +1506,7 @@ fused_kernel(DevTree tr, const uint32_t *chunks, uint32_t stride, const Coord *r
     if (2u * cap >= kFusedWarps * kWarpWindow)  // the free buffer holds every warp's window
         win = warp_window_begin<SR>(wmn, wmx, side, width, reinterpret_cast<uint32_t *>(nxt) + warp * kWarpWindow,
                                     lo, span, va, wmode);
+    const uint32_t out_min = win ? lo : 0u;
     const uint32_t leaf0 = rng[2 * (l - 1 - d0)];  // the chunk's first leaf (level order)
     if constexpr (L4) {
         const uint16_t *lsig16 = reinterpret_cast<const uint16_t *>(lsig) + lnb;
@@ -1683,7 +1516,7 @@ fused_kernel(DevTree tr, const uint32_t *chunks, uint32_t stride, const Coord *r
             c = 4u * q.c;
             li = leaf0 + j;
             lam = lsig16[j];
-        }, va, win, lo, wmode);
+        }, va, win, lo, wmode, out_min);
     } else {
         warp_leaf_rounds<SR, DIR, VW>(jb, je, [&](uint32_t j, uint32_t &lam, uint32_t &r, uint32_t &c, uint32_t &li) {
             const Coord q = cur[j];
@@ -1691,7 +1524,7 @@ fused_kernel(DevTree tr, const uint32_t *chunks, uint32_t stride, const Coord *r
             c = 2u * q.c;
             li = leaf0 + j;
             lam = snib(lsig, lnb + j);
-        }, va, win, lo, wmode);
+        }, va, win, lo, wmode, out_min);
     }
     if (win) warp_window_flush<SR>(win, lo, span, width, va, wmode);
     (void)mn;
@@ -1746,8 +1579,7 @@ struct DeviceState {
     uint32_t *scan_prefix = nullptr;
     uint32_t *err = nullptr;
     void *vec[2] = {nullptr, nullptr};
-    const uint32_t *hflag[2] = {nullptr, nullptr};  // heavy outputs, per direction (null: none)
-    const uint32_t *hdir[2] = {nullptr, nullptr};
+    const uint32_t *hdir[2] = {nullptr, nullptr};   // heavy outputs, per direction (null: none)
     const uint32_t *hlist[2] = {nullptr, nullptr};
     float *acc = nullptr;
     cudaStream_t cap_stream = nullptr;
@@ -1785,12 +1617,18 @@ void launch_fused(const k2t_tree *t, const DeviceState *d, const VecArgs &va, cu
     else launch_fused_k<SR, DIR, VW, false>(t, d, va, st);
 }
 
+// Leaf step over the tile [a, a + count) of the last internal level (coords
+// index 0 = node a): directory mode (prefix null) or scan mode.
 template <int SR, int DIR, int VW>
-void launch_flat(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix, uint32_t leaf_base, uint32_t a,
-                 uint32_t count, const Coord *src, const uint8_t *leaf, const VecArgs &va, cudaStream_t st)
+void launch_leaf_tile(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix, uint32_t leaf_base, uint32_t a,
+                      uint32_t count, const Coord *coords, const uint8_t *leaf, const VecArgs &va, cudaStream_t st)
 {
-    const unsigned grid = (unsigned)((count + kFlatThreads - 1) / kFlatThreads);
-    flat_leaf_kernel<SR, DIR, VW><<<grid, kFlatThreads, 0, st>>>(sig, dir, prefix, leaf_base, a, count, src, leaf, va);
+    const uint64_t blocks = prefix ? ((uint64_t)count + kDirS - 1) / kDirS
+                                   : ((uint64_t)a + count + kDirS - 1) / kDirS - a / kDirS;
+    const unsigned grid = (unsigned)((blocks + kCachedWarps - 1) / kCachedWarps);
+    if (grid)
+        cached_block_kernel<SR, DIR, VW><<<grid, 32 * kCachedWarps, 0, st>>>(sig, dir, prefix, leaf_base, a, count,
+                                                                             coords, leaf, va);
 }
 
 template <int SR, int DIR, int VW>
@@ -1798,10 +1636,8 @@ void launch_cached(const k2t_tree *t, const DeviceState *d, const VecArgs &va, c
 {
     const int l = t->levels;
     const uint32_t n = (uint32_t)t->nodes[(size_t)l - 2];
-    const uint32_t blocks = (n + kDirS - 1) / kDirS;
-    const unsigned grid = (unsigned)((blocks + kCachedWarps - 1) / kCachedWarps);
-    cached_block_kernel<SR, DIR, VW><<<grid, 32 * kCachedWarps, 0, st>>>(
-        d->tree.lv[l - 2].sig, d->tree.lv[l - 2].dir, n, d->cached, d->tree.lv[l - 1].sig, va);
+    launch_leaf_tile<SR, DIR, VW>(d->tree.lv[l - 2].sig, d->tree.lv[l - 2].dir, nullptr, 0u, 0u, n, d->cached,
+                                  d->tree.lv[l - 1].sig, va, st);
 }
 
 template <int SR, int DIR, int VW>
@@ -1864,8 +1700,8 @@ void run_ls(const k2t_tree *t, const DeviceState *d, const LsBufs &sb, const Vec
                 sig, dir, prefix, s.a, s.count, src, s.src_base, sb.buf[lv + 1], s.dst_base);
         } else {
             const uint32_t base = scan ? (uint32_t)level_offset(t, lv, s.a) : 0u;
-            launch_flat<SR, DIR, VW>(sig, scan ? nullptr : dir, prefix, base, s.a, s.count,
-                                     src + (s.a - s.src_base), d->tree.lv[l - 1].sig, va, st);
+            launch_leaf_tile<SR, DIR, VW>(sig, scan ? nullptr : dir, prefix, base, s.a, s.count,
+                                          src + (s.a - s.src_base), d->tree.lv[l - 1].sig, va, st);
         }
     }
 }
@@ -1892,12 +1728,10 @@ constexpr uint32_t kEngineCached4 = 100;
 // va gets no tables.
 inline bool heavy_begin(const k2t_tree *t, const DeviceState *d, int dir, int semiring, VecArgs &va, cudaStream_t st)
 {
-    va.hflag = nullptr;
     va.hdir = nullptr;
     va.hdir_len = 0u;
     va.acc = nullptr;
-    if (semiring != K2T_PLUS_TIMES || !d->hflag[dir]) return false;
-    va.hflag = d->hflag[dir];
+    if (semiring != K2T_PLUS_TIMES || !d->hdir[dir]) return false;
     va.hdir = d->hdir[dir];
     va.hdir_len = (uint32_t)t->hdir[dir].size();
     va.acc = d->acc;

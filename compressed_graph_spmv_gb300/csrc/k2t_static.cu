@@ -92,7 +92,7 @@ int k2t_spmv_noalloc(k2t_tree *t, int32_t dir, int32_t semiring, float w, const 
     if (semiring < K2T_PLUS_TIMES || semiring > K2T_MIN_PLUS) return K2T_EINVAL;
     if (!x || !y || B == 0) return K2T_EINVAL;
     if (B > K2T_MAX_BATCH) return K2T_ERANGE;
-    if (semiring == K2T_PLUS_TIMES && t->dev->hflag[dir] && B > t->opts.max_batch) return K2T_ERANGE;
+    if (semiring == K2T_PLUS_TIMES && t->dev->hdir[dir] && B > t->opts.max_batch) return K2T_ERANGE;
     if (((uintptr_t)x | (uintptr_t)y) & 3u) return K2T_EINVAL;
     const uint64_t n_in = dir == K2T_RIGHT ? t->n_cols : t->n_rows;
     const uint64_t n_out = dir == K2T_RIGHT ? t->n_rows : t->n_cols;
