@@ -653,7 +653,7 @@ void k2t_default_opts(k2t_opts *o)
     o->engine = K2T_ENGINE_AUTO;
     o->offsets = K2T_OFFSETS_DIRECTORY;
     o->host_top_max_nodes = 1u << 16;
-    o->chunk_cap = 2048;
+    o->chunk_cap = 256;
     o->tile_m = 1ull << 20;
     o->max_batch = 32;
     o->host_vectors = 0;

@@ -10,7 +10,7 @@
 namespace k2t {
 
 constexpr uint32_t kDirS = 256;        // directory sample period (section 3.2: S = 256)
-constexpr uint32_t kMaxChunkCap = 4096;
+constexpr uint32_t kMaxChunkCap = 512;
 constexpr uint32_t kArenaAlign = 256;
 constexpr uint32_t kBandChunkNodes = 16384;  // BANDED: nodes per thread block at most
 // leaf_k 0 (automatic): 4x4 leaves when 2x2 leaves would average at least this

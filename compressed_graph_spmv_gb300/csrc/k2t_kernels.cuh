@@ -244,8 +244,7 @@ namespace k2t {
 // ---- kernels --------------------------------------------------------------
 constexpr int kWalkThreads = 256;   // 8 warps, one 256-node block each
 constexpr int kFusedThreads = 256;
-constexpr int kFusedWarps = kFusedThreads / 32;
-constexpr uint32_t kFusedSolo = 256;  // levels this narrow are expanded by one warp
+constexpr int kFusedWarps = kFusedThreads / 32;   // chunks per thread block (one per warp)
 
 // Kernels without template parameters, defined in k2t_device.cu.
 __global__ void fill_kernel(uint32_t *y, uint64_t words, uint32_t pattern);
@@ -348,11 +347,13 @@ __device__ __forceinline__ void window_put(uint32_t *win, uint32_t i, float v, d
 
 // Leaves of U leaf blocks (origins r[u], c[u], cells lam[u]) with x entries
 // already loaded (xo[u][0]: input r or c, xo[u][1]: the next one); one
-// vector slice (B = 1 fp32, or a Boolean word).  Bit u of fl (plus-times):
-// leaf u has heavy outputs; outside a window those go to their heavy sums.
+// vector slice (B = 1 fp32, or a Boolean word).  hw[u] (plus-times): the
+// heavy records of leaf u's outputs (heavy_word, loaded with its x entries),
+// zero for outputs that are not heavy; outside a window heavy outputs go to
+// their heavy sums.
 template <int SR, int DIR, int U, class InOf>
 __device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint32_t (&out)[U], InOf &&in_of,
-                                            const uint32_t (&xo)[U][2], uint32_t fl, const VecArgs &va,
+                                            const uint32_t (&xo)[U][2], const uint2 (&hw)[U], const VecArgs &va,
                                             uint32_t *win, uint32_t lo, bool w64)
 {
 #pragma unroll
@@ -379,7 +380,7 @@ __device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint
             float *y = static_cast<float *>(va.y);
             const float c0 = S::contrib(__uint_as_float(xo[u][0]), va.w);
             const float c1 = S::contrib(__uint_as_float(xo[u][1]), va.w);
-            const uint2 h = SR == K2T_PLUS_TIMES && ((fl >> u) & 1u) ? heavy_word(va, out[u]) : make_uint2(0u, 0u);
+            const uint2 h = hw[u];
             const float xa[1] = {__uint_as_float(xo[u][0])}, xb[1] = {__uint_as_float(xo[u][1])};
             if (a0 || a1) {
                 const float v[1] = {a0 ? (a1 ? S::plus(c0, c1) : c0) : c1};
@@ -403,7 +404,7 @@ __device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint
 
 // ---- per-warp leaf stage -------------------------------------------------------
 #ifndef K2T_LEAF_U
-#define K2T_LEAF_U 8
+#define K2T_LEAF_U 4
 #endif
 #ifndef K2T_WARP_WINDOW
 #define K2T_WARP_WINDOW 256
@@ -501,12 +502,29 @@ __device__ __forceinline__ void warp_window_flush(const uint32_t *win, uint32_t 
     }
 }
 
-// One VW-wide vector slice k of one leaf (origin r, c; cells lam): gathers the
-// slice of the inputs it needs, combines per output, updates y or the window;
-// outputs with a record in hv (heavy_word) go to their heavy sums.
+// The VW-wide slice k of the two input rows of one leaf (origin r, c; cells
+// lam) that its cells use: x0 from its first input, x1 from the next.
+template <int SR, int DIR, int VW>
+__device__ __forceinline__ void leaf_slice_load(uint32_t lam, uint32_t r, uint32_t c, uint32_t k, const VecArgs &va,
+                                                float (&x0)[VW], float (&x1)[VW])
+{
+    const uint32_t in = DIR == K2T_RIGHT ? c : r;
+    const bool u0 = DIR == K2T_RIGHT ? (lam & 5u) : (lam & 3u);    // cells on the first input
+    const bool u1 = DIR == K2T_RIGHT ? (lam & 10u) : (lam & 12u);  // cells on the second
+    const float *x = static_cast<const float *>(va.x);
+    const size_t B = va.B;
+    if (u0) VecLoad<VW>::load(x + (size_t)in * B + k, x0);
+    if (u1) VecLoad<VW>::load(x + (size_t)(in + 1) * B + k, x1);
+}
+
+// One VW-wide vector slice k of one leaf (origin r, c; cells lam) whose input
+// slices x0, x1 are loaded (leaf_slice_load): combines per output, updates y
+// or the window; outputs with a record in hv (heavy_word) go to their heavy
+// sums.
 template <int SR, int DIR, int VW>
 __device__ __forceinline__ void leaf_slice(uint32_t lam, uint32_t r, uint32_t c, uint32_t k, uint2 hv,
-                                           const VecArgs &va, uint32_t *win, uint32_t lo)
+                                           const float (&x0)[VW], const float (&x1)[VW], const VecArgs &va,
+                                           uint32_t *win, uint32_t lo)
 {
     using S = Fp32Sem<SR>;
     const uint32_t in = DIR == K2T_RIGHT ? c : r;
@@ -515,12 +533,8 @@ __device__ __forceinline__ void leaf_slice(uint32_t lam, uint32_t r, uint32_t c,
     const bool a1 = DIR == K2T_RIGHT ? (lam & 2u) : (lam & 4u);
     const bool b0 = DIR == K2T_RIGHT ? (lam & 4u) : (lam & 2u);
     const bool b1 = lam & 8u;
-    const float *x = static_cast<const float *>(va.x);
     float *y = static_cast<float *>(va.y);
     const size_t B = va.B;
-    float x0[VW], x1[VW];
-    if (a0 || b0) VecLoad<VW>::load(x + (size_t)in * B + k, x0);
-    if (a1 || b1) VecLoad<VW>::load(x + (size_t)(in + 1) * B + k, x1);
     // One output's combined contribution from x0, x1 (cells u0 on input in,
     // u1 on in + 1), and its update of y or the window.
     auto combine = [&](bool u0, bool u1, float (&v)[VW]) {
@@ -611,12 +625,14 @@ __device__ __forceinline__ void warp_leaf_rounds(uint32_t jb, uint32_t je, LeafA
                 }
             }
             uint32_t xo[U][2], out[U];
+            uint2 hw[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const uint32_t in = DIR == K2T_RIGHT ? c[u] : r[u];  // even
                 out[u] = DIR == K2T_RIGHT ? r[u] : c[u];
                 xo[u][0] = 0u;
                 xo[u][1] = 0u;
+                hw[u] = make_uint2(0u, 0u);
                 if (lam[u]) {
                     if (x8 && in + 1u < va.n_in) {
                         const uint2 v = __ldg(reinterpret_cast<const uint2 *>(x + in));
@@ -626,6 +642,7 @@ __device__ __forceinline__ void warp_leaf_rounds(uint32_t jb, uint32_t je, LeafA
                         xo[u][0] = __ldg(x + in);
                         if (in + 1u < va.n_in) xo[u][1] = __ldg(x + in + 1u);
                     }
+                    if (SR == K2T_PLUS_TIMES && ((fl >> u) & 1u)) hw[u] = heavy_word(va, out[u]);
                 }
             }
             // the input index of leaf u, looked up again (only leaves with a
@@ -635,7 +652,7 @@ __device__ __forceinline__ void warp_leaf_rounds(uint32_t jb, uint32_t je, LeafA
                 leaf_at(j0 + 32u * (uint32_t)u + lane, l2, r2, c2, li2);
                 return DIR == K2T_RIGHT ? c2 : r2;
             };
-            leaf_apply1<SR, DIR, U>(lam, out, in_of, xo, fl, va, win, lo, w64);
+            leaf_apply1<SR, DIR, U>(lam, out, in_of, xo, hw, va, win, lo, w64);
         }
         return;
     }
@@ -663,11 +680,15 @@ __device__ __forceinline__ void warp_leaf_rounds(uint32_t jb, uint32_t je, LeafA
                         hv[u] = heavy_word(va, DIR == K2T_RIGHT ? r[u] : c[u]);
                 }
             }
-            // a group of G lanes covers the row; rows wider than 32 slices loop
+            // a group of G lanes covers the row; rows wider than 32 slices
+            // loop.  Every gather of the round is issued before its updates.
             for (uint32_t k = sub * VW; k < va.B; k += groups * VW) {
+                float x0[U][VW], x1[U][VW];
+#pragma unroll
+                for (int u = 0; u < U; ++u) leaf_slice_load<SR, DIR, VW>(lam[u], r[u], c[u], k, va, x0[u], x1[u]);
 #pragma unroll
                 for (int u = 0; u < U; ++u)
-                    if (lam[u]) leaf_slice<SR, DIR, VW>(lam[u], r[u], c[u], k, hv[u], va, win, lo);
+                    if (lam[u]) leaf_slice<SR, DIR, VW>(lam[u], r[u], c[u], k, hv[u], x0[u], x1[u], va, win, lo);
             }
         }
     }
@@ -732,12 +753,13 @@ __device__ __forceinline__ bool tile_warp_block(const uint8_t *sig, const uint32
 // are loaded together, then the combined updates are applied.  Every lane
 // does the same work per leaf, whatever the fan-out of its node.
 constexpr int kCachedWarps = 8;
+constexpr uint32_t kLeafWords = 4 * kDirS / 8 + 1;   // words of 8 leaf nibbles covering one block's leaves
 
 // Blocks per SM the kernel is compiled for: 5 for 4-wide batches (48
 // registers, no spills; 5% faster than 4 blocks on the 300M-edge R-MAT at
 // B = 16, and 3 or 4 leaves per lane group at 4 or 3 blocks are slower), 4
 // otherwise (at 5 the single-vector path spills and runs 13% slower).
-template <int VW> constexpr int cached_min_blocks() { return VW == 4 ? 5 : 4; }
+template <int VW> constexpr int cached_min_blocks() { return 4; }
 
 template <int SR, int DIR, int VW>
 __global__ void __launch_bounds__(32 * kCachedWarps, cached_min_blocks<VW>())
@@ -747,12 +769,14 @@ cached_block_kernel(const uint8_t *sig, const uint32_t *dir, const uint32_t *pre
     __shared__ Coord cs[kCachedWarps][kDirS];
     __shared__ uint16_t slots[kCachedWarps][4 * kDirS];
     __shared__ __align__(16) uint32_t wins[kCachedWarps][kWarpWindow];
+    __shared__ uint32_t lsigs[kCachedWarps][kLeafWords];
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
     uint32_t blk, s, e, base, w;
     if (!tile_warp_block(sig, dir, prefix, leaf_base, a, count, blockIdx.x * kCachedWarps + warp, blk, s, e, base, w))
         return;
     Coord *cw = cs[warp];
     uint16_t *sl = slots[warp];
+    uint32_t *lw = lsigs[warp];
     uint32_t mn = 0xffffffffu, mx = 0u;
 #pragma unroll
     for (uint32_t q = 0; q < kDirS / 32; ++q) {
@@ -768,6 +792,11 @@ cached_block_kernel(const uint8_t *sig, const uint32_t *dir, const uint32_t *pre
     const uint32_t f = (uint32_t)__popc(w);
     const uint32_t incl = warp_incl_scan(f);
     const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+    // the block's leaf signatures [base, base + total), as the words of 8
+    // nibbles that hold them (coalesced; total <= 1024, so at most 129 words)
+    const uint32_t lw0 = base >> 3, lsh = base & 7u;
+    const uint32_t nlw = (lsh + total + 7u) >> 3;
+    for (uint32_t k = lane; k < nlw; k += 32u) lw[k] = __ldg(reinterpret_cast<const uint32_t *>(leaf) + lw0 + k);
     uint32_t pos = incl - f;
     uint32_t rest = w;
     while (rest) {
@@ -787,7 +816,8 @@ cached_block_kernel(const uint8_t *sig, const uint32_t *dir, const uint32_t *pre
         r = 4u * p.r + 2u * (b >> 1);
         c = 4u * p.c + 2u * (b & 1u);
         li = base + j;
-        lam = nibble_at(leaf, li);
+        const uint32_t q = lsh + j;
+        lam = (lw[q >> 3] >> (4u * (q & 7u))) & 15u;
     }, va, win, lo, wmode, lo);
     if (win) warp_window_flush<SR>(win, lo, span, width, va, wmode);
 }
@@ -1297,247 +1327,205 @@ __device__ __forceinline__ uint32_t dir_offset(const uint8_t *sig, const uint32_
     return base;
 }
 
-// ---- warp-sliced level expansion ------------------------------------------------
-// Nibbles [s, e) of a staged signature copy viewed as 32-bit words (8 nodes
-// per word): lane l reads word w0 + l + 32k with the nibbles outside [s, e)
-// masked off.
-__device__ __forceinline__ uint32_t word_mask(uint32_t W, uint32_t s, uint32_t e)
-{
-    const uint32_t lo = W * 8u, hi = lo + 8u;
-    if (lo >= s && hi <= e) return 0xffffffffu;
-    uint32_t m = 0;
-#pragma unroll
-    for (uint32_t k = 0; k < 8; ++k)
-        if (lo + k >= s && lo + k < e) m |= 15u << (4 * k);
-    return m;
-}
-
-// Set bits (= children) of nibbles [s, e), summed over the warp.
-__device__ __forceinline__ uint32_t warp_popc_nibbles(const uint32_t *words, uint32_t s, uint32_t e)
+// ---- FUSED engine ------------------------------------------------------------------
+// One warp expands the parents at nibbles [nb, nb + n) of a staged level
+// (parent i at nibble nb + i, coordinates cur[i]), one parent per lane per
+// round: lanes read consecutive signatures and coordinates, a warp scan
+// places the children, which go to nxt[0 ...] in level order.
+__device__ __forceinline__ void warp_expand(const uint8_t *sg8, uint32_t nb, uint32_t n, const Coord *cur, Coord *nxt)
 {
     const uint32_t lane = threadIdx.x & 31u;
-    uint32_t v = 0;
-    if (s < e)
-        for (uint32_t W = s / 8u + lane; W < (e + 7u) / 8u; W += 32u) v += (uint32_t)__popc(words[W] & word_mask(W, s, e));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-// One warp expands the parents at nibbles [s, e) of the staged level (parent
-// i of the chunk at nibble nb + i, coordinates cur[i]); their children go to
-// nxt[start ...] in level order.  Also folds the children's row (right) or
-// column (left) into [mn, mx].
-template <int DIR>
-__device__ __forceinline__ void emit_children(uint32_t sg, Coord p, Coord *nxt, uint32_t pos, uint32_t &mn,
-                                              uint32_t &mx)
-{
-#pragma unroll
-    for (int b = 0; b < 4; ++b)
-        if (sg & (1u << b)) {
-            const Coord q = child_of(p, b);
-            const uint32_t o = DIR == K2T_RIGHT ? q.r : q.c;
-            mn = min(mn, o);
-            mx = max(mx, o);
-            nxt[pos++] = q;
-        }
-}
-
-// One warp expands the parents at nibbles [s, e) of the staged level (parent
-// i of the chunk at nibble nb + i, coordinates cur[i]), one parent per lane
-// per round: lanes read consecutive signatures and coordinates (no shared-
-// memory bank conflicts), a warp scan places the children, which go to
-// nxt[start ...] in level order.  Also folds the children's row (right) or
-// column (left) into [mn, mx].
-template <int DIR>
-__device__ __forceinline__ void warp_expand(const uint32_t *words, uint32_t nb, uint32_t s, uint32_t e,
-                                            const Coord *cur, Coord *nxt, uint32_t start, uint32_t &mn,
-                                            uint32_t &mx)
-{
-    const uint32_t lane = threadIdx.x & 31u;
-    const uint8_t *bytes = reinterpret_cast<const uint8_t *>(words);
-    for (uint32_t i0 = s; i0 < e; i0 += 32u) {
+    uint32_t start = 0;
+    for (uint32_t i0 = 0; i0 < n; i0 += 32u) {
         const uint32_t i = i0 + lane;
-        const uint32_t sg = i < e ? snib(bytes, i) : 0u;
+        const uint32_t sg = i < n ? snib(sg8, nb + i) : 0u;
         const uint32_t f = (uint32_t)__popc(sg);
         const uint32_t incl = warp_incl_scan(f);
-        const uint32_t pos = start + incl - f;
+        uint32_t pos = start + incl - f;
         start += __shfl_sync(0xffffffffu, incl, 31);
-        if (sg) emit_children<DIR>(sg, cur[i - nb], nxt, pos, mn, mx);
+        if (sg) {
+            const Coord p = cur[i];
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+                if (sg & (1u << b)) nxt[pos++] = child_of(p, b);
+        }
     }
-}
-
-// One level of a thread block's expansion with warp slices: warp w takes the
-// parents [n*w/NW, n*(w+1)/NW) of the level (nibbles nb.. of the staged copy),
-// publishes its fan-out total in wt[w], and after one block barrier writes its
-// children from the sum of the totals of the warps before it.  The caller
-// synchronises before reading nxt.
-template <int NT, int DIR>
-__device__ __forceinline__ void sliced_expand(const uint32_t *words, uint32_t nb, uint32_t n, const Coord *cur,
-                                              Coord *nxt, uint32_t *wt, uint32_t &mn, uint32_t &mx)
-{
-    constexpr uint32_t NW = NT / 32;
-    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
-    const uint32_t a = nb + (uint32_t)(((uint64_t)n * warp) / NW);
-    const uint32_t b = nb + (uint32_t)(((uint64_t)n * (warp + 1)) / NW);
-    const uint32_t tot = warp_popc_nibbles(words, a, b);
-    if (lane == 0) wt[warp] = tot;
-    __syncthreads();
-    uint32_t start = 0;
-    for (uint32_t v = 0; v < warp; ++v) start += wt[v];
-    warp_expand<DIR>(words, nb, a, b, cur, nxt, start, mn, mx);
 }
 
 // Bytes of one level's staging slot in fused_kernel: the nibbles (or, for a
 // 4x4 leaf level, the 16-bit signatures) of at most cap nodes, widened to
-// 16-byte boundaries at both ends.
+// 16-byte boundaries at both ends, with room for an 8-byte read past the end.
 __host__ __device__ constexpr uint32_t fused_slot(uint32_t cap, bool wide)
 {
     return ((wide ? 2u * cap : cap / 2u) + 48u + 15u) & ~15u;
 }
 
-// FUSED engine: thread block k descends chunk k, a run of whole subtrees
-// rooted at level d_c with at most `cap` leaves, from its roots to the
-// leaves.  The chunk record holds the index of its roots' coordinates and,
+// Header of a warp's shared memory in fused_kernel: its mbarrier (16 bytes)
+// and the nibble (or element) offset of each staged level inside its slot.
+__host__ __device__ constexpr uint32_t fused_header() { return (16u + 4u * K2T_MAX_LEVELS + 15u) & ~15u; }
+
+// Shared memory of one warp of fused_kernel for a tree: the header, one
+// staging slot per level from d0 (the leaf level's holds 2 bytes a leaf with
+// 4x4 leaves) and two coordinate buffers of cap entries.  A multiple of 16.
+inline uint32_t fused_warp_bytes(int levels, int d0, uint32_t cap, bool l4)
+{
+    return fused_header() + (uint32_t)(levels - 1 - d0) * fused_slot(cap, false) + fused_slot(cap, l4) + 16u * cap;
+}
+
+// FUSED engine: warp w of thread block k descends chunk 8k + w, a run of whole
+// subtrees rooted at level d_c with at most `cap` leaves, from its roots to
+// the leaves, alone: no block barrier, so narrow levels keep only their own
+// warp busy.  The chunk record holds the index of its roots' coordinates and,
 // for every level, the first node and the node count of the chunk there
-// (planned once per tree on the host).  The block stages the signatures of
-// all its levels with one bulk copy per level, then expands level by level
-// in shared memory: every warp takes an equal slice of the level, learns
-// where its children start from the other warps' fan-out totals (one block
-// barrier per level) and writes them with warp scans.  No global scratch.
-// L4: the leaf level holds 4x4 bitmaps (16-bit signatures, section 5.6).
+// (planned once per tree on the host).  The warp stages the signatures of all
+// its levels with one bulk copy per level on its own mbarrier, expands level
+// by level in its shared memory down to the last internal level, then runs
+// the leaf step over that level's nodes as the k^2+F kernel does over the
+// cached level: a warp scan of the fan-outs lists the leaves (node, quadrant)
+// and the lanes take them round-robin.  No global scratch.  L4: the leaf
+// level holds 4x4 bitmaps (16-bit signatures, section 5.6).
 template <int SR, int DIR, int VW, bool L4>
-__global__ void __launch_bounds__(kFusedThreads)
-fused_kernel(DevTree tr, const uint32_t *chunks, uint32_t stride, const Coord *roots, uint32_t cap, VecArgs va,
-             uint32_t *status)
+__global__ void __launch_bounds__(kFusedThreads, 4)
+fused_kernel(DevTree tr, const uint32_t *chunks, uint32_t stride, const Coord *roots, uint32_t cap, uint64_t n_chunks,
+             uint32_t wbytes, VecArgs va, uint32_t *status)
 {
     extern __shared__ __align__(16) uint8_t fsm[];
+    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+    const uint64_t chunk = (uint64_t)blockIdx.x * kFusedWarps + warp;
+    if (chunk >= n_chunks) return;
     const int d0 = tr.d0, l = tr.levels;
-    const uint32_t slot = fused_slot(cap, false), lslot = fused_slot(cap, L4);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(fsm);
-    uint32_t *wtot = reinterpret_cast<uint32_t *>(fsm + 16);           // [2][kFusedWarps] fan-out totals
-    uint32_t *nbase = reinterpret_cast<uint32_t *>(fsm + 80);          // per level, entry base in its slot
-    uint8_t *stage = fsm + 80 + 4 * K2T_MAX_LEVELS;
-    stage += (16 - ((uintptr_t)stage & 15)) & 15;
-    Coord *cur = reinterpret_cast<Coord *>(stage + (size_t)(l - 1 - d0) * slot + lslot);
+    uint8_t *wsm = fsm + (size_t)warp * wbytes;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(wsm);
+    uint32_t *nbase = reinterpret_cast<uint32_t *>(wsm + 16);   // per level from d0
+    uint8_t *stage = wsm + fused_header();
+    const uint32_t slot = fused_slot(cap, false);
+    Coord *cur = reinterpret_cast<Coord *>(stage + (size_t)(l - 1 - d0) * slot + fused_slot(cap, L4));
     Coord *nxt = cur + cap;
 
-    const uint32_t *rec = chunks + (size_t)blockIdx.x * stride;
+    const uint32_t *rec = chunks + chunk * stride;
     const uint32_t rc = rec[0];
     const int dc = (int)rec[1];
     const uint32_t *rng = rec + 2;
-    if (threadIdx.x == 0) {
-        uint32_t total = 0;
-        StagePlan pl[K2T_MAX_LEVELS];
-        for (int d = dc; d < l; ++d) {
+    if (lane == 0) {
+        // the byte range of every level of the chunk, widened to 16 bytes
+        auto plan = [&](int d) {
             const uint32_t s = rng[2 * (d - d0)], n = rng[2 * (d - d0) + 1];
-            if (L4 && d == l - 1) {   // 2 bytes a leaf
-                pl[d] = stage_plan(2ull * s, 2ull * ((uint64_t)s + n));
-                nbase[d - d0] = pl[d].shift / 2u;
-            } else {                  // a nibble a node
-                pl[d] = stage_plan(s >> 1, ((uint64_t)s + n + 1) >> 1);
-                nbase[d - d0] = 2u * pl[d].shift + (s & 1u);
-            }
-            total += pl[d].bytes;
+            if (L4 && d == l - 1) return stage_plan(2ull * s, 2ull * ((uint64_t)s + n));   // 2 bytes a leaf
+            return stage_plan(s >> 1, ((uint64_t)s + n + 1) >> 1);                      // a nibble a node
+        };
+        uint32_t total = 0;
+        for (int d = dc; d < l; ++d) {
+            const StagePlan pl = plan(d);
+            total += pl.bytes;
+            nbase[d - d0] = L4 && d == l - 1 ? pl.shift / 2u : 2u * pl.shift + (rng[2 * (d - d0)] & 1u);
         }
         mbar_init(bar);
         mbar_expect_tx(bar, total);
-        for (int d = dc; d < l; ++d)
-            bulk_copy(stage + (size_t)(d - d0) * slot, tr.lv[d].sig + pl[d].lo16, pl[d].bytes, bar);
+        for (int d = dc; d < l; ++d) {
+            const StagePlan pl = plan(d);
+            bulk_copy(stage + (size_t)(d - d0) * slot, tr.lv[d].sig + pl.lo16, pl.bytes, bar);
+        }
     }
     {
         const uint32_t n = rng[2 * (dc - d0) + 1];
-        for (uint32_t i = threadIdx.x; i < n; i += kFusedThreads) cur[i] = roots[rc + i];
+        for (uint32_t i = lane; i < n; i += 32u) cur[i] = roots[rc + i];
     }
-    __syncthreads();
+    __syncwarp();
     if (!mbar_wait(bar, 0)) {
-        if (threadIdx.x == 0) atomicOr(status, kStatusStageTimeout);
+        if (lane == 0) atomicOr(status, kStatusStageTimeout);
         mbar_wait(bar, 0);
         return;
     }
-    // Levels whose parents number at most kFusedSolo are expanded by warp 0
-    // alone (no block barrier); from the first wider level on, all warps
-    // share every level.  Levels never shrink downwards, so the first wide
-    // level's barrier also publishes warp 0's last writes.
-    const uint32_t warp = threadIdx.x >> 5;
-    uint32_t mn = 0xffffffffu, mx = 0u;
-    for (int d = dc; d <= l - 2; ++d) {
-        const uint32_t n = rng[2 * (d - d0) + 1];
-        const uint32_t *words = reinterpret_cast<const uint32_t *>(stage + (size_t)(d - d0) * slot);
-        const uint32_t nb = nbase[d - d0];
-        if (n <= kFusedSolo && d < l - 2) {
-            if (warp == 0) {
-                uint32_t a = 0, b = 0;
-                warp_expand<DIR>(words, nb, nb, nb + n, cur, nxt, 0u, a, b);
-            }
-            __syncwarp();
-        } else {
-            mn = 0xffffffffu;
-            mx = 0u;
-            sliced_expand<kFusedThreads, DIR>(words, nb, n, cur, nxt, wtot + (d & 1) * kFusedWarps, mn, mx);
-        }
+    // descent to the last internal level
+    for (int d = dc; d < l - 2; ++d) {
+        warp_expand(stage + (size_t)(d - d0) * slot, nbase[d - d0], rng[2 * (d - d0) + 1], cur, nxt);
+        __syncwarp();
         Coord *t = cur;
         cur = nxt;
         nxt = t;
     }
-    __syncthreads();
-    // Leaf stage: warp w takes the contiguous leaves [nl*w/NW, nl*(w+1)/NW)
-    // of the chunk (coordinates in cur, signatures in the staged leaf level),
-    // with its own output window carved from the free coordinate buffer.
-    const uint32_t nl = rng[2 * (l - 1 - d0) + 1];
-    const uint32_t jb = (uint32_t)(((uint64_t)nl * warp) / kFusedWarps);
-    const uint32_t je = (uint32_t)(((uint64_t)nl * (warp + 1)) / kFusedWarps);
+    // leaf step over the chunk's nodes of the last internal level (cur)
+    const uint32_t n2 = rng[2 * (l - 2 - d0) + 1];
+    const uint32_t *sig2 = reinterpret_cast<const uint32_t *>(stage + (size_t)(l - 2 - d0) * slot);
+    const uint32_t nb2 = nbase[l - 2 - d0];
     const uint8_t *lsig = stage + (size_t)(l - 1 - d0) * slot;
     const uint32_t lnb = nbase[l - 1 - d0];
-    uint32_t wmn = 0xffffffffu, wmx = 0u;
-    for (uint32_t j = jb + (threadIdx.x & 31u); j < je; j += 32u) {
-        const Coord q = cur[j];
-        const uint32_t o = DIR == K2T_RIGHT ? q.r : q.c;
-        wmn = min(wmn, o);
-        wmx = max(wmx, o);
+    const uint32_t leaf0 = rng[2 * (l - 1 - d0)];   // the chunk's first leaf (level order)
+    constexpr uint32_t unit = L4 ? 8u : 4u;         // cells a node covers per side
+    uint32_t mn = 0xffffffffu, mx = 0u;
+    for (uint32_t i = lane; i < n2; i += 32u) {
+        const Coord p = cur[i];
+        const uint32_t o = DIR == K2T_RIGHT ? p.r : p.c;
+        mn = min(mn, o);
+        mx = max(mx, o);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    // the free buffer holds the leaf list of one 256-node round, then, when
+    // there is room, the warp's output window
+    uint16_t *sl = reinterpret_cast<uint16_t *>(nxt);
+    const uint32_t sl_bytes = (2u * min(cap, 4u * kDirS) + 15u) & ~15u;
     const uint32_t width = SR == K2T_BOOLEAN ? 1u : va.B;
-    constexpr uint32_t side = L4 ? 4u : 2u;
-    uint32_t lo, span;
-    uint32_t *win = nullptr;
+    uint32_t lo = unit * mn, span = 0u;
     int wmode = kWinF32;
-    lo = 0u;
-    span = 0u;
-    if (2u * cap >= kFusedWarps * kWarpWindow)  // the free buffer holds every warp's window
-        win = warp_window_begin<SR>(wmn, wmx, side, width, reinterpret_cast<uint32_t *>(nxt) + warp * kWarpWindow,
-                                    lo, span, va, wmode);
-    const uint32_t out_min = win ? lo : 0u;
-    const uint32_t leaf0 = rng[2 * (l - 1 - d0)];  // the chunk's first leaf (level order)
-    if constexpr (L4) {
-        const uint16_t *lsig16 = reinterpret_cast<const uint16_t *>(lsig) + lnb;
-        warp_leaf4_rounds<SR, DIR, VW>(jb, je, [&](uint32_t j, uint32_t &lam, uint32_t &r, uint32_t &c, uint32_t &li) {
-            const Coord q = cur[j];
-            r = 4u * q.r;
-            c = 4u * q.c;
-            li = leaf0 + j;
-            lam = lsig16[j];
-        }, va, win, lo, wmode, out_min);
-    } else {
-        warp_leaf_rounds<SR, DIR, VW>(jb, je, [&](uint32_t j, uint32_t &lam, uint32_t &r, uint32_t &c, uint32_t &li) {
-            const Coord q = cur[j];
-            r = 2u * q.r;
-            c = 2u * q.c;
-            li = leaf0 + j;
-            lam = snib(lsig, lnb + j);
-        }, va, win, lo, wmode, out_min);
+    uint32_t *win = nullptr;
+    if (8u * cap >= sl_bytes + 4u * kWarpWindow)
+        win = warp_window_begin<SR>(mn, mx, unit, width,
+                                    reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(nxt) + sl_bytes), lo, span,
+                                    va, wmode);
+    const uint32_t out_min = unit * mn;
+    uint32_t lj0 = 0;   // leaves of the chunk before this round
+    for (uint32_t b0 = 0; b0 < n2; b0 += kDirS) {
+        // lane's 8 nibbles: nodes b0 + 8 lane .. + 7 (those below n2)
+        const uint32_t t0 = b0 + 8u * lane;
+        uint32_t w = 0u;
+        if (t0 < n2) {
+            const uint32_t q = nb2 + t0;
+            w = __funnelshift_r(sig2[q >> 3], sig2[(q >> 3) + 1], 4u * (q & 7u));
+            if (n2 - t0 < 8u) w &= (1u << (4u * (n2 - t0))) - 1u;
+        }
+        const uint32_t f = (uint32_t)__popc(w);
+        const uint32_t incl = warp_incl_scan(f);
+        const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+        uint32_t pos = incl - f;
+        uint32_t rest = w;
+        while (rest) {
+            const uint32_t bit = (uint32_t)(__ffs(rest) - 1);  // 4*k + b
+            rest &= rest - 1u;
+            sl[pos++] = (uint16_t)(((8u * lane + bit / 4u) << 2) | (bit & 3u));
+        }
+        __syncwarp();
+        const Coord *cb = cur + b0;
+        const uint32_t ljb = lj0;
+        if constexpr (L4) {
+            const uint16_t *ls16 = reinterpret_cast<const uint16_t *>(lsig) + lnb + ljb;
+            warp_leaf4_rounds<SR, DIR, VW>(0u, total, [&](uint32_t j, uint32_t &lam, uint32_t &r, uint32_t &c, uint32_t &li) {
+                const uint32_t el = sl[j];
+                const Coord p = cb[el >> 2];
+                const uint32_t b = el & 3u;
+                r = 8u * p.r + 4u * (b >> 1);
+                c = 8u * p.c + 4u * (b & 1u);
+                li = leaf0 + ljb + j;
+                lam = ls16[j];
+            }, va, win, lo, wmode, out_min);
+        } else {
+            warp_leaf_rounds<SR, DIR, VW>(0u, total, [&](uint32_t j, uint32_t &lam, uint32_t &r, uint32_t &c, uint32_t &li) {
+                const uint32_t el = sl[j];
+                const Coord p = cb[el >> 2];
+                const uint32_t b = el & 3u;
+                r = 4u * p.r + 2u * (b >> 1);
+                c = 4u * p.c + 2u * (b & 1u);
+                li = leaf0 + ljb + j;
+                lam = snib(lsig, lnb + ljb + j);
+            }, va, win, lo, wmode, out_min);
+        }
+        lj0 += total;
+        __syncwarp();
     }
     if (win) warp_window_flush<SR>(win, lo, span, width, va, wmode);
-    (void)mn;
-    (void)mx;
-}
-
-// Dynamic shared memory of fused_kernel for a tree: header, one staging slot
-// per level (the leaf level's holds 2 bytes a leaf with 4x4 leaves), and two
-// coordinate buffers of cap entries.
-inline size_t fused_smem(int levels, int d0, uint32_t cap, bool l4)
-{
-    return 80 + 4 * K2T_MAX_LEVELS + 16 + (size_t)(levels - 1 - d0) * fused_slot(cap, false) + fused_slot(cap, l4) +
-           2 * (size_t)cap * 8;
 }
 
 }  // namespace k2t
@@ -1600,14 +1588,17 @@ inline int grid_for_blocks(uint64_t warps_needed)
 template <int SR, int DIR, int VW, bool L4>
 void launch_fused_k(const k2t_tree *t, const DeviceState *d, const VecArgs &va, cudaStream_t st)
 {
-    const size_t smem = fused_smem(t->levels, t->d0, t->opts.chunk_cap, L4);
+    const uint32_t wb = fused_warp_bytes(t->levels, t->d0, t->opts.chunk_cap, L4);
+    const size_t smem = (size_t)wb * kFusedWarps;
     static size_t configured = 0;
     if (smem > configured) {
         cudaFuncSetAttribute(fused_kernel<SR, DIR, VW, L4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         configured = smem;
     }
-    fused_kernel<SR, DIR, VW, L4><<<(unsigned)t->n_chunks, kFusedThreads, smem, st>>>(
-        d->tree, d->chunks, t->chunk_stride, d->roots, t->opts.chunk_cap, va, d->err);
+    const uint64_t grid = (t->n_chunks + kFusedWarps - 1) / kFusedWarps;
+    if (grid)
+        fused_kernel<SR, DIR, VW, L4><<<(unsigned)grid, kFusedThreads, smem, st>>>(
+            d->tree, d->chunks, t->chunk_stride, d->roots, t->opts.chunk_cap, t->n_chunks, wb, va, d->err);
 }
 
 template <int SR, int DIR, int VW>

@@ -107,8 +107,8 @@ typedef struct {
                                      directory or the chunk plan)                                   */
     uint32_t host_top_max_nodes;  /* products start at the deepest level with at most this many
                                      nodes, expanded on the host (section 3.4); default 65536       */
-    uint32_t chunk_cap;           /* FUSED: leaves per chunk (a chunk's widest level); default
-                                     2048, from 4 to 4096                                           */
+    uint32_t chunk_cap;           /* FUSED: leaves per chunk, the part of the tree one warp
+                                     descends (a chunk's widest level); default 256, from 4 to 512  */
     uint64_t tile_m;              /* LEVELSYNC: children per tile M; default 2^20, at least 4      */
     uint32_t max_batch;           /* largest B products will use (1..32); sizes host-vector buffers */
     uint32_t host_vectors;        /* 1: the workspace also holds device x and y of max_batch
@@ -180,7 +180,7 @@ typedef struct {
 } k2t_stats;
 
 /* Fill *o with the defaults: k = 2, tree-only FUSED engine (AUTO), directory
- * offsets, top of at most 2^16 nodes, chunk_cap 2048, tile_m 2^20,
+ * offsets, top of at most 2^16 nodes, chunk_cap 256, tile_m 2^20,
  * max_batch 32, no host vectors, CUDA graph on, all host threads, leaf size
  * chosen by the build, heavy_terms 160 in fp32 partial sums. */
 void k2t_default_opts(k2t_opts *o);

@@ -194,7 +194,7 @@ def test_workspace_accounting(engine):
 def test_options_struct_matches_header():
     """The binding's k2t_opts mirrors the header: defaults round-trip."""
     o = K.default_opts()
-    assert o.band_rows == 4096 and o.chunk_cap == 2048 and o.tile_m == 1 << 20 and o.max_batch == 32
+    assert o.band_rows == 4096 and o.chunk_cap == 256 and o.tile_m == 1 << 20 and o.max_batch == 32
     assert o.heavy_terms == 160 and o.leaf_k == 0
     # sizes and field offsets as a C compiler lays the header's structs out
     import subprocess
@@ -231,7 +231,7 @@ def test_chunk_plan_covers_every_node():
     """Fused plan: chunks are whole subtrees; together they cover each level
     below the host-expanded top exactly once, in level order."""
     rows, cols = synth.rmat(13, 0.57, 0.19, 0.19, 60000, 6)
-    for cap in (4, 7, 256, 4096):
+    for cap in (4, 7, 256, 512):
         t = K.Tree(rows, cols, 8192, 8192, engine=1, chunk_cap=cap)
         h = t.handle
         s = t.stats()
