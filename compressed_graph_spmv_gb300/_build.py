@@ -17,10 +17,13 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libk2t.so")
+CHECKED_LIB = os.path.join(HERE, "libk2t_checked.so")   # same ABI, kernels with bounds tests (K2T_CHECKED)
 PROBE_LIB = os.path.join(HERE, "libk2t_probe.so")   # benchmark instrumentation, not the product ABI
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-COMMON = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC,-O3", "-I" + os.path.join(ROOT, "include")]
+# hidden visibility: only the K2T_API calls of include/k2t.h are exported
+COMMON = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC,-O3,-fvisibility=hidden",
+          "-I" + os.path.join(ROOT, "include")]
 SOURCES = ["k2t_host.cpp", "k2t_device.cu", "k2t_sr_plus_times.cu", "k2t_sr_boolean.cu", "k2t_sr_min_plus.cu",
            "k2t_static.cu", "k2t_product.cu"]
 PROBE_SOURCES = [os.path.join("probe", "k2t_probe.cu")]
@@ -55,10 +58,14 @@ def _link(objs, out: str) -> None:
 
 
 def build(force: bool = False, verbose: bool = False, extra=()) -> str:
-    """Compile the product library libk2t.so and the benchmark's probe
-    library libk2t_probe.so where a source is newer than the library (all
-    translation units in parallel); return the product library's path."""
-    targets = [(LIB, SOURCES, list(extra), "lib"), (PROBE_LIB, PROBE_SOURCES, [], "probe")]
+    """Compile the product library libk2t.so, its bounds-checked twin
+    libk2t_checked.so (-DK2T_CHECKED: the same ABI, kernels that test their
+    indexes and report a failure in the device status word) and the
+    benchmark's probe library libk2t_probe.so where a source is newer than
+    the library (all translation units in parallel); return the product
+    library's path."""
+    targets = [(LIB, SOURCES, list(extra), "lib"), (CHECKED_LIB, SOURCES, list(extra) + ["-DK2T_CHECKED"], "checked"),
+               (PROBE_LIB, PROBE_SOURCES, [], "probe")]
     todo = [t for t in targets
             if force or not os.path.exists(t[0]) or os.path.getmtime(t[0]) < _newest_input(t[1])]
     if not todo:

@@ -49,11 +49,10 @@ __global__ void __launch_bounds__(256) fill_kernel(uint32_t *y, uint64_t words, 
 
 // Heavy outputs of a plus-times product, one warp per output: output list[i]
 // of vector k receives its sum, rounded to fp32 once: the 2^bits fp32 partial
-// sums of its record (rows first .. first + 2^bits - 1 of acc) and its fp64
-// slot (the two rows after them, B doubles; for bits kHeavyFp64 the slot
-// alone), added in fp64.  The product sends every term of such an output
-// there, so y holds the fill's zero; adding it keeps the result right even if
-// it did not.
+// sums of its record (rows first .. first + 2^bits - 1 of acc) added in fp64,
+// or, for bits kHeavyFp64, its fp64 slot (rows first, first + 1: B
+// doubles).  The product sends every term of such an output there, so y
+// holds the fill's zero; adding it keeps the result right even if it did not.
 __global__ void __launch_bounds__(256) heavy_finish_kernel(const float *acc, const uint32_t *hdir,
                                                            const uint32_t *list, uint32_t h, uint32_t B, float *y)
 {
@@ -65,7 +64,7 @@ __global__ void __launch_bounds__(256) heavy_finish_kernel(const float *acc, con
         const uint32_t bits = rec & 31u;
         const uint64_t first = rec >> 5;
         const uint64_t parts = bits == kHeavyFp64 ? 0u : ((uint64_t)1 << bits);
-        const double *a64 = reinterpret_cast<const double *>(acc + (first + parts) * B);
+        const double *a64 = reinterpret_cast<const double *>(acc + first * B);   // fp64 slot (parts == 0)
         float *yo = y + (uint64_t)o * B;
         const uint64_t words = parts * B;
         const float *a = acc + first * B;
@@ -74,14 +73,14 @@ __global__ void __launch_bounds__(256) heavy_finish_kernel(const float *acc, con
             double s = 0.0;
             for (uint64_t e = lane; e < words; e += 32u) s += (double)a[e];
             for (uint32_t f = 16; f >= B; f >>= 1) s += __shfl_xor_sync(0xffffffffu, s, f);
-            if (lane < B) yo[lane] = __double2float_rn(s + a64[lane] + (double)yo[lane]);
+            if (lane < B) yo[lane] = __double2float_rn(s + (parts ? 0.0 : a64[lane]) + (double)yo[lane]);
         } else {
             for (uint32_t k = 0; k < B; ++k) {
                 double s = 0.0;
                 for (uint64_t e = k + (uint64_t)lane * B; e < words; e += 32ull * B) s += (double)a[e];
 #pragma unroll
                 for (int f = 16; f > 0; f >>= 1) s += __shfl_xor_sync(0xffffffffu, s, f);
-                if (lane == 0) yo[k] = __double2float_rn(s + a64[k] + (double)yo[k]);
+                if (lane == 0) yo[k] = __double2float_rn(s + (parts ? 0.0 : a64[k]) + (double)yo[k]);
             }
         }
     }
@@ -92,12 +91,14 @@ __global__ void __launch_bounds__(256) heavy_finish_kernel(const float *acc, con
 // children's entries, written at dst[child - dst_base].
 __global__ void __launch_bounds__(kWalkThreads)
 ls_expand_kernel(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix, uint32_t a, uint32_t count,
-                 const Coord *src, uint32_t src_base, Coord *dst, uint32_t dst_base)
+                 const Coord *src, uint32_t src_base, Coord *dst, uint32_t dst_base, uint64_t dst_entries,
+                 uint32_t *status)
 {
     const uint32_t wid = blockIdx.x * (kWalkThreads / 32) + (threadIdx.x >> 5);
     uint32_t s, e, base;
     if (!tile_block(sig, dir, prefix, a, count, dst_base, wid, s, e, base)) return;
     warp_walk(sig, s, e, base, [&](uint32_t t, uint32_t sg, uint32_t pos) {
+        if (!K2T_IN_RANGE((uint64_t)(pos - dst_base) + (uint32_t)__popc(sg) <= dst_entries, status)) return;
         const Coord p = src[t - src_base];
         Coord *o = dst + (pos - dst_base);
 #pragma unroll
@@ -270,6 +271,7 @@ int enqueue_product(k2t_tree *t, int32_t dir, int32_t semiring, float w, const v
     va.mask = B >= 32 ? 0xffffffffu : ((1u << B) - 1u);
     va.n_out = n_out;
     va.n_in = dir == K2T_RIGHT ? t->n_cols : t->n_rows;
+    va.status = d->err;
     const bool heavy = heavy_begin(t, d, dir, semiring, va, st);
     uint32_t engine = t->engine;
     if (engine == K2T_ENGINE_CACHED && t->leaf_k4) engine = kEngineCached4;

@@ -268,21 +268,28 @@ uint64_t count_last(const k2t_tree *t, int d, uint64_t a, uint64_t b)
     return b - a;
 }
 
+// Plans the chunks of a range of top nodes into its own lists (several run
+// in parallel over parts of the top level, then join_fused_plans appends
+// them in order); a chunk rooted below the top stores its roots in `roots`,
+// indexed from 0 within the planner.
 struct FusedPlanner {
-    k2t_tree *t;
+    const k2t_tree *t;
     uint64_t cap;
+    std::vector<uint32_t> chunks;
+    std::vector<Coord> roots;
+    uint64_t n_chunks = 0;
 
     void emit(int d, uint64_t a, uint64_t b, const Coord *coords, bool from_top)
     {
-        std::vector<uint32_t> &ch = t->chunks;
+        std::vector<uint32_t> &ch = chunks;
         size_t base = ch.size();
         ch.resize(base + t->chunk_stride, 0);
         uint32_t *rec = &ch[base];
         if (from_top) {
             rec[0] = (uint32_t)a;
         } else {
-            rec[0] = (uint32_t)t->roots.size();
-            for (uint64_t i = a; i < b; ++i) t->roots.push_back(coords[i - a]);
+            rec[0] = (uint32_t)roots.size();
+            for (uint64_t i = a; i < b; ++i) roots.push_back(coords[i - a]);
         }
         rec[1] = (uint32_t)d;
         uint64_t s = a, e = b;
@@ -294,7 +301,7 @@ struct FusedPlanner {
                 e = level_offset(t, lv, e);
             }
         }
-        t->n_chunks++;
+        n_chunks++;
     }
 
     // nodes [a, b) of level d are whole subtrees; coords[i - a] is node i's block
@@ -444,8 +451,7 @@ void plan_bands(k2t_tree *t, int nt)
 // its terms are summed, in rows of max_batch fp32 words:
 //   - mode 1: in an fp64 slot of two rows (record bits kHeavyFp64);
 //   - mode 0: in 2^bits rows of fp32 partial sums, a term going to partial
-//     heavy_partial(its leaf's first input, bits), then the two rows of an
-//     fp64 slot (where warp windows hand over fp64 sums).  The builder counts
+//     heavy_partial(its leaf's first input, bits).  The builder counts
 //     the terms every partial receives and raises bits until none holds more
 //     than `limit`, so every fp32 sum the product forms, in whatever order
 //     its atomics land, has at most `limit` terms.  An output whose inputs
@@ -526,14 +532,16 @@ void heavy_outputs(const uint32_t *out_ids, const uint32_t *in_ids, uint64_t nnz
             }
         }
     }
-    // rows: the fp32 partial sums, then two rows (B doubles) of fp64 slot; the
-    // first row of every output is even, so every slot is 8-byte aligned
+    // rows: the fp32 partial sums (2^bits, bits >= 1), or two rows (B doubles)
+    // of fp64 slot; the first row of every output is even, so every slot is
+    // 8-byte aligned
     uint64_t rows = 0;
     for (size_t id = 0; id < h; ++id) {
         const uint64_t parts = bits[id] == kHeavyFp64 ? 0 : (1ull << bits[id]);
-        if (rows + parts + 2 > kHeavyMaxRows) throw std::length_error("heavy partial sums");
+        const uint64_t take = parts ? parts : 2;
+        if (rows + take > kHeavyMaxRows) throw std::length_error("heavy partial sums");
         hdir[list[id]] = (uint32_t)(rows << 5) | bits[id];
-        rows += parts + 2;
+        rows += take;
         t->hparts[dir] += parts;
         t->hfp64[dir] += parts ? 0 : 1;
     }
@@ -638,6 +646,225 @@ void compute_layout(k2t_tree *t)
     L.total = off;
 }
 
+// Everything of a build once the sorted distinct path keys of the cells are
+// known (keys[0..m), for dim_bits `bits` and the leaf side leaf_k4): heavy
+// outputs (counted over the input list rows/cols of nnz pairs), the levels
+// bottom-up with the cached and top coordinates, directories, plans and the
+// arena layout.  keys and tmp are consumed.  Errors: K2T_ERANGE.
+int finish_build(k2t_tree *t, const k2t_opts &o, int nt, std::vector<uint64_t> &keys, std::vector<uint64_t> &tmp,
+                 size_t m, int bits, int leaf_k4, const uint32_t *rows, const uint32_t *cols, uint64_t nnz)
+{
+    const uint64_t n_rows = t->n_rows, n_cols = t->n_cols;
+    t->opts.leaf_k = leaf_k4 ? 4u : 2u;
+    t->dim_bits = bits;
+    t->leaf_k4 = leaf_k4;
+    t->levels = bits - t->n_k4 - leaf_k4;
+    const int l = t->levels;
+    heavy_outputs(rows, cols, nnz, n_rows, o.heavy_terms, o.heavy_mode, nt, t, 0);
+    heavy_outputs(cols, rows, nnz, n_cols, o.heavy_terms, o.heavy_mode, nt, t, 1);
+    for (int dd = 0; dd < 2; ++dd)
+        if (t->hlist[dd].size() >= (1u << 28)) return K2T_ERANGE;
+
+    t->nodes.assign((size_t)l, 0);
+    t->sig.assign((size_t)l, std::vector<uint64_t>());
+    t->nnz = m;
+
+    if (m == 0) {
+        t->empty = true;
+        for (int dd = 0; dd < 2; ++dd) {
+            t->hlist[dd].clear();
+            t->hdir[dd].clear();
+            t->hrows[dd] = t->hparts[dd] = t->hfp64[dd] = 0;
+        }
+        t->nodes[0] = 1;
+        t->sig[0].assign(2, 0);
+        for (int d = 1; d < l; ++d) t->sig[(size_t)d].assign(1, 0);
+        t->d0 = 0;
+    } else {
+        std::vector<uint16_t> sg(m);
+        bool have_top = false;
+        uint64_t top_max = o.host_top_max_nodes;
+        // cells -> leaves -> ... -> root
+        uint64_t *cur = keys.data(), *nxt = tmp.data();
+        size_t ncur = m;
+        for (int d = l - 1; d >= 0; --d) {
+            int s = level_is_k4(t, d) ? 4 : 2;
+            size_t nn = group_level(cur, ncur, s, nxt, sg.data(), nt);
+            if (nn >= (1ull << 32)) return K2T_ERANGE;
+            t->nodes[(size_t)d] = nn;
+            pack_level(t, d, sg.data(), nn, nt);
+            if (d == l - 2 && (t->engine == K2T_ENGINE_CACHED || t->engine == K2T_ENGINE_BANDED)) {
+                t->cached.resize(nn);
+                parallel_for(nt, [&](int th) {
+                    size_t lo = nn * th / nt, hi = nn * (th + 1) / nt;
+                    for (size_t i = lo; i < hi; ++i) t->cached[i] = prefix_coord(nxt[i], d, t->n_k4);
+                });
+            }
+            if (!have_top && d <= l - 2 && d >= t->n_k4 && (nn <= top_max || d == t->n_k4)) {
+                have_top = true;
+                t->d0 = d;
+                t->top.resize(nn);
+                for (size_t i = 0; i < nn; ++i) t->top[i] = prefix_coord(nxt[i], d, t->n_k4);
+            }
+            std::swap(cur, nxt);
+            ncur = nn;
+        }
+    }
+    std::vector<uint64_t>().swap(keys);
+    std::vector<uint64_t>().swap(tmp);
+
+    if (!t->empty) {
+        t->dir.assign((size_t)(l - 1 - t->d0), std::vector<uint32_t>());
+        for (int d = t->d0; d <= l - 2; ++d) build_directory(t, d, nt);
+        if (t->engine == K2T_ENGINE_BANDED) plan_bands(t, nt);
+        if (t->engine == K2T_ENGINE_FUSED) {
+            // the top level cut into one part per thread, planned in
+            // parallel and joined in order (a chunk never spans two parts);
+            // roots below the top follow the top's coordinates
+            t->chunk_stride = 2 + 2 * (uint32_t)(l - t->d0);
+            t->roots = t->top;
+            const uint64_t n0 = t->nodes[(size_t)t->d0];
+            std::vector<FusedPlanner> parts((size_t)nt, FusedPlanner{t, o.chunk_cap, {}, {}, 0});
+            parallel_for(nt, [&](int th) {
+                const uint64_t lo = n0 * th / nt, hi = n0 * (th + 1) / nt;
+                if (lo < hi) parts[(size_t)th].range(t->d0, lo, hi, t->top.data() + lo, true);
+            });
+            for (FusedPlanner &pp : parts) {
+                const uint32_t shift = (uint32_t)t->roots.size();
+                for (size_t c = 0; c < pp.n_chunks; ++c) {
+                    uint32_t *rec = &pp.chunks[c * t->chunk_stride];
+                    if ((int)rec[1] != t->d0) rec[0] += shift;
+                }
+                t->chunks.insert(t->chunks.end(), pp.chunks.begin(), pp.chunks.end());
+                t->roots.insert(t->roots.end(), pp.roots.begin(), pp.roots.end());
+                t->n_chunks += pp.n_chunks;
+            }
+        } else if (t->engine == K2T_ENGINE_LEVELSYNC) {
+            LsPlanner p{t, o.tile_m, std::vector<uint64_t>((size_t)l + 1, 0)};
+            p.range(t->d0, 0, t->nodes[(size_t)t->d0], 0xff, 0);
+        }
+    }
+    compute_layout(t);
+    return K2T_OK;
+}
+
+// Options with defaults filled in and checked for a matrix of n_rows x n_cols.
+int normalize_opts(const k2t_opts *opts, uint64_t n_rows, uint64_t n_cols, k2t_opts &o)
+{
+    if (opts) o = *opts; else k2t_default_opts(&o);
+    if (o.engine > K2T_ENGINE_BANDED || o.offsets > K2T_OFFSETS_SCAN) return K2T_EINVAL;
+    if (o.band_rows < 16 || o.band_rows > 65536 || (o.band_rows & (o.band_rows - 1))) return K2T_EINVAL;
+    if (o.band_cols && (o.band_cols < 16 || (o.band_cols & (o.band_cols - 1)))) return K2T_EINVAL;
+    if (!o.band_cols) o.band_cols = 1u << 31;
+    if (!o.heavy_terms) o.heavy_terms = kDefaultHeavyTerms;
+    if (o.heavy_mode > 1) return K2T_EINVAL;
+    if (o.leaf_k != 0 && o.leaf_k != 2 && o.leaf_k != 4) return K2T_EINVAL;
+    if (o.chunk_cap < 4 || o.chunk_cap > kMaxChunkCap || o.tile_m < 4) return K2T_EINVAL;
+    if (o.max_batch < 1 || o.max_batch > K2T_MAX_BATCH) return K2T_ERANGE;
+    if (o.host_top_max_nodes < 1) return K2T_EINVAL;
+    if (o.n_k4_levels > 15) return K2T_EINVAL;
+    if (n_rows > (1ull << 32) || n_cols > (1ull << 32)) return K2T_ERANGE;
+    if ((o.engine == K2T_ENGINE_CACHED || o.engine == K2T_ENGINE_BANDED) && !o.cache_last_internal) return K2T_EINVAL;
+    // 4x4 leaves: the CACHED and FUSED engines
+    const bool leaf4_ok = o.engine == K2T_ENGINE_AUTO || o.engine == K2T_ENGINE_CACHED || o.engine == K2T_ENGINE_FUSED;
+    if (o.leaf_k == 4 && !leaf4_ok) return K2T_EINVAL;
+
+    return K2T_OK;
+}
+
+// Bits 0, 2, 4, ... of x, packed (the inverse of spread_bits).
+inline uint32_t compact_bits(uint64_t x)
+{
+    x &= 0x5555555555555555ull;
+    x = (x | (x >> 1)) & 0x3333333333333333ull;
+    x = (x | (x >> 2)) & 0x0F0F0F0F0F0F0F0Full;
+    x = (x | (x >> 4)) & 0x00FF00FF00FF00FFull;
+    x = (x | (x >> 8)) & 0x0000FFFF0000FFFFull;
+    x = (x | (x >> 16)) & 0x00000000FFFFFFFFull;
+    return (uint32_t)x;
+}
+
+int build_from_sorted_keys(const uint64_t *keys, uint64_t m, uint64_t n_rows, uint64_t n_cols, const k2t_opts *opts,
+                           k2t_tree **out)
+{
+    if (!out) return K2T_EINVAL;
+    *out = nullptr;
+    if (n_rows == 0 || n_cols == 0 || (m && !keys)) return K2T_EINVAL;
+    k2t_opts o;
+    int rc = normalize_opts(opts, n_rows, n_cols, o);
+    if (rc) return rc;
+    if (o.n_k4_levels) return K2T_EINVAL;
+    const bool leaf4_ok = o.engine == K2T_ENGINE_AUTO || o.engine == K2T_ENGINE_CACHED || o.engine == K2T_ENGINE_FUSED;
+    uint64_t n = std::max(n_rows, n_cols);
+    int bits0 = 0;
+    while ((1ull << bits0) < n) ++bits0;
+    bits0 = std::max(bits0, 2);
+    const int nt = thread_count(o);
+    try {
+        // keys strictly increasing, inside the padded side
+        std::vector<int> bad((size_t)nt, 0);
+        const uint64_t lim = bits0 >= 32 ? ~0ull : (1ull << (2 * bits0));
+        parallel_for(nt, [&](int th) {
+            uint64_t lo = m * th / nt, hi = m * (th + 1) / nt;
+            for (uint64_t i = lo; i < hi; ++i)
+                if (keys[i] >= lim || (i && keys[i] <= keys[i - 1])) { bad[(size_t)th] = 1; break; }
+        });
+        for (int b : bad) if (b) return K2T_EINVAL;
+        // the leaf side: 4x4 when chosen, or when 2x2 leaves would be dense
+        bool four = o.leaf_k == 4;
+        if (o.leaf_k == 0 && leaf4_ok && m > 0) {
+            std::vector<uint64_t> part((size_t)nt, 0);
+            parallel_for(nt, [&](int th) {
+                uint64_t lo = m * th / nt, hi = m * (th + 1) / nt, c = 0;
+                for (uint64_t i = lo; i < hi; ++i) c += (i == 0 || (keys[i] >> 2) != (keys[i - 1] >> 2)) ? 1 : 0;
+                part[(size_t)th] = c;
+            });
+            uint64_t leaves = 0;
+            for (uint64_t c : part) leaves += c;
+            four = (double)m >= kAutoLeaf4Density * (double)leaves;
+        }
+        // the cells as pairs: the input list of the heavy outputs (and of a
+        // 4x4-leaf build, which needs keys of another digit order)
+        std::vector<uint32_t> rows, cols;
+        if (four || o.heavy_terms != 0xffffffffu) {
+            rows.resize(m);
+            cols.resize(m);
+            parallel_for(nt, [&](int th) {
+                uint64_t lo = m * th / nt, hi = m * (th + 1) / nt;
+                for (uint64_t i = lo; i < hi; ++i) {
+                    rows[i] = compact_bits(keys[i] >> 1);
+                    cols[i] = compact_bits(keys[i]);
+                    if (rows[i] >= n_rows || cols[i] >= n_cols) { bad[(size_t)th] = 1; break; }
+                }
+            });
+            for (int b : bad) if (b) return K2T_ERANGE;
+        }
+        if (four) return k2t_build(rows.data(), cols.data(), m, n_rows, n_cols, &o, out);
+        k2t_tree *t = new (std::nothrow) k2t_tree;
+        if (!t) return K2T_ENOMEM;
+        try {
+            t->opts = o;
+            t->n_rows = n_rows;
+            t->n_cols = n_cols;
+            t->n_k4 = 0;
+            t->engine = o.engine == K2T_ENGINE_AUTO ? (o.cache_last_internal ? K2T_ENGINE_CACHED : K2T_ENGINE_FUSED)
+                                                    : o.engine;
+            std::vector<uint64_t> kv(keys, keys + m), tmp(m);
+            rc = finish_build(t, o, nt, kv, tmp, m, bits0, 0, rows.data(), cols.data(), rows.size());
+        } catch (...) {
+            delete t;
+            throw;
+        }
+        if (rc) { delete t; return rc; }
+        *out = t;
+        return K2T_OK;
+    } catch (const std::bad_alloc &) {
+        return K2T_ENOMEM;
+    } catch (const std::length_error &) {
+        return K2T_ERANGE;
+    }
+}
+
 }  // namespace k2t
 
 using namespace k2t;
@@ -673,24 +900,9 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
     if (n_rows == 0 || n_cols == 0) return K2T_EINVAL;
     if (nnz && (!rows || !cols)) return K2T_EINVAL;
     k2t_opts o;
-    if (opts) o = *opts; else k2t_default_opts(&o);
-    if (o.engine > K2T_ENGINE_BANDED || o.offsets > K2T_OFFSETS_SCAN) return K2T_EINVAL;
-    if (o.band_rows < 16 || o.band_rows > 65536 || (o.band_rows & (o.band_rows - 1))) return K2T_EINVAL;
-    if (o.band_cols && (o.band_cols < 16 || (o.band_cols & (o.band_cols - 1)))) return K2T_EINVAL;
-    if (!o.band_cols) o.band_cols = 1u << 31;
-    if (!o.heavy_terms) o.heavy_terms = kDefaultHeavyTerms;
-    if (o.heavy_mode > 1) return K2T_EINVAL;
-    if (o.leaf_k != 0 && o.leaf_k != 2 && o.leaf_k != 4) return K2T_EINVAL;
-    if (o.chunk_cap < 4 || o.chunk_cap > kMaxChunkCap || o.tile_m < 4) return K2T_EINVAL;
-    if (o.max_batch < 1 || o.max_batch > K2T_MAX_BATCH) return K2T_ERANGE;
-    if (o.host_top_max_nodes < 1) return K2T_EINVAL;
-    if (o.n_k4_levels > 15) return K2T_EINVAL;
-    if (n_rows > (1ull << 32) || n_cols > (1ull << 32)) return K2T_ERANGE;
-    if ((o.engine == K2T_ENGINE_CACHED || o.engine == K2T_ENGINE_BANDED) && !o.cache_last_internal) return K2T_EINVAL;
-    // 4x4 leaves: the CACHED and FUSED engines
+    int rc = normalize_opts(opts, n_rows, n_cols, o);
+    if (rc) return rc;
     const bool leaf4_ok = o.engine == K2T_ENGINE_AUTO || o.engine == K2T_ENGINE_CACHED || o.engine == K2T_ENGINE_FUSED;
-    if (o.leaf_k == 4 && !leaf4_ok) return K2T_EINVAL;
-
     k2t_tree *t = new (std::nothrow) k2t_tree;
     if (!t) return K2T_ENOMEM;
     try {
@@ -755,79 +967,8 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
                 make_keys(1);
             }
         }
-        t->opts.leaf_k = leaf_k4 ? 4u : 2u;
-        t->dim_bits = bits;
-        t->leaf_k4 = leaf_k4;
-        t->levels = bits - t->n_k4 - leaf_k4;
-        const int l = t->levels;
-        heavy_outputs(rows, cols, nnz, n_rows, o.heavy_terms, o.heavy_mode, nt, t, 0);
-        heavy_outputs(cols, rows, nnz, n_cols, o.heavy_terms, o.heavy_mode, nt, t, 1);
-        for (int dd = 0; dd < 2; ++dd)
-            if (t->hlist[dd].size() >= (1u << 28)) { delete t; return K2T_ERANGE; }
-
-        t->nodes.assign((size_t)l, 0);
-        t->sig.assign((size_t)l, std::vector<uint64_t>());
-        t->nnz = m;
-
-        if (m == 0) {
-            t->empty = true;
-            for (int dd = 0; dd < 2; ++dd) {
-                t->hlist[dd].clear();
-                t->hdir[dd].clear();
-                t->hrows[dd] = t->hparts[dd] = t->hfp64[dd] = 0;
-            }
-            t->nodes[0] = 1;
-            t->sig[0].assign(2, 0);
-            for (int d = 1; d < l; ++d) t->sig[(size_t)d].assign(1, 0);
-            t->d0 = 0;
-        } else {
-            std::vector<uint16_t> sg(m);
-            bool have_top = false;
-            uint64_t top_max = o.host_top_max_nodes;
-            // cells -> leaves -> ... -> root
-            uint64_t *cur = keys.data(), *nxt = tmp.data();
-            size_t ncur = m;
-            for (int d = l - 1; d >= 0; --d) {
-                int s = level_is_k4(t, d) ? 4 : 2;
-                size_t nn = group_level(cur, ncur, s, nxt, sg.data(), nt);
-                if (nn >= (1ull << 32)) { delete t; return K2T_ERANGE; }
-                t->nodes[(size_t)d] = nn;
-                pack_level(t, d, sg.data(), nn, nt);
-                if (d == l - 2 && (t->engine == K2T_ENGINE_CACHED || t->engine == K2T_ENGINE_BANDED)) {
-                    t->cached.resize(nn);
-                    parallel_for(nt, [&](int th) {
-                        size_t lo = nn * th / nt, hi = nn * (th + 1) / nt;
-                        for (size_t i = lo; i < hi; ++i) t->cached[i] = prefix_coord(nxt[i], d, t->n_k4);
-                    });
-                }
-                if (!have_top && d <= l - 2 && d >= t->n_k4 && (nn <= top_max || d == t->n_k4)) {
-                    have_top = true;
-                    t->d0 = d;
-                    t->top.resize(nn);
-                    for (size_t i = 0; i < nn; ++i) t->top[i] = prefix_coord(nxt[i], d, t->n_k4);
-                }
-                std::swap(cur, nxt);
-                ncur = nn;
-            }
-        }
-        std::vector<uint64_t>().swap(keys);
-        std::vector<uint64_t>().swap(tmp);
-
-        if (!t->empty) {
-            t->dir.assign((size_t)(l - 1 - t->d0), std::vector<uint32_t>());
-            for (int d = t->d0; d <= l - 2; ++d) build_directory(t, d, nt);
-            if (t->engine == K2T_ENGINE_BANDED) plan_bands(t, nt);
-            if (t->engine == K2T_ENGINE_FUSED) {
-                t->chunk_stride = 2 + 2 * (uint32_t)(l - t->d0);
-                t->roots = t->top;
-                FusedPlanner p{t, o.chunk_cap};
-                p.range(t->d0, 0, t->nodes[(size_t)t->d0], t->top.data(), true);
-            } else if (t->engine == K2T_ENGINE_LEVELSYNC) {
-                LsPlanner p{t, o.tile_m, std::vector<uint64_t>((size_t)l + 1, 0)};
-                p.range(t->d0, 0, t->nodes[(size_t)t->d0], 0xff, 0);
-            }
-        }
-        compute_layout(t);
+        rc = finish_build(t, o, nt, keys, tmp, m, bits, leaf_k4, rows, cols, nnz);
+        if (rc) { delete t; return rc; }
     } catch (const std::bad_alloc &) {
         delete t;
         return K2T_ENOMEM;

@@ -19,9 +19,9 @@ constexpr double kAutoLeaf4Density = 1.75;
 // Heavy plus-times outputs (more non-zeros than one fp32 sum may hold within
 // the bound |y - y_ref| <= 1e-5 * sum|w x| + 1e-6): each is summed in 2^bits
 // fp32 partial sums, a term going to the partial that a multiplicative hash
-// of its leaf's first input picks, plus an fp64 slot; or in the fp64 slot
-// alone (bits = kHeavyFp64).  Its record (one uint32 per output, 0 for the
-// others) is (first row << 5) | bits, rows of max_batch fp32 words.
+// of its leaf's first input run picks; or in an fp64 slot of two rows
+// (bits = kHeavyFp64).  Its record (one uint32 per output, 0 for the others)
+// is (first row << 5) | bits, rows of max_batch fp32 words.
 constexpr uint32_t kDefaultHeavyTerms = 160;
 constexpr uint32_t kHeavyHash = 2654435761u;
 constexpr uint32_t kHeavyFp64 = 31u;
@@ -146,4 +146,11 @@ void compute_layout(k2t_tree *t);
 void level_directory(const k2t_tree *t, int d, std::vector<uint32_t> &dir, int nt);
 // implemented in k2t_device.cu
 void device_release(k2t_tree *t);
+// A tree from the sorted distinct path keys of its cells (plain k = 2 levels;
+// key of cell (r, c): r's bits at odd positions, c's at even ones), as
+// k2t_build would make it from those cells with opts: the device-side
+// product of two trees hands its result over this way.  Errors as
+// k2t_build, EINVAL for keys out of order or past the padded side.
+int build_from_sorted_keys(const uint64_t *keys, uint64_t m, uint64_t n_rows, uint64_t n_cols, const k2t_opts *opts,
+                           k2t_tree **out);
 }  // namespace k2t

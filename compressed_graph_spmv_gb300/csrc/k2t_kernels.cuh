@@ -39,7 +39,28 @@ struct VecArgs {
     const uint32_t *hdir;   // per output below hdir_len: its record, 0 if not heavy
     uint32_t hdir_len;
     float *acc;             // rows of B fp32 words: partial sums and fp64 slots of heavy outputs
+    uint32_t *status;       // the tree's device status word (checked builds report into it)
 };
+
+// ---- checked build ---------------------------------------------------------
+// Compiled with -DK2T_CHECKED (libk2t_checked.so), the kernels test the
+// indexes they take from the tree and its plan against the bounds of what
+// those address: outputs and inputs of every leaf against n_out and n_in,
+// a chunk's level widths against the FUSED staging slots, expand positions
+// against the LEVELSYNC frontier buffers.  A failed test sets
+// K2T_STATUS_OUT_OF_RANGE in the status word and the access is skipped, so a
+// planning or indexing fault shows up as K2T_EDEVICE instead of a memory
+// fault.  In the product build the tests compile away.
+#ifdef K2T_CHECKED
+__device__ __forceinline__ bool in_range(bool ok, uint32_t *status)
+{
+    if (!ok && status) atomicOr(status, K2T_STATUS_OUT_OF_RANGE);
+    return ok;
+}
+#define K2T_IN_RANGE(cond, status) ::k2t::in_range((cond), (status))
+#else
+#define K2T_IN_RANGE(cond, status) true
+#endif
 
 __device__ __forceinline__ uint32_t nibble_at(const uint8_t *sig, uint32_t t)
 {
@@ -143,9 +164,8 @@ __device__ __forceinline__ bool is_noop_word(uint32_t v)
 // An output with more non-zeros than one fp32 sum can take within the bound
 // is "heavy".  Its record (one word per output, built once per tree) names rows of
 // the accumulator array acc (B fp32 words a row): 2^bits fp32 partial sums,
-// each receiving at most heavy_terms terms, then an fp64 slot of two rows (B
-// doubles) for the sums fp64 warp windows hand over; or, bits kHeavyFp64, the
-// fp64 slot alone, which then takes every term.  The records cover the
+// each receiving at most heavy_terms terms; or, bits kHeavyFp64, an fp64 slot
+// of two rows (B doubles), which then takes every term.  The records cover the
 // outputs below hdir_len (the last heavy output, rounded up to a multiple of
 // 4, plus 4): heavy_near(out) says whether a leaf with first output `out`
 // may have a heavy output; heavy_word: the records of a 2x2 leaf's outputs
@@ -160,12 +180,10 @@ __device__ __forceinline__ uint2 heavy_word(const VecArgs &va, uint32_t out)
     return __ldg(reinterpret_cast<const uint2 *>(va.hdir + out));
 }
 
-// fp64 slot (B doubles) of a heavy output's record.
+// fp64 slot (B doubles) of a heavy output summed in fp64 (bits kHeavyFp64).
 __device__ __forceinline__ double *heavy_slot64(const VecArgs &va, uint32_t rec)
 {
-    const uint32_t bits = rec & 31u;
-    const size_t row = (size_t)(rec >> 5) + (bits == kHeavyFp64 ? 0u : (1u << bits));
-    return reinterpret_cast<double *>(va.acc + row * va.B);
+    return reinterpret_cast<double *>(va.acc + (size_t)(rec >> 5) * va.B);
 }
 
 // Where a heavy output (record rec, slice k) sums the terms of a leaf with
@@ -251,7 +269,8 @@ __global__ void fill_kernel(uint32_t *y, uint64_t words, uint32_t pattern);
 __global__ void heavy_finish_kernel(const float *acc, const uint32_t *hdir, const uint32_t *list, uint32_t h,
                                     uint32_t B, float *y);
 __global__ void ls_expand_kernel(const uint8_t *sig, const uint32_t *dir, const uint32_t *prefix, uint32_t a,
-                                 uint32_t count, const Coord *src, uint32_t src_base, Coord *dst, uint32_t dst_base);
+                                 uint32_t count, const Coord *src, uint32_t src_base, Coord *dst, uint32_t dst_base,
+                                 uint64_t dst_entries, uint32_t *status);
 __global__ void ls_block_sums_kernel(const uint8_t *sig, uint32_t a, uint32_t count, uint32_t *sums);
 __global__ void ls_scan_kernel(const uint32_t *sums, uint32_t nblocks, uint32_t *prefix);
 
@@ -330,20 +349,6 @@ __device__ __forceinline__ bool tile_block(const uint8_t *sig, const uint32_t *d
     return true;
 }
 
-// One single-slice update of a warp window entry: the semiring's shared
-// atomic on a 32-bit word, or (w64, plus-times) an fp64 add of d, the leaf's
-// cells w*x_j summed in fp64, on entry i of a window of doubles.
-template <int SR>
-__device__ __forceinline__ void window_put(uint32_t *win, uint32_t i, float v, double d, bool w64)
-{
-    if constexpr (SR == K2T_PLUS_TIMES) {
-        if (w64) {
-            atomicAdd(reinterpret_cast<double *>(win) + i, d);
-            return;
-        }
-    }
-    smem_update<SR>(win + i, __float_as_uint(v));
-}
 
 // Leaves of U leaf blocks (origins r[u], c[u], cells lam[u]) with x entries
 // already loaded (xo[u][0]: input r or c, xo[u][1]: the next one); one
@@ -354,7 +359,7 @@ __device__ __forceinline__ void window_put(uint32_t *win, uint32_t i, float v, d
 template <int SR, int DIR, int U, class InOf>
 __device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint32_t (&out)[U], InOf &&in_of,
                                             const uint32_t (&xo)[U][2], const uint2 (&hw)[U], const VecArgs &va,
-                                            uint32_t *win, uint32_t lo, bool w64)
+                                            uint32_t *win, uint32_t lo)
 {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -364,6 +369,7 @@ __device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint
         const bool a1 = DIR == K2T_RIGHT ? (l & 2u) : (l & 4u);
         const bool b0 = DIR == K2T_RIGHT ? (l & 4u) : (l & 2u);
         const bool b1 = l & 8u;
+        if (!K2T_IN_RANGE(out[u] + ((b0 || b1) ? 1u : 0u) < va.n_out, va.status)) continue;
         if constexpr (SR == K2T_BOOLEAN) {
             uint32_t *y = static_cast<uint32_t *>(va.y);
             const uint32_t v0 = ((a0 ? xo[u][0] : 0u) | (a1 ? xo[u][1] : 0u)) & va.mask;
@@ -386,7 +392,7 @@ __device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint
                 const float v[1] = {a0 ? (a1 ? S::plus(c0, c1) : c0) : c1};
                 if (h.x) heavy_put<SR, 1>(va, h.x, in_of(u), 0u, v, xa, xb, a0, a1);
                 else if (!S::skip(v[0])) {
-                    if (win) window_put<SR>(win, out[u] - lo, v[0], (a0 ? (double)c0 : 0.0) + (a1 ? (double)c1 : 0.0), w64);
+                    if (win) smem_update<SR>(win + (out[u] - lo), __float_as_uint(v[0]));
                     else S::update(y + out[u], v);
                 }
             }
@@ -394,7 +400,7 @@ __device__ __forceinline__ void leaf_apply1(const uint32_t (&lam)[U], const uint
                 const float v[1] = {b0 ? (b1 ? S::plus(c0, c1) : c0) : c1};
                 if (h.y) heavy_put<SR, 1>(va, h.y, in_of(u), 0u, v, xa, xb, b0, b1);
                 else if (!S::skip(v[0])) {
-                    if (win) window_put<SR>(win, out[u] + 1 - lo, v[0], (b0 ? (double)c0 : 0.0) + (b1 ? (double)c1 : 0.0), w64);
+                    if (win) smem_update<SR>(win + (out[u] + 1 - lo), __float_as_uint(v[0]));
                     else S::update(y + out[u] + 1, v);
                 }
             }
@@ -422,15 +428,13 @@ constexpr uint32_t kWarpWindow = K2T_WARP_WINDOW;   // words of a warp's output 
 // atomic per warp instead of one per non-zero.
 //
 // Window modes (wmode):
-//   kWinF32     32-bit words, no heavy plus-times output among the window's
-//               outputs, so leaves need no heavy lookups;
-//   kWinF64     plus-times, single vectors, the span holds heavy outputs:
-//               entries are fp64 (half as many), every output in the span is
-//               summed there; the flush adds heavy outputs to their fp64
-//               slots and rounds the others to fp32 once into y;
-//   kWinShared  a block window that may hold heavy outputs (BANDED): heavy
-//               outputs are routed per leaf and never enter it.
-constexpr int kWinF32 = 0, kWinF64 = 1, kWinShared = 2;
+//   kWinF32     no heavy plus-times output among the window's outputs, so
+//               leaves need no heavy lookups;
+//   kWinShared  the span holds heavy outputs (or, BANDED, it may): heavy
+//               outputs are routed per leaf to their partial sums and never
+//               enter the window, whose sums stay within the fp32 term bound
+//               of the outputs that do.
+constexpr int kWinF32 = 0, kWinShared = 2;
 
 // Heavy plus-times outputs among [lo, lo + span) (span <= kWarpWindow), over
 // the warp: the lanes read the range's records (coalesced).
@@ -460,13 +464,11 @@ __device__ __forceinline__ uint32_t *warp_window_begin(uint32_t mn, uint32_t mx,
     if (mn > mx) return nullptr;
     const uint64_t span64 = (uint64_t)unit * ((uint64_t)mx - mn + 1u);
     if (span64 * width > kWarpWindow) return nullptr;
-    if (SR == K2T_PLUS_TIMES && va.hdir != nullptr && warp_span_has_heavy(va, lo, (uint32_t)span64)) {
-        if (width != 1u || 2u * span64 > kWarpWindow) return nullptr;
-        wmode = kWinF64;
-    }
+    if (SR == K2T_PLUS_TIMES && va.hdir != nullptr && warp_span_has_heavy(va, lo, (uint32_t)span64))
+        wmode = kWinShared;
     span = (uint32_t)span64;
-    const uint32_t words = wmode == kWinF64 ? 2u * span : span * width;
-    for (uint32_t i = lane; i < words; i += 32u) mem[i] = wmode == kWinF64 ? 0u : zero_word<SR>();
+    const uint32_t words = span * width;
+    for (uint32_t i = lane; i < words; i += 32u) mem[i] = zero_word<SR>();
     __syncwarp();
     return mem;
 }
@@ -477,22 +479,7 @@ __device__ __forceinline__ void warp_window_flush(const uint32_t *win, uint32_t 
 {
     const uint32_t lane = threadIdx.x & 31u;
     __syncwarp();
-    if constexpr (SR == K2T_PLUS_TIMES) {
-        if (wmode == kWinF64) {   // single vectors: width 1
-            const double *w64 = reinterpret_cast<const double *>(win);
-            float *y = static_cast<float *>(va.y);
-            const uint64_t limit = va.n_out - lo;
-            for (uint32_t i = lane; i < span; i += 32u) {
-                const double v = w64[i];
-                if (v == 0.0 || i >= limit) continue;
-                const uint32_t o = lo + i;
-                const uint32_t rec = o < va.hdir_len ? __ldg(va.hdir + o) : 0u;
-                if (rec) atomicAdd(heavy_slot64(va, rec), v);
-                else atomicAdd(y + o, (float)v);
-            }
-            return;
-        }
-    }
+    (void)wmode;
     uint32_t *y = static_cast<uint32_t *>(va.y) + (size_t)lo * width;
     const uint64_t limit = (va.n_out - lo) * width;
     for (uint32_t i = lane; i < span * width; i += 32u) {
@@ -513,6 +500,7 @@ __device__ __forceinline__ void leaf_slice_load(uint32_t lam, uint32_t r, uint32
     const bool u1 = DIR == K2T_RIGHT ? (lam & 10u) : (lam & 12u);  // cells on the second
     const float *x = static_cast<const float *>(va.x);
     const size_t B = va.B;
+    if (!K2T_IN_RANGE(in + (u1 ? 1u : 0u) < va.n_in, va.status)) return;
     if (u0) VecLoad<VW>::load(x + (size_t)in * B + k, x0);
     if (u1) VecLoad<VW>::load(x + (size_t)(in + 1) * B + k, x1);
 }
@@ -533,6 +521,8 @@ __device__ __forceinline__ void leaf_slice(uint32_t lam, uint32_t r, uint32_t c,
     const bool a1 = DIR == K2T_RIGHT ? (lam & 2u) : (lam & 4u);
     const bool b0 = DIR == K2T_RIGHT ? (lam & 4u) : (lam & 2u);
     const bool b1 = lam & 8u;
+    if (!K2T_IN_RANGE(out + ((b0 || b1) ? 1u : 0u) < va.n_out && in + ((a1 || b1) ? 1u : 0u) < va.n_in, va.status))
+        return;
     float *y = static_cast<float *>(va.y);
     const size_t B = va.B;
     // One output's combined contribution from x0, x1 (cells u0 on input in,
@@ -605,7 +595,6 @@ __device__ __forceinline__ void warp_leaf_rounds(uint32_t jb, uint32_t je, LeafA
     const uint32_t lane = threadIdx.x & 31u;
     const bool heavy = SR == K2T_PLUS_TIMES && va.hdir != nullptr && out_min < va.hdir_len &&
                        (!win || wmode == kWinShared);
-    const bool w64 = win && wmode == kWinF64;
     if (SR == K2T_BOOLEAN || (VW == 1 && va.B == 1)) {
         constexpr int U = kLeafU;
         const uint32_t *x = static_cast<const uint32_t *>(va.x);
@@ -652,7 +641,7 @@ __device__ __forceinline__ void warp_leaf_rounds(uint32_t jb, uint32_t je, LeafA
                 leaf_at(j0 + 32u * (uint32_t)u + lane, l2, r2, c2, li2);
                 return DIR == K2T_RIGHT ? c2 : r2;
             };
-            leaf_apply1<SR, DIR, U>(lam, out, in_of, xo, hw, va, win, lo, w64);
+            leaf_apply1<SR, DIR, U>(lam, out, in_of, xo, hw, va, win, lo);
         }
         return;
     }
@@ -868,12 +857,15 @@ __device__ __forceinline__ uint32_t rec_at(const uint4 &h, int q)
 template <int SR, int DIR, int U, class InOf>
 __device__ __forceinline__ void leaf4_apply1(const uint32_t (&lam)[U], const uint32_t (&out)[U], InOf &&in_of,
                                              const uint32_t (&xo)[U][4], uint32_t fl, const VecArgs &va,
-                                             uint32_t *win, uint32_t lo, bool w64)
+                                             uint32_t *win, uint32_t lo)
 {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const uint32_t l = lam[u];
         if (!l) continue;
+        if (!K2T_IN_RANGE(out[u] + 31u - (uint32_t)__clz(used4<DIR == K2T_RIGHT ? K2T_LEFT : K2T_RIGHT>(l)) < va.n_out,
+                          va.status))
+            continue;
         if constexpr (SR == K2T_BOOLEAN) {
             uint32_t *y = static_cast<uint32_t *>(va.y);
 #pragma unroll
@@ -908,14 +900,12 @@ __device__ __forceinline__ void leaf4_apply1(const uint32_t (&lam)[U], const uin
                     }
                 }
                 float v[1] = {S::zero()};
-                double d = 0.0;
                 bool any = false;
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     if ((s >> i) & 1u) {
                         const float c = S::contrib(__uint_as_float(xo[u][i]), va.w);
                         v[0] = any ? S::plus(v[0], c) : c;
-                        if (SR == K2T_PLUS_TIMES && w64) d += (double)c;
                         any = true;
                     }
                 if (hd.p32) {
@@ -923,7 +913,7 @@ __device__ __forceinline__ void leaf4_apply1(const uint32_t (&lam)[U], const uin
                     continue;
                 }
                 if (S::skip(v[0])) continue;
-                if (win) window_put<SR>(win, out[u] + q - lo, v[0], d, w64);
+                if (win) smem_update<SR>(win + (out[u] + q - lo), __float_as_uint(v[0]));
                 else S::update(y + out[u] + q, v);
             }
         }
@@ -943,6 +933,10 @@ __device__ __forceinline__ void leaf4_slice(uint32_t lam, uint32_t r, uint32_t c
     float *y = static_cast<float *>(va.y);
     const size_t B = va.B;
     float xv[4][VW];
+    if (!K2T_IN_RANGE(in + 31u - (uint32_t)__clz(use) < va.n_in &&
+                          out + 31u - (uint32_t)__clz(used4<DIR == K2T_RIGHT ? K2T_LEFT : K2T_RIGHT>(lam)) < va.n_out,
+                      va.status))
+        return;
 #pragma unroll
     for (int i = 0; i < 4; ++i)
         if ((use >> i) & 1u) VecLoad<VW>::load(x + (size_t)(in + i) * B + k, xv[i]);
@@ -1002,7 +996,6 @@ __device__ __forceinline__ void warp_leaf4_rounds(uint32_t jb, uint32_t je, Leaf
     const uint32_t lane = threadIdx.x & 31u;
     const bool heavy = SR == K2T_PLUS_TIMES && va.hdir != nullptr && out_min < va.hdir_len &&
                        (!win || wmode == kWinShared);
-    const bool w64 = win && wmode == kWinF64;
     if (SR == K2T_BOOLEAN || (VW == 1 && va.B == 1)) {
         constexpr int U = K2T_LEAF4_U;
         const uint32_t *x = static_cast<const uint32_t *>(va.x);
@@ -1047,7 +1040,7 @@ __device__ __forceinline__ void warp_leaf4_rounds(uint32_t jb, uint32_t je, Leaf
                 leaf_at(j0 + 32u * (uint32_t)u + lane, l2, r2, c2, li2);
                 return DIR == K2T_RIGHT ? c2 : r2;
             };
-            leaf4_apply1<SR, DIR, U>(lam, out, in_of, xo, fl, va, win, lo, w64);
+            leaf4_apply1<SR, DIR, U>(lam, out, in_of, xo, fl, va, win, lo);
         }
         return;
     }
@@ -1406,6 +1399,13 @@ fused_kernel(DevTree tr, const uint32_t *chunks, uint32_t stride, const Coord *r
     const uint32_t rc = rec[0];
     const int dc = (int)rec[1];
     const uint32_t *rng = rec + 2;
+#ifdef K2T_CHECKED
+    {
+        bool fits = dc >= d0 && dc <= l - 2;
+        for (int d = dc; fits && d < l; ++d) fits = rng[2 * (d - d0) + 1] <= cap;
+        if (!K2T_IN_RANGE(fits, status)) return;
+    }
+#endif
     if (lane == 0) {
         // the byte range of every level of the chunk, widened to 16 bytes
         auto plan = [&](int d) {
@@ -1665,6 +1665,7 @@ struct LsBufs {
     Coord *buf[K2T_MAX_LEVELS];
     uint32_t *sums;
     uint32_t *prefix;
+    uint64_t buf_entries;   // entries of each frontier buffer
 };
 
 // The planned launch sequence of the level-synchronous engine (section 3.4).
@@ -1688,7 +1689,7 @@ void run_ls(const k2t_tree *t, const DeviceState *d, const LsBufs &sb, const Vec
         }
         if (s.kind == 0) {
             ls_expand_kernel<<<grid_for_blocks(blocks), kWalkThreads, 0, st>>>(
-                sig, dir, prefix, s.a, s.count, src, s.src_base, sb.buf[lv + 1], s.dst_base);
+                sig, dir, prefix, s.a, s.count, src, s.src_base, sb.buf[lv + 1], s.dst_base, sb.buf_entries, va.status);
         } else {
             const uint32_t base = scan ? (uint32_t)level_offset(t, lv, s.a) : 0u;
             launch_leaf_tile<SR, DIR, VW>(sig, scan ? nullptr : dir, prefix, base, s.a, s.count,
@@ -1704,6 +1705,7 @@ void launch_ls(const k2t_tree *t, const DeviceState *d, const VecArgs &va, cudaS
     for (int lv = 0; lv < K2T_MAX_LEVELS; ++lv) sb.buf[lv] = d->buf[lv];
     sb.sums = d->scan_sums;
     sb.prefix = d->scan_prefix;
+    sb.buf_entries = t->layout.buf_bytes / sizeof(Coord);
     run_ls<SR, DIR, VW>(t, d, sb, va, st);
 }
 

@@ -21,8 +21,16 @@
 //    one record (leaf row, leaf column, 4-bit bitmap) of C.
 //  * The frontier is processed depth first in tiles: a tile of at most M/8
 //    pairs has at most M children, so every level needs one buffer of M
-//    pairs.  The records of C, with repeats (several k reach one block), go to
-//    the host, which builds C's tree with k2t_build (repeats collapse there).
+//    pairs.
+//  * C's cells stay on the device.  Whenever the record buffer fills, and at
+//    the end, the records are merged into a sorted set of C's distinct leaves:
+//    leaf path keys sorted with their products, repeats (several k reach one
+//    block) OR-ed together (CUB radix sort and reduce-by-key).  The set then
+//    expands into the sorted path keys of C's cells, which is the order the
+//    builder packs levels in; only those keys go to the host, which packs the
+//    levels without sorting.  The transitive closure keeps C's keys on the
+//    device from one squaring to the next and forms C or C C there (merge of
+//    two sorted key sets).
 //
 // Requirements: A is n x m and B is m x p with the same padded side and
 // k = 2 on every level (no hybrid top, 2x2 leaves).  The trees need not be
@@ -30,6 +38,11 @@
 // directory) to its own device memory and frees it on return.
 #include <algorithm>
 #include <vector>
+
+#include <cub/device/device_radix_sort.cuh>
+#include <cub/device/device_reduce.cuh>
+#include <cub/device/device_scan.cuh>
+#include <cub/device/device_select.cuh>
 
 #include "k2t_kernels.cuh"
 
@@ -194,7 +207,215 @@ __global__ void __launch_bounds__(kProdThreads) pair_leaf_kernel(ProdLevel la, P
     }
 }
 
+// bit i of v -> bit 2i
+__host__ __device__ __forceinline__ uint64_t spread2(uint32_t v)
+{
+    uint64_t x = v;
+    x = (x | (x << 16)) & 0x0000FFFF0000FFFFull;
+    x = (x | (x << 8)) & 0x00FF00FF00FF00FFull;
+    x = (x | (x << 4)) & 0x0F0F0F0F0F0F0F0Full;
+    x = (x | (x << 2)) & 0x3333333333333333ull;
+    x = (x | (x << 1)) & 0x5555555555555555ull;
+    return x;
+}
+
+// Path key of leaf block (lr, lc) (lr's bits at odd positions) and the 2x2
+// product of each record, written at key[at + i], bits[at + i].
+__global__ void __launch_bounds__(kProdThreads) record_keys_kernel(const uint32_t *rec, uint64_t n, uint64_t at,
+                                                                   uint64_t *key, uint32_t *bits)
+{
+    const uint64_t i = (uint64_t)blockIdx.x * kProdThreads + threadIdx.x;
+    if (i >= n) return;
+    key[at + i] = (spread2(rec[3 * i]) << 1) | spread2(rec[3 * i + 1]);
+    bits[at + i] = rec[3 * i + 2];
+}
+
+// cnt[i] = cells of distinct leaf i.
+__global__ void __launch_bounds__(kProdThreads) leaf_count_kernel(const uint32_t *bits, uint64_t n, uint64_t *cnt)
+{
+    const uint64_t i = (uint64_t)blockIdx.x * kProdThreads + threadIdx.x;
+    if (i < n) cnt[i] = (uint64_t)__popc(bits[i]);
+}
+
+// The cells of distinct leaf i as path keys (leaf key, then the cell digit
+// 2r + c), in digit order, at cell[pos[i] ...]: sorted leaves give sorted
+// cells.
+__global__ void __launch_bounds__(kProdThreads) leaf_cells_kernel(const uint64_t *leaf, const uint32_t *bits,
+                                                                  const uint64_t *pos, uint64_t n, uint64_t *cell)
+{
+    const uint64_t i = (uint64_t)blockIdx.x * kProdThreads + threadIdx.x;
+    if (i >= n) return;
+    const uint32_t b = bits[i];
+    uint64_t o = pos[i];
+#pragma unroll
+    for (uint32_t q = 0; q < 4; ++q)
+        if ((b >> q) & 1u) cell[o++] = (leaf[i] << 2) | q;
+}
+
+// Path keys of cells (r, c) given as pairs.
+__global__ void __launch_bounds__(kProdThreads) cell_keys_kernel(const uint32_t *r, const uint32_t *c, uint64_t n,
+                                                                 uint64_t *key)
+{
+    const uint64_t i = (uint64_t)blockIdx.x * kProdThreads + threadIdx.x;
+    if (i < n) key[i] = (spread2(r[i]) << 1) | spread2(c[i]);
+}
+
+struct BitOr {
+    __device__ __forceinline__ uint32_t operator()(uint32_t a, uint32_t b) const { return a | b; }
+};
+
 namespace {
+
+inline unsigned grid_of(uint64_t n) { return (unsigned)((n + kProdThreads - 1) / kProdThreads); }
+
+// One device allocation, freed with its owner.
+struct DevMem {
+    void *p = nullptr;
+    DevMem() = default;
+    DevMem(const DevMem &) = delete;
+    DevMem &operator=(const DevMem &) = delete;
+    ~DevMem() { if (p) cudaFree(p); }
+    int alloc(size_t bytes)
+    {
+        if (p) { cudaFree(p); p = nullptr; }
+        cudaError_t e = cudaMalloc(&p, bytes ? bytes : 16);
+        if (e != cudaSuccess) { g_last_cuda = (int)e; p = nullptr; return K2T_ENOMEM; }
+        return K2T_OK;
+    }
+    template <class T> T *as() const { return static_cast<T *>(p); }
+    void swap(DevMem &o) { std::swap(p, o.p); }
+};
+
+// A sorted set of distinct leaves of C on the device: path keys and the OR of
+// their 2x2 products.
+struct LeafSet {
+    DevMem key, bits;
+    uint64_t n = 0;
+};
+
+// CUB's scratch for one call (queried, then allocated).
+template <class F>
+int cub_run(F &&f, cudaStream_t st)
+{
+    size_t bytes = 0;
+    K2T_CUDA(f(nullptr, bytes));
+    DevMem tmp;
+    int rc = tmp.alloc(bytes);
+    if (rc) return rc;
+    K2T_CUDA(f(tmp.p, bytes));
+    (void)st;
+    return K2T_OK;
+}
+
+// Merge c records (device, 3 words each) into the set: their leaf keys and
+// products with the set's entries, sorted by key (bits [0, key_bits)),
+// repeats OR-ed together.
+int absorb(LeafSet &s, const uint32_t *rec, uint64_t c, int key_bits, cudaStream_t st)
+{
+    if (!c) return K2T_OK;
+    const uint64_t n = s.n + c;
+    DevMem k0, b0, k1, b1, runs;
+    int rc = k0.alloc(n * 8);
+    if (!rc) rc = b0.alloc(n * 4);
+    if (!rc) rc = k1.alloc(n * 8);
+    if (!rc) rc = b1.alloc(n * 4);
+    if (!rc) rc = runs.alloc(8);
+    if (rc) return rc;
+    if (s.n) {
+        K2T_CUDA(cudaMemcpyAsync(k0.p, s.key.p, s.n * 8, cudaMemcpyDeviceToDevice, st));
+        K2T_CUDA(cudaMemcpyAsync(b0.p, s.bits.p, s.n * 4, cudaMemcpyDeviceToDevice, st));
+    }
+    record_keys_kernel<<<grid_of(c), kProdThreads, 0, st>>>(rec, c, s.n, k0.as<uint64_t>(), b0.as<uint32_t>());
+    K2T_CUDA(cudaGetLastError());
+    const int64_t ni = (int64_t)n;
+    rc = cub_run([&](void *t, size_t &b) {
+        return cub::DeviceRadixSort::SortPairs(t, b, k0.as<uint64_t>(), k1.as<uint64_t>(), b0.as<uint32_t>(),
+                                               b1.as<uint32_t>(), ni, 0, key_bits, st);
+    }, st);
+    if (rc) return rc;
+    rc = cub_run([&](void *t, size_t &b) {
+        return cub::DeviceReduce::ReduceByKey(t, b, k1.as<uint64_t>(), k0.as<uint64_t>(), b1.as<uint32_t>(),
+                                              b0.as<uint32_t>(), runs.as<int64_t>(), BitOr(), ni, st);
+    }, st);
+    if (rc) return rc;
+    int64_t m = 0;
+    K2T_CUDA(cudaMemcpyAsync(&m, runs.p, 8, cudaMemcpyDeviceToHost, st));
+    K2T_CUDA(cudaStreamSynchronize(st));
+    s.key.swap(k0);
+    s.bits.swap(b0);
+    s.n = (uint64_t)m;
+    return K2T_OK;
+}
+
+// The sorted path keys of the set's cells, on the device (*m of them).
+int set_cells(const LeafSet &s, DevMem &cells, uint64_t *m, cudaStream_t st)
+{
+    *m = 0;
+    if (!s.n) return cells.alloc(16);
+    DevMem cnt, pos;
+    int rc = cnt.alloc(s.n * 8);
+    if (!rc) rc = pos.alloc(s.n * 8);
+    if (rc) return rc;
+    leaf_count_kernel<<<grid_of(s.n), kProdThreads, 0, st>>>(s.bits.as<uint32_t>(), s.n, cnt.as<uint64_t>());
+    K2T_CUDA(cudaGetLastError());
+    const int64_t ni = (int64_t)s.n;
+    rc = cub_run([&](void *t, size_t &b) {
+        return cub::DeviceScan::ExclusiveSum(t, b, cnt.as<uint64_t>(), pos.as<uint64_t>(), ni, st);
+    }, st);
+    if (rc) return rc;
+    uint64_t last[2] = {0, 0};
+    K2T_CUDA(cudaMemcpyAsync(&last[0], pos.as<uint64_t>() + s.n - 1, 8, cudaMemcpyDeviceToHost, st));
+    K2T_CUDA(cudaMemcpyAsync(&last[1], cnt.as<uint64_t>() + s.n - 1, 8, cudaMemcpyDeviceToHost, st));
+    K2T_CUDA(cudaStreamSynchronize(st));
+    *m = last[0] + last[1];
+    rc = cells.alloc(*m * 8);
+    if (rc) return rc;
+    leaf_cells_kernel<<<grid_of(s.n), kProdThreads, 0, st>>>(s.key.as<uint64_t>(), s.bits.as<uint32_t>(),
+                                                              pos.as<uint64_t>(), s.n, cells.as<uint64_t>());
+    K2T_CUDA(cudaGetLastError());
+    return K2T_OK;
+}
+
+// out = the sorted union of two sorted key sets (device; *m keys).
+int key_union(const uint64_t *a, uint64_t na, const uint64_t *b, uint64_t nb, int key_bits, DevMem &out, uint64_t *m,
+              cudaStream_t st)
+{
+    const uint64_t n = na + nb;
+    DevMem k0, k1, cnt;
+    int rc = k0.alloc(n * 8);
+    if (!rc) rc = k1.alloc(n * 8);
+    if (!rc) rc = cnt.alloc(8);
+    if (rc) return rc;
+    if (na) K2T_CUDA(cudaMemcpyAsync(k0.p, a, na * 8, cudaMemcpyDeviceToDevice, st));
+    if (nb) K2T_CUDA(cudaMemcpyAsync(k0.as<uint64_t>() + na, b, nb * 8, cudaMemcpyDeviceToDevice, st));
+    const int64_t ni = (int64_t)n;
+    rc = cub_run([&](void *t, size_t &bb) {
+        return cub::DeviceRadixSort::SortKeys(t, bb, k0.as<uint64_t>(), k1.as<uint64_t>(), ni, 0, key_bits, st);
+    }, st);
+    if (rc) return rc;
+    rc = cub_run([&](void *t, size_t &bb) {
+        return cub::DeviceSelect::Unique(t, bb, k1.as<uint64_t>(), k0.as<uint64_t>(), cnt.as<int64_t>(), ni, st);
+    }, st);
+    if (rc) return rc;
+    int64_t got = 0;
+    K2T_CUDA(cudaMemcpyAsync(&got, cnt.p, 8, cudaMemcpyDeviceToHost, st));
+    K2T_CUDA(cudaStreamSynchronize(st));
+    out.swap(k0);
+    *m = (uint64_t)got;
+    return K2T_OK;
+}
+
+// Device keys -> host, then C's tree from them.
+int tree_from_device_keys(const DevMem &cells, uint64_t m, uint64_t n_rows, uint64_t n_cols, const k2t_opts *opts,
+                          cudaStream_t st, std::vector<uint64_t> &host, k2t_tree **out)
+{
+    host.resize(m);
+    if (m) {
+        K2T_CUDA(cudaMemcpyAsync(host.data(), cells.p, m * 8, cudaMemcpyDeviceToHost, st));
+        K2T_CUDA(cudaStreamSynchronize(st));
+    }
+    return build_from_sorted_keys(host.data(), m, n_rows, n_cols, opts, out);
+}
 
 // One tree's levels on the device: signatures of levels 0..l-1 and
 // directories of levels 0..l-2, in one allocation.
@@ -251,19 +472,19 @@ struct Product {
     uint64_t rec_cap = 0;
     unsigned long long *count = nullptr; // records written since the last drain
     void *scratch = nullptr;
-    std::vector<uint32_t> out;           // drained records (3 words each)
+    LeafSet set;                         // C's distinct leaves so far
+    int key_bits = 64;                   // significant bits of a leaf key
 
+    // merge the records written since the last drain into the leaf set
     int drain()
     {
         unsigned long long c = 0;
         K2T_CUDA(cudaMemcpyAsync(&c, count, sizeof(c), cudaMemcpyDeviceToHost, st));
         K2T_CUDA(cudaStreamSynchronize(st));
         if (c) {
-            const size_t at = out.size();
-            out.resize(at + 3 * (size_t)c);
-            K2T_CUDA(cudaMemcpyAsync(out.data() + at, rec, 3 * (size_t)c * sizeof(uint32_t), cudaMemcpyDeviceToHost, st));
+            int rc = absorb(set, rec, (uint64_t)c, key_bits, st);
+            if (rc) return rc;
             K2T_CUDA(cudaMemsetAsync(count, 0, sizeof(unsigned long long), st));
-            K2T_CUDA(cudaStreamSynchronize(st));
         }
         return K2T_OK;
     }
@@ -316,51 +537,23 @@ struct Product {
 
 bool plain_k2(const k2t_tree *t) { return t->n_k4 == 0 && !t->leaf_k4; }
 
-// Distinct cells of C from the records, then C's tree.
-int build_from_records(const std::vector<uint32_t> &recs, uint64_t n_rows, uint64_t n_cols, const k2t_opts *opts,
-                       k2t_tree **out)
+// C = A B on the device: the pair descent, its records merged into C's leaf
+// set, then the sorted path keys of C's cells (*m of them) in `cells`.
+int run_product(const k2t_tree *a, const k2t_tree *b, cudaStream_t st, DevMem &cells, uint64_t *m)
 {
-    std::vector<uint32_t> rows, cols;
-    const size_t nrec = recs.size() / 3;
-    rows.reserve(nrec * 2);
-    cols.reserve(nrec * 2);
-    for (size_t r = 0; r < nrec; ++r) {
-        const uint32_t lr = recs[3 * r], lc = recs[3 * r + 1], bits = recs[3 * r + 2];
-        for (uint32_t b = 0; b < 4; ++b)
-            if ((bits >> b) & 1u) {
-                rows.push_back(2u * lr + (b >> 1));
-                cols.push_back(2u * lc + (b & 1u));
-            }
-    }
-    return k2t_build(rows.data(), cols.data(), rows.size(), n_rows, n_cols, opts, out);
-}
-
-}  // namespace
-}  // namespace k2t
-
-using namespace k2t;
-
-extern "C" {
-
-int k2t_bool_product(const k2t_tree *a, const k2t_tree *b, const k2t_opts *opts, k2t_tree **out, void *stream)
-{
-    if (!a || !b || !out) return K2T_EINVAL;
-    *out = nullptr;
-    if (a->n_cols != b->n_rows || a->dim_bits != b->dim_bits || !plain_k2(a) || !plain_k2(b)) return K2T_EINVAL;
-    if (a->empty || b->empty) {
-        std::vector<uint32_t> none;
-        return build_from_records(none, a->n_rows, b->n_cols, opts, out);
-    }
+    *m = 0;
+    if (a->empty || b->empty) return cells.alloc(16);
     Product P;
     P.a = a;
     P.b = b;
-    P.st = static_cast<cudaStream_t>(stream);
+    P.st = st;
+    P.key_bits = std::max(2 * (a->dim_bits - 1), 1);
     int rc = upload_levels(a, P.ta, P.st);
     if (!rc) rc = upload_levels(b, P.tb, P.st);
     if (rc) return rc;
     const int l = a->levels;
     P.m = 1u << 20;
-    P.rec_cap = 8ull * P.m;  // a full level buffer of pairs has at most 8 leaf products each
+    P.rec_cap = 32ull * P.m;  // records between merges into the leaf set
     const uint32_t tile = P.m / 8;
     const uint32_t tblocks = (tile + kProdThreads - 1) / kProdThreads;
     uint64_t bytes = 0;
@@ -401,8 +594,29 @@ int k2t_bool_product(const k2t_tree *a, const k2t_tree *b, const k2t_opts *opts,
     K2T_CUDA(cudaStreamSynchronize(P.st));
     rc = P.process(0, root, 1u);
     if (!rc) rc = P.drain();
+    if (!rc) rc = set_cells(P.set, cells, m, st);
+    return rc;
+}
+
+}  // namespace
+}  // namespace k2t
+
+using namespace k2t;
+
+extern "C" {
+
+int k2t_bool_product(const k2t_tree *a, const k2t_tree *b, const k2t_opts *opts, k2t_tree **out, void *stream)
+{
+    if (!a || !b || !out) return K2T_EINVAL;
+    *out = nullptr;
+    if (a->n_cols != b->n_rows || a->dim_bits != b->dim_bits || !plain_k2(a) || !plain_k2(b)) return K2T_EINVAL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    DevMem cells;
+    uint64_t m = 0;
+    int rc = run_product(a, b, st, cells, &m);
     if (rc) return rc;
-    return build_from_records(P.out, a->n_rows, b->n_cols, opts, out);
+    std::vector<uint64_t> host;
+    return tree_from_device_keys(cells, m, a->n_rows, b->n_cols, opts, st, host, out);
 }
 
 int k2t_bool_closure(const k2t_tree *a, const k2t_opts *opts, uint32_t max_iters, k2t_tree **out, uint32_t *iters,
@@ -412,43 +626,67 @@ int k2t_bool_closure(const k2t_tree *a, const k2t_opts *opts, uint32_t max_iters
     *out = nullptr;
     *iters = 0;
     if (a->n_rows != a->n_cols || !plain_k2(a)) return K2T_EINVAL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
     // every squaring takes a tree with 2x2 leaves: an automatic leaf size
     // resolves to 2 here (an explicit 4 fails in the first squaring)
     k2t_opts wo;
     if (opts) wo = *opts; else k2t_default_opts(&wo);
     if (wo.leaf_k == 0) wo.leaf_k = 2;
-    opts = &wo;
-    // C <- A, rebuilt with the caller's options
+    if (wo.leaf_k != 2) return K2T_EINVAL;
+    // the trees between squarings only feed the next product: no heavy tables
+    k2t_opts io = wo;
+    io.heavy_terms = 0xffffffffu;
+    // C <- A: its cells, in level order, are its sorted path keys
     std::vector<uint32_t> r(a->nnz), c(a->nnz);
     uint64_t got = 0;
     int rc = k2t_decode(a, r.data(), c.data(), a->nnz, &got);
     if (rc) return rc;
+    const int key_bits = std::max(2 * a->dim_bits, 1);
+    DevMem cur_keys;
+    uint64_t m_cur = got;
+    {
+        DevMem dr, dc;
+        rc = dr.alloc(got * 4);
+        if (!rc) rc = dc.alloc(got * 4);
+        if (!rc) rc = cur_keys.alloc(got * 8);
+        if (rc) return rc;
+        if (got) {
+            K2T_CUDA(cudaMemcpyAsync(dr.p, r.data(), got * 4, cudaMemcpyHostToDevice, st));
+            K2T_CUDA(cudaMemcpyAsync(dc.p, c.data(), got * 4, cudaMemcpyHostToDevice, st));
+            cell_keys_kernel<<<grid_of(got), kProdThreads, 0, st>>>(dr.as<uint32_t>(), dc.as<uint32_t>(), got,
+                                                                      cur_keys.as<uint64_t>());
+            K2T_CUDA(cudaGetLastError());
+        }
+        K2T_CUDA(cudaStreamSynchronize(st));
+    }
+    std::vector<uint64_t> host;
     k2t_tree *cur = nullptr;
-    rc = k2t_build(r.data(), c.data(), got, a->n_rows, a->n_cols, opts, &cur);
+    rc = tree_from_device_keys(cur_keys, m_cur, a->n_rows, a->n_cols, &io, st, host, &cur);
     if (rc) return rc;
     for (uint32_t it = 0; it < max_iters; ++it) {
-        if (cur->dim_bits != a->dim_bits || !plain_k2(cur)) { k2t_free(cur); return K2T_EINVAL; }
-        k2t_tree *sq = nullptr;
-        rc = k2t_bool_product(cur, cur, opts, &sq, stream);
+        DevMem sq;
+        uint64_t m_sq = 0;
+        rc = run_product(cur, cur, st, sq, &m_sq);
         if (rc) { k2t_free(cur); return rc; }
         *iters = it + 1;
-        // C or C C
-        std::vector<uint32_t> rr(cur->nnz + sq->nnz), cc(cur->nnz + sq->nnz);
-        uint64_t n1 = 0, n2 = 0;
-        rc = k2t_decode(cur, rr.data(), cc.data(), cur->nnz, &n1);
-        if (!rc) rc = k2t_decode(sq, rr.data() + n1, cc.data() + n1, sq->nnz, &n2);
-        k2t_free(sq);
+        // C or C C, on the device
+        DevMem nxt;
+        uint64_t m_nxt = 0;
+        rc = key_union(cur_keys.as<uint64_t>(), m_cur, sq.as<uint64_t>(), m_sq, key_bits, nxt, &m_nxt, st);
         if (rc) { k2t_free(cur); return rc; }
-        k2t_tree *nxt = nullptr;
-        rc = k2t_build(rr.data(), cc.data(), n1 + n2, a->n_rows, a->n_cols, opts, &nxt);
-        if (rc) { k2t_free(cur); return rc; }
-        const bool done = nxt->nnz == cur->nnz;
+        if (m_nxt == m_cur) break;   // C stopped growing
         k2t_free(cur);
-        cur = nxt;
-        if (done) break;
+        cur = nullptr;
+        cur_keys.swap(nxt);
+        m_cur = m_nxt;
+        if (it + 1 < max_iters) {
+            rc = tree_from_device_keys(cur_keys, m_cur, a->n_rows, a->n_cols, &io, st, host, &cur);
+            if (rc) return rc;
+        }
     }
-    *out = cur;
-    return K2T_OK;
+    if (cur) k2t_free(cur);
+    // the result, with the caller's options
+    return tree_from_device_keys(cur_keys, m_cur, a->n_rows, a->n_cols, &wo, st, host, out);
 }
 
 }  // extern "C"

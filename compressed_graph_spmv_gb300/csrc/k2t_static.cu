@@ -111,6 +111,7 @@ int k2t_spmv_noalloc(k2t_tree *t, int32_t dir, int32_t semiring, float w, const 
     const int l = t->levels;
     uint64_t need = 0;
     LsBufs sb{};
+    sb.buf_entries = L.buf_bytes / sizeof(Coord);
     void *base = nullptr;
     int rc = static_scratch(cur, &base);
     if (rc) return rc;
@@ -148,6 +149,7 @@ int k2t_spmv_noalloc(k2t_tree *t, int32_t dir, int32_t semiring, float w, const 
         va.w = w;
         va.mask = B >= 32 ? 0xffffffffu : ((1u << B) - 1u);
         va.n_out = n_out;
+        va.status = t->dev->err;
         va.n_in = n_in;
         const bool heavy = heavy_begin(t, t->dev, dir, semiring, va, st);
         pick_static(semiring, dir, vw)(t, t->dev, sb, va, st);

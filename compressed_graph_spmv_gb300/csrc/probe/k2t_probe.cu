@@ -75,7 +75,7 @@ __global__ void probe_smem_red(float *y, uint64_t m)
 
 extern "C" {
 
-int k2t_probe(int32_t kind, const void *x, void *y, uint64_t n, uint64_t m, void *stream);
+K2T_API int k2t_probe(int32_t kind, const void *x, void *y, uint64_t n, uint64_t m, void *stream);
 
 /* Launch one probe pass on `stream` (the caller times it):
  *   kind 0: copy n floats x -> y (n a multiple of 4)

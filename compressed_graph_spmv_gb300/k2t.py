@@ -15,6 +15,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libk2t.so")
+CHECKED_LIB_PATH = os.path.join(_HERE, "libk2t_checked.so")   # same ABI, bounds-tested kernels
 PROBE_LIB_PATH = os.path.join(_HERE, "libk2t_probe.so")   # benchmark instrumentation
 
 RIGHT, LEFT = 0, 1

@@ -39,6 +39,17 @@
 
 #include <stdint.h>
 
+/* Only the calls below are exported: the library is built with hidden
+ * symbol visibility, so its C++ internals (template instances and their
+ * function-local state) stay private to each library file, and two builds
+ * (libk2t.so and the bounds-checked libk2t_checked.so) can be loaded into one
+ * process side by side. */
+#if defined(__GNUC__)
+#define K2T_API __attribute__((visibility("default")))
+#else
+#define K2T_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -183,7 +194,7 @@ typedef struct {
  * offsets, top of at most 2^16 nodes, chunk_cap 256, tile_m 2^20,
  * max_batch 32, no host vectors, CUDA graph on, all host threads, leaf size
  * chosen by the build, heavy_terms 160 in fp32 partial sums. */
-void k2t_default_opts(k2t_opts *o);
+K2T_API void k2t_default_opts(k2t_opts *o);
 
 /* Build the tree of the n_rows x n_cols Boolean matrix whose non-zeros are
  * (rows[i], cols[i]), i < nnz, on the host (section 2.1; construction is the
@@ -195,7 +206,7 @@ void k2t_default_opts(k2t_opts *o);
  * Errors: EINVAL (null out/arrays with nnz > 0, zero side, bad option),
  * ERANGE (an id >= its side, side > 2^32, a level wider than 2^32 - 1 nodes),
  * ENOMEM.  On error *out is NULL. */
-int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
+K2T_API int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
               uint64_t n_rows, uint64_t n_cols, const k2t_opts *opts, k2t_tree **out);
 
 /* Exact device bytes k2t_upload places in its arena (tree, directory, top,
@@ -203,14 +214,14 @@ int k2t_build(const uint32_t *rows, const uint32_t *cols, uint64_t nnz,
  * optional host-product vectors), known before
  * any kernel runs (section 1, "Our approach").  Dense x and y of device
  * products are the caller's and not included. */
-int k2t_workspace_bytes(const k2t_tree *t, uint64_t *bytes);
+K2T_API int k2t_workspace_bytes(const k2t_tree *t, uint64_t *bytes);
 
 /* Copy the device image into `arena` (device memory of at least
  * k2t_workspace_bytes, 256-byte aligned) or, if arena is NULL, into one
  * cudaMalloc of exactly that size that the library owns.  Uploading twice
  * is ESTATE.  Errors: EINVAL (misaligned arena), ENOMEM (arena_bytes too
  * small or allocation failure), ECUDA. */
-int k2t_upload(k2t_tree *t, void *arena, uint64_t arena_bytes, void *stream);
+K2T_API int k2t_upload(k2t_tree *t, void *arena, uint64_t arena_bytes, void *stream);
 
 /* y = A x (dir K2T_RIGHT) or y^T = x^T A (K2T_LEFT) over `semiring` with edge
  * weight w (Table 1: plus-times w = 1, tropical w = 1 for hop counts; the
@@ -236,7 +247,7 @@ int k2t_upload(k2t_tree *t, void *arena, uint64_t arena_bytes, void *stream);
  * Errors: ESTATE (not uploaded, or another device current), EINVAL (bad
  * dir/semiring, null, B = 0, overlap), ERANGE (B > 32; plus-times with heavy
  * outputs and B > opts.max_batch), ECUDA (launch failure). */
-int k2t_spmv(k2t_tree *t, int32_t dir, int32_t semiring, float w,
+K2T_API int k2t_spmv(k2t_tree *t, int32_t dir, int32_t semiring, float w,
              const void *x, void *y, uint32_t B, void *stream);
 
 /* k2t_spmv that also records the cudaEvent_t `event_after_fill` on the stream
@@ -244,7 +255,7 @@ int k2t_spmv(k2t_tree *t, int32_t dir, int32_t semiring, float w,
  * two apart with CUDA events.  When the level-synchronous engine replays a
  * CUDA graph the event is recorded before the graph (it then marks the start
  * of the whole product).  Same errors as k2t_spmv. */
-int k2t_spmv_marked(k2t_tree *t, int32_t dir, int32_t semiring, float w,
+K2T_API int k2t_spmv_marked(k2t_tree *t, int32_t dir, int32_t semiring, float w,
                     const void *x, void *y, uint32_t B, void *stream, void *event_after_fill);
 
 /* Same product on HOST buffers: copies x to the device vectors of the
@@ -252,7 +263,7 @@ int k2t_spmv_marked(k2t_tree *t, int32_t dir, int32_t semiring, float w,
  * Needs opts.host_vectors = 1 and B <= opts.max_batch (else ESTATE/ERANGE).
  * Host buffers may be pageable; pinned buffers copy faster.  After the copy
  * back it reads the device status word: ETIMEOUT or EDEVICE if it is set. */
-int k2t_spmv_host(k2t_tree *t, int32_t dir, int32_t semiring, float w,
+K2T_API int k2t_spmv_host(k2t_tree *t, int32_t dir, int32_t semiring, float w,
                   const void *x_host, void *y_host, uint32_t B, void *stream);
 
 /* The level-synchronous product of k2t_spmv for callers that cannot call
@@ -280,17 +291,17 @@ int k2t_spmv_host(k2t_tree *t, int32_t dir, int32_t semiring, float w,
  *     tree's arena, which this call leaves unused: the device memory in use
  *     is the workspace plus the 64 MiB array.
  *   - Other errors as k2t_spmv. */
-int k2t_spmv_noalloc(k2t_tree *t, int32_t dir, int32_t semiring, float w,
+K2T_API int k2t_spmv_noalloc(k2t_tree *t, int32_t dir, int32_t semiring, float w,
                      const void *x, void *y, uint32_t B, void *stream);
 
 /* Read the tree's device status word (see "Device status word"): waits for
  * the work queued on `stream`, stores the word in *word and, if clear != 0,
  * resets it to 0.  Returns K2T_OK, or ESTATE (not uploaded), EINVAL (null),
  * ECUDA. */
-int k2t_status(k2t_tree *t, uint32_t *word, int32_t clear, void *stream);
+K2T_API int k2t_status(k2t_tree *t, uint32_t *word, int32_t clear, void *stream);
 
 /* Size in bytes of the device array k2t_spmv_noalloc works in. */
-uint64_t k2t_noalloc_scratch_limit(void);
+K2T_API uint64_t k2t_noalloc_scratch_limit(void);
 
 /* Boolean product C = A B of two trees: A n x m, B m x p (a->n_cols ==
  * b->n_rows), built with the same padded side and k = 2 on every level
@@ -303,7 +314,7 @@ uint64_t k2t_noalloc_scratch_limit(void);
  * on the host with k2t_build(opts) into *out (caller frees with k2t_free).
  * Errors: EINVAL (null, shapes or tree kinds that do not match), ENOMEM,
  * ECUDA, and k2t_build's errors. */
-int k2t_bool_product(const k2t_tree *a, const k2t_tree *b, const k2t_opts *opts, k2t_tree **out, void *stream);
+K2T_API int k2t_bool_product(const k2t_tree *a, const k2t_tree *b, const k2t_opts *opts, k2t_tree **out, void *stream);
 
 /* Transitive closure A+ (pairs joined by a path of one or more edges) of a
  * square tree by repeated squaring, C <- C or C C (section 7), until C stops
@@ -311,7 +322,7 @@ int k2t_bool_product(const k2t_tree *a, const k2t_tree *b, const k2t_opts *opts,
  * tree built with opts (an automatic leaf size resolves to 2x2 leaves, which
  * every squaring needs).  Errors as k2t_bool_product; EINVAL for a
  * non-square tree. */
-int k2t_bool_closure(const k2t_tree *a, const k2t_opts *opts, uint32_t max_iters, k2t_tree **out,
+K2T_API int k2t_bool_closure(const k2t_tree *a, const k2t_opts *opts, uint32_t max_iters, k2t_tree **out,
                      uint32_t *iters, void *stream);
 
 /* Multi-source breadth-first search to the fixed point (section 5.8): hop
@@ -332,40 +343,40 @@ int k2t_bool_closure(const k2t_tree *a, const k2t_opts *opts, uint32_t max_iters
  * Errors: ESTATE (not uploaded), EINVAL (non-square, bad dir, null),
  * ERANGE (B = 0 or > 32, a source >= n), ECUDA, ETIMEOUT / EDEVICE (status
  * word set). */
-int k2t_msbfs(k2t_tree *t, int32_t dir, const uint32_t *sources, uint32_t B, int32_t *dist, void *work,
+K2T_API int k2t_msbfs(k2t_tree *t, int32_t dir, const uint32_t *sources, uint32_t B, int32_t *dist, void *work,
               uint32_t max_levels, uint32_t *levels, void *stream);
 
 /* Bytes of the work buffer k2t_msbfs needs for this tree. */
-uint64_t k2t_msbfs_work_bytes(const k2t_tree *t);
+K2T_API uint64_t k2t_msbfs_work_bytes(const k2t_tree *t);
 
 /* Shape, per-level sizes and the device footprint broken down by part. */
-int k2t_stats_get(const k2t_tree *t, k2t_stats *s);
+K2T_API int k2t_stats_get(const k2t_tree *t, k2t_stats *s);
 
 /* Signatures of one level as one byte per node (low 4 bits for k = 2 levels;
  * low 8 bits of the 16-bit signature in out[2i], high 8 bits in out[2i+1]
  * for k = 4 levels: the n_k4 top levels, and the leaf level of a tree with
  * leaf_k = 4).  cap is the capacity of out in bytes; *written is the
  * number of bytes the level needs.  ERANGE if cap is too small. */
-int k2t_level_signatures(const k2t_tree *t, uint32_t level, uint8_t *out, uint64_t cap,
+K2T_API int k2t_level_signatures(const k2t_tree *t, uint32_t level, uint8_t *out, uint64_t cap,
                          uint64_t *written);
 
 /* Device pointers of the uploaded image, for instrumentation: the signature
  * bytes of a level (nibble t of the level at byte t/2, low nibble first; the
  * 16-bit signature of node t at bytes 2t, 2t+1 for a leaf level with
  * leaf_k = 4) and its directory (NULL where absent). */
-int k2t_device_level(const k2t_tree *t, uint32_t level, const void **sig, const void **dir);
+K2T_API int k2t_device_level(const k2t_tree *t, uint32_t level, const void **sig, const void **dir);
 
 /* The cells of the matrix, decoded from the tree on the host, in level order
  * of their leaves.  ERANGE if cap < nnz (then *n_out = nnz). */
-int k2t_decode(const k2t_tree *t, uint32_t *rows, uint32_t *cols, uint64_t cap, uint64_t *n_out);
+K2T_API int k2t_decode(const k2t_tree *t, uint32_t *rows, uint32_t *cols, uint64_t cap, uint64_t *n_out);
 
 /* Release the tree, its host image and any library-owned device memory. */
-void k2t_free(k2t_tree *t);
+K2T_API void k2t_free(k2t_tree *t);
 
-const char *k2t_strerror(int status);
+K2T_API const char *k2t_strerror(int status);
 
 /* The last CUDA error code seen by this thread inside the library (0 if none). */
-int k2t_last_cuda_error(void);
+K2T_API int k2t_last_cuda_error(void);
 
 #ifdef __cplusplus
 }

@@ -247,6 +247,11 @@ def test_library_exports_every_declared_symbol():
     for name in declared:
         assert hasattr(lib, name), name
     assert declared == set(K.EXPORTED)
+    # the bounds-checked build exports the same ABI
+    import ctypes
+    checked = ctypes.CDLL(K.CHECKED_LIB_PATH)
+    for name in declared:
+        assert hasattr(checked, name), name
 
 
 @pytest.mark.parametrize("heavy_terms", [0, 5, 30, 0xFFFFFFFF])
@@ -256,8 +261,8 @@ def test_heavy_outputs_stats(heavy_terms):
     tables take one word per heavy output (the list) and one record word per
     output up to the last heavy one (padded for a 16-byte read); the sums
     take, for the direction with more, rows of max_batch fp32
-    words: 2^bits partial sums and two rows of fp64 slot per heavy output (the
-    slot alone for an output summed in fp64)."""
+    words: 2^bits partial sums per heavy output, or two rows of fp64 slot for
+    an output summed in fp64."""
     rng = np.random.default_rng(21)
     nr, nc = 300, 200
     rows, cols, _ = synth.random_small(3, nr, nc, 0.05)
@@ -285,7 +290,7 @@ def test_heavy_outputs_stats(heavy_terms):
             last = int(np.nonzero(cnt > lim)[0].max())
             hdir = ((last + 1 + 3) // 4 * 4 + 4) * 4
             tables += 4 * h + hdir
-            acc_rows = max(acc_rows, int(s.heavy_partials[d]) + 2 * h)
+            acc_rows = max(acc_rows, int(s.heavy_partials[d]) + 2 * int(s.heavy_fp64[d]))
     want = tables + acc_rows * 4 * 4
     assert s.heavy_kib == (want + 1023) // 1024
     if hr:
