@@ -261,7 +261,7 @@ namespace k2t {
 
 // ---- kernels --------------------------------------------------------------
 constexpr int kWalkThreads = 256;   // 8 warps, one 256-node block each
-constexpr int kFusedThreads = 256;
+constexpr int kFusedThreads = 64;   // two warps: a block frees its slot once its two chunks are done
 constexpr int kFusedWarps = kFusedThreads / 32;   // chunks per thread block (one per warp)
 
 // Kernels without template parameters, defined in k2t_device.cu.
@@ -1365,7 +1365,7 @@ inline uint32_t fused_warp_bytes(int levels, int d0, uint32_t cap, bool l4)
     return fused_header() + (uint32_t)(levels - 1 - d0) * fused_slot(cap, false) + fused_slot(cap, l4) + 16u * cap;
 }
 
-// FUSED engine: warp w of thread block k descends chunk 8k + w, a run of whole
+// FUSED engine: warp w of thread block k descends chunk 2k + w, a run of whole
 // subtrees rooted at level d_c with at most `cap` leaves, from its roots to
 // the leaves, alone: no block barrier, so narrow levels keep only their own
 // warp busy.  The chunk record holds the index of its roots' coordinates and,
@@ -1378,7 +1378,7 @@ inline uint32_t fused_warp_bytes(int levels, int d0, uint32_t cap, bool l4)
 // and the lanes take them round-robin.  No global scratch.  L4: the leaf
 // level holds 4x4 bitmaps (16-bit signatures, section 5.6).
 template <int SR, int DIR, int VW, bool L4>
-__global__ void __launch_bounds__(kFusedThreads, 4)
+__global__ void __launch_bounds__(kFusedThreads, 16)
 fused_kernel(DevTree tr, const uint32_t *chunks, uint32_t stride, const Coord *roots, uint32_t cap, uint64_t n_chunks,
              uint32_t wbytes, VecArgs va, uint32_t *status)
 {
