@@ -190,15 +190,21 @@ def measured_peak():
 
 # --- measured DRAM traffic ---------------------------------------------------------
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the product kernel,
-# from one ncu capture of a smaller workload of the same recipe (R-MAT, ids
-# permuted then BFS-ordered, the cached engine; the capture command is in the
-# profile summary of the cached kernel).  A workload of the same recipe takes
-# the captured bytes scaled by its non-zeros (traffic grows in proportion to
-# the edges: the tree, the cached level and the scattered x / y accesses all
-# do).  The numbers hold only for the device sources they were taken on:
-# "digest" is the SHA-256 of those sources, and any later change to them
-# makes roofline.traffic null until a new capture.
-MEASURED_TRAFFIC = {"digest": None, "workload": None, "nnz": None, "bytes": {}}
+# captured by ncu on the full-size workload itself (these three metrics take one
+# pass, so the capture replays nothing):
+#   python bench.py --steps 2 --warmup 1 --no-cpu-baseline --no-parity --no-ceilings
+#   ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum \
+#       --clock-control none -k regex:cached_block -s 4 -c 4 --csv --log-file dram27.csv <same command>
+# Traffic does not grow in proportion to the edges (on the same recipe at 2^24
+# the B = 16 launches move 1.3-1.6x their algorithmic bytes, at 2^27 2.6-3.1x:
+# the rows of x and y in flight outgrow L2), so the numbers serve only the
+# workload they were taken on.  They hold only for the device sources they were
+# taken on: "digest" is the SHA-256 of those sources, and any later change to
+# them makes roofline.traffic null until a new capture.
+MEASURED_TRAFFIC = {"digest": "29cd9dc78fb44eed3a99cc4c72481beab5da7ce65b2fefeab8ea747b938da3ad",
+                    "workload": "rmat27-bfs-1200M", "nnz": 1200000000,
+                    "bytes": {"right B=1": 16156469760, "left B=1": 18788308992,
+                              "right B=16": 95999932672, "left B=16": 112268192256}}
 
 
 def _code_only(text: str) -> str:
@@ -223,18 +229,16 @@ def device_digest() -> str:
 
 
 def measured_traffic(wl_name: str, nnz: int, product: str):
-    """(bytes per launch, source) for a product of an R-MAT workload, scaled
-    from the recorded capture by non-zeros; (None, why) when there is no
-    capture of the current device code."""
+    """(bytes per launch, source) for a product of the captured workload;
+    (None, why) for any other workload or device code."""
     t = MEASURED_TRAFFIC
     if not t["digest"] or product not in t["bytes"]:
         return None, "no capture recorded"
-    if not wl_name.startswith("rmat") or "bfs" not in wl_name:
-        return None, "no capture of this recipe"
+    if wl_name != t["workload"] or nnz != t["nnz"]:
+        return None, "captured on %s only (traffic does not scale with the edges)" % t["workload"]
     if t["digest"] != device_digest():
         return None, "device code changed since the capture"
-    scale = nnz / t["nnz"]
-    return int(t["bytes"][product] * scale), "ncu on %s, scaled by non-zeros x%.3f" % (t["workload"], scale)
+    return int(t["bytes"][product]), "ncu dram__bytes_read.sum + dram__bytes_write.sum on %s" % t["workload"]
 
 
 # --- byte accounting ------------------------------------------------------------

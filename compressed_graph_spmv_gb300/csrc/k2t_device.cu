@@ -47,18 +47,45 @@ __global__ void __launch_bounds__(256) fill_kernel(uint32_t *y, uint64_t words, 
     for (uint64_t k = tail + i; k < words; k += stride) y[k] = pattern;
 }
 
-// Heavy outputs of a plus-times product, one warp per output: output list[i]
-// of vector k receives its sum, rounded to fp32 once: the 2^bits fp32 partial
-// sums of its record (rows first .. first + 2^bits - 1 of acc) added in fp64,
-// or, for bits kHeavyFp64, its fp64 slot (rows first, first + 1: B
-// doubles).  The product sends every term of such an output there, so y
-// holds the fill's zero; adding it keeps the result right even if it did not.
+// Heavy outputs of a plus-times product: output list[i] of vector k receives
+// its sum, rounded to fp32 once: the 2^bits fp32 partial sums of its record
+// (rows first .. first + 2^bits - 1 of acc) added in fp64, or, for bits
+// kHeavyFp64, its fp64 slot (rows first, first + 1: B doubles).  The product
+// sends every term of such an output there, so y holds the fill's zero;
+// adding it keeps the result right even if it did not.
+//  - B >= 8 dividing 32: a group of B lanes per output (32 / B outputs per
+//    warp at once), lane k summing slice k down the partial rows, four rows
+//    in flight;
+//  - otherwise one warp per output, the lanes striding over its words.
 __global__ void __launch_bounds__(256) heavy_finish_kernel(const float *acc, const uint32_t *hdir,
                                                            const uint32_t *list, uint32_t h, uint32_t B, float *y)
 {
     const uint32_t lane = threadIdx.x & 31u;
     const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x >> 5);
-    for (uint64_t id = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); id < h; id += warps) {
+    const uint64_t gw = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (B >= 8u && 32u % B == 0) {
+        const uint32_t per = 32u / B, sub = lane / B, k = lane % B;
+        for (uint64_t id = gw * per + sub; id < (uint64_t)h + sub; id += warps * per) {
+            if (id >= h) continue;
+            const uint32_t o = __ldg(list + id);
+            const uint32_t rec = __ldg(hdir + o);
+            const uint32_t bits = rec & 31u;
+            const uint64_t first = rec >> 5;
+            const uint64_t parts = bits == kHeavyFp64 ? 0u : ((uint64_t)1 << bits);
+            const float *a = acc + first * B + k;
+            double s = 0.0;
+            uint64_t p = 0;
+            for (; p + 4 <= parts; p += 4)
+                s += ((double)__ldg(a + p * B) + (double)__ldg(a + (p + 1) * B)) +
+                     ((double)__ldg(a + (p + 2) * B) + (double)__ldg(a + (p + 3) * B));
+            for (; p < parts; ++p) s += (double)__ldg(a + p * B);
+            if (!parts) s = reinterpret_cast<const double *>(acc + first * B)[k];   // fp64 slot
+            float *yo = y + (uint64_t)o * B + k;
+            *yo = __double2float_rn(s + (double)*yo);
+        }
+        return;
+    }
+    for (uint64_t id = gw; id < h; id += warps) {
         const uint32_t o = __ldg(list + id);
         const uint32_t rec = __ldg(hdir + o);
         const uint32_t bits = rec & 31u;

@@ -1737,7 +1737,7 @@ inline bool heavy_begin(const k2t_tree *t, const DeviceState *d, int dir, int se
 inline void heavy_end(const k2t_tree *t, const DeviceState *d, int dir, const VecArgs &va, cudaStream_t st)
 {
     const uint32_t h = (uint32_t)t->hlist[dir].size();
-    const uint64_t blocks = std::min<uint64_t>(((uint64_t)h + 7) / 8, 152ull * 16);
+    const uint64_t blocks = std::min<uint64_t>(((uint64_t)h + 7) / 8, 152ull * 32);
     heavy_finish_kernel<<<(unsigned)blocks, 256, 0, st>>>(d->acc, d->hdir[dir], d->hlist[dir], h, va.B,
                                                           static_cast<float *>(va.y));
 }
