@@ -331,20 +331,27 @@ def test_product_argument_errors_on_host():
 
 
 def test_bench_traffic_follows_device_sources(monkeypatch):
-    """roofline.traffic is reported only while the device sources match the
-    digest the capture was taken on."""
+    """roofline.traffic is reported only for the workload the capture was
+    taken on (traffic does not scale with the edges) and only while the
+    device sources match the digest of that capture."""
     import bench
     table = bench.MEASURED_TRAFFIC
     monkeypatch.setitem(table, "digest", bench.device_digest())
-    monkeypatch.setitem(table, "workload", "rmat24-bfs")
-    monkeypatch.setitem(table, "nnz", 1000)
+    monkeypatch.setitem(table, "workload", "rmat27-bfs-1200M")
+    monkeypatch.setitem(table, "nnz", 4000)
     monkeypatch.setitem(table, "bytes", {"right B=1": 123000})
-    # scaled by non-zeros to a workload of the same recipe
-    assert bench.measured_traffic("rmat27-bfs-1200M", 4000, "right B=1")[0] == 492000
+    assert bench.measured_traffic("rmat27-bfs-1200M", 4000, "right B=1")[0] == 123000
     assert bench.measured_traffic("rmat27-bfs-1200M", 4000, "left B=1")[0] is None
+    assert bench.measured_traffic("rmat24-bfs-150M", 1000, "right B=1")[0] is None
     assert bench.measured_traffic("weblike22", 4000, "right B=1")[0] is None
     monkeypatch.setitem(table, "digest", "0" * 64)
     assert bench.measured_traffic("rmat27-bfs-1200M", 4000, "right B=1")[0] is None
+
+
+def test_bench_traffic_table_matches_device_sources():
+    """The recorded capture was taken on the device sources as they stand."""
+    import bench
+    assert bench.MEASURED_TRAFFIC["digest"] == bench.device_digest()
 
 
 def test_clustered_generator_shape():
