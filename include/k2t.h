@@ -88,8 +88,9 @@ typedef struct k2t_tree k2t_tree;
 
 /* Engines: how a product walks the tree. */
 #define K2T_ENGINE_AUTO      0  /* CACHED if the last level is cached, else FUSED      */
-#define K2T_ENGINE_FUSED     1  /* tree-only, one launch: a thread block descends a
-                                   chunk of whole subtrees in shared memory           */
+#define K2T_ENGINE_FUSED     1  /* tree-only, one launch: each warp descends a chunk
+                                   of whole subtrees (at most chunk_cap leaves) in
+                                   shared memory                                      */
 #define K2T_ENGINE_LEVELSYNC 2  /* tree-only, Algorithm 1 as written: one expand
                                    launch per tile and level into global frontier
                                    buffers of at most tile_M codes (section 3.4)      */
