@@ -254,6 +254,22 @@ def test_library_exports_every_declared_symbol():
         assert hasattr(checked, name), name
 
 
+def test_libraries_export_only_the_c_api():
+    """Both builds export the declared calls and no k2t C++ symbol (hidden
+    visibility), so the two can be loaded into one process without their
+    template instances and function-local state binding to each other."""
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not installed")
+    for path in (K.LIB_PATH, K.CHECKED_LIB_PATH):
+        out = subprocess.run([nm, "-D", "--defined-only", path], capture_output=True, text=True, check=True).stdout
+        names = {ln.split()[-1] for ln in out.splitlines() if ln.strip()}
+        assert set(K.EXPORTED) <= names, path
+        assert not [n for n in names if "3k2t" in n], path   # no mangled k2t:: symbol
+
+
 @pytest.mark.parametrize("heavy_terms", [0, 5, 30, 0xFFFFFFFF])
 def test_heavy_outputs_stats(heavy_terms):
     """Heavy outputs are those with more than heavy_terms non-zeros in the
