@@ -442,3 +442,32 @@ def test_status_needs_upload():
         t.status()
     assert e.value.status == -5
     assert K.load().k2t_strerror(-7) == b"device-side wait ran out"
+
+
+def test_bench_oracle_sample_takes_whole_random_bands():
+    """The CPU baseline's sample: every non-zero of the chosen 2^band_bits-row
+    bands and nothing else, bands drawn uniformly (not the leading hub rows),
+    about the target edge count."""
+    import bench
+    wl = synth.rmat_c2(scale=14, edges_per_vertex=8, seed=3)
+    r, c, desc = bench.oracle_sample(wl, 20000, band_bits=6, seed=17)
+    bands = np.unique(r >> 6)
+    rows_in = np.isin(wl.rows >> 6, bands)
+    assert r.size == int(rows_in.sum())                      # whole bands
+    assert set(zip(r.tolist(), c.tolist())) == set(zip(wl.rows[rows_in].tolist(), wl.cols[rows_in].tolist()))
+    assert 20000 <= r.size <= 20000 + int(np.bincount(wl.rows >> 6).max())
+    nb = (wl.n_rows + 63) >> 6
+    assert bands.max() > nb // 2 and bands.min() < nb // 2   # spread over the id range
+    assert "random row bands" in desc
+
+
+def test_bench_algorithmic_bytes_formula():
+    """A product's algorithmic bytes: the tree parts its engine reads, x read
+    once (4 bytes a vector entry) and y read and written once (8 bytes);
+    Boolean vectors take one word whatever B."""
+    import bench
+    rows, cols = synth.rmat(10, 0.57, 0.19, 0.19, 6000, 4)
+    s = K.Tree(rows, cols, 1024, 768 + 256, cache_last_internal=1).stats()
+    tree = s.t_bytes_device + s.l_bytes_device + s.dir_bytes + s.top_bytes + s.cached_bytes + s.plan_bytes
+    assert bench.algorithmic_bytes(s, synth.PLUS_TIMES, 0, 16) == tree + 4 * s.n_cols * 16 + 8 * s.n_rows * 16
+    assert bench.algorithmic_bytes(s, synth.BOOLEAN, 1, 32) == tree + 4 * s.n_rows + 8 * s.n_cols
